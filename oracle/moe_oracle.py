@@ -1,0 +1,457 @@
+"""CPU oracle for the MoE layer hot path (test infrastructure only).
+
+This module is a plain, slow, deliberately unoptimised restatement of what the
+hot path computes.  It exists to check the CUDA library and is used only by the
+tests, by ``__graft_entry__.smoke()`` and by the benchmark's CPU-baseline leg;
+the product path never imports it.  It shares no code with the CUDA path.
+
+Floating point: expert arithmetic is carried in float64 from exact bf16 inputs.
+Values are rounded to bf16 (round-to-nearest-even) only where the method stores
+a bf16 tensor (the SwiGLU intermediate H and the expert output y); routing
+gates and the combined output are produced in float64 and compared to fp32.
+Where floating point decides an integer (which experts a token selects), the
+oracle takes that decision in fp32, as the router does.
+
+Sources (page title, section):
+  [M6.6]  "M6.6 - MoE Runtime Systems: Placement, Dispatch, Kernels, and Topology"
+  [M6.2]  "M6.2 - Expert Parallelism and DeepSeek MoE: Load Balancing, Shared
+          Experts, and Fine-Grained Routing"
+  [POOL]  "Fixed pooled-wave all-to-all for the 8-of-384 MoE"
+  [DISP]  "Dispatch and combine: preserve token identity across expert ranks"
+
+Readings where the pages are silent are noted at each function.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+import math
+
+import numpy as np
+
+EMPTY_HEADER = 0xFFFF  # header element of an empty pool row
+
+
+# ----------------------------------------------------------------------------
+# bf16 helpers (bit-level; no library rounding routine is trusted)
+# ----------------------------------------------------------------------------
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """uint16 bf16 bits -> float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """float64 -> bf16 bits, one rounding, to nearest with ties to even.
+
+    bf16 keeps 8 significant bits and fp32's exponent range.  For |v| with
+    frexp exponent e (v = m * 2^e, 0.5 <= |m| < 1) the bf16 grid spacing is
+    2^(e-8) for normal numbers and 2^-133 below 2^-126.  Dividing by a power of
+    two is exact, np.rint rounds half to even, and the rounded value is exactly
+    representable in fp32, whose top 16 bits are then the bf16 encoding.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    _, e = np.frexp(v)
+    q = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    r = np.rint(v / q) * q
+    with np.errstate(over="ignore"):
+        f = r.astype(np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# Capacity  ([M6.2] 0x01C "Capacity Converts Dynamic Routing Into Bounded
+# Buffers": C = ceil(c_f * T * k / E); [POOL] 04 "Capacity and memory")
+# ----------------------------------------------------------------------------
+
+def _ceil_frac(x: Fraction) -> int:
+    return -((-x.numerator) // x.denominator)
+
+
+def capacity(cf: float, T: int, k: int, E: int) -> int:
+    """Per-expert capacity ceil(cf * T * k / E), in exact rational arithmetic.
+
+    cf is read as the decimal it is written as (1.25, 1.1, ...), so that a
+    product that is an integer on paper is not pushed up by binary rounding.
+    """
+    return _ceil_frac(Fraction(str(cf)) * T * k / E)
+
+
+def pool_capacity(cf: float, T: int, k: int, n_dest: int, n_waves: int) -> int:
+    """Sender pool rows per destination per wave: ceil(cf * T*k / n_dest / n_waves)."""
+    return _ceil_frac(Fraction(str(cf)) * T * k / n_dest / n_waves)
+
+
+def local_capacity(cf: float, T: int, k: int, n_local: int, n_waves: int) -> int:
+    """Receiver rows per local expert per wave: ceil(cf * T*k / n_local / n_waves)."""
+    return _ceil_frac(Fraction(str(cf)) * T * k / n_local / n_waves)
+
+
+# ----------------------------------------------------------------------------
+# Routing
+# ----------------------------------------------------------------------------
+
+def _order_desc_lowest_index(scores: np.ndarray) -> np.ndarray:
+    """Per row, expert indices by (score descending, index ascending).
+
+    A stable sort of the negated scores keeps equal scores in index order;
+    +0.0 and -0.0 compare equal and therefore also fall back to index order.
+    """
+    return np.argsort(-scores, axis=-1, kind="stable")
+
+
+def route_softmax(logits: np.ndarray, k: int):
+    """Top-k over fp32 logits with gates = softmax over the selected logits.
+
+    [M6.2] 0x06L1: the Mixtral family applies an FP32 softmax and renormalises
+    the selected top-k probabilities to one, which equals a softmax taken over
+    the k selected logits.  Reading: selection is made on the fp32 logits
+    themselves (softmax is monotone, and exp can merge distinct logits),
+    slot 0 holds the best expert, ties go to the lower expert index.
+
+    Returns ids int32 [T,k] and gates float64 [T,k].
+    """
+    z = np.asarray(logits, dtype=np.float32)
+    ids = _order_desc_lowest_index(z)[:, :k].astype(np.int32)
+    zs = np.take_along_axis(z, ids, axis=1).astype(np.float64)
+    m = zs.max(axis=1, keepdims=True)
+    ez = np.exp(zs - m)
+    gates = ez / ez.sum(axis=1, keepdims=True)
+    return ids, gates
+
+
+# Own exp for the sigmoid that decides the grouped router's selection.  The
+# selection must come out identical on the CPU and the GPU, so both sides run
+# the same fp32 operations in the same order, each one correctly rounded and
+# none fused:
+#   Cody-Waite range reduction (Cody & Waite, "Software Manual for the
+#   Elementary Functions", 1980): n = rint(x*log2(e)), r = (x - n*L1) - n*L2,
+#   with L1 = ln2 cut to 16 significant bits (so n*L1 is exact for |n| <= 256)
+#   and L2 = ln2 - L1; then e^r by its degree-7 Taylor polynomial in Horner
+#   form; then multiplication by 2^n built from the exponent bits.
+_LOG2E_F32 = np.float32(1.0 / math.log(2.0))
+_LN2_HI_F32 = np.float32(45426.0 / 65536.0)  # round(ln2 * 2^16) / 2^16
+_LN2_LO_F32 = np.float32(math.log(2.0) - 45426.0 / 65536.0)
+_TAYLOR_F32 = [np.float32(1.0 / math.factorial(i)) for i in range(8)]  # 1/0! .. 1/7!
+_EXP_CLAMP_F32 = np.float32(87.0)
+
+
+def exp_det_f32(x) -> np.ndarray:
+    """e^x in fp32 by the fixed recipe above; x is clamped to [-87, 87].
+
+    The clamp keeps 2^n within the normal fp32 range, so no subnormal or
+    infinite intermediate appears and both implementations agree exactly.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    x = np.minimum(np.maximum(x, -_EXP_CLAMP_F32), _EXP_CLAMP_F32)
+    n = np.rint(x * _LOG2E_F32).astype(np.float32)
+    r = (x - n * _LN2_HI_F32) - n * _LN2_LO_F32
+    p = _TAYLOR_F32[7]
+    for c in _TAYLOR_F32[6::-1]:
+        p = p * r + c
+    ni = n.astype(np.int32)
+    two_n = ((ni + 127).astype(np.uint32) << 23).view(np.float32)
+    return (p * two_n).astype(np.float32)
+
+
+def sigmoid_det_f32(z) -> np.ndarray:
+    """sigma(z) = 1 / (1 + e^-z) in fp32 with the fixed exp above."""
+    z = np.asarray(z, dtype=np.float32)
+    one = np.float32(1.0)
+    return (one / (one + exp_det_f32(-z))).astype(np.float32)
+
+
+def route_sigmoid_group(logits: np.ndarray, sel_bias, k: int, n_group: int, topk_group: int,
+                        route_scale: float, return_groups: bool = False):
+    """DeepSeek-V3 group-limited routing.
+
+    [M6.2] 0x06A-0x06D and 0x06I: s = sigmoid(z); corrected score
+    s~ = s + b (fp32, b is selection-only state); per contiguous logical group
+    the score is the sum of its two largest s~; keep the top ``topk_group``
+    groups; experts outside them are not eligible; choose the top k experts by
+    s~ among the eligible; gate = route_scale * s_e / sum of s over the
+    selected experts (the original affinity, not the corrected score).
+    Ties resolve to the lower expert index and the lower group index.
+
+    Returns ids int32 [T,k] and gates float64 [T,k] (plus the kept groups
+    [T,topk_group] and the group scores [T,n_group] when return_groups).
+    """
+    z = np.asarray(logits, dtype=np.float32)
+    T, E = z.shape
+    assert E % n_group == 0
+    s = sigmoid_det_f32(z)
+    b = np.zeros(E, np.float32) if sel_bias is None else np.asarray(sel_bias, np.float32)
+    st = (s + b[None, :]).astype(np.float32)
+    grouped = st.reshape(T, n_group, E // n_group)
+    top2 = np.take_along_axis(grouped, _order_desc_lowest_index(grouped)[:, :, :2], axis=2)
+    gscore = (top2[:, :, 0] + top2[:, :, 1]).astype(np.float32)
+    keep = _order_desc_lowest_index(gscore)[:, :topk_group]
+    eligible = np.zeros((T, n_group), dtype=bool)
+    np.put_along_axis(eligible, keep, True, axis=1)
+    eligible = np.repeat(eligible, E // n_group, axis=1)
+    masked = np.where(eligible, st, np.float32(-np.inf)).astype(np.float32)
+    ids = _order_desc_lowest_index(masked)[:, :k].astype(np.int32)
+    ssel = np.take_along_axis(s, ids, axis=1).astype(np.float64)
+    gates = route_scale * ssel / ssel.sum(axis=1, keepdims=True)
+    if return_groups:
+        return ids, gates, keep.astype(np.int32), gscore
+    return ids, gates
+
+
+# ----------------------------------------------------------------------------
+# Admission, count, prefix, permute  ([M6.2] 0x03B "Count, Prefix, Permute";
+# [M6.6] 0x03B "Count, Prefix Sum, Permute"; [DISP] inverse bijection)
+# ----------------------------------------------------------------------------
+
+def permute(ids: np.ndarray, E: int, cap: int):
+    """Stable expert-major permutation of accepted routes and its inverse.
+
+    Route r = t*k + j carries expert ids[t, j].  Reading (admission order): a
+    route is accepted iff fewer than ``cap`` earlier routes (in route id order)
+    went to the same expert; cap < 0 means dropless.  Then
+      c_e       = accepted routes of expert e,
+      o_0 = 0,  o_{e+1} = o_e + c_e,
+      pi        = accepted route ids ordered by (expert, route id)  (row -> route),
+      pi_inv    = inverse of pi over accepted routes (route -> row, -1 if dropped).
+
+    Returns dict(counts, offsets, row_to_route, route_to_row, n_dropped, ordinal).
+    """
+    e = np.asarray(ids, dtype=np.int64).reshape(-1)
+    R = e.size
+    if R and (e.min() < 0 or e.max() >= E):
+        raise ValueError("expert id out of range")
+    order = np.argsort(e, kind="stable")  # by (expert, route id)
+    se = e[order]
+    first = np.searchsorted(se, np.arange(E), side="left")
+    ordinal = np.empty(R, dtype=np.int64)
+    ordinal[order] = np.arange(R) - first[se]
+    accepted = ordinal < cap if cap >= 0 else np.ones(R, dtype=bool)
+    counts = np.bincount(e[accepted], minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    route_to_row = np.full(R, -1, dtype=np.int64)
+    route_to_row[accepted] = offsets[e[accepted]] + ordinal[accepted]
+    row_to_route = np.empty(int(offsets[-1]), dtype=np.int64)
+    acc_ids = np.nonzero(accepted)[0]
+    row_to_route[route_to_row[acc_ids]] = acc_ids
+    return dict(counts=counts, offsets=offsets, row_to_route=row_to_route,
+                route_to_row=route_to_row, n_dropped=int(R - accepted.sum()), ordinal=ordinal)
+
+
+def gather_rows(x_bits: np.ndarray, row_to_route: np.ndarray, k: int) -> np.ndarray:
+    """x_perm[row] = x[token of route row_to_route[row]] (bit copy)."""
+    return np.asarray(x_bits)[np.asarray(row_to_route) // k]
+
+
+# ----------------------------------------------------------------------------
+# SwiGLU expert  ([M6.6] 0x04A "The Frozen Six-Segment Input":
+# E(X) = (SiLU(X Wg) * (X Wu)) W2, F = 6 n d d_ff; 0x04C "Variable Grouped GEMM")
+# ----------------------------------------------------------------------------
+
+def silu(g: np.ndarray) -> np.ndarray:
+    return g / (1.0 + np.exp(-g))
+
+
+def swiglu(x_f64: np.ndarray, wg_f64: np.ndarray, wu_f64: np.ndarray, wd_f64: np.ndarray,
+           round_h: bool = True, round_y: bool = True):
+    """One expert on rows x [n,d] with weights Wg,Wu [d,I], Wd [I,d] (float64).
+
+    Reading: H is stored as bf16 between the two products and y is returned
+    as bf16 (the pages fix a BF16 returned row); accumulation is exact-ish in
+    float64.  With round_* False the unrounded float64 values are returned.
+    Returns (h, y) as float64 (bf16-valued when rounded).
+    """
+    g = x_f64 @ wg_f64
+    u = x_f64 @ wu_f64
+    h = silu(g) * u
+    if round_h:
+        h = bf16_to_f64(f64_to_bf16(h))
+    y = h @ wd_f64
+    if round_y:
+        y = bf16_to_f64(f64_to_bf16(y))
+    return h, y
+
+
+def grouped_swiglu_rows(x_bits, seg_begin, seg_count, wg_bits, wu_bits, wd_bits, rows=None):
+    """Grouped SwiGLU over row segments of x (bf16 bits); segment q uses expert q's weights.
+
+    Returns (y_bits dict row -> bf16 bits [d], h_bits dict row -> bits [I]) for the
+    requested ``rows`` (all segment rows if None).  Rows are grouped by segment
+    so each expert's weights are converted once.
+    """
+    y_out, h_out = {}, {}
+    for q, (b, c) in enumerate(zip(seg_begin, seg_count)):
+        b, c = int(b), int(c)
+        if c <= 0:
+            continue
+        rs = np.arange(b, b + c)
+        if rows is not None:
+            rs = np.intersect1d(rs, np.asarray(rows))
+            if rs.size == 0:
+                continue
+        x = bf16_to_f64(np.asarray(x_bits)[rs])
+        h, y = swiglu(x, bf16_to_f64(wg_bits[q]), bf16_to_f64(wu_bits[q]),
+                      bf16_to_f64(wd_bits[q]))
+        hb, yb = f64_to_bf16(h), f64_to_bf16(y)
+        for i, r in enumerate(rs):
+            y_out[int(r)] = yb[i]
+            h_out[int(r)] = hb[i]
+    return y_out, h_out
+
+
+def swiglu_flops(rows: int, d: int, d_ff: int) -> int:
+    """Matmul FLOPs of a SwiGLU expert over ``rows`` rows: 6 * rows * d * d_ff."""
+    return 6 * rows * d * d_ff
+
+
+# ----------------------------------------------------------------------------
+# Combine  ([M6.6] 0x03C3 "Round-Trip Identity And Weighted Combine",
+# 0x0CD; [M6.2] 0x03C "Forward Transpose Identity"; 0x0AE: gate applied once,
+# after the expert, token accumulation in FP32)
+# ----------------------------------------------------------------------------
+
+def combine(y_rows_f64: np.ndarray, route_to_row: np.ndarray, gates: np.ndarray, T: int, k: int,
+            shared_y_f64=None, out_init=None) -> np.ndarray:
+    """out[t] = out_init[t] + sum over accepted slots j of gate[t,j] * y[row(t,j)] (+ shared[t]).
+
+    Dropped routes (row -1) contribute nothing and the surviving gates are not
+    renormalised.  The shared expert, when present, is added with weight one.
+    Returns float64 [T, d].
+    """
+    r2r = np.asarray(route_to_row).reshape(T, k)
+    g = np.asarray(gates, dtype=np.float64).reshape(T, k)
+    d = y_rows_f64.shape[1]
+    out = np.zeros((T, d)) if out_init is None else np.array(out_init, dtype=np.float64)
+    for j in range(k):
+        rows = r2r[:, j]
+        ok = rows >= 0
+        out[ok] += g[ok, j:j + 1] * y_rows_f64[rows[ok]]
+    if shared_y_f64 is not None:
+        out += shared_y_f64
+    return out
+
+
+def combine_token(y_lookup, route_to_row_t, gates_t, shared_t=None, init_t=None):
+    """combine() for one token given a row -> y (float64 [d]) lookup."""
+    acc = None if init_t is None else np.array(init_t, dtype=np.float64)
+    for j, r in enumerate(route_to_row_t):
+        if r < 0:
+            continue
+        term = float(gates_t[j]) * y_lookup(int(r))
+        acc = term if acc is None else acc + term
+    if shared_t is not None:
+        acc = shared_t if acc is None else acc + shared_t
+    return acc
+
+
+# ----------------------------------------------------------------------------
+# Pooled-wave layout  ([POOL] 02 "One pool for each destination GPU", 03 "Static
+# shapes from send to combine", 04 "Capacity and memory", 05 "Carry expert IDs
+# in-band", "Report both receiver rates", 07 "fixed source order")
+# ----------------------------------------------------------------------------
+
+def expert_to_dest_local(e, local_per_dest: int):
+    """Expert e lives on destination e // L as local expert e % L (GPU 42 owns E252..E257)."""
+    e = np.asarray(e)
+    return e // local_per_dest, e % local_per_dest
+
+
+def pool_pack(ids: np.ndarray, x_bits: np.ndarray, n_dest: int, local_per_dest: int,
+              n_waves: int, pool_cap: int, wave: int, policy: str = "stripe"):
+    """Sender side of one wave: fill the fixed per-destination pools.
+
+    Routes to destination D are enumerated in route id order (ordinal j_D).
+    Reading of the wave rule (policy):
+      "stripe"  : wave = j_D mod n_waves, pool row = j_D div n_waves
+      "destmod" : wave = D mod n_waves,   pool row = j_D
+    A route of this wave whose row is >= pool_cap is a sender drop.  Pool
+    row 0 is the header: element r < pool_cap holds the local expert id of
+    payload row r (raw uint16 in the bf16 slot), EMPTY_HEADER if row r is
+    unused; elements >= pool_cap are EMPTY_HEADER.  Payload row r is pool row
+    1 + r, a bit copy of the token's activation row.  Unfilled payload rows
+    are left zero here and are not part of the contract.
+
+    Returns dict(pools uint16 [n_dest, pool_cap+1, d], route_to_poolrow int64 [R]
+    (D*pool_cap + row, -1 when not placed in this wave), fill [n_dest],
+    sender_drops (this wave), in_wave (bool [R])).
+    """
+    e = np.asarray(ids, dtype=np.int64).reshape(-1)
+    R = e.size
+    k = R // x_bits.shape[0]
+    d = x_bits.shape[1]
+    D, L = expert_to_dest_local(e, local_per_dest)
+    order = np.argsort(D, kind="stable")
+    sD = D[order]
+    first = np.searchsorted(sD, np.arange(n_dest), side="left")
+    jD = np.empty(R, dtype=np.int64)
+    jD[order] = np.arange(R) - first[sD]
+    if policy == "stripe":
+        wv, row = jD % n_waves, jD // n_waves
+    elif policy == "destmod":
+        wv, row = D % n_waves, jD
+    else:
+        raise ValueError(policy)
+    in_wave = wv == wave
+    placed = in_wave & (row < pool_cap)
+    pools = np.zeros((n_dest, pool_cap + 1, d), dtype=np.uint16)
+    pools[:, 0, :] = EMPTY_HEADER
+    pools[D[placed], 1 + row[placed]] = np.asarray(x_bits)[np.nonzero(placed)[0] // k]
+    pools[D[placed], 0, row[placed]] = L[placed]
+    route_to_poolrow = np.full(R, -1, dtype=np.int64)
+    route_to_poolrow[placed] = D[placed] * pool_cap + row[placed]
+    fill = np.bincount(D[placed], minlength=n_dest)
+    return dict(pools=pools, route_to_poolrow=route_to_poolrow, fill=fill,
+                sender_drops=int((in_wave & ~placed).sum()), in_wave=in_wave)
+
+
+def pool_compact(pools: np.ndarray, pool_cap: int, n_local: int, local_cap: int):
+    """Receiver side of one wave: group pooled rows into fixed per-local-expert arrays.
+
+    Rows are visited in fixed source order (source pool ascending, then row);
+    a row whose header id is l takes the next slot of local expert l, and is a
+    receiver drop once that expert already holds local_cap rows.  Header ids
+    that are neither < n_local nor EMPTY_HEADER are invalid and skipped.
+
+    Returns dict(compact uint16 [n_local, local_cap, d] (unfilled rows zero, not
+    part of the contract), local_counts [n_local], poolrow_to_row int64
+    [n_src*pool_cap] (l*local_cap + slot or -1), receiver_drops, bad_headers).
+    """
+    n_src, _, d = pools.shape
+    hdr = pools[:, 0, :pool_cap].astype(np.int64).reshape(-1)  # [n_src*pool_cap], src-major
+    valid = hdr < n_local
+    bad = int(((hdr != EMPTY_HEADER) & ~valid).sum())
+    ordinal = np.full(hdr.size, -1, dtype=np.int64)
+    vi = np.nonzero(valid)[0]
+    lv = hdr[vi]
+    order = np.argsort(lv, kind="stable")
+    sl = lv[order]
+    first = np.searchsorted(sl, np.arange(n_local), side="left")
+    ov = np.empty(vi.size, dtype=np.int64)
+    ov[order] = np.arange(vi.size) - first[sl]
+    ordinal[vi] = ov
+    keep = valid & (ordinal < local_cap) & (ordinal >= 0)
+    poolrow_to_row = np.full(hdr.size, -1, dtype=np.int64)
+    poolrow_to_row[keep] = hdr[keep] * local_cap + ordinal[keep]
+    compact = np.zeros((n_local, local_cap, d), dtype=np.uint16)
+    ki = np.nonzero(keep)[0]
+    src, r = ki // pool_cap, ki % pool_cap
+    compact[hdr[ki], ordinal[ki]] = pools[src, 1 + r]
+    counts = np.minimum(np.bincount(hdr[vi], minlength=n_local), local_cap)
+    return dict(compact=compact, local_counts=counts, poolrow_to_row=poolrow_to_row,
+                receiver_drops=int(valid.sum() - keep.sum()), bad_headers=bad)
+
+
+def compose_map(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """out[i] = b[a[i]] where a[i] >= 0, else -1 (route -> pool row -> compact row)."""
+    a = np.asarray(a, dtype=np.int64)
+    out = np.full(a.shape, -1, dtype=np.int64)
+    ok = a >= 0
+    out[ok] = np.asarray(b, dtype=np.int64)[a[ok]]
+    return out
+
+
+def drop_rates(total: int, sender: int, receiver: int):
+    """[POOL] 05 'Report both receiver rates': S/T, R/T (additive) and R/(T-S)."""
+    return dict(sender=sender / total, receiver=receiver / total,
+                total=(sender + receiver) / total,
+                receiver_conditional=(receiver / (total - sender)) if total > sender else 0.0)
