@@ -1,0 +1,213 @@
+"""ctypes binding of the C ABI in include/moe.h (argument marshalling only).
+
+Functions keep the C names.  Tensor arguments are torch tensors (or None for a
+NULL pointer) whose ``data_ptr()`` is passed through; ``stream`` defaults to
+torch's current CUDA stream.  Every computation happens in the CUDA library;
+nothing here falls back to another implementation.  A non-OK status raises
+MoeError; loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE_TOO_SMALL = 3
+MOE_ERR_CUDA = 4
+
+MOE_DEV_NONFINITE_LOGIT = 1
+MOE_DEV_BAD_EXPERT_ID = 2
+MOE_DEV_BAD_HEADER_ID = 4
+MOE_DEV_BAD_ROW = 8
+MOE_DEV_TIMEOUT = 16
+
+MOE_SCORE_SOFTMAX = 0
+MOE_SCORE_SIGMOID_GROUP = 1
+MOE_WAVE_STRIPE = 0
+MOE_WAVE_DESTMOD = 1
+MOE_POOL_EMPTY = 0xFFFF
+
+EXPORTED = [
+    "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
+    "moe_permute_workspace_size", "moe_permute", "moe_grouped_swiglu_workspace_size",
+    "moe_grouped_swiglu", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
+    "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+class RouteParams(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("score_fn", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("route_scale", ctypes.c_float)]
+
+
+class PoolParams(ctypes.Structure):
+    _fields_ = [("n_dest", ctypes.c_int32), ("local_per_dest", ctypes.c_int32),
+                ("n_waves", ctypes.c_int32), ("pool_cap", ctypes.c_int32),
+                ("wave_policy", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_version": (_I32, []),
+    "moe_status_string": (ctypes.c_char_p, [_I32]),
+    "moe_capacity": (_I64, [_I64, _I64, _I64, _I64]),
+    "moe_route": (_I32, [ctypes.POINTER(RouteParams), _P, _P, _P, _P, _P, _P]),
+    "moe_sigmoid_det": (_I32, [_I64, _P, _P, _P]),
+    "moe_permute_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "moe_permute": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                           _P, _P]),
+    "moe_grouped_swiglu_workspace_size": (_SZ, [_I32, _I32]),
+    "moe_grouped_swiglu": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                  _P, _P]),
+    "moe_combine": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
+    "moe_pool_pack_workspace_size": (_SZ, [ctypes.POINTER(PoolParams), _I32, _I32]),
+    "moe_pool_pack": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _I32, _P, _P, _P, _P,
+                             _P, _P, _P, _SZ, _P, _P]),
+    "moe_pool_compact_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "moe_pool_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                _P]),
+    "moe_compose_map": (_I32, [_I64, _P, _P, _I64, _P, _P, _P]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIBPATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing "
+                               "(run grouped_expert_gemm_gb300.build.build())")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != MOE_OK:
+        raise MoeError(fn, st, lib().moe_status_string(st).decode())
+
+
+# ----------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------
+
+def moe_version() -> int:
+    return lib().moe_version()
+
+
+def moe_capacity(cf_num: int, cf_den: int, assignments: int, slots: int) -> int:
+    return lib().moe_capacity(cf_num, cf_den, assignments, slots)
+
+
+def moe_route(p: RouteParams, logits, sel_bias, topk_ids, gates, dev_status=None, stream=None):
+    _check("moe_route", lib().moe_route(ctypes.byref(p), _ptr(logits), _ptr(sel_bias),
+                                        _ptr(topk_ids), _ptr(gates), _ptr(dev_status),
+                                        _stream(stream)))
+
+
+def moe_sigmoid_det(n: int, z, s, stream=None):
+    _check("moe_sigmoid_det", lib().moe_sigmoid_det(n, _ptr(z), _ptr(s), _stream(stream)))
+
+
+def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
+    return lib().moe_permute_workspace_size(T, k, E)
+
+
+def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
+                route_to_row, n_dropped, ws, ws_bytes, dev_status=None, stream=None):
+    _check("moe_permute", lib().moe_permute(
+        T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
+        _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(ws), ws_bytes,
+        _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_swiglu_workspace_size(max_rows: int, I: int) -> int:
+    return lib().moe_grouped_swiglu_workspace_size(max_rows, I)
+
+
+def moe_grouped_swiglu(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, w_down, y,
+                       ws, ws_bytes, dev_status=None, stream=None):
+    _check("moe_grouped_swiglu", lib().moe_grouped_swiglu(
+        n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def moe_combine(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, out,
+                dev_status=None, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        T, k, d, _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates), _ptr(shared_y),
+        int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def moe_pool_pack_workspace_size(p: PoolParams, T: int, k: int) -> int:
+    return lib().moe_pool_pack_workspace_size(ctypes.byref(p), T, k)
+
+
+def moe_pool_pack(p: PoolParams, T, d, k, wave, topk_ids, x, pools, route_to_poolrow, pool_fill,
+                  sender_drops, ws, ws_bytes, dev_status=None, stream=None):
+    _check("moe_pool_pack", lib().moe_pool_pack(
+        ctypes.byref(p), T, d, k, wave, _ptr(topk_ids), _ptr(x), _ptr(pools),
+        _ptr(route_to_poolrow), _ptr(pool_fill), _ptr(sender_drops), _ptr(ws), ws_bytes,
+        _ptr(dev_status), _stream(stream)))
+
+
+def moe_pool_compact_workspace_size(n_src: int, pool_cap: int, n_local: int) -> int:
+    return lib().moe_pool_compact_workspace_size(n_src, pool_cap, n_local)
+
+
+def moe_pool_compact(n_src, pool_cap, d, n_local, local_cap, pools, compact, local_counts,
+                     poolrow_to_row, receiver_drops, ws, ws_bytes, dev_status=None, stream=None):
+    _check("moe_pool_compact", lib().moe_pool_compact(
+        n_src, pool_cap, d, n_local, local_cap, _ptr(pools), _ptr(compact), _ptr(local_counts),
+        _ptr(poolrow_to_row), _ptr(receiver_drops), _ptr(ws), ws_bytes, _ptr(dev_status),
+        _stream(stream)))
+
+
+def moe_compose_map(n, a, b, b_len, out, dev_status=None, stream=None):
+    _check("moe_compose_map", lib().moe_compose_map(n, _ptr(a), _ptr(b), b_len, _ptr(out),
+                                                    _ptr(dev_status), _stream(stream)))

@@ -1,0 +1,107 @@
+// Combine: gate-weighted scatter-add of expert output rows back to token order.
+//
+// [M6.6] 0x03C3 "Round-Trip Identity And Weighted Combine" and 0x0CD; [M6.2]
+// 0x03C: out[t] = sum over the token's surviving routes of g_r * z_r, with the
+// gate applied once, after the expert ([M6.6] 0x0AE), and fp32 accumulation of
+// bf16 returned rows.  [POOL] 03: waves add into one fp32 accumulator
+// (accumulate != 0).
+//
+// One block covers one token and up to 128 16-byte column chunks (8 outputs per
+// thread).  The token's k row indices and gates are staged once in shared
+// memory; every thread then issues k independent 16-byte loads of y, sums in
+// fp32 in slot order, and writes two 16-byte fp32 stores.  No atomics: each
+// output element has exactly one writer, so the result is deterministic.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCombThreads = 128;
+
+__global__ void __launch_bounds__(kCombThreads)
+combine_kernel(int k, int chunks, const uint4* __restrict__ y, int64_t y_rows,
+               const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
+               const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
+               uint32_t* __restrict__ dev_status) {
+  __shared__ int32_t s_row[16];
+  __shared__ float s_gate[16];
+  const int64_t t = blockIdx.y;
+  if (threadIdx.x < k) {
+    int32_t r = __ldg(route_to_row + t * k + threadIdx.x);
+    if (r >= 0 && r >= y_rows) {
+      report(dev_status, MOE_DEV_BAD_ROW);
+      r = -1;
+    }
+    s_row[threadIdx.x] = r;
+    s_gate[threadIdx.x] = __ldg(gates + t * k + threadIdx.x);
+  }
+  __syncthreads();
+  const int c = blockIdx.x * kCombThreads + threadIdx.x;
+  if (c >= chunks) return;
+  float acc[8];
+  float4* o = out + (t * chunks + c) * 2;
+  if (accumulate) {
+    const float4 a = o[0], b = o[1];
+    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  }
+  uint4 v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < k && s_row[j] >= 0) v[j] = __ldg(y + static_cast<int64_t>(s_row[j]) * chunks + c);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < k && s_row[j] >= 0) {
+      float f[8];
+      unpack8(v[j], f);
+      const float g = s_gate[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    }
+  }
+  if (shared_y != nullptr) {
+    float f[8];
+    unpack8(__ldg(shared_y + t * chunks + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
+  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
+                               const int32_t* route_to_row, const float* gates,
+                               const moe_bf16* shared_y, int32_t accumulate, float* out,
+                               uint32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || k <= 0 || d <= 0 || y_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (k > 16 || d % 8 != 0 || T > 65535 * 1024) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (out == nullptr || route_to_row == nullptr || gates == nullptr ||
+      (y == nullptr && y_rows > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(out) || (y != nullptr && !aligned16(y)) ||
+      (shared_y != nullptr && !aligned16(shared_y)))
+    return MOE_ERR_UNSUPPORTED;
+  const int chunks = d / 8;
+  // grid.y is limited to 65535: fold larger token counts into several launches.
+  cudaStream_t s = as_cuda(stream);
+  for (int64_t t0 = 0; t0 < T; t0 += 65535) {
+    const int64_t nt = T - t0 < 65535 ? T - t0 : 65535;
+    const dim3 grid(static_cast<unsigned>(ceil_div(chunks, kCombThreads)), static_cast<unsigned>(nt));
+    combine_kernel<<<grid, kCombThreads, 0, s>>>(
+        k, chunks, reinterpret_cast<const uint4*>(y), y_rows, route_to_row + t0 * k,
+        gates + t0 * k,
+        shared_y ? reinterpret_cast<const uint4*>(shared_y) + t0 * chunks : nullptr, accumulate,
+        reinterpret_cast<float4*>(out) + t0 * chunks * 2, dev_status);
+  }
+  return launch_status();
+}

@@ -1,0 +1,60 @@
+// Shared device/host helpers of the MoE hot-path library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline cudaStream_t as_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch-error check used at the end of every entry point.
+inline moe_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+__device__ __forceinline__ void report(uint32_t* dev_status, uint32_t bits) {
+  if (dev_status != nullptr) atomicOr(dev_status, bits);
+}
+
+// Workspace carving: 256-byte aligned sub-buffers.
+struct Carver {
+  size_t off = 0;
+  template <typename T>
+  size_t take(size_t count) {
+    size_t o = (off + 255) & ~size_t(255);
+    off = o + count * sizeof(T);
+    return o;
+  }
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Unpack 8 bf16 held in a uint4 into 8 floats (element order preserved).
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Pack two floats into bf16x2 with round-to-nearest-even (lo element first).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace moe

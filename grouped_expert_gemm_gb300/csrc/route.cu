@@ -1,0 +1,254 @@
+// Router: top-k selection over fp32 logits with softmax-over-selected gates, or
+// DeepSeek-V3 group-limited sigmoid routing.
+//
+// [M6.2] 0x06L1 (family table), 0x06A-0x06D and 0x06I (V3 group rule and gate).
+//
+// One warp owns one token.  Lane l holds experts e = 32*i + l (coalesced 128-byte
+// row segments per load).  Each selection round is a warp all-reduce of 64-bit
+// keys (orderable score bits << 32 | ~expert), so the maximum key is the highest
+// score and, among equal scores, the lowest expert index; +0.0 and -0.0 are
+// folded together first so they tie.  NaN logits are reported and replaced by
+// -inf, which ranks below every number.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// ---- deterministic fp32 sigmoid -------------------------------------------
+// e^x: Cody-Waite reduction with ln2 split at 16 significant bits, degree-7
+// Taylor polynomial of e^r in Horner form, scale by 2^n from exponent bits.
+// Every step is an explicitly rounded single fp32 operation (no contraction),
+// so a host implementation of the same steps gets identical bits.
+__device__ __forceinline__ float exp_det(float x) {
+  x = fminf(fmaxf(x, -87.0f), 87.0f);
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));                 // x * log2(e)
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0x1.62e4p-1f)),  // - n * ln2_hi
+                            __fmul_rn(n, 0x1.7f7d1cp-20f));            // - n * ln2_lo
+  float p = 0x1.a01a02p-13f;                                           // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);                     // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);                      // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);                      // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);                      // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);                                // 1/2!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                                // 1/1!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                                // 1/0!
+  const float two_n = __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23);
+  return __fmul_rn(p, two_n);
+}
+
+__device__ __forceinline__ float sigmoid_det(float z) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_det(-z)));
+}
+
+// Orderable bits of a float: unsigned comparison of the result follows float order.
+__device__ __forceinline__ uint32_t ord_bits(float v) {
+  if (v == 0.0f) v = 0.0f;  // fold -0.0 into +0.0
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_to_float(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+__device__ __forceinline__ uint64_t make_key(float v, int e) {
+  return (static_cast<uint64_t>(ord_bits(v)) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
+}
+
+__device__ __forceinline__ int key_expert(uint64_t key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+constexpr int kTokensPerBlock = 8;
+
+template <int VPL, bool GROUPED>
+__global__ void __launch_bounds__(kTokensPerBlock * 32)
+route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale,
+             const float* __restrict__ logits, const float* __restrict__ sel_bias,
+             int32_t* __restrict__ topk_ids, float* __restrict__ gates,
+             uint32_t* __restrict__ dev_status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTokensPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + static_cast<int64_t>(t) * E;
+
+  float sel[VPL];  // selection score: the logit, or the corrected sigmoid s~
+  float aff[VPL];  // gate source (V3: original affinity s)
+  uint32_t taken = 0;
+  bool saw_nan = false;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = i * 32 + lane;
+    float z = -INFINITY;
+    if (e < E) {
+      z = __ldg(row + e);
+      if (z != z) { saw_nan = true; z = -INFINITY; }
+    } else {
+      taken |= 1u << i;
+    }
+    if (GROUPED) {
+      aff[i] = sigmoid_det(z);
+      const float b = (sel_bias != nullptr && e < E) ? __ldg(sel_bias + e) : 0.0f;
+      sel[i] = __fadd_rn(aff[i], b);
+    } else {
+      sel[i] = z;
+      aff[i] = 0.0f;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, saw_nan) && lane == 0) report(dev_status, MOE_DEV_NONFINITE_LOGIT);
+
+  if (GROUPED) {
+    // Group score: sum of the two largest corrected scores of each contiguous group.
+    const int gs = E / n_group;
+    float my_gscore = -INFINITY;
+    for (int g = 0; g < n_group; ++g) {
+      float b1 = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = i * 32 + lane;
+        if (e < E && e / gs == g) {
+          const float v = sel[i];
+          if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o);
+        const float o2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
+        const float n1 = fmaxf(b1, o1);
+        const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
+        b1 = n1; b2 = n2;
+      }
+      if (lane == g) my_gscore = __fadd_rn(b1, b2);
+    }
+    // Keep the topk_group best groups (ties to the lower group index).
+    uint32_t keep = 0;
+    uint64_t gkey = lane < n_group ? make_key(my_gscore, lane) : 0ull;
+    for (int r = 0; r < topk_group; ++r) {
+      const uint64_t best = warp_max_u64(gkey);
+      const int g = key_expert(best);
+      keep |= 1u << g;
+      if (lane == g) gkey = 0ull;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < E && !((keep >> (e / gs)) & 1u)) taken |= 1u << i;
+    }
+  }
+
+  // k rounds of warp arg-max; lane j keeps the j-th winner.
+  int my_id = 0;
+  float my_sel = 0.0f, my_aff = 0.0f, top_sel = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    uint64_t local = 0ull;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (!((taken >> i) & 1u)) {
+        const uint64_t key = make_key(sel[i], i * 32 + lane);
+        local = key > local ? key : local;
+      }
+    }
+    const uint64_t best = warp_max_u64(local);
+    const int e = key_expert(best);
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (i * 32 + lane == e) { taken |= 1u << i; a = aff[i]; }
+    }
+    a = __shfl_sync(0xFFFFFFFFu, a, e & 31);
+    const float v = ord_to_float(static_cast<uint32_t>(best >> 32));
+    if (j == 0) top_sel = v;
+    if (lane == j) { my_id = e; my_sel = v; my_aff = a; }
+  }
+
+  float g;
+  if (GROUPED) {
+    const float s = warp_sum(lane < k ? my_aff : 0.0f);
+    g = route_scale * my_aff / s;
+  } else {
+    const float ex = lane < k ? expf(my_sel - top_sel) : 0.0f;
+    const float s = warp_sum(ex);
+    g = ex / s;
+  }
+  if (lane < k) {
+    topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
+    gates[static_cast<int64_t>(t) * k + lane] = g;
+  }
+}
+
+template <bool GROUPED>
+moe_status launch_route(const moe_route_params* p, const float* logits, const float* sel_bias,
+                        int32_t* ids, float* gates, uint32_t* st, cudaStream_t s) {
+  const int vpl = static_cast<int>(ceil_div(p->E, 32));
+  const dim3 grid(static_cast<unsigned>(ceil_div(p->T, kTokensPerBlock)));
+  const dim3 block(kTokensPerBlock * 32);
+#define MOE_ROUTE_CASE(V)                                                                     \
+  route_kernel<V, GROUPED><<<grid, block, 0, s>>>(p->T, p->E, p->k, p->n_group, p->topk_group, \
+                                                  p->route_scale, logits, sel_bias, ids,      \
+                                                  gates, st)
+  if (vpl <= 1) MOE_ROUTE_CASE(1);
+  else if (vpl <= 2) MOE_ROUTE_CASE(2);
+  else if (vpl <= 4) MOE_ROUTE_CASE(4);
+  else if (vpl <= 8) MOE_ROUTE_CASE(8);
+  else if (vpl <= 12) MOE_ROUTE_CASE(12);
+  else MOE_ROUTE_CASE(16);
+#undef MOE_ROUTE_CASE
+  return launch_status();
+}
+
+__global__ void sigmoid_det_kernel(int64_t n, const float* __restrict__ z, float* __restrict__ s) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    s[i] = sigmoid_det(z[i]);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_route(const moe_route_params* p, const float* logits,
+                             const float* sel_bias, int32_t* topk_ids, float* gates,
+                             uint32_t* dev_status, moe_stream_t stream) {
+  if (p == nullptr || logits == nullptr || topk_ids == nullptr || gates == nullptr)
+    return p && p->T == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->E <= 0 || p->k <= 0 || p->k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->E > 512 || p->k > 16) return MOE_ERR_UNSUPPORTED;
+  if (p->T == 0) return MOE_OK;
+  if (p->score_fn == MOE_SCORE_SOFTMAX) {
+    if (sel_bias != nullptr) return MOE_ERR_INVALID_ARG;
+    return launch_route<false>(p, logits, nullptr, topk_ids, gates, dev_status, as_cuda(stream));
+  }
+  if (p->score_fn != MOE_SCORE_SIGMOID_GROUP) return MOE_ERR_INVALID_ARG;
+  if (p->n_group <= 0 || p->topk_group <= 0 || p->topk_group > p->n_group ||
+      p->E % p->n_group != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (p->n_group > 32 || p->E / p->n_group < 2 || p->topk_group * (p->E / p->n_group) < p->k)
+    return MOE_ERR_UNSUPPORTED;
+  return launch_route<true>(p, logits, sel_bias, topk_ids, gates, dev_status, as_cuda(stream));
+}
+
+MOE_API moe_status moe_sigmoid_det(int64_t n, const float* z, float* s, moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (z == nullptr || s == nullptr))) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  const int64_t blocks = ceil_div(n, 256);
+  sigmoid_det_kernel<<<static_cast<unsigned>(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0,
+                       as_cuda(stream)>>>(n, z, s);
+  return launch_status();
+}

@@ -1,0 +1,193 @@
+"""The MoE layer hot path composed from the C-ABI calls.
+
+``MoELayer``       route -> permute (capacity or dropless) -> grouped SwiGLU over
+                   the expert segments (+ an optional always-on shared expert)
+                   -> gate-weighted fp32 combine.
+``PooledMoELayer`` route -> for each wave: pool pack (sender) -> pool compact
+                   (receiver; the pools are read in place, there is no
+                   communication) -> grouped SwiGLU over the local-expert
+                   arrays -> map composition -> fp32 combine accumulated across
+                   waves.
+
+PyTorch only provides device memory and the stream; every step is a kernel of
+the CUDA library.  Buffers are allocated once per layer and reused, so a
+forward call enqueues kernels only (it can be captured into a CUDA graph).
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+from typing import Optional
+
+import torch
+
+from . import abi
+
+
+def capacity_from_factor(cf: float, assignments: int, slots: int) -> int:
+    """ceil(cf * assignments / slots) via the library, cf read as its decimal."""
+    fr = Fraction(str(cf))
+    return abi.moe_capacity(fr.numerator, fr.denominator, assignments, slots)
+
+
+def _u8(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    def __init__(self, T: int, d: int, E: int, k: int, I: int, w_gate, w_up, w_down,
+                 capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
+                 topk_group: int = 1, route_scale: float = 1.0, sel_bias=None,
+                 shared_weights=None, device="cuda"):
+        self.T, self.d, self.E, self.k, self.I = T, d, E, k, I
+        self.capacity = capacity
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.sel_bias = sel_bias
+        self.params = abi.RouteParams(T, E, k, score_fn, n_group, topk_group, route_scale)
+        R = T * k
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_ids = torch.empty((T, k), **i32)
+        self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.x_perm = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
+        self.counts = torch.empty((E,), **i32)
+        self.offsets = torch.empty((E + 1,), **i32)
+        self.row_to_route = torch.empty((max(R, 1),), **i32)
+        self.route_to_row = torch.empty((max(R, 1),), **i32)
+        self.n_dropped = torch.zeros((1,), **i32)
+        self.perm_ws_bytes = abi.moe_permute_workspace_size(T, k, E)
+        self.perm_ws = _u8(self.perm_ws_bytes, dev)
+        self.y = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
+        self.gemm_ws_bytes = abi.moe_grouped_swiglu_workspace_size(max(R, 1), I)
+        self.gemm_ws = _u8(self.gemm_ws_bytes, dev)
+        self.out = torch.empty((T, d), dtype=torch.float32, device=dev)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.shared = shared_weights
+        if shared_weights is not None:
+            sg, su, sd = shared_weights
+            self.I_shared = sg.shape[-1]
+            self.shared_y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+            self.shared_ws_bytes = abi.moe_grouped_swiglu_workspace_size(T, self.I_shared)
+            self.shared_ws = _u8(self.shared_ws_bytes, dev)
+            self.shared_begin = torch.zeros((1,), **i32)
+            self.shared_count = torch.full((1,), T, **i32)
+
+    @property
+    def H(self) -> torch.Tensor:
+        """The bf16 SwiGLU intermediate [T*k, I] left in the GEMM workspace."""
+        R = max(self.T * self.k, 1)
+        return self.gemm_ws[: R * self.I * 2].view(torch.bfloat16).view(R, self.I)
+
+    def route(self, logits, stream=None):
+        abi.moe_route(self.params, logits, self.sel_bias, self.topk_ids, self.gates,
+                      self.dev_status, stream)
+
+    def permute(self, x, stream=None):
+        abi.moe_permute(self.T, self.d, self.E, self.k, self.capacity, self.topk_ids, x,
+                        self.x_perm, self.counts, self.offsets, self.row_to_route,
+                        self.route_to_row, self.n_dropped, self.perm_ws, self.perm_ws_bytes,
+                        self.dev_status, stream)
+
+    def experts(self, stream=None):
+        R = max(self.T * self.k, 1)
+        abi.moe_grouped_swiglu(self.E, self.d, self.I, R, self.x_perm, self.offsets, self.counts,
+                               self.w_gate, self.w_up, self.w_down, self.y, self.gemm_ws,
+                               self.gemm_ws_bytes, self.dev_status, stream)
+
+    def shared_expert(self, x, stream=None):
+        sg, su, sd = self.shared
+        abi.moe_grouped_swiglu(1, self.d, self.I_shared, self.T, x, self.shared_begin,
+                               self.shared_count, sg, su, sd, self.shared_y, self.shared_ws,
+                               self.shared_ws_bytes, self.dev_status, stream)
+
+    def combine(self, stream=None):
+        R = max(self.T * self.k, 1)
+        abi.moe_combine(self.T, self.k, self.d, self.y, R, self.route_to_row, self.gates,
+                        self.shared_y if self.shared is not None else None, 0, self.out,
+                        self.dev_status, stream)
+
+    def forward(self, logits, x, stream=None) -> torch.Tensor:
+        """Enqueue the whole layer on `stream`; returns the fp32 output buffer [T, d]."""
+        self.route(logits, stream)
+        self.permute(x, stream)
+        self.experts(stream)
+        if self.shared is not None:
+            self.shared_expert(x, stream)
+        self.combine(stream)
+        return self.out
+
+
+class PooledMoELayer:
+    """8-of-384-style static pooled waves on one GPU (one emulated sender and receiver)."""
+
+    def __init__(self, T: int, d: int, k: int, I: int, n_dest: int, local_per_dest: int,
+                 n_waves: int, pool_cap: int, local_cap: int, w_gate, w_up, w_down,
+                 wave_policy: int = abi.MOE_WAVE_STRIPE, device="cuda"):
+        self.T, self.d, self.k, self.I = T, d, k, I
+        self.E = n_dest * local_per_dest
+        self.n_dest, self.L, self.n_waves = n_dest, local_per_dest, n_waves
+        self.pool_cap, self.local_cap = pool_cap, local_cap
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.params = abi.RouteParams(T, self.E, k, abi.MOE_SCORE_SOFTMAX, 1, 1, 1.0)
+        self.pool_params = abi.PoolParams(n_dest, local_per_dest, n_waves, pool_cap, wave_policy)
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        R = T * k
+        self.topk_ids = torch.empty((T, k), **i32)
+        self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.pools = torch.empty((n_dest, pool_cap + 1, d), dtype=torch.bfloat16, device=dev)
+        self.route_to_poolrow = torch.empty((R,), **i32)
+        self.pool_fill = torch.empty((n_dest,), **i32)
+        self.sender_drops = torch.zeros((n_waves,), **i32)
+        self.pack_ws_bytes = abi.moe_pool_pack_workspace_size(self.pool_params, T, k)
+        self.pack_ws = _u8(self.pack_ws_bytes, dev)
+        self.rows = local_per_dest * local_cap
+        self.compact = torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev)
+        self.local_counts = torch.empty((local_per_dest,), **i32)
+        self.local_begin = torch.arange(local_per_dest, **i32) * local_cap
+        self.poolrow_to_row = torch.empty((n_dest * pool_cap,), **i32)
+        self.receiver_drops = torch.zeros((n_waves,), **i32)
+        self.compact_ws_bytes = abi.moe_pool_compact_workspace_size(n_dest, pool_cap,
+                                                                    local_per_dest)
+        self.compact_ws = _u8(self.compact_ws_bytes, dev)
+        self.y = torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev)
+        self.gemm_ws_bytes = abi.moe_grouped_swiglu_workspace_size(self.rows, I)
+        self.gemm_ws = _u8(self.gemm_ws_bytes, dev)
+        self.route_to_row = torch.empty((R,), **i32)
+        self.out = torch.empty((T, d), dtype=torch.float32, device=dev)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def route(self, logits, stream=None):
+        abi.moe_route(self.params, logits, None, self.topk_ids, self.gates, self.dev_status, stream)
+
+    def pack(self, x, wave, stream=None):
+        abi.moe_pool_pack(self.pool_params, self.T, self.d, self.k, wave, self.topk_ids, x,
+                          self.pools, self.route_to_poolrow, self.pool_fill,
+                          self.sender_drops[wave:wave + 1], self.pack_ws, self.pack_ws_bytes,
+                          self.dev_status, stream)
+
+    def compact_wave(self, wave, stream=None):
+        abi.moe_pool_compact(self.n_dest, self.pool_cap, self.d, self.L, self.local_cap,
+                             self.pools, self.compact, self.local_counts, self.poolrow_to_row,
+                             self.receiver_drops[wave:wave + 1], self.compact_ws,
+                             self.compact_ws_bytes, self.dev_status, stream)
+
+    def experts(self, stream=None):
+        abi.moe_grouped_swiglu(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,
+                               self.local_counts, self.w_gate, self.w_up, self.w_down, self.y,
+                               self.gemm_ws, self.gemm_ws_bytes, self.dev_status, stream)
+
+    def combine_wave(self, wave, stream=None):
+        abi.moe_compose_map(self.T * self.k, self.route_to_poolrow, self.poolrow_to_row,
+                            self.n_dest * self.pool_cap, self.route_to_row, self.dev_status,
+                            stream)
+        abi.moe_combine(self.T, self.k, self.d, self.y, self.rows, self.route_to_row, self.gates,
+                        None, 1 if wave > 0 else 0, self.out, self.dev_status, stream)
+
+    def forward(self, logits, x, stream=None) -> torch.Tensor:
+        self.route(logits, stream)
+        for w in range(self.n_waves):
+            self.pack(x, w, stream)
+            self.compact_wave(w, stream)
+            self.experts(stream)
+            self.combine_wave(w, stream)
+        return self.out

@@ -1,0 +1,252 @@
+/*
+ * moe.h -- C ABI of the GB300 MoE layer hot path (route -> permute -> grouped
+ * SwiGLU expert GEMM -> combine, plus the static-shape pooled-wave layout).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Array arguments are DEVICE pointers to memory the caller owns and keeps
+ *    alive until the work enqueued on `stream` has finished.  Nothing here
+ *    allocates, frees or retains device memory; scratch space is passed in as
+ *    a caller-owned workspace sized by the matching *_workspace_size() call.
+ *  - moe_bf16 is the raw 16-bit pattern of a bfloat16 value.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronises the host, so a whole layer can be
+ *    enqueued back to back or captured into a CUDA graph.
+ *  - Arguments are validated on the host BEFORE anything is enqueued: a
+ *    non-OK return means no work was launched.  MOE_ERR_CUDA means a launch
+ *    itself failed (the CUDA error is left for cudaGetLastError()).
+ *  - Data errors found on the device are OR-ed into *dev_status (a device
+ *    uint32 the caller zeroes; may be NULL): the offending element is skipped,
+ *    the kernel never traps.  Bits: MOE_DEV_*.
+ *  - Row-major layouts throughout; [a,b] means b is contiguous.
+ *
+ * Vocabulary follows the pages' problem statement: T tokens of width d, E
+ * experts, top-k routes per token (route id r = t*k + j, slot j = 0 is the
+ * best expert), capacity C, SwiGLU intermediate width I.
+ *
+ * Sources (page title, section):
+ *  [M6.6] "M6.6 - MoE Runtime Systems: Placement, Dispatch, Kernels, and Topology"
+ *  [M6.2] "M6.2 - Expert Parallelism and DeepSeek MoE: Load Balancing, Shared
+ *         Experts, and Fine-Grained Routing"
+ *  [POOL] "Fixed pooled-wave all-to-all for the 8-of-384 MoE"
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+typedef int32_t moe_status;
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k > E, ...   */
+  MOE_ERR_UNSUPPORTED = 2,          /* outside the shape limits stated per call  */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < the *_workspace_size() value   */
+  MOE_ERR_CUDA = 4                  /* a CUDA launch or driver call failed       */
+};
+
+enum {
+  MOE_DEV_NONFINITE_LOGIT = 1u, /* a NaN logit was met; it ranked below every number */
+  MOE_DEV_BAD_EXPERT_ID = 2u,   /* an expert id outside [0,E); the route was skipped */
+  MOE_DEV_BAD_HEADER_ID = 4u,   /* a pool header id >= n_local that is not EMPTY     */
+  MOE_DEV_BAD_ROW = 8u,         /* a map entry outside the row space; skipped        */
+  MOE_DEV_TIMEOUT = 16u         /* a bounded pipeline wait gave up; output invalid   */
+};
+
+#define MOE_POOL_EMPTY 0xFFFFu /* header element of an unused pool row */
+
+/* Library version (major*10000 + minor*100 + patch) and a status message. */
+int32_t moe_version(void);
+const char* moe_status_string(moe_status s);
+
+/* ------------------------------------------------------------------------ */
+/* Capacity                                                                 */
+/* ------------------------------------------------------------------------ */
+/* ceil(cf * assignments / slots) with cf = cf_num / cf_den, in exact integer
+ * arithmetic.  [M6.2] 0x01C: per-expert capacity C = ceil(c_f * T*k / E)
+ * (slots = E).  [POOL] 04: sender pool rows ceil(1.10 * 524288 / 64 / 3) and
+ * receiver rows ceil(1.15 * 524288 / 6 / 3) (slots = n_dest*n_waves and
+ * n_local*n_waves).  Returns -1 on a non-positive denominator or overflow.  */
+int64_t moe_capacity(int64_t cf_num, int64_t cf_den, int64_t assignments, int64_t slots);
+
+/* ------------------------------------------------------------------------ */
+/* Route                                                                    */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t T, E, k;
+  int32_t score_fn;   /* MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID_GROUP           */
+  int32_t n_group;    /* sigmoid_group: contiguous logical groups (E % n_group == 0) */
+  int32_t topk_group; /* sigmoid_group: groups kept before the expert top-k     */
+  float route_scale;  /* sigmoid_group: gates sum to route_scale                */
+} moe_route_params;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID_GROUP = 1 };
+
+/* Top-k routing of fp32 logits [T,E] -> topk_ids int32 [T,k], gates fp32 [T,k].
+ *
+ * MOE_SCORE_SOFTMAX ([M6.2] 0x06L1, Mixtral row): the k largest logits, slot 0
+ * the largest, ties to the lower expert index; gate_j = exp(z_j - z_max) /
+ * sum over the selected exp(z_i - z_max), i.e. the selected softmax
+ * probabilities renormalised to one.  sel_bias must be NULL.
+ *
+ * MOE_SCORE_SIGMOID_GROUP ([M6.2] 0x06A-0x06D, 0x06I, DeepSeek-V3): s =
+ * sigmoid(z) computed by a fixed fp32 recipe (see moe_sigmoid_det), corrected
+ * score s~ = s + sel_bias[e] (sel_bias fp32 [E] or NULL = 0); group score =
+ * sum of the two largest s~ in each of n_group contiguous groups; the
+ * topk_group best groups stay eligible; the top-k experts by s~ among them are
+ * selected; gate = route_scale * s_e / sum of s over the selected.  Ties to
+ * the lower expert / group index.
+ *
+ * Limits (MOE_ERR_UNSUPPORTED): 1 <= E <= 512, 1 <= k <= min(E, 16); for
+ * sigmoid_group also n_group <= 32, E/n_group >= 2, topk_group*E/n_group >= k.
+ * NaN logits set MOE_DEV_NONFINITE_LOGIT and rank below every number.      */
+moe_status moe_route(const moe_route_params* p, const float* logits, const float* sel_bias,
+                     int32_t* topk_ids, float* gates, uint32_t* dev_status, moe_stream_t stream);
+
+/* s[i] = sigmoid(z[i]) by the router's fixed fp32 recipe: e^x from a
+ * Cody-Waite reduction (ln2 split at 16 bits), a degree-7 Taylor polynomial
+ * and an exponent-bit scale, x clamped to [-87, 87], every operation a single
+ * correctly rounded fp32 add/sub/mul/div with no fused multiply-add.  Exposed
+ * so that its bit pattern can be checked over all inputs.                   */
+moe_status moe_sigmoid_det(int64_t n, const float* z, float* s, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Permute: admission, count, prefix, stable scatter, row gather            */
+/* ------------------------------------------------------------------------ */
+/* [M6.2] 0x03B "Count, Prefix, Permute" and [M6.6] 0x03B.  Route r = t*k + j
+ * goes to expert topk_ids[r]; it is ACCEPTED iff fewer than `capacity`
+ * earlier routes (in route id order) chose the same expert (capacity < 0:
+ * dropless).  Outputs:
+ *   counts[E]          accepted routes per expert (c_e),
+ *   offsets[E+1]       o_0 = 0, o_{e+1} = o_e + c_e (sentinel = accepted total),
+ *   row_to_route[R]    rows [0, offsets[E]) hold accepted route ids ordered by
+ *                      (expert, route id) -- the permutation pi; the rest of
+ *                      the array is left untouched,
+ *   route_to_row[R]    the inverse: row of route r, or -1 if r was dropped,
+ *   n_dropped[1]       R - accepted,
+ *   x_perm[R,d]        x_perm[row] = x[token of row_to_route[row]] (bit copy);
+ *                      rows >= offsets[E] are left untouched.
+ * x is [T,d].  Workspace: moe_permute_workspace_size(T,k,E) bytes.
+ * Limits: 1 <= E <= 512, 1 <= k <= 16, 0 <= T, T*k < 2^31, d % 8 == 0,
+ * 16-byte aligned x / x_perm.  Out-of-range ids set MOE_DEV_BAD_EXPERT_ID and
+ * the route is treated as dropped.                                          */
+size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E);
+moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                       const int32_t* topk_ids, const moe_bf16* x, moe_bf16* x_perm,
+                       int32_t* counts, int32_t* offsets, int32_t* row_to_route,
+                       int32_t* route_to_row, int32_t* n_dropped, void* ws, size_t ws_bytes,
+                       uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped SwiGLU expert GEMM over ragged row segments                      */
+/* ------------------------------------------------------------------------ */
+/* [M6.6] 0x04A and 0x04C "Variable Grouped GEMM": for every segment q with
+ * rows [b, b+c), b = seg_begin[q], c = seg_count[q] (device arrays, read on the
+ * device -- no host synchronisation):
+ *   G = X_q W_gate[q],  U = X_q W_up[q]        (bf16 in, fp32 accumulate)
+ *   H = bf16( SiLU(G) * U )                      (stored bf16, round to nearest even)
+ *   y[b:b+c] = bf16( H W_down[q] )
+ * with x, y [max_rows, d], W_gate / W_up [n_seg, d, I], W_down [n_seg, I, d].
+ * Only segment rows of y are written.  Segments may be empty and need not be
+ * contiguous, but must not overlap and must lie in [0, max_rows).  Runs on the
+ * 5th-generation tensor cores (tcgen05, accumulators in tensor memory, operands
+ * staged by TMA).
+ * Workspace: moe_grouped_swiglu_workspace_size(max_rows, I) bytes; after the
+ * stream reaches this call's end its first max_rows*I*2 bytes hold H in the
+ * same row space as x.
+ * Limits: d % 64 == 0, I % 128 == 0, 64 <= d, I <= 65536; pointers 16-byte
+ * aligned; n_seg >= 1.  Rows outside [0,max_rows) in a segment set
+ * MOE_DEV_BAD_ROW and that segment is skipped.                              */
+size_t moe_grouped_swiglu_workspace_size(int32_t max_rows, int32_t I);
+moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                              const moe_bf16* x, const int32_t* seg_begin,
+                              const int32_t* seg_count, const moe_bf16* w_gate,
+                              const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* y,
+                              void* ws, size_t ws_bytes, uint32_t* dev_status,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Combine                                                                  */
+/* ------------------------------------------------------------------------ */
+/* [M6.6] 0x03C3 and 0x0CD, [M6.2] 0x03C: weighted scatter-add back to token
+ * order, gate applied exactly once and after the expert ([M6.6] 0x0AE), fp32
+ * token accumulation:
+ *   out[t] = (accumulate ? out[t] : 0)
+ *            + sum_{j=0..k-1, route_to_row[t*k+j] >= 0} gates[t*k+j] * y[route_to_row[t*k+j]]
+ *            + (shared_y ? shared_y[t] : 0)
+ * summed in slot order in fp32.  Dropped routes contribute nothing and the
+ * remaining gates are not renormalised.  y is [y_rows, d] bf16, shared_y
+ * [T,d] bf16 or NULL, out [T,d] fp32.  Limits: d % 8 == 0, k <= 16.  Rows
+ * >= y_rows set MOE_DEV_BAD_ROW and are skipped.                            */
+moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
+                       const int32_t* route_to_row, const float* gates,
+                       const moe_bf16* shared_y, int32_t accumulate, float* out,
+                       uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Pooled-wave static-shape layout (in-memory only; no communication)       */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_dest;         /* destinations; expert e lives on e / local_per_dest */
+  int32_t local_per_dest; /* local experts per destination (local id = e % L)   */
+  int32_t n_waves;
+  int32_t pool_cap;       /* payload rows per destination pool per wave         */
+  int32_t wave_policy;    /* MOE_WAVE_STRIPE or MOE_WAVE_DESTMOD                */
+} moe_pool_params;
+
+enum { MOE_WAVE_STRIPE = 0, MOE_WAVE_DESTMOD = 1 };
+
+/* Sender side of one wave ([POOL] 02-04).  Routes to destination D, taken in
+ * route id order, get ordinal j_D.  MOE_WAVE_STRIPE: wave = j_D % n_waves,
+ * row = j_D / n_waves.  MOE_WAVE_DESTMOD: wave = D % n_waves, row = j_D.  A
+ * route of `wave` with row < pool_cap is copied to pools[D][1+row] and its
+ * local id written to header element pools[D][0][row]; one with row >=
+ * pool_cap is a sender drop.  pools is [n_dest, pool_cap+1, d]: row 0 is the
+ * header (elements < pool_cap: local id of that payload row or MOE_POOL_EMPTY;
+ * elements >= pool_cap: MOE_POOL_EMPTY), payload rows fill from 0.  Unused
+ * payload rows are not written.  Outputs: route_to_poolrow[T*k] =
+ * D*pool_cap + row, or -1 (not in this wave, or dropped); pool_fill[n_dest];
+ * sender_drops[1] = this wave's sender drops.
+ * Workspace: moe_pool_pack_workspace_size(). Limits: pool_cap <= d (the header
+ * fits one row), local_per_dest <= 65534, n_dest*local_per_dest <= 512,
+ * k <= 16, d % 8 == 0.                                                       */
+size_t moe_pool_pack_workspace_size(const moe_pool_params* p, int32_t T, int32_t k);
+moe_status moe_pool_pack(const moe_pool_params* p, int32_t T, int32_t d, int32_t k, int32_t wave,
+                         const int32_t* topk_ids, const moe_bf16* x, moe_bf16* pools,
+                         int32_t* route_to_poolrow, int32_t* pool_fill, int32_t* sender_drops,
+                         void* ws, size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
+
+/* Receiver side of one wave ([POOL] 03 "Receiver compact", 05 "Carry expert IDs
+ * in-band", 07 fixed source order).  Payload rows of n_src pools shaped
+ * [n_src, pool_cap+1, d] are visited in (source, row) order; a row whose
+ * header id is l < n_local takes the next free row of local expert l in
+ * compact [n_local, local_cap, d], or is a receiver drop once that expert holds
+ * local_cap rows.  Outputs: local_counts[n_local]; poolrow_to_row[n_src*pool_cap]
+ * = l*local_cap + slot, or -1; receiver_drops[1] = this wave's receiver drops.
+ * Header ids >= n_local other than MOE_POOL_EMPTY set MOE_DEV_BAD_HEADER_ID
+ * and the row is skipped.  Unfilled compact rows are not written.
+ * Workspace: moe_pool_compact_workspace_size().  Limits as moe_pool_pack.     */
+size_t moe_pool_compact_workspace_size(int32_t n_src, int32_t pool_cap, int32_t n_local);
+moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
+                            int32_t local_cap, const moe_bf16* pools, moe_bf16* compact,
+                            int32_t* local_counts, int32_t* poolrow_to_row,
+                            int32_t* receiver_drops, void* ws, size_t ws_bytes,
+                            uint32_t* dev_status, moe_stream_t stream);
+
+/* out[i] = a[i] < 0 ? -1 : b[a[i]] for i < n (route -> pool row -> compact row;
+ * the inverse composition of [M6.6] 0x03C3).  Entries a[i] >= b_len set
+ * MOE_DEV_BAD_ROW and give -1.                                               */
+moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b, int64_t b_len,
+                           int32_t* out, uint32_t* dev_status, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

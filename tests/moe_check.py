@@ -1,0 +1,97 @@
+"""Helpers shared by the GPU parity tests: tolerance checks and the oracle's
+pipeline on host copies of the inputs the CUDA path received."""
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+# Floating-point parity bar (derived from the stated thresholds):
+#   max_rel  = max_i |x_i - r_i| / max(|r_i|, rms(r))   <= 1e-2
+#   normwise = ||x - r||_2 / ||r||_2                     <= 2e-3
+# The rms floor keeps an element whose reference cancels to ~0 from dominating.
+MAX_REL = 1e-2
+NORMWISE = 2e-3
+# Gates are fp32 results of a few fp32 operations: relative 2e-6 plus 1e-7 absolute.
+GATE_RTOL, GATE_ATOL = 2e-6, 1e-7
+
+
+def float_errors(got, ref):
+    got = np.asarray(got, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    if ref.size == 0:
+        return 0.0, 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    denom = np.maximum(np.abs(ref), rms if rms > 0 else 1.0)
+    max_rel = float(np.max(np.abs(got - ref) / denom))
+    nref = float(np.linalg.norm(ref))
+    normwise = float(np.linalg.norm(got - ref) / (nref if nref > 0 else 1.0))
+    return max_rel, normwise
+
+
+def assert_float_parity(got, ref, what=""):
+    mr, nw = float_errors(got, ref)
+    assert np.all(np.isfinite(np.asarray(got, dtype=np.float64))), f"{what}: non-finite output"
+    assert mr <= MAX_REL and nw <= NORMWISE, f"{what}: max_rel={mr:.3e} normwise={nw:.3e}"
+    return mr, nw
+
+
+def assert_gates(got, ref):
+    np.testing.assert_allclose(np.asarray(got, np.float64), np.asarray(ref, np.float64),
+                               rtol=GATE_RTOL, atol=GATE_ATOL)
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def bits(t):
+    return workloads.bf16_bits(t)
+
+
+def oracle_route(w, logits, sel_bias):
+    z = host(logits)
+    if w.score_fn == "softmax":
+        return oracle.route_softmax(z, w.k)
+    b = None if sel_bias is None else host(sel_bias)
+    return oracle.route_sigmoid_group(z, b, w.k, w.n_group, w.topk_group, w.route_scale)
+
+
+def oracle_capacity(w):
+    if w.capacity_factor is None:
+        return -1
+    return oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
+
+
+def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, wg_b, wu_b, wd_b, shared=None):
+    """Oracle combined output rows for `tokens` (float64 [n, d]) and their y rows by row.
+
+    Each sampled route's expert output is computed from the token row and that
+    expert's weights (converted once per expert)."""
+    k = w.k
+    need = {}
+    for t in tokens:
+        for j in range(k):
+            r = t * k + j
+            if perm["route_to_row"][r] >= 0:
+                need.setdefault(int(ids[t, j]), []).append(r)
+    y_of_row = {}
+    for e, routes in need.items():
+        xr = oracle.bf16_to_f64(x_bits[np.array(routes) // k])
+        _, y = oracle.swiglu(xr, oracle.bf16_to_f64(wg_b[e]), oracle.bf16_to_f64(wu_b[e]),
+                             oracle.bf16_to_f64(wd_b[e]))
+        for i, r in enumerate(routes):
+            y_of_row[int(perm["route_to_row"][r])] = y[i]
+    sh = None
+    if shared is not None:
+        sg, su, sd = shared
+        _, sh = oracle.swiglu(oracle.bf16_to_f64(x_bits[np.array(tokens)]),
+                              oracle.bf16_to_f64(sg[0]), oracle.bf16_to_f64(su[0]),
+                              oracle.bf16_to_f64(sd[0]))
+    outs = []
+    for i, t in enumerate(tokens):
+        rows = perm["route_to_row"][t * k:(t + 1) * k]
+        acc = oracle.combine_token(lambda r: y_of_row[r], rows, gates[t],
+                                   None if sh is None else sh[i])
+        outs.append(np.zeros(x_bits.shape[1]) if acc is None else acc)
+    return np.stack(outs), y_of_row

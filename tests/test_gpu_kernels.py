@@ -1,0 +1,414 @@
+"""Per-kernel parity of the CUDA library against the CPU oracle, through the C
+ABI, at sizes the oracle finishes in seconds: several tiles, ragged tails and
+the degenerate cases (empty experts, capacity 0 and 1, T = 1, k = E, ties).
+Integer outputs must match bit for bit; floats within the stated tolerances.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from moe_check import assert_float_parity, assert_gates, bits, host
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from grouped_expert_gemm_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def G():
+    import grouped_expert_gemm_gb300 as g
+    return g
+
+
+def status0():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+# ----------------------------------------------------------------------------
+# Router
+# ----------------------------------------------------------------------------
+
+def test_sigmoid_det_is_bitwise_identical_to_the_oracle():
+    g = G()
+    # every 13th fp32 bit pattern with |z| in [2^-24, 128), both signs, plus specials
+    pos = np.arange(0x33800000, 0x43000000, 13, dtype=np.uint32)
+    z = np.concatenate([pos.view(np.float32), -pos.view(np.float32),
+                        np.array([0.0, -0.0, 87.0, -87.0, 88.0, -88.0, 1e30, -1e30, 3.4e38,
+                                  -3.4e38], np.float32)])
+    zd = torch.from_numpy(z).to(DEV)
+    sd = torch.empty_like(zd)
+    g.moe_sigmoid_det(z.size, zd, sd)
+    torch.cuda.synchronize()
+    got = host(sd).view(np.uint32)
+    ref = oracle.sigmoid_det_f32(z).view(np.uint32)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first z={z[bad[:5]]}"
+
+
+def _route(w, logits, sel_bias):
+    g = G()
+    score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
+    p = g.RouteParams(w.T, w.E, w.k, score, w.n_group, w.topk_group, w.route_scale)
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device=DEV)
+    st = status0()
+    g.moe_route(p, logits, sel_bias, ids, gates, st)
+    torch.cuda.synchronize()
+    return host(ids), host(gates), int(host(st)[0])
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (257, 8, 2), (300, 128, 8), (77, 384, 8),
+                                   (64, 512, 16), (33, 5, 5), (40, 33, 3), (19, 1, 1)])
+def test_route_softmax_parity(T, E, k):
+    w = workloads.scaled(workloads.tiny(), T=T, E=E, k=k)
+    logits, _ = workloads.make_router_inputs(w, DEV)
+    ids, gates, st = _route(w, logits, None)
+    rids, rgates = oracle.route_softmax(host(logits), k)
+    assert st == 0
+    assert np.array_equal(ids, rids)
+    assert_gates(gates, rgates)
+
+
+def test_route_softmax_ties_and_signed_zeros():
+    rng = np.random.default_rng(0)
+    z = rng.choice(np.array([-1.0, -0.0, 0.0, 0.5, 2.0], np.float32), size=(512, 40))
+    w = workloads.scaled(workloads.tiny(), T=512, E=40, k=6)
+    ids, gates, _ = _route(w, torch.from_numpy(z).to(DEV), None)
+    rids, rgates = oracle.route_softmax(z, 6)
+    assert np.array_equal(ids, rids)
+    assert_gates(gates, rgates)
+
+
+def test_route_nan_logit_is_reported_and_ranked_last():
+    z = np.zeros((4, 8), np.float32)
+    z[:, 3] = 1.0
+    z[1, 5] = np.nan
+    w = workloads.scaled(workloads.tiny(), T=4, E=8, k=2)
+    ids, _, st = _route(w, torch.from_numpy(z).to(DEV), None)
+    g = G()
+    assert st & g.MOE_DEV_NONFINITE_LOGIT
+    assert ids[1].tolist() == [3, 0]
+
+
+@pytest.mark.parametrize("T,E,n_group,topk_group,k", [(1, 256, 8, 4, 8), (513, 256, 8, 4, 8),
+                                                      (100, 64, 4, 2, 6), (50, 12, 4, 2, 4)])
+def test_route_sigmoid_group_parity(T, E, n_group, topk_group, k):
+    w = workloads.scaled(workloads.v3(), T=T, E=E, k=k, n_group=n_group, topk_group=topk_group)
+    logits, sel_bias = workloads.make_router_inputs(w, DEV)
+    ids, gates, st = _route(w, logits, sel_bias)
+    rids, rgates = oracle.route_sigmoid_group(host(logits), host(sel_bias), k, n_group,
+                                              topk_group, 2.5)
+    assert st == 0
+    assert np.array_equal(ids, rids)
+    assert_gates(gates, rgates)
+
+
+def test_route_sigmoid_group_page_fixture():
+    import json, os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "m62_v3_group_gate.json")) as f:
+        fx = json.load(f)
+    p = np.asarray(fx["affinity"], np.float64)
+    z = np.float32(np.log(p / (1 - p)))[None, :]
+    w = workloads.scaled(workloads.v3(), T=1, E=12, k=4, n_group=4, topk_group=2)
+    ids, gates, _ = _route(w, torch.from_numpy(z).to(DEV),
+                           torch.tensor(fx["bias"], dtype=torch.float32, device=DEV))
+    assert ids[0].tolist() == fx["ids_with_bias"]
+    np.testing.assert_allclose(gates[0], fx["gates_with_bias"], atol=1.5e-6)
+
+
+# ----------------------------------------------------------------------------
+# Permute
+# ----------------------------------------------------------------------------
+
+def _permute(T, d, E, k, cap, ids_np, x):
+    g = G()
+    R = T * k
+    ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(DEV)
+    xp = torch.full((max(R, 1), d), -1, dtype=torch.bfloat16, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    r2r = torch.full((max(R, 1),), -7, dtype=torch.int32, device=DEV)
+    inv = torch.full((max(R, 1),), -7, dtype=torch.int32, device=DEV)
+    nd = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = g.moe_permute_workspace_size(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    g.moe_permute(T, d, E, k, cap, ids, x, xp, counts, offsets, r2r, inv, nd, ws, wsb, st)
+    torch.cuda.synchronize()
+    return dict(x_perm=bits(xp), counts=host(counts), offsets=host(offsets),
+                row_to_route=host(r2r), route_to_row=host(inv), n_dropped=int(host(nd)[0]),
+                status=int(host(st)[0]))
+
+
+def _check_permute(T, d, E, k, cap, ids_np, seed=0):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn((max(T, 1), d), generator=gen, device=DEV).to(torch.bfloat16)[:T]
+    got = _permute(T, d, E, k, cap, ids_np, x)
+    ref = oracle.permute(ids_np, E, cap)
+    acc = int(ref["offsets"][-1])
+    assert got["status"] == 0
+    assert np.array_equal(got["counts"], ref["counts"])
+    assert np.array_equal(got["offsets"], ref["offsets"])
+    assert np.array_equal(got["row_to_route"][:acc], ref["row_to_route"])
+    assert np.array_equal(got["route_to_row"][:T * k], ref["route_to_row"])
+    assert got["n_dropped"] == ref["n_dropped"]
+    xb = bits(x)
+    assert np.array_equal(got["x_perm"][:acc], oracle.gather_rows(xb, ref["row_to_route"], k))
+
+
+@pytest.mark.parametrize("T,d,E,k,cap", [(256, 64, 8, 2, 80), (1, 64, 8, 2, -1), (3, 64, 8, 8, -1),
+                                         (1000, 128, 128, 8, -1), (997, 64, 256, 8, 31),
+                                         (4099, 64, 8, 2, 0), (500, 64, 16, 4, 1),
+                                         (129, 192, 384, 8, -1), (2000, 64, 512, 16, 40),
+                                         (64, 64, 1, 1, -1)])
+def test_permute_parity(T, d, E, k, cap):
+    rng = np.random.default_rng(T + E)
+    # skewed expert choice so that some experts are empty and some overflow
+    p = rng.dirichlet(np.ones(E) * 0.3)
+    ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    _check_permute(T, d, E, k, cap, ids)
+
+
+def test_permute_empty_input():
+    got = _permute(0, 64, 8, 2, -1, np.zeros((0, 2), np.int32),
+                   torch.empty((0, 64), dtype=torch.bfloat16, device=DEV))
+    assert got["counts"].tolist() == [0] * 8
+    assert got["offsets"].tolist() == [0] * 9
+    assert got["n_dropped"] == 0
+
+
+def test_permute_bad_expert_id_is_reported_and_dropped():
+    ids = np.array([[0, 1], [9, 2], [1, -3]], np.int32)
+    x = torch.zeros((3, 64), dtype=torch.bfloat16, device=DEV)
+    got = _permute(3, 64, 4, 2, -1, ids, x)
+    g = G()
+    assert got["status"] & g.MOE_DEV_BAD_EXPERT_ID
+    assert got["route_to_row"][2] == -1 and got["route_to_row"][5] == -1
+    assert got["counts"].tolist() == [1, 2, 1, 0]
+    assert got["n_dropped"] == 2
+
+
+# ----------------------------------------------------------------------------
+# Combine
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,k,d,rows,shared,accumulate", [(256, 2, 64, 400, False, False),
+                                                          (33, 8, 2048, 200, True, False),
+                                                          (100, 16, 1032, 999, False, True),
+                                                          (1, 1, 8, 1, True, True)])
+def test_combine_parity(T, k, d, rows, shared, accumulate):
+    g = G()
+    rng = np.random.default_rng(T * k)
+    gen = torch.Generator(device=DEV).manual_seed(1)
+    y = torch.randn((rows, d), generator=gen, device=DEV).to(torch.bfloat16)
+    r2r = rng.integers(-1, rows, size=T * k).astype(np.int32)
+    gates = rng.uniform(0, 1, size=T * k).astype(np.float32)
+    sh = torch.randn((T, d), generator=gen, device=DEV).to(torch.bfloat16) if shared else None
+    init = torch.randn((T, d), generator=gen, device=DEV, dtype=torch.float32)
+    out = init.clone()
+    st = status0()
+    g.moe_combine(T, k, d, y, rows, torch.from_numpy(r2r).to(DEV), torch.from_numpy(gates).to(DEV),
+                  sh, accumulate, out, st)
+    torch.cuda.synchronize()
+    ref = oracle.combine(oracle.bf16_to_f64(bits(y)), r2r, gates, T, k,
+                         None if sh is None else oracle.bf16_to_f64(bits(sh)),
+                         host(init) if accumulate else None)
+    assert int(host(st)[0]) == 0
+    assert_float_parity(host(out), ref, "combine")
+    # fp32 accumulation of at most k+2 terms: far inside the bar
+    np.testing.assert_allclose(host(out), ref, rtol=1e-5, atol=1e-5)
+
+
+def test_combine_bad_row_is_reported_and_skipped():
+    g = G()
+    y = torch.ones((4, 8), dtype=torch.bfloat16, device=DEV)
+    r2r = torch.tensor([0, 7], dtype=torch.int32, device=DEV)
+    gates = torch.tensor([0.5, 0.5], dtype=torch.float32, device=DEV)
+    out = torch.empty((1, 8), dtype=torch.float32, device=DEV)
+    st = status0()
+    g.moe_combine(1, 2, 8, y, 4, r2r, gates, None, 0, out, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) & g.MOE_DEV_BAD_ROW
+    assert np.allclose(host(out), 0.5)
+
+
+# ----------------------------------------------------------------------------
+# Grouped SwiGLU GEMM
+# ----------------------------------------------------------------------------
+
+def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None):
+    g = G()
+    counts = np.asarray(counts, np.int32)
+    if begins is None:
+        begins = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int32)
+    begins = np.asarray(begins, np.int32)
+    if max_rows is None:
+        max_rows = int((begins + counts).max()) if len(counts) else 1
+    w = workloads.scaled(workloads.tiny(), d=d, I=I, E=n_seg, seed=seed)
+    gen = torch.Generator(device=DEV).manual_seed(seed + 7)
+    x = torch.randn((max_rows, d), generator=gen, device=DEV).to(torch.bfloat16)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV, n_experts=n_seg)
+    y = torch.full((max_rows, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    wsb = g.moe_grouped_swiglu_workspace_size(max_rows, I)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    g.moe_grouped_swiglu(n_seg, d, I, max_rows, x, torch.from_numpy(begins).to(DEV),
+                         torch.from_numpy(counts).to(DEV), wg, wu, wd, y, ws, wsb, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    H = ws[: max_rows * I * 2].view(torch.bfloat16).view(max_rows, I)
+    yr, hr = oracle.grouped_swiglu_rows(bits(x), begins, counts, bits(wg), bits(wu), bits(wd))
+    rows = sorted(yr)
+    yb, hb = bits(y), bits(H)
+    if rows:
+        assert_float_parity(oracle.bf16_to_f64(hb[rows]),
+                            oracle.bf16_to_f64(np.stack([hr[r] for r in rows])), "H")
+        assert_float_parity(oracle.bf16_to_f64(yb[rows]),
+                            oracle.bf16_to_f64(np.stack([yr[r] for r in rows])), "y")
+    # rows outside every segment are never written
+    untouched = np.setdiff1d(np.arange(max_rows), rows)
+    assert np.all(yb[untouched] == bits(torch.tensor([7.0], dtype=torch.bfloat16))[0])
+
+
+@pytest.mark.parametrize("n_seg,d,I,counts", [
+    (1, 64, 128, [128]),
+    (1, 64, 128, [1]),
+    (4, 64, 128, [130, 0, 7, 300]),
+    (3, 128, 256, [255, 256, 257]),
+    (5, 256, 384, [1, 129, 0, 64, 200]),
+    (8, 512, 128, [33, 97, 128, 5, 0, 0, 140, 61]),
+    (2, 192, 192, [150, 170]),       # I not a multiple of 128, d not of 256
+    (6, 1024, 512, [400, 10, 300, 0, 129, 77]),
+])
+def test_grouped_swiglu_parity(n_seg, d, I, counts):
+    _gemm_case(n_seg, d, I, counts)
+
+
+def test_grouped_swiglu_gapped_segments():
+    # segments with gaps between them (the pooled layout's fixed-stride arrays)
+    _gemm_case(3, 128, 128, [100, 0, 250], begins=[0, 300, 600], max_rows=900)
+
+
+def test_grouped_swiglu_many_small_segments():
+    rng = np.random.default_rng(3)
+    counts = rng.integers(0, 40, size=256)
+    _gemm_case(256, 64, 128, counts)
+
+
+def test_grouped_swiglu_bad_segment_is_reported():
+    g = G()
+    d, I = 64, 128
+    x = torch.zeros((16, d), dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros((1, d, I), dtype=torch.bfloat16, device=DEV)
+    wd = torch.zeros((1, I, d), dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros((16, d), dtype=torch.bfloat16, device=DEV)
+    wsb = g.moe_grouped_swiglu_workspace_size(16, I)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    g.moe_grouped_swiglu(1, d, I, 16, x, torch.tensor([10], dtype=torch.int32, device=DEV),
+                         torch.tensor([20], dtype=torch.int32, device=DEV), w, w, wd, y, ws, wsb, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) & g.MOE_DEV_BAD_ROW
+
+
+# ----------------------------------------------------------------------------
+# Pooled layout
+# ----------------------------------------------------------------------------
+
+def _pool_case(T, d, k, n_dest, L, n_waves, pool_cap, local_cap, policy, seed=0):
+    g = G()
+    rng = np.random.default_rng(seed)
+    E = n_dest * L
+    p = rng.dirichlet(np.ones(E) * 0.5)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn((T, d), generator=gen, device=DEV).to(torch.bfloat16)
+    xb = bits(x)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    pp = g.PoolParams(n_dest, L, n_waves, pool_cap, policy)
+    pols = {g.MOE_WAVE_STRIPE: "stripe", g.MOE_WAVE_DESTMOD: "destmod"}
+    pools = torch.zeros((n_dest, pool_cap + 1, d), dtype=torch.bfloat16, device=DEV)
+    r2p = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    fill = torch.empty(n_dest, dtype=torch.int32, device=DEV)
+    sdrop = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pwsb = g.moe_pool_pack_workspace_size(pp, T, k)
+    pws = torch.empty(pwsb, dtype=torch.uint8, device=DEV)
+    compact = torch.zeros((L * local_cap, d), dtype=torch.bfloat16, device=DEV)
+    lcounts = torch.empty(L, dtype=torch.int32, device=DEV)
+    p2r = torch.empty(n_dest * pool_cap, dtype=torch.int32, device=DEV)
+    rdrop = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cwsb = g.moe_pool_compact_workspace_size(n_dest, pool_cap, L)
+    cws = torch.empty(cwsb, dtype=torch.uint8, device=DEV)
+    comp = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    total = 0
+    for wave in range(n_waves):
+        st = status0()
+        g.moe_pool_pack(pp, T, d, k, wave, ids, x, pools, r2p, fill, sdrop, pws, pwsb, st)
+        g.moe_pool_compact(n_dest, pool_cap, d, L, local_cap, pools, compact, lcounts, p2r, rdrop,
+                           cws, cwsb, st)
+        g.moe_compose_map(T * k, r2p, p2r, n_dest * pool_cap, comp, st)
+        torch.cuda.synchronize()
+        assert int(host(st)[0]) == 0
+        rp = oracle.pool_pack(ids_np, xb, n_dest, L, n_waves, pool_cap, wave, pols[policy])
+        pb = bits(pools)
+        assert np.array_equal(pb[:, 0, :], rp["pools"][:, 0, :])  # whole header rows
+        assert np.array_equal(host(r2p), rp["route_to_poolrow"])
+        assert np.array_equal(host(fill), rp["fill"])
+        assert int(host(sdrop)[0]) == rp["sender_drops"]
+        for D in range(n_dest):
+            f = rp["fill"][D]
+            assert np.array_equal(pb[D, 1:1 + f], rp["pools"][D, 1:1 + f])
+        rc = oracle.pool_compact(rp["pools"], pool_cap, L, local_cap)
+        assert np.array_equal(host(p2r), rc["poolrow_to_row"])
+        assert np.array_equal(host(lcounts), rc["local_counts"])
+        assert int(host(rdrop)[0]) == rc["receiver_drops"]
+        cb = bits(compact).reshape(L, local_cap, d)
+        for l in range(L):
+            c = rc["local_counts"][l]
+            assert np.array_equal(cb[l, :c], rc["compact"][l, :c])
+        rcomp = oracle.compose_map(rp["route_to_poolrow"], rc["poolrow_to_row"])
+        assert np.array_equal(host(comp), rcomp)
+        total += rp["sender_drops"] + rc["receiver_drops"] + int((rcomp >= 0).sum())
+    assert total == T * k
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+@pytest.mark.parametrize("T,d,k,n_dest,L,n_waves,pool_cap,local_cap", [
+    (300, 64, 4, 4, 3, 3, 40, 50),
+    (1000, 128, 8, 16, 6, 3, 64, 150),
+    (77, 64, 2, 2, 2, 1, 64, 1000),     # nothing dropped
+    (500, 64, 8, 8, 4, 2, 5, 7),        # heavy drops on both sides
+])
+def test_pool_pack_compact_parity(policy, T, d, k, n_dest, L, n_waves, pool_cap, local_cap):
+    _pool_case(T, d, k, n_dest, L, n_waves, pool_cap, local_cap, policy)
+
+
+def test_pool_compact_bad_header_is_reported():
+    g = G()
+    d, cap = 16, 4
+    pools = torch.full((2, cap + 1, d), 0, dtype=torch.int16, device=DEV)
+    hdr = np.full((2, d), 0xFFFF, np.uint16)
+    hdr[0, :3] = [0, 9, 1]
+    pools[:, 0, :] = torch.from_numpy(hdr.view(np.int16)).to(DEV)
+    pools = pools.view(torch.bfloat16)
+    compact = torch.zeros((2 * 8, d), dtype=torch.bfloat16, device=DEV)
+    lc = torch.empty(2, dtype=torch.int32, device=DEV)
+    p2r = torch.empty(2 * cap, dtype=torch.int32, device=DEV)
+    rd = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = g.moe_pool_compact_workspace_size(2, cap, 2)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    g.moe_pool_compact(2, cap, d, 2, 8, pools, compact, lc, p2r, rd, ws, wsb, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) & g.MOE_DEV_BAD_HEADER_ID
+    assert host(p2r).tolist() == [0, -1, 8, -1, -1, -1, -1, -1]
