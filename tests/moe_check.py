@@ -63,11 +63,11 @@ def oracle_capacity(w):
     return oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
 
 
-def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, wg_b, wu_b, wd_b, shared=None):
+def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, weights_of, shared=None):
     """Oracle combined output rows for `tokens` (float64 [n, d]) and their y rows by row.
 
     Each sampled route's expert output is computed from the token row and that
-    expert's weights (converted once per expert)."""
+    expert's weights; ``weights_of(e)`` returns expert e's (Wg, Wu, Wd) bf16 bits."""
     k = w.k
     need = {}
     for t in tokens:
@@ -78,8 +78,9 @@ def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, wg_b, wu_b, wd_b, 
     y_of_row = {}
     for e, routes in need.items():
         xr = oracle.bf16_to_f64(x_bits[np.array(routes) // k])
-        _, y = oracle.swiglu(xr, oracle.bf16_to_f64(wg_b[e]), oracle.bf16_to_f64(wu_b[e]),
-                             oracle.bf16_to_f64(wd_b[e]))
+        wg_e, wu_e, wd_e = weights_of(e)
+        _, y = oracle.swiglu(xr, oracle.bf16_to_f64(wg_e), oracle.bf16_to_f64(wu_e),
+                             oracle.bf16_to_f64(wd_e))
         for i, r in enumerate(routes):
             y_of_row[int(perm["route_to_row"][r])] = y[i]
     sh = None
@@ -95,3 +96,14 @@ def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, wg_b, wu_b, wd_b, 
                                    None if sh is None else sh[i])
         outs.append(np.zeros(x_bits.shape[1]) if acc is None else acc)
     return np.stack(outs), y_of_row
+
+
+def weights_fetcher(wg, wu, wd):
+    """Host bf16 bits of one expert's weights, fetched on demand (weights stay on the GPU)."""
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = (bits(wg[e]), bits(wu[e]), bits(wd[e]))
+        return cache[e]
+    return get

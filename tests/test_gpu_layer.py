@@ -1,0 +1,204 @@
+"""End-to-end parity of the MoE layer (the launch configuration the benchmark
+times) against the CPU oracle.
+
+Small workloads are checked in full.  The full-size workloads are run whole on
+the GPU; routing, admission, permutation, pool headers and maps are compared in
+full (bit-exact), payload copies and float outputs on a seeded sample of tokens
+and rows that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from moe_check import (assert_float_parity, assert_gates, bits, host, oracle_capacity,
+                       oracle_route, oracle_token_outputs, weights_fetcher)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from grouped_expert_gemm_gb300 import build
+    build.build()
+
+
+def make_layer(w, wg, wu, wd, sel_bias=None, shared=None):
+    import grouped_expert_gemm_gb300 as g
+    cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
+    score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
+    return g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
+                      n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
+                      sel_bias=sel_bias, shared_weights=shared, device=DEV)
+
+
+def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None):
+    logits, sel_bias = workloads.make_router_inputs(w, DEV)
+    x = workloads.make_activations(w, DEV)
+    wg, wu, wd = weights if weights is not None else workloads.make_expert_weights(w, DEV)
+    shared = workloads.make_shared_weights(w, DEV)
+    layer = make_layer(w, wg, wu, wd, sel_bias, shared)
+    out = layer.forward(logits, x)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+
+    # routing and admission: bit-exact in full
+    ids, gates = oracle_route(w, logits, sel_bias)
+    assert np.array_equal(host(layer.topk_ids), ids)
+    assert_gates(host(layer.gates), gates)
+    cap = oracle_capacity(w)
+    perm = oracle.permute(ids, w.E, cap)
+    assert np.array_equal(host(layer.counts), perm["counts"])
+    assert np.array_equal(host(layer.offsets), perm["offsets"])
+    acc = int(perm["offsets"][-1])
+    assert np.array_equal(host(layer.row_to_route)[:acc], perm["row_to_route"])
+    assert np.array_equal(host(layer.route_to_row)[: w.R], perm["route_to_row"])
+    assert int(layer.n_dropped.item()) == perm["n_dropped"]
+
+    xb = bits(x)
+    rng = np.random.default_rng(seed)
+    rows = np.arange(acc) if acc <= sample_rows else np.sort(rng.choice(acc, sample_rows, False))
+    # permuted payload rows: bit copies
+    assert np.array_equal(bits(layer.x_perm[torch.from_numpy(rows).to(DEV)]),
+                          xb[perm["row_to_route"][rows] // w.k])
+
+    tokens = np.arange(w.T) if sample_tokens is None else np.sort(
+        rng.choice(w.T, min(sample_tokens, w.T), replace=False))
+    shared_bits = None if shared is None else tuple(bits(s) for s in shared)
+    ref_out, y_of_row = oracle_token_outputs(w, tokens, xb, ids, gates, perm,
+                                             weights_fetcher(wg, wu, wd), shared_bits)
+    if y_of_row:
+        yrows = np.array(sorted(y_of_row))
+        got_y = oracle.bf16_to_f64(bits(layer.y[torch.from_numpy(yrows).to(DEV)]))
+        assert_float_parity(got_y, np.stack([y_of_row[r] for r in yrows]), "expert rows y")
+    got = host(out)[tokens]
+    assert_float_parity(got, ref_out, "combined output")
+    return layer, perm
+
+
+def test_tiny_full():
+    w = workloads.tiny()
+    layer, perm = run_and_check(w)
+    assert oracle.capacity(1.25, 256, 2, 8) == layer.capacity == 80
+
+
+@pytest.fixture(scope="module")
+def decode_weights():
+    return workloads.make_expert_weights(workloads.decode(128), DEV)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128])
+def test_decode_sweep_full(T, decode_weights):
+    run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096)
+
+
+@pytest.mark.slow
+def test_prefill_full_size_sampled():
+    run_and_check(workloads.prefill(), sample_tokens=12, sample_rows=256, seed=2)
+
+
+@pytest.mark.slow
+def test_v3_full_size_sampled():
+    layer, perm = run_and_check(workloads.v3(), sample_tokens=6, sample_rows=256, seed=3)
+    assert layer.capacity == 256
+    # capacity 1.0 with a skewed selection bias must actually drop routes
+    assert perm["n_dropped"] > 0
+
+
+def test_v3_small_full():
+    w = workloads.scaled(workloads.v3(), T=64, d=256, I=256, shared_I=128)
+    run_and_check(w, sample_rows=10**6)
+
+
+# ----------------------------------------------------------------------------
+# pooled waves
+# ----------------------------------------------------------------------------
+
+def pooled_check(w, policy, sample_tokens, sample_rows, seed):
+    import grouped_expert_gemm_gb300 as g
+    logits, _ = workloads.make_router_inputs(w, DEV)
+    x = workloads.make_activations(w, DEV)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    pool_cap = g.capacity_from_factor(w.sender_cf, w.R, w.n_dest * w.n_waves)
+    local_cap = g.capacity_from_factor(w.receiver_cf, w.R, w.local_per_dest * w.n_waves)
+    assert pool_cap == oracle.pool_capacity(w.sender_cf, w.T, w.k, w.n_dest, w.n_waves)
+    assert local_cap == oracle.local_capacity(w.receiver_cf, w.T, w.k, w.local_per_dest, w.n_waves)
+    layer = g.PooledMoELayer(w.T, w.d, w.k, w.I, w.n_dest, w.local_per_dest, w.n_waves, pool_cap,
+                             local_cap, wg, wu, wd, wave_policy=policy, device=DEV)
+    pol = "stripe" if policy == g.MOE_WAVE_STRIPE else "destmod"
+    layer.route(logits)
+    torch.cuda.synchronize()
+    ids, gates = oracle.route_softmax(host(logits), w.k)
+    assert np.array_equal(host(layer.topk_ids), ids)
+    assert_gates(host(layer.gates), gates)
+    xb = bits(x)
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(w.T, min(sample_tokens, w.T), replace=False))
+    fetch = weights_fetcher(wg, wu, wd)
+    ref_out = np.zeros((len(tokens), w.d))
+    totals = dict(sender=0, receiver=0, accepted=0)
+    for wave in range(w.n_waves):
+        layer.pack(x, wave)
+        layer.compact_wave(wave)
+        layer.experts()
+        layer.combine_wave(wave)
+        torch.cuda.synchronize()
+        assert int(layer.dev_status.item()) == 0
+        rp = oracle.pool_pack(ids, xb, w.n_dest, w.local_per_dest, w.n_waves, pool_cap, wave, pol)
+        hdr = bits(layer.pools[:, 0, :])
+        assert np.array_equal(hdr, rp["pools"][:, 0, :])
+        assert np.array_equal(host(layer.route_to_poolrow), rp["route_to_poolrow"])
+        assert np.array_equal(host(layer.pool_fill), rp["fill"])
+        assert int(host(layer.sender_drops)[wave]) == rp["sender_drops"]
+        rc = oracle.pool_compact(rp["pools"], pool_cap, w.local_per_dest, local_cap)
+        assert np.array_equal(host(layer.poolrow_to_row), rc["poolrow_to_row"])
+        assert np.array_equal(host(layer.local_counts), rc["local_counts"])
+        assert int(host(layer.receiver_drops)[wave]) == rc["receiver_drops"]
+        comp = oracle.compose_map(rp["route_to_poolrow"], rc["poolrow_to_row"])
+        assert np.array_equal(host(layer.route_to_row), comp)
+        # payload rows: sampled bit copies in pools and in the compact arrays
+        placed = np.nonzero(rp["route_to_poolrow"] >= 0)[0]
+        if placed.size:
+            pick = rng.choice(placed, min(sample_rows, placed.size), replace=False)
+            pr = rp["route_to_poolrow"][pick]
+            got_pool = bits(layer.pools.view(-1, w.d)[torch.from_numpy(
+                (pr // pool_cap) * (pool_cap + 1) + 1 + pr % pool_cap).to(DEV)])
+            assert np.array_equal(got_pool, xb[pick // w.k])
+            cr = comp[pick]
+            keep = cr >= 0
+            got_c = bits(layer.compact[torch.from_numpy(cr[keep]).to(DEV)])
+            assert np.array_equal(got_c, xb[pick[keep] // w.k])
+        # sampled expert rows and this wave's contribution to the sampled tokens
+        for i, t in enumerate(tokens):
+            for j in range(w.k):
+                row = comp[t * w.k + j]
+                if row < 0:
+                    continue
+                l = row // local_cap
+                wgl, wul, wdl = fetch(l)
+                _, y = oracle.swiglu(oracle.bf16_to_f64(xb[t:t + 1]), oracle.bf16_to_f64(wgl),
+                                     oracle.bf16_to_f64(wul), oracle.bf16_to_f64(wdl))
+                got_y = oracle.bf16_to_f64(bits(layer.y[row:row + 1]))
+                assert_float_parity(got_y, y, "pooled expert row")
+                ref_out[i] += gates[t, j] * y[0]
+        totals["sender"] += rp["sender_drops"]
+        totals["receiver"] += rc["receiver_drops"]
+        totals["accepted"] += int((comp >= 0).sum())
+    assert totals["sender"] + totals["receiver"] + totals["accepted"] == w.R
+    assert_float_parity(host(layer.out)[tokens], ref_out, "pooled combined output")
+    return totals
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+def test_pooled_small(policy):
+    w = workloads.scaled(workloads.pooled(), T=2048, d=256, I=256, n_dest=8)
+    pooled_check(w, policy, sample_tokens=64, sample_rows=512, seed=4)
+
+
+@pytest.mark.slow
+def test_pooled_full_size_sampled():
+    totals = pooled_check(workloads.pooled(), 0, sample_tokens=8, sample_rows=256, seed=4)
+    rates = oracle.drop_rates(65536 * 8, totals["sender"], totals["receiver"])
+    assert 0 < rates["total"] < 0.5
