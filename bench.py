@@ -1,0 +1,565 @@
+#!/usr/bin/env python
+"""MoE layer hot-path benchmark: tokens/s of route + permute + grouped SwiGLU GEMM
++ combine on one GB300 (N GPUs = N independent replicas), with the dominant
+kernel's roofline fraction, an end-to-end number through host buffers, the SM
+clocks seen during the timed region, and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|tiny|prefill|v3|pooled]
+                  [--tokens T] [--impl ours|reference]
+
+One JSON line on stdout (rank 0).  ``--impl reference`` times the CPU oracle on
+the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE layer tokens/s (route+permute+grouped GEMM+combine); % HBM / TC roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode",
+                    choices=["decode", "tiny", "prefill", "v3", "pooled"])
+    ap.add_argument("--tokens", type=int, default=128, help="decode batch (1, 8, 32, 128)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline sample")
+    return ap.parse_args()
+
+
+def workload_for(args) -> workloads.Workload:
+    return {"decode": lambda: workloads.decode(args.tokens), "tiny": workloads.tiny,
+            "prefill": workloads.prefill, "v3": workloads.v3,
+            "pooled": workloads.pooled}[args.config]()
+
+
+DEFAULT_STEPS = {"decode": 200, "tiny": 200, "prefill": 20, "v3": 10, "pooled": 5}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and a max over ranks)
+# ----------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64,
+                         device=f"cuda:{self.local}" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# SM clock sampling during the timed region (NVML read-only queries)
+# ----------------------------------------------------------------------------
+
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class ClockSampler:
+    """Polls the SM clock and the clock-event reasons of this process's GPU every ~2 ms."""
+
+    def __init__(self, device_index: int):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.dev = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+                if self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev)) != 0:
+                    return
+            m = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        get_r = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if get_r(self.dev, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in _REASONS.items() if self.reasons & b),
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per stage (bytes that must move, flops that must be done)
+# ----------------------------------------------------------------------------
+
+def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d):
+    """(bytes, flops) the method needs for one launch of stage `name`."""
+    T, k, E = w.T, w.k, w.E
+    touched = int((counts > 0).sum())
+    if name == "route":
+        return T * E * 4 + T * k * 8, 0
+    if name == "permute":
+        return T * k * 4 + T * d * 2 + acc_rows * d * 2 + 2 * T * k * 4 + (2 * E + 1) * 4, 0
+    if name == "gate_up":
+        return touched * 2 * d * I * 2 + acc_rows * d * 2 + acc_rows * I * 2, 4 * acc_rows * d * I
+    if name == "down":
+        return touched * I * d * 2 + acc_rows * I * 2 + acc_rows * d * 2, 2 * acc_rows * I * d
+    if name == "shared_expert":
+        Is = w.shared_I
+        return 3 * d * Is * 2 + T * d * 2 * 2 + 2 * T * Is * 2, 6 * T * d * Is
+    if name == "combine":
+        b = acc_rows * d * 2 + T * k * 8 + T * d * 4 + (T * d * 2 if w.shared_I else 0)
+        if w.pooled:
+            # map composition (route -> pool row -> compact row) and, in every wave
+            # after the first, the read of the fp32 accumulator
+            b += T * k * 4 * 2 + acc_rows * 4 + T * d * 4 * (w.n_waves - 1) / w.n_waves
+        return int(b), 0
+    if name == "pool_pack":
+        return T * k * 4 + 2 * acc_rows * d * 2 + w.n_dest * d * 2 + T * k * 4, 0
+    if name == "pool_compact":
+        return 2 * acc_rows * d * 2 + w.n_dest * d * 2 + 2 * acc_rows * 4, 0
+    return 0, 0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return (float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j["bf16_tflops_sustained"]),
+                "measured")
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_sha(name):
+    src = {"gate_up": "grouped_swiglu.cu", "down": "grouped_swiglu.cu",
+           "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
+           "combine": "combine.cu", "pool_pack": "pool.cu", "pool_compact": "pool.cu"}[name]
+    with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", src), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def lookup_traffic(stage, workload_name):
+    """DRAM bytes per launch of `stage` from a committed ncu summary, if it was taken
+    on the current kernel source (profiles/*.md lines 'traffic: <stage> <workload>
+    <bytes_per_launch> <source sha256[:16]>')."""
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    sha = kernel_source_sha(stage)
+    pat = re.compile(r"^traffic:\s+(\S+)\s+(\S+)\s+(\d+)\s+([0-9a-f]{16})\s*$")
+    for fn in sorted(os.listdir(prof)):
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(prof, fn)) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m and m.group(1) == stage and m.group(2) == workload_name and m.group(4) == sha:
+                    return int(m.group(3))
+    return None
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def build_layer(w, device):
+    import grouped_expert_gemm_gb300 as g
+    logits, sel_bias = workloads.make_router_inputs(w, device)
+    x = workloads.make_activations(w, device)
+    wg, wu, wd = workloads.make_expert_weights(w, device)
+    if w.pooled:
+        pool_cap = g.capacity_from_factor(w.sender_cf, w.R, w.n_dest * w.n_waves)
+        local_cap = g.capacity_from_factor(w.receiver_cf, w.R, w.local_per_dest * w.n_waves)
+        layer = g.PooledMoELayer(w.T, w.d, w.k, w.I, w.n_dest, w.local_per_dest, w.n_waves,
+                                 pool_cap, local_cap, wg, wu, wd, device=device)
+    else:
+        cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
+        score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
+        layer = g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
+                           n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
+                           sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
+                           device=device)
+    return layer, logits, sel_bias, x
+
+
+def run_ours(args, dist, w):
+    import grouped_expert_gemm_gb300 as g
+    from grouped_expert_gemm_gb300 import abi, build
+    build.build()
+    device = torch.device(f"cuda:{dist.local}")
+    torch.cuda.set_device(device)
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
+    layer, logits, sel_bias, x = build_layer(w, device)
+    stream = torch.cuda.Stream(device)
+    stages = layer.stages(logits, x)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for _, fn in stages:
+                fn(stream)
+    stream.synchronize()
+    if int(layer.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.dev_status.item())} after warm-up")
+
+    # timed region: K whole steps, with an event after every stage
+    names = [n for n, _ in stages]
+    n_ev = len(stages) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    launches0 = abi.launch_count()
+    sampler = ClockSampler(dist.local)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    with sampler:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(steps):
+            evs[s][0].record(stream)
+            for i, (_, fn) in enumerate(stages):
+                fn(stream)
+                evs[s][i + 1].record(stream)
+        t_end.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    launches = abi.launch_count() - launches0
+    elapsed_ms = t_start.elapsed_time(t_end)
+    max_ms = dist.max(elapsed_ms)
+    if int(layer.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.dev_status.item())} after timed steps")
+
+    # per-stage device time (same stage name summed within a step)
+    stage_ms = {}
+    for s in range(steps):
+        for i, n in enumerate(names):
+            stage_ms[n] = stage_ms.get(n, 0.0) + evs[s][i].elapsed_time(evs[s][i + 1])
+    launches_per_step = {n: 0 for n in names}
+    for n in names:
+        launches_per_step[n] += 1
+    step_ms = max_ms / steps
+    value = dist.world * w.T * steps / (max_ms / 1e3)
+
+    # algorithmic work and the dominant kernel's roofline
+    if w.pooled:
+        acc_rows = int(layer.local_counts.sum().item())  # last wave's rows (per-wave unit)
+        counts = layer.local_counts.cpu().numpy()
+        I, d = w.I, w.d
+    else:
+        acc_rows = int(layer.offsets[-1].item())
+        counts = layer.counts.cpu().numpy()
+        I, d = w.I, w.d
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    long_region = max_ms > 2000.0
+    tf_peak = tf_sust if long_region else tf_burst
+    per_stage = {}
+    for n in stage_ms:
+        per_launch_ms = stage_ms[n] / (steps * launches_per_step[n])
+        b, f = stage_work(w, layer, n, counts, acc_rows, w.E, I, d)
+        t_hbm = b / (hbm * 1e9)
+        t_tc = f / (tf_peak * 1e12) if f else 0.0
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        if bound == "tensor":
+            achieved = f / (per_launch_ms * 1e-3) / 1e12
+            frac = achieved / tf_peak
+        else:
+            achieved = b / (per_launch_ms * 1e-3) / 1e9
+            frac = achieved / hbm
+        per_stage[n] = {"ms_per_launch": round(per_launch_ms, 5),
+                        "share": round(stage_ms[n] / sum(stage_ms.values()), 4),
+                        "bound": bound, "achieved": round(achieved, 2),
+                        "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                        "frac": round(frac, 4), "alg_bytes": int(b), "alg_flops": int(f)}
+    dom = max(stage_ms, key=lambda n: stage_ms[n])
+    ds = per_stage[dom]
+    roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
+                "peak": tf_peak if ds["bound"] == "tensor" else hbm, "unit": ds["unit"],
+                "frac": ds["frac"], "traffic": lookup_traffic(dom, w.name),
+                "peak_source": f"{peak_src} ({'sustained' if long_region and ds['bound'] == 'tensor' else 'burst'})"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the workload, random-init expert weights)",
+        "config": config_dict(w, layer),
+        "roofline": roofline, "stages": per_stage, "clocks": sampler.summary(),
+        "gpu_launches": int(launches),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps)
+    return result, layer, logits, sel_bias, x
+
+
+def config_dict(w, layer):
+    c = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I,
+         "router": w.score_fn, "parallelism": "replicas only (no data-path collective)"}
+    if w.capacity_factor is not None:
+        c["capacity_factor"] = w.capacity_factor
+        c["capacity"] = layer.capacity
+    else:
+        c["capacity"] = "dropless"
+    if w.shared_I:
+        c["shared_I"] = w.shared_I
+    if w.pooled:
+        c.update({"n_dest": w.n_dest, "local_per_dest": w.local_per_dest, "n_waves": w.n_waves,
+                  "pool_cap": layer.pool_cap, "local_cap": layer.local_cap,
+                  "wave_policy": "stripe"})
+    wbytes = sum(t.numel() * 2 for t in (layer.w_gate, layer.w_up, layer.w_down))
+    c["expert_weight_bytes"] = wbytes
+    c["l2"] = ("expert weights ({:.2f} GB) exceed L2 (129 MB): every step streams them from HBM"
+               .format(wbytes / 1e9) if wbytes > 129e6 else "working set below L2 size")
+    return c
+
+
+def run_e2e(args, dist, w, layer, logits, x, stream, steps):
+    """Same metric through the host-buffer API: H2D of the step's inputs, the layer,
+    D2H of the fp32 result, every step, all inside the timed region."""
+    lh = logits.cpu().pin_memory()
+    xh = x.cpu().pin_memory()
+    oh = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    for _ in range(max(args.warmup, 3)):
+        layer.forward_host(lh, xh, oh, stream)
+    stream.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        layer.forward_host(lh, xh, oh, stream)
+    b.record(stream)
+    stream.synchronize()
+    dist.barrier()
+    ms = dist.max(a.elapsed_time(b))
+    return {"value": round(dist.world * w.T * steps / (ms / 1e3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(lh.numel() * 4 + xh.numel() * 2),
+            "d2h_bytes_per_step": int(oh.numel() * 4)}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (baseline leg and --impl reference)
+# ----------------------------------------------------------------------------
+
+def oracle_step(w, host_inputs, tokens):
+    """One oracle pass over the workload for the sampled `tokens` (routing, admission and
+    permutation over all tokens, expert math and combine for the sample)."""
+    import oracle
+    logits, sel_bias, xb, weights_of, shared = host_inputs
+    if w.score_fn == "softmax":
+        ids, gates = oracle.route_softmax(logits, w.k)
+    else:
+        ids, gates = oracle.route_sigmoid_group(logits, sel_bias, w.k, w.n_group, w.topk_group,
+                                                w.route_scale)
+    if w.pooled:
+        # the pooled layout's per-route fate over all waves; expert = local id
+        pc = oracle.pool_capacity(w.sender_cf, w.T, w.k, w.n_dest, w.n_waves)
+        lc = oracle.local_capacity(w.receiver_cf, w.T, w.k, w.local_per_dest, w.n_waves)
+        row_of = np.full(w.R, -1)
+        expert_of_row = {}
+        for wave in range(w.n_waves):
+            rp = oracle.pool_pack(ids, xb, w.n_dest, w.local_per_dest, w.n_waves, pc, wave)
+            rc = oracle.pool_compact(rp["pools"], pc, w.local_per_dest, lc)
+            comp = oracle.compose_map(rp["route_to_poolrow"], rc["poolrow_to_row"])
+            ok = comp >= 0
+            row_of[ok] = comp[ok] + wave * w.local_per_dest * lc
+        perm = {"route_to_row": row_of}
+        eids = ids % w.local_per_dest
+    else:
+        cap = -1 if w.capacity_factor is None else oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
+        perm = oracle.permute(ids, w.E, cap)
+        eids = ids
+    k = w.k
+    need = {}
+    for t in tokens:
+        for j in range(k):
+            if perm["route_to_row"][t * k + j] >= 0:
+                need.setdefault(int(eids[t, j]), []).append(t * k + j)
+    y = {}
+    for e, routes in need.items():
+        wg, wu, wd = weights_of(e)
+        _, ye = oracle.swiglu(oracle.bf16_to_f64(xb[np.array(routes) // k]), oracle.bf16_to_f64(wg),
+                              oracle.bf16_to_f64(wu), oracle.bf16_to_f64(wd))
+        for i, r in enumerate(routes):
+            y[int(perm["route_to_row"][r])] = ye[i]
+    sh = None
+    if shared is not None:
+        sg, su, sd = shared
+        _, sh = oracle.swiglu(oracle.bf16_to_f64(xb[np.array(tokens)]), oracle.bf16_to_f64(sg[0]),
+                              oracle.bf16_to_f64(su[0]), oracle.bf16_to_f64(sd[0]))
+    out = [oracle.combine_token(lambda r: y[r], perm["route_to_row"][t * k:(t + 1) * k], gates[t],
+                                None if sh is None else sh[i]) for i, t in enumerate(tokens)]
+    return out
+
+
+def host_inputs_of(w, logits, sel_bias, x, layer):
+    """Host copies of the inputs (weights fetched per expert on demand)."""
+    cache = {}
+
+    def weights_of(e):
+        if e not in cache:
+            cache[e] = tuple(workloads.bf16_bits(t[e]) for t in (layer.w_gate, layer.w_up, layer.w_down))
+        return cache[e]
+    shared = None
+    if getattr(layer, "shared", None) is not None:
+        shared = tuple(workloads.bf16_bits(t) for t in layer.shared)
+    return (logits.cpu().numpy(), None if sel_bias is None else sel_bias.cpu().numpy(),
+            workloads.bf16_bits(x), weights_of, shared)
+
+
+def cpu_sample_tokens(w, budget_s, host_inputs, rng):
+    """Grow the token sample until one oracle pass takes about `budget_s` seconds."""
+    n = 1
+    while True:
+        toks = np.sort(rng.choice(w.T, min(n, w.T), replace=False))
+        t0 = time.perf_counter()
+        oracle_step(w, host_inputs, toks)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or n >= w.T:
+            return toks, dt
+        n = min(w.T, n * 4 if dt < budget_s / 16 else n * 2)
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_cpu_baseline(args, w, layer, logits, sel_bias, x):
+    hi = host_inputs_of(w, logits, sel_bias, x, layer)
+    rng = np.random.default_rng(0)
+    toks, dt = cpu_sample_tokens(w, args.cpu_budget, hi, rng)
+    return {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": cores(),
+            "kind": "oracle",
+            "sample": f"{len(toks)} of {w.T} tokens of {w.name} (routing/admission over all "
+                      f"tokens, expert math + combine for the sample), one pass, {dt:.1f} s"}
+
+
+def run_reference(args, dist, w):
+    if dist.rank != 0:
+        return None
+    steps = args.steps if args.steps is not None else 5
+    device = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
+    if device.type == "cuda":
+        from grouped_expert_gemm_gb300 import build
+        build.build()
+        layer, logits, sel_bias, x = build_layer(w, device)
+    else:
+        raise RuntimeError("the reference arm generates the same seeded inputs on the GPU")
+    hi = host_inputs_of(w, logits, sel_bias, x, layer)
+    rng = np.random.default_rng(0)
+    # size the per-step sample so that one step takes ~2 s of oracle work
+    toks, _ = cpu_sample_tokens(w, 4.0, hi, rng)
+    for _ in range(args.warmup):
+        oracle_step(w, hi, toks)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(w, hi, toks)
+    dt = time.perf_counter() - t0
+    value = len(toks) * steps / dt
+    sample = f"{len(toks)} of {w.T} tokens of {w.name} per step (routing/admission over all tokens)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    w = workload_for(args)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist, w)
+            if res is not None:
+                print(json.dumps(res), flush=True)
+            return
+        res, layer, logits, sel_bias, x = run_ours(args, dist, w)
+        if dist.rank == 0 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(args, w, layer, logits, sel_bias, x)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -37,7 +37,7 @@ MOE_POOL_EMPTY = 0xFFFF
 EXPORTED = [
     "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
     "moe_permute_workspace_size", "moe_permute", "moe_grouped_swiglu_workspace_size",
-    "moe_grouped_swiglu", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
+    "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
 ]
 
@@ -77,6 +77,8 @@ _SIGS = {
     "moe_grouped_swiglu_workspace_size": (_SZ, [_I32, _I32]),
     "moe_grouped_swiglu": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                   _P, _P]),
+    "moe_grouped_gate_up": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_grouped_down": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_pool_pack_workspace_size": (_SZ, [ctypes.POINTER(PoolParams), _I32, _I32]),
     "moe_pool_pack": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _I32, _P, _P, _P, _P,
@@ -88,6 +90,16 @@ _SIGS = {
 }
 
 _lib: Optional[ctypes.CDLL] = None
+_launches = [0]
+
+
+def launch_count() -> int:
+    """Kernels launched through this binding so far (each call knows its launch count)."""
+    return _launches[0]
+
+
+def _count(n: int):
+    _launches[0] += n
 
 
 def library_path() -> str:
@@ -148,10 +160,12 @@ def moe_route(p: RouteParams, logits, sel_bias, topk_ids, gates, dev_status=None
     _check("moe_route", lib().moe_route(ctypes.byref(p), _ptr(logits), _ptr(sel_bias),
                                         _ptr(topk_ids), _ptr(gates), _ptr(dev_status),
                                         _stream(stream)))
+    _count(1 if p.T > 0 else 0)
 
 
 def moe_sigmoid_det(n: int, z, s, stream=None):
     _check("moe_sigmoid_det", lib().moe_sigmoid_det(n, _ptr(z), _ptr(s), _stream(stream)))
+    _count(1 if n > 0 else 0)
 
 
 def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
@@ -164,6 +178,7 @@ def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
+    _count(3 if T > 0 else 1)
 
 
 def moe_grouped_swiglu_workspace_size(max_rows: int, I: int) -> int:
@@ -175,6 +190,23 @@ def moe_grouped_swiglu(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w
     _check("moe_grouped_swiglu", lib().moe_grouped_swiglu(
         n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
         _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+    _count(2 if max_rows > 0 else 0)
+
+
+def moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, h,
+                        dev_status=None, stream=None):
+    _check("moe_grouped_gate_up", lib().moe_grouped_gate_up(
+        n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
+        _ptr(w_up), _ptr(h), _ptr(dev_status), _stream(stream)))
+    _count(1 if max_rows > 0 else 0)
+
+
+def moe_grouped_down(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status=None,
+                     stream=None):
+    _check("moe_grouped_down", lib().moe_grouped_down(
+        n_seg, I, d, max_rows, _ptr(h), _ptr(seg_begin), _ptr(seg_count), _ptr(w_down), _ptr(y),
+        _ptr(dev_status), _stream(stream)))
+    _count(1 if max_rows > 0 else 0)
 
 
 def moe_combine(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, out,
@@ -182,6 +214,7 @@ def moe_combine(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, o
     _check("moe_combine", lib().moe_combine(
         T, k, d, _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates), _ptr(shared_y),
         int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
+    _count((T + 65534) // 65535)
 
 
 def moe_pool_pack_workspace_size(p: PoolParams, T: int, k: int) -> int:
@@ -194,6 +227,7 @@ def moe_pool_pack(p: PoolParams, T, d, k, wave, topk_ids, x, pools, route_to_poo
         ctypes.byref(p), T, d, k, wave, _ptr(topk_ids), _ptr(x), _ptr(pools),
         _ptr(route_to_poolrow), _ptr(pool_fill), _ptr(sender_drops), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
+    _count(3 if T > 0 else 2)
 
 
 def moe_pool_compact_workspace_size(n_src: int, pool_cap: int, n_local: int) -> int:
@@ -206,8 +240,10 @@ def moe_pool_compact(n_src, pool_cap, d, n_local, local_cap, pools, compact, loc
         n_src, pool_cap, d, n_local, local_cap, _ptr(pools), _ptr(compact), _ptr(local_counts),
         _ptr(poolrow_to_row), _ptr(receiver_drops), _ptr(ws), ws_bytes, _ptr(dev_status),
         _stream(stream)))
+    _count(3)
 
 
 def moe_compose_map(n, a, b, b_len, out, dev_status=None, stream=None):
     _check("moe_compose_map", lib().moe_compose_map(n, _ptr(a), _ptr(b), b_len, _ptr(out),
                                                     _ptr(dev_status), _stream(stream)))
+    _count(1 if n > 0 else 0)

@@ -555,19 +555,68 @@ MOE_API size_t moe_grouped_swiglu_workspace_size(int32_t max_rows, int32_t I) {
   return static_cast<size_t>(max_rows) * I * 2 + 256;
 }
 
+static moe_status check_common(int32_t n_seg, int32_t K, int32_t N, int32_t max_rows) {
+  if (n_seg <= 0 || K <= 0 || N <= 0 || max_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % 64 != 0 || K > 65536 || N > 65536 || n_seg > kMaxSeg)
+    return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(n_seg) * K >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(n_seg) * N >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                                       const moe_bf16* x, const int32_t* seg_begin,
+                                       const int32_t* seg_count, const moe_bf16* w_gate,
+                                       const moe_bf16* w_up, moe_bf16* h, uint32_t* dev_status,
+                                       moe_stream_t stream) {
+  moe_status st = check_common(n_seg, d, I, max_rows);
+  if (st != MOE_OK || max_rows == 0) return st;
+  if (x == nullptr || seg_begin == nullptr || seg_count == nullptr || w_gate == nullptr ||
+      w_up == nullptr || h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up))
+    return MOE_ERR_UNSUPPORTED;
+  CUtensorMap m_x, m_wg, m_wu;
+  if (!make_map(&m_x, x, max_rows, d, kBM) || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
+      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
+    return MOE_ERR_CUDA;
+  GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
+             dev_status};
+  cudaStream_t s = as_cuda(stream);
+  return (I % 128 == 0) ? launch_gemm<4, true>(m_x, m_wg, m_wu, a, s)
+                        : launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+}
+
+MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                                    const moe_bf16* h, const int32_t* seg_begin,
+                                    const int32_t* seg_count, const moe_bf16* w_down, moe_bf16* y,
+                                    uint32_t* dev_status, moe_stream_t stream) {
+  moe_status st = check_common(n_seg, I, d, max_rows);
+  if (st != MOE_OK || max_rows == 0) return st;
+  if (h == nullptr || seg_begin == nullptr || seg_count == nullptr || w_down == nullptr ||
+      y == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(y) || !aligned16(w_down)) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap m_h, m_wd;
+  if (!make_map(&m_h, h, max_rows, I, kBM) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
+    return MOE_ERR_CUDA;
+  GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
+             dev_status};
+  cudaStream_t s = as_cuda(stream);
+  if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
+  if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
+  return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
+}
+
 MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
                                       const moe_bf16* x, const int32_t* seg_begin,
                                       const int32_t* seg_count, const moe_bf16* w_gate,
                                       const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* y,
                                       void* ws, size_t ws_bytes, uint32_t* dev_status,
                                       moe_stream_t stream) {
-  if (n_seg <= 0 || d <= 0 || I <= 0 || max_rows < 0) return MOE_ERR_INVALID_ARG;
-  if (d % 64 != 0 || I % 64 != 0 || d > 65536 || I > 65536 || n_seg > kMaxSeg)
-    return MOE_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(n_seg) * d >= (int64_t(1) << 31) ||
-      static_cast<int64_t>(n_seg) * I >= (int64_t(1) << 31))
-    return MOE_ERR_UNSUPPORTED;
-  if (max_rows == 0) return MOE_OK;
+  moe_status st = check_common(n_seg, d, I, max_rows);
+  if (st != MOE_OK || max_rows == 0) return st;
   if (x == nullptr || seg_begin == nullptr || seg_count == nullptr || w_gate == nullptr ||
       w_up == nullptr || w_down == nullptr || y == nullptr || ws == nullptr)
     return MOE_ERR_INVALID_ARG;
@@ -575,20 +624,10 @@ MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32
       !aligned16(w_up) || !aligned16(w_down))
     return MOE_ERR_UNSUPPORTED;
   if (ws_bytes < moe_grouped_swiglu_workspace_size(max_rows, I)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  uint16_t* h = static_cast<uint16_t*>(ws);
-  CUtensorMap m_x, m_wg, m_wu, m_h, m_wd;
-  if (!make_map(&m_x, x, max_rows, d, kBM) || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
-      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK) || !make_map(&m_h, h, max_rows, I, kBM) ||
-      !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
-    return MOE_ERR_CUDA;
-  cudaStream_t s = as_cuda(stream);
-  GemmArgs a1{seg_begin, seg_count, n_seg, d, I, max_rows, h, dev_status};
-  moe_status st = (I % 128 == 0) ? launch_gemm<4, true>(m_x, m_wg, m_wu, a1, s)
-                                 : launch_gemm<2, true>(m_x, m_wg, m_wu, a1, s);
+  moe_bf16* h = static_cast<moe_bf16*>(ws);
+  st = moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, h,
+                           dev_status, stream);
   if (st != MOE_OK) return st;
-  GemmArgs a2{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
-              dev_status};
-  if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a2, s);
-  if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a2, s);
-  return launch_gemm<1, false>(m_h, m_wd, m_wd, a2, s);
+  return moe_grouped_down(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status,
+                          stream);
 }

@@ -87,11 +87,19 @@ class MoELayer:
                         self.route_to_row, self.n_dropped, self.perm_ws, self.perm_ws_bytes,
                         self.dev_status, stream)
 
-    def experts(self, stream=None):
+    def experts_gate_up(self, stream=None):
         R = max(self.T * self.k, 1)
-        abi.moe_grouped_swiglu(self.E, self.d, self.I, R, self.x_perm, self.offsets, self.counts,
-                               self.w_gate, self.w_up, self.w_down, self.y, self.gemm_ws,
-                               self.gemm_ws_bytes, self.dev_status, stream)
+        abi.moe_grouped_gate_up(self.E, self.d, self.I, R, self.x_perm, self.offsets, self.counts,
+                                self.w_gate, self.w_up, self.H, self.dev_status, stream)
+
+    def experts_down(self, stream=None):
+        R = max(self.T * self.k, 1)
+        abi.moe_grouped_down(self.E, self.I, self.d, R, self.H, self.offsets, self.counts,
+                             self.w_down, self.y, self.dev_status, stream)
+
+    def experts(self, stream=None):
+        self.experts_gate_up(stream)
+        self.experts_down(stream)
 
     def shared_expert(self, x, stream=None):
         sg, su, sd = self.shared
@@ -105,15 +113,38 @@ class MoELayer:
                         self.shared_y if self.shared is not None else None, 0, self.out,
                         self.dev_status, stream)
 
+    def stages(self, logits, x):
+        """The layer as (name, callable(stream)) steps, in launch order."""
+        st = [("route", lambda s: self.route(logits, s)),
+              ("permute", lambda s: self.permute(x, s)),
+              ("gate_up", self.experts_gate_up),
+              ("down", self.experts_down)]
+        if self.shared is not None:
+            st.append(("shared_expert", lambda s: self.shared_expert(x, s)))
+        st.append(("combine", self.combine))
+        return st
+
     def forward(self, logits, x, stream=None) -> torch.Tensor:
         """Enqueue the whole layer on `stream`; returns the fp32 output buffer [T, d]."""
-        self.route(logits, stream)
-        self.permute(x, stream)
-        self.experts(stream)
-        if self.shared is not None:
-            self.shared_expert(x, stream)
-        self.combine(stream)
+        for _, fn in self.stages(logits, x):
+            fn(stream)
         return self.out
+
+    def forward_host(self, logits_host, x_host, out_host, stream=None):
+        """Layer forward for host-resident inputs: copies logits and x from (pinned) host
+        memory, runs the layer and copies the fp32 result back into ``out_host``, all
+        enqueued on one stream (the host is not synchronised)."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            if not hasattr(self, "_in_logits"):
+                self._in_logits = torch.empty(logits_host.shape, dtype=logits_host.dtype,
+                                              device=self.out.device)
+                self._in_x = torch.empty(x_host.shape, dtype=x_host.dtype, device=self.out.device)
+            self._in_logits.copy_(logits_host, non_blocking=True)
+            self._in_x.copy_(x_host, non_blocking=True)
+            self.forward(self._in_logits, self._in_x, s)
+            out_host.copy_(self.out, non_blocking=True)
+        return out_host
 
 
 class PooledMoELayer:
@@ -183,11 +214,32 @@ class PooledMoELayer:
         abi.moe_combine(self.T, self.k, self.d, self.y, self.rows, self.route_to_row, self.gates,
                         None, 1 if wave > 0 else 0, self.out, self.dev_status, stream)
 
-    def forward(self, logits, x, stream=None) -> torch.Tensor:
-        self.route(logits, stream)
+    def experts_gate_up(self, stream=None):
+        abi.moe_grouped_gate_up(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,
+                                self.local_counts, self.w_gate, self.w_up, self.H,
+                                self.dev_status, stream)
+
+    def experts_down(self, stream=None):
+        abi.moe_grouped_down(self.L, self.I, self.d, self.rows, self.H, self.local_begin,
+                             self.local_counts, self.w_down, self.y, self.dev_status, stream)
+
+    @property
+    def H(self) -> torch.Tensor:
+        return self.gemm_ws[: self.rows * self.I * 2].view(torch.bfloat16).view(self.rows, self.I)
+
+    def stages(self, logits, x):
+        st = [("route", lambda s: self.route(logits, s))]
         for w in range(self.n_waves):
-            self.pack(x, w, stream)
-            self.compact_wave(w, stream)
-            self.experts(stream)
-            self.combine_wave(w, stream)
+            st += [("pool_pack", lambda s, w=w: self.pack(x, w, s)),
+                   ("pool_compact", lambda s, w=w: self.compact_wave(w, s)),
+                   ("gate_up", self.experts_gate_up),
+                   ("down", self.experts_down),
+                   ("combine", lambda s, w=w: self.combine_wave(w, s))]
+        return st
+
+    def forward(self, logits, x, stream=None) -> torch.Tensor:
+        for _, fn in self.stages(logits, x):
+            fn(stream)
         return self.out
+
+    forward_host = MoELayer.forward_host

@@ -161,8 +161,8 @@ moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capac
  * Workspace: moe_grouped_swiglu_workspace_size(max_rows, I) bytes; after the
  * stream reaches this call's end its first max_rows*I*2 bytes hold H in the
  * same row space as x.
- * Limits: d % 64 == 0, I % 128 == 0, 64 <= d, I <= 65536; pointers 16-byte
- * aligned; n_seg >= 1.  Rows outside [0,max_rows) in a segment set
+ * Limits: d % 64 == 0, I % 64 == 0, d, I <= 65536, n_seg <= 1024; pointers
+ * 16-byte aligned; n_seg >= 1.  Rows outside [0,max_rows) in a segment set
  * MOE_DEV_BAD_ROW and that segment is skipped.                              */
 size_t moe_grouped_swiglu_workspace_size(int32_t max_rows, int32_t I);
 moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
@@ -171,6 +171,22 @@ moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32_t max_r
                               const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* y,
                               void* ws, size_t ws_bytes, uint32_t* dev_status,
                               moe_stream_t stream);
+
+/* The two passes of moe_grouped_swiglu as separate calls (same segment rules,
+ * limits and device-side error reporting; no workspace):
+ *   moe_grouped_gate_up: h[b:b+c] = bf16(SiLU(X_q W_gate[q]) * (X_q W_up[q]))
+ *                        x [max_rows, d], h [max_rows, I]   ([M6.6] 0x04C, "gate/up")
+ *   moe_grouped_down:    y[b:b+c] = bf16(H_q W_down[q])
+ *                        h [max_rows, I], y [max_rows, d]   ([M6.6] 0x04C, "down")  */
+moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                               const moe_bf16* x, const int32_t* seg_begin,
+                               const int32_t* seg_count, const moe_bf16* w_gate,
+                               const moe_bf16* w_up, moe_bf16* h, uint32_t* dev_status,
+                               moe_stream_t stream);
+moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                            const moe_bf16* h, const int32_t* seg_begin, const int32_t* seg_count,
+                            const moe_bf16* w_down, moe_bf16* y, uint32_t* dev_status,
+                            moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Combine                                                                  */
