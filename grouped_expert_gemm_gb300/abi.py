@@ -36,7 +36,8 @@ MOE_POOL_EMPTY = 0xFFFF
 
 EXPORTED = [
     "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
-    "moe_permute_workspace_size", "moe_permute", "moe_grouped_swiglu_workspace_size",
+    "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
+    "moe_grouped_swiglu_workspace_size",
     "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
 ]
@@ -74,6 +75,8 @@ _SIGS = {
     "moe_permute_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "moe_permute": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                            _P, _P]),
+    "moe_permute_noalloc": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _P]),
     "moe_grouped_swiglu_workspace_size": (_SZ, [_I32, _I32]),
     "moe_grouped_swiglu": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                   _P, _P]),
@@ -178,6 +181,18 @@ def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
+    _count(3 if T > 0 else 1)
+
+
+def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
+                        route_to_row, n_dropped, dev_status=None, stream=None):
+    """moe_permute without a workspace: scratch is a fixed 1 MiB device array of the library.
+    Calls that overlap on the GPU race on it; the first call on a device should precede
+    any stream capture."""
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
+        _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(dev_status),
+        _stream(stream)))
     _count(3 if T > 0 else 1)
 
 

@@ -235,3 +235,61 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
       route_to_row);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of moe_permute.
+//
+// Some callers cannot call cudaMalloc and have no workspace to hand over: for
+// example an inference runtime's plugin hook that may only enqueue work on the
+// stream it is given, or a latency-critical serving loop where an allocation
+// could synchronise the device or break a fixed memory budget.  For them the
+// per-tile histogram lives in a fixed file-scope device array instead of a
+// caller workspace.  The array is part of the library image: every GPU that
+// loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device, looked up once per
+// device (in host code the array's name is only a host-side stand-in).
+moe_status static_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API moe_status moe_permute_noalloc(int32_t T, int32_t d, int32_t E, int32_t k,
+                                       int32_t capacity, const int32_t* topk_ids,
+                                       const moe_bf16* x, moe_bf16* x_perm, int32_t* counts,
+                                       int32_t* offsets, int32_t* row_to_route,
+                                       int32_t* route_to_row, int32_t* n_dropped,
+                                       uint32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || k <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (moe_permute_workspace_size(T, k, E) > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const moe_status st = static_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  return moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
+                     route_to_row, n_dropped, scratch, kStaticScratchBytes, dev_status, stream);
+}

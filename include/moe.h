@@ -144,6 +144,30 @@ moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capac
                        int32_t* route_to_row, int32_t* n_dropped, void* ws, size_t ws_bytes,
                        uint32_t* dev_status, moe_stream_t stream);
 
+/* moe_permute for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this call: it exists for code that must not call
+ * cudaMalloc and has no workspace to lend -- for example an inference
+ * runtime's plugin hook that may only enqueue on the stream it is handed, or a
+ * latency-critical loop where an allocation could synchronise the device.
+ * Same arguments, outputs, limits and errors as moe_permute minus the
+ * workspace: the per-tile histogram lives in a 1 MiB file-scope device array
+ * of the library, which every GPU that loads the library holds until the
+ * process exits.  Sizes whose moe_permute_workspace_size(T,k,E) exceeds 1 MiB
+ * are rejected with MOE_ERR_UNSUPPORTED (for E = 512 that is beyond about
+ * 2 million routes T*k).  Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the last call's contents (each call overwrites every entry it reads
+ * before reading it, so nothing needs clearing).  Calls whose work overlaps on
+ * the GPU -- other streams, other host threads -- race on the array: serialise
+ * them.                                                                     */
+moe_status moe_permute_noalloc(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                               const int32_t* topk_ids, const moe_bf16* x, moe_bf16* x_perm,
+                               int32_t* counts, int32_t* offsets, int32_t* row_to_route,
+                               int32_t* route_to_row, int32_t* n_dropped, uint32_t* dev_status,
+                               moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped SwiGLU expert GEMM over ragged row segments                      */
 /* ------------------------------------------------------------------------ */
