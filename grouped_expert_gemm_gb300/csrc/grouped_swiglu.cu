@@ -447,7 +447,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
               for (int h = 0; h < 2; ++h) {
                 const float gv = __uint_as_float(g[2 * i + h]);
                 const float uv = __uint_as_float(u[2 * i + h]);
-                h2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                h2[h] = __fdiv_rn(gv, 1.0f + expf(-gv)) * uv;  // SiLU(g) * u
               }
               pk[i] = pack_bf16x2(h2[0], h2[1]);
             }

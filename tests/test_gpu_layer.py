@@ -193,7 +193,7 @@ def pooled_check(w, policy, sample_tokens, sample_rows, seed):
 
 @pytest.mark.parametrize("policy", [0, 1])
 def test_pooled_small(policy):
-    w = workloads.scaled(workloads.pooled(), T=2048, d=256, I=256, n_dest=8, E=8 * 6)
+    w = workloads.scaled(workloads.pooled(), T=2048, d=256, I=256, n_dest=32, E=32 * 6)
     pooled_check(w, policy, sample_tokens=64, sample_rows=512, seed=4)
 
 
