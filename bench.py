@@ -44,7 +44,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode",
                     choices=["decode", "tiny", "prefill", "v3", "pooled"])
-    ap.add_argument("--tokens", type=int, default=128, help="decode batch (1, 8, 32, 128)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
+                         "a smaller T for short profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -53,9 +55,13 @@ def parse_args():
 
 
 def workload_for(args) -> workloads.Workload:
-    return {"decode": lambda: workloads.decode(args.tokens), "tiny": workloads.tiny,
-            "prefill": workloads.prefill, "v3": workloads.v3,
-            "pooled": workloads.pooled}[args.config]()
+    if args.config == "decode":
+        return workloads.decode(args.tokens or 128)
+    w = {"tiny": workloads.tiny, "prefill": workloads.prefill, "v3": workloads.v3,
+         "pooled": workloads.pooled}[args.config]()
+    if args.tokens:
+        w = workloads.scaled(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
+    return w
 
 
 DEFAULT_STEPS = {"decode": 200, "tiny": 200, "prefill": 20, "v3": 10, "pooled": 5}

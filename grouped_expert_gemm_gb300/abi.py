@@ -186,7 +186,7 @@ def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_
 
 def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
                         route_to_row, n_dropped, dev_status=None, stream=None):
-    """moe_permute without a workspace: scratch is a fixed 1 MiB device array of the library.
+    """moe_permute without a workspace: scratch is a fixed 64 KiB device array of the library.
     Calls that overlap on the GPU race on it; the first call on a device should precede
     any stream capture."""
     _check("moe_permute_noalloc", lib().moe_permute_noalloc(
@@ -229,7 +229,7 @@ def moe_combine(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, o
     _check("moe_combine", lib().moe_combine(
         T, k, d, _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates), _ptr(shared_y),
         int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
-    _count((T + 65534) // 65535)
+    _count(1 if T > 0 else 0)
 
 
 def moe_pool_pack_workspace_size(p: PoolParams, T: int, k: int) -> int:

@@ -6,11 +6,12 @@
 // bf16 returned rows.  [POOL] 03: waves add into one fp32 accumulator
 // (accumulate != 0).
 //
-// One block covers one token and up to 128 16-byte column chunks (8 outputs per
-// thread).  The token's k row indices and gates are staged once in shared
-// memory; every thread then issues k independent 16-byte loads of y, sums in
-// fp32 in slot order, and writes two 16-byte fp32 stores.  No atomics: each
-// output element has exactly one writer, so the result is deterministic.
+// One block owns one token at a time (grid-stride over tokens).  The token's k
+// row indices and gates are staged once in shared memory; each thread then
+// handles 16-byte column chunks, issuing all k (up to KMAX) independent 16-byte
+// loads of y for UNROLL chunks before using them, sums in fp32 in slot order,
+// and writes two 16-byte fp32 stores per chunk.  No atomics: each output element
+// has exactly one writer, so the result is deterministic.
 #include "common.cuh"
 
 namespace moe {
@@ -18,59 +19,77 @@ namespace {
 
 constexpr int kCombThreads = 128;
 
+template <int KMAX>
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int k, int chunks, const uint4* __restrict__ y, int64_t y_rows,
+combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
                const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
                uint32_t* __restrict__ dev_status) {
-  __shared__ int32_t s_row[16];
-  __shared__ float s_gate[16];
-  const int64_t t = blockIdx.y;
-  if (threadIdx.x < k) {
-    int32_t r = __ldg(route_to_row + t * k + threadIdx.x);
-    if (r >= 0 && r >= y_rows) {
-      report(dev_status, MOE_DEV_BAD_ROW);
-      r = -1;
+  constexpr int UNROLL = KMAX >= 8 ? 1 : (KMAX >= 4 ? 2 : 4);
+  __shared__ int32_t s_row[KMAX];
+  __shared__ float s_gate[KMAX];
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < KMAX) {
+      int32_t r = -1;
+      float g = 0.0f;
+      if (threadIdx.x < k) {
+        r = __ldg(route_to_row + t * k + threadIdx.x);
+        g = __ldg(gates + t * k + threadIdx.x);
+        if (r >= 0 && r >= y_rows) {
+          report(dev_status, MOE_DEV_BAD_ROW);
+          r = -1;
+        }
+      }
+      s_row[threadIdx.x] = r;
+      s_gate[threadIdx.x] = g;
     }
-    s_row[threadIdx.x] = r;
-    s_gate[threadIdx.x] = __ldg(gates + t * k + threadIdx.x);
-  }
-  __syncthreads();
-  const int c = blockIdx.x * kCombThreads + threadIdx.x;
-  if (c >= chunks) return;
-  float acc[8];
-  float4* o = out + (t * chunks + c) * 2;
-  if (accumulate) {
-    const float4 a = o[0], b = o[1];
-    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-  } else {
+    __syncthreads();
+    for (int c0 = threadIdx.x; c0 < chunks; c0 += kCombThreads * UNROLL) {
+      uint4 v[UNROLL][KMAX];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  }
-  uint4 v[16];
+      for (int u = 0; u < UNROLL; ++u) {
+        const int c = c0 + u * kCombThreads;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (j < k && s_row[j] >= 0) v[j] = __ldg(y + static_cast<int64_t>(s_row[j]) * chunks + c);
-  }
+        for (int j = 0; j < KMAX; ++j)
+          if (c < chunks && s_row[j] >= 0)
+            v[u][j] = __ldg(y + static_cast<int64_t>(s_row[j]) * chunks + c);
+      }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (j < k && s_row[j] >= 0) {
-      float f[8];
-      unpack8(v[j], f);
-      const float g = s_gate[j];
+      for (int u = 0; u < UNROLL; ++u) {
+        const int c = c0 + u * kCombThreads;
+        if (c >= chunks) continue;
+        float acc[8];
+        float4* o = out + (t * chunks + c) * 2;
+        if (accumulate) {
+          const float4 a = o[0], b = o[1];
+          acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+          acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+        } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (s_row[j] >= 0) {
+            float f[8];
+            unpack8(v[u][j], f);
+            const float g = s_gate[j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+          }
+        }
+        if (shared_y != nullptr) {
+          float f[8];
+          unpack8(__ldg(shared_y + t * chunks + c), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      }
     }
+    __syncthreads();
   }
-  if (shared_y != nullptr) {
-    float f[8];
-    unpack8(__ldg(shared_y + t * chunks + c), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += f[i];
-  }
-  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 }  // namespace
@@ -83,7 +102,7 @@ MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* 
                                const moe_bf16* shared_y, int32_t accumulate, float* out,
                                uint32_t* dev_status, moe_stream_t stream) {
   if (T < 0 || k <= 0 || d <= 0 || y_rows < 0) return MOE_ERR_INVALID_ARG;
-  if (k > 16 || d % 8 != 0 || T > 65535 * 1024) return MOE_ERR_UNSUPPORTED;
+  if (k > 16 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (out == nullptr || route_to_row == nullptr || gates == nullptr ||
       (y == nullptr && y_rows > 0))
@@ -92,16 +111,20 @@ MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* 
       (shared_y != nullptr && !aligned16(shared_y)))
     return MOE_ERR_UNSUPPORTED;
   const int chunks = d / 8;
-  // grid.y is limited to 65535: fold larger token counts into several launches.
   cudaStream_t s = as_cuda(stream);
-  for (int64_t t0 = 0; t0 < T; t0 += 65535) {
-    const int64_t nt = T - t0 < 65535 ? T - t0 : 65535;
-    const dim3 grid(static_cast<unsigned>(ceil_div(chunks, kCombThreads)), static_cast<unsigned>(nt));
-    combine_kernel<<<grid, kCombThreads, 0, s>>>(
-        k, chunks, reinterpret_cast<const uint4*>(y), y_rows, route_to_row + t0 * k,
-        gates + t0 * k,
-        shared_y ? reinterpret_cast<const uint4*>(shared_y) + t0 * chunks : nullptr, accumulate,
-        reinterpret_cast<float4*>(out) + t0 * chunks * 2, dev_status);
-  }
+  const unsigned grid = static_cast<unsigned>(T < 152 * 24 ? T : 152 * 24);
+#define MOE_COMBINE_CASE(K)                                                                      \
+  combine_kernel<K><<<grid, kCombThreads, 0, s>>>(T, k, chunks,                                  \
+                                                  reinterpret_cast<const uint4*>(y), y_rows,     \
+                                                  route_to_row, gates,                           \
+                                                  reinterpret_cast<const uint4*>(shared_y),      \
+                                                  accumulate, reinterpret_cast<float4*>(out),    \
+                                                  dev_status)
+  if (k <= 1) MOE_COMBINE_CASE(1);
+  else if (k <= 2) MOE_COMBINE_CASE(2);
+  else if (k <= 4) MOE_COMBINE_CASE(4);
+  else if (k <= 8) MOE_COMBINE_CASE(8);
+  else MOE_COMBINE_CASE(16);
+#undef MOE_COMBINE_CASE
   return launch_status();
 }

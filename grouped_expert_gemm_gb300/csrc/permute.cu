@@ -8,41 +8,45 @@
 // expert of capacity C keeps) takes routes in route id order.
 //
 // Three launches, no host synchronisation and no inter-block waiting:
-//   1. permute_hist   one block per tile of consecutive tokens: per-tile
-//                     expert histogram -> ws hist[tile][E]
-//   2. permute_scan   one block: per expert an exclusive scan over tiles (the
-//                     tile's first ordinal), admitted counts, offsets, drops
-//   3. permute_scatter one block per tile: stable in-tile ranks (warp sub-ranges
-//                     in order, __match_any_sync + popc within 32 routes),
-//                     ordinal -> row, both maps, then a token-major row copy
-//                     that reads every token row once and writes its admitted
-//                     copies with 16-byte accesses.
+//   1. permute_hist  one block per tile of consecutive routes (at most 128
+//                    tiles): per-tile expert histogram -> ws hist[tile][E].
+//   2. permute_rank  one block per tile.  Each block reads the whole (small)
+//                    histogram matrix with independent loads to get its tile's
+//                    first ordinal per expert and every expert's total, hence
+//                    the admitted counts and the offsets (block 0 writes them);
+//                    then stable in-tile ranks (warp sub-ranges in route order,
+//                    __match_any_sync + popc within 32 routes) give each route
+//                    its ordinal, its row and both maps.
+//   3. permute_copy  token-major row copy over many blocks: every token row is
+//                    read once and written to its admitted rows with 16-byte
+//                    accesses.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kPermThreads = 256;
-constexpr int kPermWarps = kPermThreads / 32;
-constexpr int kMaxTileRoutes = 4096;
+constexpr int kHistThreads = 256;
+constexpr int kRankThreads = 512;  // one thread per expert (E <= 512)
+constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kMinTileRoutes = 2048;
+constexpr int kMaxTiles = 128;
+constexpr int kCopyThreads = 256;
 
 struct PermTiling {
-  int tokens_per_tile;
+  int routes_per_tile;
   int n_tiles;
 };
 
-PermTiling permute_tiling(int T, int k) {
+PermTiling permute_tiling(int64_t R) {
   PermTiling p;
-  // Aim for about two tiles per SM so the row copy fills the GPU.
-  int64_t tpt = ceil_div(T, 2 * 152);
-  if (tpt < 1) tpt = 1;
-  if (tpt * k > kMaxTileRoutes) tpt = kMaxTileRoutes / k;
-  p.tokens_per_tile = static_cast<int>(tpt);
-  p.n_tiles = static_cast<int>(ceil_div(T, tpt));
+  int64_t rpt = ceil_div(R, kMaxTiles);
+  if (rpt < kMinTileRoutes) rpt = kMinTileRoutes;
+  p.routes_per_tile = static_cast<int>(rpt);
+  p.n_tiles = R > 0 ? static_cast<int>(ceil_div(R, rpt)) : 0;
   return p;
 }
 
-__global__ void __launch_bounds__(kPermThreads)
+__global__ void __launch_bounds__(kHistThreads)
 permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
              int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];  // [E]
@@ -61,33 +65,42 @@ permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
   for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = sh[e];
 }
 
-__global__ void __launch_bounds__(512)
-permute_scan(int R, int E, int n_tiles, int capacity, int32_t* __restrict__ hist,
+__global__ void __launch_bounds__(kRankThreads)
+permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
+             const int32_t* __restrict__ ids, const int32_t* __restrict__ hist,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-             int32_t* __restrict__ n_dropped) {
-  __shared__ int32_t warp_tot[16];
+             int32_t* __restrict__ n_dropped, int32_t* __restrict__ row_to_route,
+             int32_t* __restrict__ route_to_row) {
+  extern __shared__ int32_t sh[];
+  int32_t* cnt = sh;                    // [kRankWarps][E]
+  int32_t* off = cnt + kRankWarps * E;  // [E]
+  __shared__ int32_t warp_tot[kRankWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int tile = blockIdx.x;
+
+  // 1. this tile's first ordinal per expert, every expert's total, admitted counts
   const int e = threadIdx.x;
-  int32_t run = 0;
+  int32_t base = 0, total = 0;
   if (e < E) {
     int t = 0;
-    for (; t + 4 <= n_tiles; t += 4) {
-      const int64_t b = static_cast<int64_t>(t) * E + e;
-      const int32_t v0 = hist[b], v1 = hist[b + E], v2 = hist[b + 2 * E], v3 = hist[b + 3 * E];
-      hist[b] = run; run += v0;
-      hist[b + E] = run; run += v1;
-      hist[b + 2 * E] = run; run += v2;
-      hist[b + 3 * E] = run; run += v3;
+    for (; t + 8 <= n_tiles; t += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(hist + static_cast<int64_t>(t + i) * E + e);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        base += (t + i < tile) ? v[i] : 0;
+        total += v[i];
+      }
     }
     for (; t < n_tiles; ++t) {
-      const int64_t b = static_cast<int64_t>(t) * E + e;
-      const int32_t v = hist[b];
-      hist[b] = run;
-      run += v;
+      const int32_t v = __ldg(hist + static_cast<int64_t>(t) * E + e);
+      base += (t < tile) ? v : 0;
+      total += v;
     }
   }
-  const int32_t c = (e < E) ? (capacity < 0 ? run : min(run, capacity)) : 0;
-  // Block-wide exclusive scan of c over experts.
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int32_t c = (e < E) ? (capacity < 0 ? total : min(total, capacity)) : 0;
+  // 2. offsets: block-wide exclusive scan of the admitted counts
   int32_t incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -95,92 +108,91 @@ permute_scan(int R, int E, int n_tiles, int capacity, int32_t* __restrict__ hist
     if (lane >= o) incl += v;
   }
   if (lane == 31) warp_tot[w] = incl;
+  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   int32_t before = 0;
   for (int i = 0; i < w; ++i) before += warp_tot[i];
   if (e < E) {
-    counts[e] = c;
-    offsets[e] = before + incl - c;
+    off[e] = before + incl - c;
+    if (tile == 0) {
+      counts[e] = c;
+      offsets[e] = before + incl - c;
+      if (e == E - 1) {
+        offsets[E] = before + incl;
+        *n_dropped = R - (before + incl);
+      }
+    }
   }
-  if (e == E - 1) {
-    offsets[E] = before + incl;
-    *n_dropped = R - (before + incl);
-  }
-}
-
-__global__ void __launch_bounds__(kPermThreads)
-permute_scatter(int T, int d, int E, int k, int tokens_per_tile, int capacity,
-                const int32_t* __restrict__ ids, const int32_t* __restrict__ tile_base,
-                const int32_t* __restrict__ offsets, const uint4* __restrict__ x,
-                uint4* __restrict__ x_perm, int32_t* __restrict__ row_to_route,
-                int32_t* __restrict__ route_to_row) {
-  extern __shared__ int32_t sh[];
-  int32_t* cnt = sh;                        // [kPermWarps][E]
-  int32_t* off = cnt + kPermWarps * E;      // [E]
-  int32_t* rows = off + E;                  // [routes in tile]
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * tokens_per_tile;
-  const int t1 = min(T, t0 + tokens_per_tile);
-  const int r0 = t0 * k, r1 = t1 * k, nr = r1 - r0;
-  const int sub = (nr + kPermWarps - 1) / kPermWarps;
+  const int r0 = tile * routes_per_tile;
+  const int r1 = min(R, r0 + routes_per_tile);
+  const int sub = (r1 - r0 + kRankWarps - 1) / kRankWarps;
   const int s0 = r0 + w * sub, s1 = min(r1, s0 + sub);
-
-  for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) cnt[i] = 0;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) off[e] = __ldg(offsets + e);
-  __syncthreads();
-  // 1. per-warp expert counts of the warp's contiguous sub-range
+  // 3. per-warp expert counts of the warp's contiguous sub-range
   for (int r = s0 + lane; r < s1; r += 32) {
-    const int e = __ldg(ids + r);
-    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
+    const int ee = __ldg(ids + r);
+    if (ee >= 0 && ee < E) atomicAdd(&cnt[w * E + ee], 1);
   }
   __syncthreads();
-  // 2. turn counts into each warp's first ordinal: tile base + earlier warps
-  const int32_t* base = tile_base + static_cast<int64_t>(blockIdx.x) * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = __ldg(base + e);
-    for (int ww = 0; ww < kPermWarps; ++ww) {
+  // 4. each warp's first ordinal per expert: tile base + earlier warps
+  if (e < E) {
+    int32_t run = base;
+    for (int ww = 0; ww < kRankWarps; ++ww) {
       const int32_t v = cnt[ww * E + e];
       cnt[ww * E + e] = run;
       run += v;
     }
   }
   __syncthreads();
-  // 3. stable ranks, 32 routes at a time in route order
+  // 5. stable ranks, 32 routes at a time in route order
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int c0 = s0; c0 < s1; c0 += 32) {
     const int r = c0 + lane;
-    int e = -1;
+    int ee = -1;
     if (r < s1) {
-      e = __ldg(ids + r);
-      if (e < 0 || e >= E) e = -2;  // invalid id: its own group, never admitted
+      ee = __ldg(ids + r);
+      if (ee < 0 || ee >= E) ee = -2;  // invalid id: its own group, never admitted
     }
-    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ee);
     int32_t ordinal = 0;
-    if (e >= 0) ordinal = cnt[w * E + e] + __popc(peers & lt_mask);
+    if (ee >= 0) ordinal = cnt[w * E + ee] + __popc(peers & lt_mask);
     __syncwarp();
-    if (e >= 0 && (peers & lt_mask) == 0) cnt[w * E + e] += __popc(peers);
+    if (ee >= 0 && (peers & lt_mask) == 0) cnt[w * E + ee] += __popc(peers);
     __syncwarp();
     if (r < s1) {
       int32_t row = -1;
-      if (e >= 0 && (capacity < 0 || ordinal < capacity)) {
-        row = off[e] + ordinal;
+      if (ee >= 0 && (capacity < 0 || ordinal < capacity)) {
+        row = off[ee] + ordinal;
         row_to_route[row] = r;
       }
       route_to_row[r] = row;
-      rows[r - r0] = row;
     }
   }
-  __syncthreads();
-  // 4. token-major row copy: each token row is read once
-  const int chunks = d >> 3;  // 16-byte chunks per row
-  for (int t = t0 + w; t < t1; t += kPermWarps) {
+}
+
+// One warp per token: read the row once, store it to each admitted row.
+__global__ void __launch_bounds__(kCopyThreads)
+permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
+             const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+    const int32_t my_row = lane < k ? __ldg(route_to_row + static_cast<int64_t>(t) * k + lane) : -1;
     const uint4* src = x + static_cast<int64_t>(t) * chunks;
-    const int32_t* trow = rows + (t - t0) * k;
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 v = __ldg(src + c);
+    // The chunk loop runs uniformly over the warp (lanes past the row end only
+    // skip their accesses) because its body broadcasts rows with __shfl_sync.
+    for (int cb = 0; cb < chunks; cb += 32 * 4) {
+      const int c = cb + lane;
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < chunks) v[u] = __ldg(src + c + 32 * u);
       for (int j = 0; j < k; ++j) {
-        const int32_t row = trow[j];
-        if (row >= 0) x_perm[static_cast<int64_t>(row) * chunks + c] = v;
+        const int32_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+        if (row < 0) continue;
+        uint4* dst = x_perm + static_cast<int64_t>(row) * chunks;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + 32 * u < chunks) dst[c + 32 * u] = v[u];
       }
     }
   }
@@ -193,7 +205,7 @@ using namespace moe;
 
 MOE_API size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E) {
   if (T <= 0 || k <= 0 || E <= 0) return 256;
-  const PermTiling tl = permute_tiling(T, k);
+  const PermTiling tl = permute_tiling(static_cast<int64_t>(T) * k);
   Carver c;
   c.take<int32_t>(static_cast<size_t>(tl.n_tiles) * E);
   return c.off + 256;
@@ -215,24 +227,28 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
   if (ws_bytes < moe_permute_workspace_size(T, k, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = as_cuda(stream);
   const int R = T * k;
-  if (T == 0) {
-    // No routes: empty segments.  The scan kernel with zero tiles writes them.
-    permute_scan<<<1, 512, 0, s>>>(0, E, 0, capacity, nullptr, counts, offsets, n_dropped);
+  const PermTiling tl = permute_tiling(R);
+  int32_t* hist = static_cast<int32_t*>(ws);
+  const size_t rank_smem = (static_cast<size_t>(kRankWarps) * E + E) * sizeof(int32_t);
+  if (R == 0) {
+    // No routes: one rank block with no tiles writes empty counts and offsets.
+    permute_rank<<<1, kRankThreads, rank_smem, s>>>(0, E, 1, 0, capacity, topk_ids, hist, counts,
+                                                    offsets, n_dropped, row_to_route,
+                                                    route_to_row);
     return launch_status();
   }
-  const PermTiling tl = permute_tiling(T, k);
-  Carver c;
-  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
-                                             c.take<int32_t>(static_cast<size_t>(tl.n_tiles) * E));
-  const int rpt = tl.tokens_per_tile * k;
-  permute_hist<<<tl.n_tiles, kPermThreads, E * sizeof(int32_t), s>>>(R, E, rpt, topk_ids, hist,
-                                                                   dev_status);
-  permute_scan<<<1, 512, 0, s>>>(R, E, tl.n_tiles, capacity, hist, counts, offsets, n_dropped);
-  const size_t smem = (static_cast<size_t>(kPermWarps) * E + E + rpt) * sizeof(int32_t);
-  permute_scatter<<<tl.n_tiles, kPermThreads, smem, s>>>(
-      T, d, E, k, tl.tokens_per_tile, capacity, topk_ids, hist, offsets,
-      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_perm), row_to_route,
-      route_to_row);
+  permute_hist<<<tl.n_tiles, kHistThreads, E * sizeof(int32_t), s>>>(R, E, tl.routes_per_tile,
+                                                                    topk_ids, hist, dev_status);
+  permute_rank<<<tl.n_tiles, kRankThreads, rank_smem, s>>>(R, E, tl.routes_per_tile, tl.n_tiles,
+                                                           capacity, topk_ids, hist, counts,
+                                                           offsets, n_dropped, row_to_route,
+                                                           route_to_row);
+  const int warps = kCopyThreads / 32;
+  int64_t blocks = ceil_div(T, warps);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  permute_copy<<<static_cast<unsigned>(blocks), kCopyThreads, 0, s>>>(
+      T, k, d / 8, route_to_row, reinterpret_cast<const uint4*>(x),
+      reinterpret_cast<uint4*>(x_perm));
   return launch_status();
 }
 
@@ -252,7 +268,7 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
 namespace moe {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+constexpr size_t kStaticScratchBytes = size_t(64) << 10;  // 64 KiB
 static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;

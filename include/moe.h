@@ -150,11 +150,12 @@ moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capac
  * runtime's plugin hook that may only enqueue on the stream it is handed, or a
  * latency-critical loop where an allocation could synchronise the device.
  * Same arguments, outputs, limits and errors as moe_permute minus the
- * workspace: the per-tile histogram lives in a 1 MiB file-scope device array
+ * workspace: the per-tile histogram lives in a 64 KiB file-scope device array
  * of the library, which every GPU that loads the library holds until the
- * process exits.  Sizes whose moe_permute_workspace_size(T,k,E) exceeds 1 MiB
- * are rejected with MOE_ERR_UNSUPPORTED (for E = 512 that is beyond about
- * 2 million routes T*k).  Nothing is allocated or freed.
+ * process exits.  Sizes whose moe_permute_workspace_size(T,k,E) exceeds 64 KiB
+ * are rejected with MOE_ERR_UNSUPPORTED before anything is enqueued: beyond
+ * 63,488 routes T*k for E = 512, 129,024 for E = 256, 260,096 for E = 128;
+ * up to E = 127 every size fits.  Nothing is allocated or freed.
  * The first call on a device looks up the array's device address for that
  * device (cudaGetSymbolAddress, with the device current); make that first call
  * before any stream capture.  Every call on a device shares the one array and

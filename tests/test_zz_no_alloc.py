@@ -78,9 +78,9 @@ def test_noalloc_matches_permute_on_two_calls_in_a_row(lib, T, d, E, k, cap):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
-    # T*k*E large enough that the per-tile histogram would not fit the 1 MiB array
+    # T*k*E large enough that the per-tile histogram would not fit the 64 KiB array
     T, k, E = 400000, 16, 512
-    assert lib.moe_permute_workspace_size(T, k, E) > (1 << 20)
+    assert lib.moe_permute_workspace_size(T, k, E) > (64 << 10)
     null = ctypes.c_void_p(16)
     st = lib.moe_permute_noalloc(T, 64, E, k, -1, null, null, null, null, null, null, null, null,
                                  None, None)
