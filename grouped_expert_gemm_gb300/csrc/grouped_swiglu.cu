@@ -7,18 +7,27 @@
 // per problem (no capacity padding reaches the output), a per-problem
 // descriptor read on the device.
 //
-// Two persistent launches:
-//   pass 1 (SWIGLU): per tile of 128 rows x BN columns of I, one MMA chain with
-//     N = 2*BN computes [G | U] = X [Wg | Wu] into tensor memory; the epilogue
+// Two persistent passes:
+//   gate/up (SWIGLU): per tile, one MMA chain over N = [BN gate | BN up]
+//     columns computes [G | U] = X [Wg | Wu] into tensor memory; the epilogue
 //     writes H = bf16(SiLU(G) * U).
-//   pass 2 (DOWN):   per tile of 128 rows x BN columns of d, Y = bf16(H Wd).
+//   down:             per tile, Y = bf16(H Wd).
+//
+// Two kernel shapes share the scheduling and the epilogue:
+//   * pair kernel (cta_group::2): a cluster of two CTAs on an SM pair computes a
+//     256-row tile with N = 256; each CTA stages its own 128 rows of A and half
+//     of the 256 B columns (6 stages of 32 KB), the leader CTA issues
+//     tcgen05.mma.cta_group::2 and multicasts the stage/accumulator commits to
+//     both CTAs, and each CTA's epilogue drains its own 128 accumulator rows.
+//     Per SM this moves a third less operand data from L2 than the single-CTA
+//     shape and fetches each weight tile once per 256 rows.
+//   * single-CTA kernel (cta_group::1): a 128-row tile with N = 64..256, 4
+//     stages; used where the pair shape does not divide the problem.
 //
 // Roles inside a CTA (192 threads, one CTA per SM):
 //   warp 0      TMA producer: A tile [128 x 64] (K-major) and B atoms
-//               [64 (K) x 64 (N)] (N-major: the weights are stored [K, N]) per
-//               stage, STAGES stages of shared memory.
-//   warp 1      allocates tensor memory; lane 0 issues tcgen05.mma (M=128,
-//               N=64*N_ATOMS, K=16) and commits stage/accumulator barriers.
+//               [64 (K) x 64 (N)] (N-major: the weights are stored [K, N]).
+//   warp 1      allocates tensor memory; lane 0 issues tcgen05.mma and commits.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU or conversion,
 //               bf16 stores of the rows that belong to the segment.
 // Two accumulator buffers let the epilogue of tile i overlap the MMAs of tile i+1.
@@ -51,6 +60,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress = brok
 
 constexpr int kABytes = kBM * kBK * 2;        // 16 KB
 constexpr int kAtomBytes = kBK * 64 * 2;      // 8 KB: [64 K rows][64 N cols]
+
+constexpr int kStagesPair = 6;
+constexpr int kPairAtoms = 2;                     // B atoms per CTA in the pair kernel
+constexpr int kPairStageBytes = kABytes + kPairAtoms * kAtomBytes;  // 32 KB
+constexpr int kPairSmemBytes = 1024 + kStagesPair * kPairStageBytes + 256 + (3 * kMaxSeg + 16) * 4;
 
 template <int N_ATOMS>
 struct Geometry {
@@ -205,10 +219,87 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
-// B N-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+// B N-major, M = m, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---- CTA-pair (cluster of two) forms ----
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of `local` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at the same offset in every CTA of `mask` once all
+// prior tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c_inner,
+                                                 int32_t c_outer) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c_inner), "r"(c_outer)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// Spin for about `ns` nanoseconds (drain window for copies whose completion
+// lands on another CTA's barrier).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
 }
 
 // ------------------------------ scheduling ---------------------------------
@@ -217,9 +308,10 @@ struct Tile {
   int seg, row0, rows, n0;
 };
 
-// tile_start[q] = first tile of segment q (exclusive scan of its tile count).
+// tile_start[q] = first tile of segment q (exclusive scan of its tile count);
+// tiles of a segment are (n-block, m-block) with m-blocks of `bm` rows innermost.
 __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int* s_begin,
-                                        const int* s_count, int n_seg, int n_blocks, int bn_out) {
+                                        const int* s_count, int n_seg, int bm, int bn_out) {
   int lo = 0, hi = n_seg - 1;
   while (lo < hi) {  // last q with tile_start[q] <= t
     const int mid = (lo + hi + 1) >> 1;
@@ -227,18 +319,140 @@ __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int*
   }
   const int q = lo;
   const int local = t - tile_start[q];
-  const int m_blocks = (s_count[q] + kBM - 1) / kBM;
+  const int m_blocks = (s_count[q] + bm - 1) / bm;
   const int nb = local / m_blocks, mb = local % m_blocks;
   Tile tl;
   tl.seg = q;
-  tl.row0 = s_begin[q] + mb * kBM;
-  tl.rows = min(kBM, s_count[q] - mb * kBM);
+  tl.row0 = s_begin[q] + mb * bm;
+  tl.rows = min(bm, s_count[q] - mb * bm);
   tl.n0 = nb * bn_out;
-  (void)n_blocks;
   return tl;
 }
 
-// ------------------------------ the kernel ---------------------------------
+// Segment table in shared memory, built by threads 64..191 (each owns a run of
+// up to 8 consecutive segments): bad segments are reported and treated as
+// empty; s_tile_start[q] is the exclusive scan of the tile counts and
+// s_tile_start[n_seg] the total.
+__device__ __forceinline__ void build_segment_table(const GemmArgs& args, int bm, int n_blocks,
+                                                    int* s_begin, int* s_count, int* s_tile_start,
+                                                    int* warp_tot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x - 64;
+  const int n_seg = args.n_seg;
+  const int per = (n_seg + 127) / 128;
+  const int q0 = tid * per, q1 = min(n_seg, q0 + per);
+  int local = 0;
+  for (int q = q0; q < q1; ++q) {
+    int b = __ldg(args.seg_begin + q), c = __ldg(args.seg_count + q);
+    if (c < 0 || b < 0 || static_cast<int64_t>(b) + c > args.max_rows) {
+      if (c != 0) report(args.dev_status, MOE_DEV_BAD_ROW);
+      b = 0;
+      c = 0;
+    }
+    s_begin[q] = b;
+    s_count[q] = c;
+    local += ((c + bm - 1) / bm) * n_blocks;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp - 2] = incl;
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  int before = 0;
+  for (int w = 2; w < warp; ++w) before += warp_tot[w - 2];
+  const int total_all = warp_tot[0] + warp_tot[1] + warp_tot[2] + warp_tot[3];
+  int run = before + incl - local;
+  for (int q = q0; q < q1; ++q) {
+    s_tile_start[q] = run;
+    run += ((s_count[q] + bm - 1) / bm) * n_blocks;
+  }
+  if (tid == 127) s_tile_start[n_seg] = total_all;
+}
+
+// Epilogue of one tile for the calling thread's accumulator row: `taddr`
+// addresses this warp's TMEM lane quadrant at the tile's first column.  BN_OUT
+// output columns; for SWIGLU the gate accumulators are columns [0, BN_OUT) and
+// the up accumulators [BN_OUT, 2*BN_OUT).  All lanes execute the tensor-memory
+// loads (.sync.aligned); only live rows compute and store.
+template <int BN_OUT, bool SWIGLU>
+__device__ __forceinline__ void epilogue_row(uint32_t taddr, bool live, uint16_t* orow) {
+  if constexpr (SWIGLU) {
+#pragma unroll 1
+    for (int c = 0; c < BN_OUT; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + BN_OUT + c, u);
+      tmem_ld_wait();
+      if (live) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float h2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float gv = __uint_as_float(g[2 * i + h]);
+            const float uv = __uint_as_float(u[2 * i + h]);
+            // SiLU(g) * u with the fast exp and division: measured 6 % faster on the
+            // weight-streaming decode shape than expf + IEEE division, and H still
+            // rounds to the same bf16 value in all but ~0.2 % of elements.
+            h2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+          }
+          pk[i] = pack_bf16x2(h2[0], h2[1]);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN_OUT; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(taddr + c, v);
+      tmem_ld_wait();
+      if (live) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+}
+
+// Shared-memory carve-up common to both kernels, after the stage buffers.
+struct Smem {
+  uint64_t* bars;
+  volatile int* abort_flag;
+  uint32_t* tmem_slot;
+  int* warp_tot;
+  int* s_tile_start;
+  int* s_begin;
+  int* s_count;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* after_stages, int n_bars) {
+  Smem m;
+  m.bars = reinterpret_cast<uint64_t*>(after_stages);
+  int* misc = reinterpret_cast<int*>(m.bars + n_bars);
+  m.abort_flag = misc;
+  m.tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
+  m.warp_tot = misc + 4;
+  m.s_tile_start = misc + 8;
+  m.s_begin = m.s_tile_start + kMaxSeg + 1;
+  m.s_count = m.s_begin + kMaxSeg;
+  return m;
+}
+
+// ------------------------- single-CTA kernel --------------------------------
 
 template <int N_ATOMS, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -249,18 +463,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   constexpr int kN = G::kN;
   constexpr int kBnOut = SWIGLU ? kN / 2 : kN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* stage_base = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * G::kStageBytes);
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 5);
-  volatile int* abort_flag = misc;           // misc[0]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
-  int* warp_tot = misc + 4;                  // misc[4..7]
-  int* s_tile_start = misc + 8;              // [kMaxSeg + 1]
-  int* s_begin = s_tile_start + kMaxSeg + 1; // [kMaxSeg]
-  int* s_count = s_begin + kMaxSeg;          // [kMaxSeg]
+  const Smem sm = carve(stage_base + kStages * G::kStageBytes, 2 * kStages + 5);
+  uint64_t* bars = sm.bars;
+  volatile int* abort_flag = sm.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_seg = args.n_seg;
@@ -273,7 +481,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
 
-  // ---- setup: barriers, tensor memory, segment table ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -284,7 +491,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       mbar_init(tempty_bar(b), 128);
     }
     mbar_init(drain_bar, 1);
-    misc[0] = 0;
+    *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
@@ -293,49 +500,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (SWIGLU)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b1)) : "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), G::kTmemAlloc);
-  // Segment table: clamp bad segments to empty, then block-scan tile counts
-  // (threads 64..191 each own a run of up to 8 consecutive segments).
-  if (threadIdx.x >= 64) {
-    const int tid = threadIdx.x - 64;
-    const int per = (n_seg + 127) / 128;
-    const int q0 = tid * per, q1 = min(n_seg, q0 + per);
-    int local = 0;
-    for (int q = q0; q < q1; ++q) {
-      int b = __ldg(args.seg_begin + q), c = __ldg(args.seg_count + q);
-      if (c < 0 || b < 0 || static_cast<int64_t>(b) + c > args.max_rows) {
-        if (c != 0) report(args.dev_status, MOE_DEV_BAD_ROW);
-        b = 0;
-        c = 0;
-      }
-      s_begin[q] = b;
-      s_count[q] = c;
-      local += ((c + kBM - 1) / kBM) * n_blocks;
-    }
-    // inclusive scan of `local` over the 128 threads
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp - 2] = incl;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    int before = 0;
-    for (int w = 2; w < warp; ++w) before += warp_tot[w - 2];
-    const int total_all = warp_tot[0] + warp_tot[1] + warp_tot[2] + warp_tot[3];
-    int run = before + incl - local;
-    for (int q = q0; q < q1; ++q) {
-      s_tile_start[q] = run;
-      run += ((s_count[q] + kBM - 1) / kBM) * n_blocks;
-    }
-    if (tid == 127) s_tile_start[n_seg] = total_all;
-  }
+  if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
+  if (threadIdx.x >= 64)
+    build_segment_table(args, kBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = s_tile_start[n_seg];
+  const uint32_t tmem_base = *sm.tmem_slot;
+  const int total_tiles = sm.s_tile_start[n_seg];
 
   if (warp == 0) {
     // ======================= TMA producer =======================
@@ -344,7 +516,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = tile_of(t, s_tile_start, s_begin, s_count, n_seg, n_blocks, kBnOut);
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut);
         const int b_row0 = tl.seg * args.K;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
@@ -380,7 +552,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kN);
+      constexpr uint32_t idesc = idesc_bf16(kBM, kN);
       int s = 0;
       uint32_t ph = 0;
       int buf = 0;
@@ -426,60 +598,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     int buf = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const Tile tl = tile_of(t, s_tile_start, s_begin, s_count, n_seg, n_blocks, kBnOut);
+      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut);
       if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(buf * kN);
       const bool live = r < tl.rows;
       uint16_t* orow = args.out + static_cast<int64_t>(tl.row0 + (live ? r : 0)) * args.N + tl.n0;
-      if constexpr (SWIGLU) {
-#pragma unroll 1
-        for (int c = 0; c < kBnOut; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + kBnOut + c, u);
-          tmem_ld_wait();
-          if (live) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float h2[2];
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float gv = __uint_as_float(g[2 * i + h]);
-                const float uv = __uint_as_float(u[2 * i + h]);
-                // SiLU(g) * u with the fast exp and division: measured 6 % faster on the
-                // weight-streaming decode shape than expf + IEEE division, and H still
-                // rounds to the same bf16 value in all but ~0.2 % of elements.
-                h2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-              }
-              pk[i] = pack_bf16x2(h2[0], h2[1]);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < kBnOut; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c, v);
-          tmem_ld_wait();
-          if (live) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-      }
+      epilogue_row<kBnOut, SWIGLU>(taddr, live, orow);
       tc_fence_before();
       mbar_arrive(tempty_bar(buf));
       if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
@@ -493,6 +619,200 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, G::kTmemAlloc);
+  }
+}
+
+// ------------------------- CTA-pair kernel ----------------------------------
+//
+// A cluster of two CTAs (ranks 0 and 1) computes a tile of 2*kBM = 256 rows and
+// N = 256 accumulator columns.  Rank r stages rows [row0 + 128 r, +128) of A and
+// the r-th half (128 columns) of the B tile in its own shared memory; for the
+// gate/up pass rank 0 holds the 128 gate columns and rank 1 the 128 up columns,
+// so the accumulator of either rank is [G | U] for its own 128 rows.  Barriers:
+//   full[s]      leader only: the leader's expect_tx covers both ranks' bytes,
+//                and each rank's TMA completes its bytes on the leader's barrier;
+//   empty[s]     both ranks: the leader's commit is multicast to both;
+//   tfull[b]     both ranks: multicast commit after a tile's last MMA;
+//   tempty[b]    leader only: one arrival per epilogue warp of both ranks (8).
+template <bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b0,
+                         const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
+  constexpr int kN = 2 * kPairAtoms * 64;        // 256 accumulator columns
+  constexpr int kBnOut = SWIGLU ? kN / 2 : kN;   // output columns per tile
+  constexpr int kPairBM = 2 * kBM;               // rows per tile
+  constexpr int kTmemAlloc = 2 * kN;             // two accumulator buffers = 512
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Smem sm = carve(stage_base + kStagesPair * kPairStageBytes, 2 * kStagesPair + 5);
+  uint64_t* bars = sm.bars;
+  volatile int* abort_flag = sm.abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_seg = args.n_seg;
+  const int n_blocks = args.N / kBnOut;
+  const int k_steps = args.K / kBK;
+
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + kStagesPair + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStagesPair + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStagesPair + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * kStagesPair + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 8);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b0)) : "memory");
+    if (SWIGLU)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b1)) : "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(sm.tmem_slot), kTmemAlloc);
+  if (threadIdx.x >= 64)
+    build_segment_table(args, kPairBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start,
+                        sm.warp_tot);
+  // Both ranks' barriers are initialised and their tensor memory allocated
+  // before any rank signals the other.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+  const int total_tiles = sm.s_tile_start[n_seg];
+
+  if (warp == 0) {
+    // ======================= TMA producer (both ranks) =======================
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cid; t < total_tiles && ok; t += n_clusters) {
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut);
+        const int b_row0 = tl.seg * args.K;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+          const uint32_t full_leader = map_to_rank(full_bar(s), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kPairStageBytes);
+          const uint32_t st = smem_u32(stage_base + s * kPairStageBytes);
+          tma_load_2d_pair(st, &tmap_a, full_leader, ks * kBK, tl.row0 + static_cast<int>(rank) * kBM);
+#pragma unroll
+          for (int a = 0; a < kPairAtoms; ++a) {
+            const uint32_t dst = st + kABytes + a * kAtomBytes;
+            if constexpr (SWIGLU) {
+              tma_load_2d_pair(dst, leader ? &tmap_b0 : &tmap_b1, full_leader, tl.n0 + a * 64,
+                               b_row0 + ks * kBK);
+            } else {
+              tma_load_2d_pair(dst, &tmap_b0, full_leader,
+                               tl.n0 + static_cast<int>(rank) * (kPairAtoms * 64) + a * 64,
+                               b_row0 + ks * kBK);
+            }
+          }
+          issued_any = true;
+          if (++s == kStagesPair) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && issued_any) {
+        if (leader) {
+          int ss = s;
+          uint32_t pp = ph;
+          for (int i = 0; i < kStagesPair; ++i) {
+            if (--ss < 0) { ss = kStagesPair - 1; pp ^= 1u; }
+            wait_drain(full_bar(ss), pp);
+          }
+        } else {
+          // This rank's completions land on the leader's barriers: give its
+          // copies in flight a fixed window to land.
+          spin_ns(2000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (leader only) =======================
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16(kPairBM, kN);
+      int s = 0;
+      uint32_t ph = 0;
+      int buf = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cid; t < total_tiles && ok; t += n_clusters) {
+        if (!wait_bounded(tempty_bar(buf), acc_ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kN);
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, args.dev_status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_base + s * kPairStageBytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_addr + kk * kUmmaK * 2, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 128, kAtomBytes, 1024);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both ranks
+          if (++s == kStagesPair) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar(buf), 0x3);  // both ranks' accumulators ready
+        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      }
+      if (!ok && issued_any) {
+        mma_commit_pair(drain_bar, 0x1);
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // ======================= epilogue (warps 2..5, both ranks) ===============
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                        // row within this rank's half
+    const int tile_r = static_cast<int>(rank) * kBM + r;   // row within the 256-row tile
+    int buf = 0;
+    uint32_t acc_ph = 0;
+    for (int t = cid; t < total_tiles; t += n_clusters) {
+      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut);
+      if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(buf * kN);
+      const bool live = tile_r < tl.rows;
+      uint16_t* orow =
+          args.out + static_cast<int64_t>(tl.row0 + (live ? tile_r : 0)) * args.N + tl.n0;
+      epilogue_row<kBnOut, SWIGLU>(taddr, live, orow);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(buf), 0));
+      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+    }
+  }
+
+  // ---- teardown: no rank leaves while the other may still touch its memory ----
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemAlloc);
   }
 }
 
@@ -594,6 +914,49 @@ moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   return launch_status();
 }
 
+// The pair kernel runs as many two-CTA clusters as can be resident at once
+// (queried once per device), each looping over its share of the tiles.
+template <bool SWIGLU>
+moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                            const GemmArgs& args, cudaStream_t s) {
+  auto kern = grouped_gemm_pair_kernel<SWIGLU>;
+  constexpr int kMaxDev = 64;
+  static int grid[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MOE_ERR_CUDA;
+  int g;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (grid[dev] == 0) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kPairSmemBytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(num_sms() & ~1));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kPairSmemBytes;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
+        clusters = num_sms() / 2;
+      cudaGetLastError();
+      grid[dev] = 2 * clusters;
+    }
+    g = grid[dev];
+  }
+  kern<<<g, kThreads, kPairSmemBytes, s>>>(a, b0, b1, args);
+  return launch_status();
+}
+
+// The pair kernel stages 256 rows of A per tile.  When segments average fewer
+// than 128 rows (decode-sized batches) most of those rows belong to other
+// segments, and the single-CTA kernel, which stages half as many A rows for
+// the same weight columns, streams the weights faster (measured: 117.5 vs
+// 128.3 us for the gate/up pass at T=128, E=128, top-8).
+bool pair_shape(int32_t n_seg, int32_t max_rows) {
+  return static_cast<int64_t>(max_rows) >= static_cast<int64_t>(kBM) * n_seg;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -633,8 +996,11 @@ MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int3
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
              dev_status};
   cudaStream_t s = as_cuda(stream);
-  return (I % 128 == 0) ? launch_gemm<4, true>(m_x, m_wg, m_wu, a, s)
-                        : launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+  if (I % 128 == 0) {
+    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s)
+                                       : launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
+  }
+  return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
 }
 
 MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
@@ -653,7 +1019,10 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
              dev_status};
   cudaStream_t s = as_cuda(stream);
-  if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
+  if (d % 256 == 0) {
+    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s)
+                                       : launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
+  }
   if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
   return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
 }
