@@ -48,6 +48,8 @@ def parse_args():
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
                          "a smaller T for short profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -261,6 +263,21 @@ def build_layer(w, device):
     return layer, logits, sel_bias, x
 
 
+_LIBCUDA = None
+
+
+def record_external(ev, stream):
+    """Record `ev` on `stream` as an event node of the graph being captured (an external
+    event record, so it keeps a timestamp on every replay)."""
+    global _LIBCUDA
+    if _LIBCUDA is None:
+        _LIBCUDA = ctypes.CDLL("libcuda.so.1")
+        _LIBCUDA.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    r = _LIBCUDA.cuEventRecordWithFlags(ev.cuda_event, stream.cuda_stream, 1)  # ..._EXTERNAL
+    if r != 0:
+        raise RuntimeError(f"cuEventRecordWithFlags failed ({r})")
+
+
 def run_ours(args, dist, w):
     import grouped_expert_gemm_gb300 as g
     from grouped_expert_gemm_gb300 import abi, build
@@ -271,6 +288,7 @@ def run_ours(args, dist, w):
     layer, logits, sel_bias, x = build_layer(w, device)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
+    names = [n for n, _ in stages]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             for _, fn in stages:
@@ -279,10 +297,33 @@ def run_ours(args, dist, w):
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after warm-up")
 
-    # timed region: K whole steps, with an event after every stage
-    names = [n for n, _ in stages]
-    n_ev = len(stages) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    # An event after every stage of every step, inside the timed region.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+           for _ in range(steps)]
+    use_graph = not args.no_graph
+    graph = None
+    if use_graph:
+        # The K timed steps as one CUDA graph (every call is asynchronous and
+        # allocation-free), with the stage events as external event nodes.
+        for row in evs:
+            for e in row:
+                e.record(stream)  # creates the event objects
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        l0 = abi.launch_count()
+        with torch.cuda.graph(graph, stream=stream):
+            cur = torch.cuda.current_stream()
+            for s in range(steps):
+                record_external(evs[s][0], cur)
+                for i, (_, fn) in enumerate(stages):
+                    fn(None)
+                    record_external(evs[s][i + 1], cur)
+        graph_launches = abi.launch_count() - l0
+        with torch.cuda.stream(stream):
+            graph.replay()  # warm replay (untimed)
+        stream.synchronize()
+
+    # timed region: K whole steps
     launches0 = abi.launch_count()
     sampler = ClockSampler(dist.local)
     dist.barrier()
@@ -291,29 +332,30 @@ def run_ours(args, dist, w):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for s in range(steps):
-            evs[s][0].record(stream)
-            for i, (_, fn) in enumerate(stages):
-                fn(stream)
-                evs[s][i + 1].record(stream)
+        with torch.cuda.stream(stream):
+            if use_graph:
+                graph.replay()
+            else:
+                for s in range(steps):
+                    evs[s][0].record(stream)
+                    for i, (_, fn) in enumerate(stages):
+                        fn(stream)
+                        evs[s][i + 1].record(stream)
         t_end.record(stream)
         stream.synchronize()
     torch.cuda.synchronize(device)
     dist.barrier()
-    launches = abi.launch_count() - launches0
+    launches = graph_launches if use_graph else (abi.launch_count() - launches0)
     elapsed_ms = t_start.elapsed_time(t_end)
     max_ms = dist.max(elapsed_ms)
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after timed steps")
 
-    # per-stage device time (same stage name summed within a step)
     stage_ms = {}
     for s in range(steps):
         for i, n in enumerate(names):
             stage_ms[n] = stage_ms.get(n, 0.0) + evs[s][i].elapsed_time(evs[s][i + 1])
-    launches_per_step = {n: 0 for n in names}
-    for n in names:
-        launches_per_step[n] += 1
+    per_step = {n: names.count(n) for n in names}
     step_ms = max_ms / steps
     value = dist.world * w.T * steps / (max_ms / 1e3)
 
@@ -321,17 +363,16 @@ def run_ours(args, dist, w):
     if w.pooled:
         acc_rows = int(layer.local_counts.sum().item())  # last wave's rows (per-wave unit)
         counts = layer.local_counts.cpu().numpy()
-        I, d = w.I, w.d
     else:
         acc_rows = int(layer.offsets[-1].item())
         counts = layer.counts.cpu().numpy()
-        I, d = w.I, w.d
+    I, d = w.I, w.d
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
     long_region = max_ms > 2000.0
     tf_peak = tf_sust if long_region else tf_burst
     per_stage = {}
     for n in stage_ms:
-        per_launch_ms = stage_ms[n] / (steps * launches_per_step[n])
+        per_launch_ms = stage_ms[n] / (steps * per_step[n])
         b, f = stage_work(w, layer, n, counts, acc_rows, w.E, I, d)
         t_hbm = b / (hbm * 1e9)
         t_tc = f / (tf_peak * 1e12) if f else 0.0
@@ -360,11 +401,15 @@ def run_ours(args, dist, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the workload, random-init expert weights)",
         "config": config_dict(w, layer),
-        "roofline": roofline, "stages": per_stage, "clocks": sampler.summary(),
+        "roofline": roofline, "stages": per_stage,
+        "timing": ("the K steps replayed from one captured CUDA graph" if use_graph else
+                   "eager launches") + "; stage times from CUDA events between the stages of "
+                   "every timed step, on the launching stream",
+        "clocks": sampler.summary(),
         "gpu_launches": int(launches),
     }
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps)
+        result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph)
     return result, layer, logits, sel_bias, x
 
 
@@ -389,7 +434,7 @@ def config_dict(w, layer):
     return c
 
 
-def run_e2e(args, dist, w, layer, logits, x, stream, steps):
+def run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph):
     """Same metric through the host-buffer API: H2D of the step's inputs, the layer,
     D2H of the fp32 result, every step, all inside the timed region."""
     lh = logits.cpu().pin_memory()
@@ -398,13 +443,26 @@ def run_e2e(args, dist, w, layer, logits, x, stream, steps):
     for _ in range(max(args.warmup, 3)):
         layer.forward_host(lh, xh, oh, stream)
     stream.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layer.forward_host(lh, xh, oh, None)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        stream.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        layer.forward_host(lh, xh, oh, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            if use_graph:
+                graph.replay()
+            else:
+                layer.forward_host(lh, xh, oh, stream)
     b.record(stream)
     stream.synchronize()
     dist.barrier()

@@ -85,6 +85,7 @@ struct GemmArgs {
   int max_rows;
   uint16_t* out; // [max_rows, N] bf16 bits
   uint32_t* dev_status;
+  int m_outer;   // tile order inside a segment: 0 = n-block outer, 1 = m-block outer
 };
 
 // ------------------------------ PTX wrappers -------------------------------
@@ -308,10 +309,14 @@ struct Tile {
   int seg, row0, rows, n0;
 };
 
-// tile_start[q] = first tile of segment q (exclusive scan of its tile count);
-// tiles of a segment are (n-block, m-block) with m-blocks of `bm` rows innermost.
+// tile_start[q] = first tile of segment q (exclusive scan of its tile count).
+// Inside a segment the tiles run n-block outer / m-block inner (neighbouring
+// CTAs share one weight tile and walk the segment's rows), or, with m_outer,
+// m-block outer / n-block inner (neighbouring CTAs share one block of rows and
+// walk the expert's weight columns).  m-blocks have `bm` rows.
 __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int* s_begin,
-                                        const int* s_count, int n_seg, int bm, int bn_out) {
+                                        const int* s_count, int n_seg, int bm, int bn_out,
+                                        int n_blocks, int m_outer) {
   int lo = 0, hi = n_seg - 1;
   while (lo < hi) {  // last q with tile_start[q] <= t
     const int mid = (lo + hi + 1) >> 1;
@@ -320,7 +325,8 @@ __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int*
   const int q = lo;
   const int local = t - tile_start[q];
   const int m_blocks = (s_count[q] + bm - 1) / bm;
-  const int nb = local / m_blocks, mb = local % m_blocks;
+  const int nb = m_outer ? local % n_blocks : local / m_blocks;
+  const int mb = m_outer ? local / n_blocks : local % m_blocks;
   Tile tl;
   tl.seg = q;
   tl.row0 = s_begin[q] + mb * bm;
@@ -516,7 +522,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut);
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut, n_blocks,
+                              args.m_outer);
         const int b_row0 = tl.seg * args.K;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
@@ -598,7 +605,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     int buf = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut);
+      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut, n_blocks,
+                              args.m_outer);
       if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
@@ -704,7 +712,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
       bool ok = true;
       bool issued_any = false;
       for (int t = cid; t < total_tiles && ok; t += n_clusters) {
-        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut);
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut,
+                              n_blocks, args.m_outer);
         const int b_row0 = tl.seg * args.K;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
@@ -789,7 +798,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     int buf = 0;
     uint32_t acc_ph = 0;
     for (int t = cid; t < total_tiles; t += n_clusters) {
-      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut);
+      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut,
+                              n_blocks, args.m_outer);
       if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
@@ -953,6 +963,19 @@ moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const C
 // segments, and the single-CTA kernel, which stages half as many A rows for
 // the same weight columns, streams the weights faster (measured: 117.5 vs
 // 128.3 us for the gate/up pass at T=128, E=128, top-8).
+// Tile order that keeps HBM re-reads down.  With n-block outer, a segment's
+// rows of A are re-read once per n-block unless they stay in L2; with m-block
+// outer, the expert's B columns are re-read once per m-block unless they stay in
+// L2.  Rows-inner (n-block outer) is the default; m-block outer is chosen when
+// an average segment of A is too large for L2 while one expert's B fits
+// (e.g. 29 K rows x 3072 of A against 18.9 MB of gate+up weights).
+int choose_m_outer(int32_t n_seg, int32_t max_rows, int32_t K, int64_t b_cols_per_seg) {
+  constexpr int64_t kL2Budget = 48ll << 20;  // of the 129 MB L2, leaving room for concurrency
+  const int64_t a_seg = static_cast<int64_t>(max_rows) / n_seg * K * 2;
+  const int64_t b_seg = static_cast<int64_t>(K) * b_cols_per_seg * 2;
+  return (a_seg > kL2Budget && b_seg <= kL2Budget) ? 1 : 0;
+}
+
 bool pair_shape(int32_t n_seg, int32_t max_rows) {
   return static_cast<int64_t>(max_rows) >= static_cast<int64_t>(kBM) * n_seg;
 }
@@ -994,7 +1017,7 @@ MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int3
       !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
-             dev_status};
+             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I))};
   cudaStream_t s = as_cuda(stream);
   if (I % 128 == 0) {
     return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s)
@@ -1017,7 +1040,7 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   if (!make_map(&m_h, h, max_rows, I, kBM) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
-             dev_status};
+             dev_status, choose_m_outer(n_seg, max_rows, I, d)};
   cudaStream_t s = as_cuda(stream);
   if (d % 256 == 0) {
     return pair_shape(n_seg, max_rows) ? launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s)

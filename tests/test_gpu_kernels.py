@@ -246,7 +246,7 @@ def test_combine_bad_row_is_reported_and_skipped():
 # Grouped SwiGLU GEMM
 # ----------------------------------------------------------------------------
 
-def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None):
+def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None, sample=None):
     g = G()
     counts = np.asarray(counts, np.int32)
     if begins is None:
@@ -267,7 +267,12 @@ def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None):
     torch.cuda.synchronize()
     assert int(host(st)[0]) == 0
     H = ws[: max_rows * I * 2].view(torch.bfloat16).view(max_rows, I)
-    yr, hr = oracle.grouped_swiglu_rows(bits(x), begins, counts, bits(wg), bits(wu), bits(wd))
+    pick = None
+    if sample is not None:
+        all_rows = np.concatenate([np.arange(b, b + c) for b, c in zip(begins, counts)])
+        pick = np.sort(np.random.default_rng(seed).choice(all_rows, sample, replace=False))
+    yr, hr = oracle.grouped_swiglu_rows(bits(x), begins, counts, bits(wg), bits(wu), bits(wd),
+                                        rows=pick)
     rows = sorted(yr)
     yb, hb = bits(y), bits(H)
     if rows:
@@ -276,7 +281,9 @@ def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None):
         assert_float_parity(oracle.bf16_to_f64(yb[rows]),
                             oracle.bf16_to_f64(np.stack([yr[r] for r in rows])), "y")
     # rows outside every segment are never written
-    untouched = np.setdiff1d(np.arange(max_rows), rows)
+    seg_rows = np.concatenate([np.arange(b, b + c) for b, c in zip(begins, counts)]) \
+        if len(counts) else np.zeros(0, int)
+    untouched = np.setdiff1d(np.arange(max_rows), seg_rows)
     assert np.all(yb[untouched] == bits(torch.tensor([7.0], dtype=torch.bfloat16))[0])
 
 
@@ -292,6 +299,14 @@ def _gemm_case(n_seg, d, I, counts, begins=None, seed=0, max_rows=None):
 ])
 def test_grouped_swiglu_parity(n_seg, d, I, counts):
     _gemm_case(n_seg, d, I, counts)
+
+
+@pytest.mark.parametrize("d,I", [(4096, 256), (256, 8192)])
+def test_grouped_swiglu_large_segments_row_block_outer_order(d, I):
+    # Segments of ~8 K rows whose A does not fit the L2 budget while one expert's
+    # weights do: the gate/up pass (d=4096) or the down pass (I=8192) then walks
+    # each block of rows across all weight columns before the next block.
+    _gemm_case(2, d, I, [8191, 8193], sample=300)
 
 
 def test_grouped_swiglu_gapped_segments():
