@@ -163,16 +163,21 @@ class ClockSampler:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
         return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(self.samples), "sm_mhz_max_seen": max(self.samples),
                 "reasons": sorted(n for b, n in _REASONS.items() if self.reasons & b),
-                "samples": len(self.samples)}
+                "reasons_mask": hex(self.reasons), "samples": len(self.samples)}
 
 
 # ----------------------------------------------------------------------------
 # algorithmic work per stage (bytes that must move, flops that must be done)
 # ----------------------------------------------------------------------------
 
-def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d):
-    """(bytes, flops) the method needs for one launch of stage `name`."""
+def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
+    """(bytes, flops) the method needs for one launch of stage `name`.
+
+    For the pooled stages `pool` holds the last wave's measured unit counts:
+    placed (rows packed into pools), tokens (tokens with at least one placed
+    row: each such token row is read once) and kept (rows compacted)."""
     T, k, E = w.T, w.k, w.E
     touched = int((counts > 0).sum())
     if name == "route":
@@ -194,9 +199,10 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d):
             b += T * k * 4 * 2 + acc_rows * 4 + T * d * 4 * (w.n_waves - 1) / w.n_waves
         return int(b), 0
     if name == "pool_pack":
-        return T * k * 4 + 2 * acc_rows * d * 2 + w.n_dest * d * 2 + T * k * 4, 0
+        return (T * k * 4 + pool["tokens"] * d * 2 + pool["placed"] * d * 2 + w.n_dest * d * 2
+                + T * k * 4), 0
     if name == "pool_compact":
-        return 2 * acc_rows * d * 2 + w.n_dest * d * 2 + 2 * acc_rows * 4, 0
+        return 2 * pool["kept"] * d * 2 + w.n_dest * d * 2 + 2 * w.n_dest * layer.pool_cap * 4, 0
     return 0, 0
 
 
@@ -297,14 +303,16 @@ def run_ours(args, dist, w):
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after warm-up")
 
-    # An event after every stage of every step, inside the timed region.
+    # An event after every stage of every step.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
            for _ in range(steps)]
     use_graph = not args.no_graph
-    graph = None
     if use_graph:
         # The K timed steps as one CUDA graph (every call is asynchronous and
-        # allocation-free), with the stage events as external event nodes.
+        # allocation-free), plus an instrumented copy of it with the stage events as
+        # external event nodes.  Event nodes add a few microseconds of gap each, so
+        # the step time comes from the plain graph and the kernel durations from the
+        # instrumented one, replayed right after it.
         for row in evs:
             for e in row:
                 e.record(stream)  # creates the event objects
@@ -312,15 +320,21 @@ def run_ours(args, dist, w):
         graph = torch.cuda.CUDAGraph()
         l0 = abi.launch_count()
         with torch.cuda.graph(graph, stream=stream):
+            for s in range(steps):
+                for _, fn in stages:
+                    fn(None)
+        graph_launches = abi.launch_count() - l0
+        graph_inst = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_inst, stream=stream):
             cur = torch.cuda.current_stream()
             for s in range(steps):
                 record_external(evs[s][0], cur)
                 for i, (_, fn) in enumerate(stages):
                     fn(None)
                     record_external(evs[s][i + 1], cur)
-        graph_launches = abi.launch_count() - l0
         with torch.cuda.stream(stream):
-            graph.replay()  # warm replay (untimed)
+            graph.replay()  # warm replays (untimed)
+            graph_inst.replay()
         stream.synchronize()
 
     # timed region: K whole steps
@@ -343,6 +357,10 @@ def run_ours(args, dist, w):
                         evs[s][i + 1].record(stream)
         t_end.record(stream)
         stream.synchronize()
+        if use_graph:
+            with torch.cuda.stream(stream):
+                graph_inst.replay()
+            stream.synchronize()
     torch.cuda.synchronize(device)
     dist.barrier()
     launches = graph_launches if use_graph else (abi.launch_count() - launches0)
@@ -360,9 +378,13 @@ def run_ours(args, dist, w):
     value = dist.world * w.T * steps / (max_ms / 1e3)
 
     # algorithmic work and the dominant kernel's roofline
+    pool = None
     if w.pooled:
         acc_rows = int(layer.local_counts.sum().item())  # last wave's rows (per-wave unit)
         counts = layer.local_counts.cpu().numpy()
+        placed = layer.route_to_poolrow.view(w.T, w.k) >= 0
+        pool = {"placed": int(placed.sum().item()), "tokens": int(placed.any(1).sum().item()),
+                "kept": acc_rows}
     else:
         acc_rows = int(layer.offsets[-1].item())
         counts = layer.counts.cpu().numpy()
@@ -373,7 +395,7 @@ def run_ours(args, dist, w):
     per_stage = {}
     for n in stage_ms:
         per_launch_ms = stage_ms[n] / (steps * per_step[n])
-        b, f = stage_work(w, layer, n, counts, acc_rows, w.E, I, d)
+        b, f = stage_work(w, layer, n, counts, acc_rows, w.E, I, d, pool)
         t_hbm = b / (hbm * 1e9)
         t_tc = f / (tf_peak * 1e12) if f else 0.0
         bound = "tensor" if t_tc > t_hbm else "hbm"
@@ -402,9 +424,10 @@ def run_ours(args, dist, w):
         "data": "synthetic (seeded; shapes of the workload, random-init expert weights)",
         "config": config_dict(w, layer),
         "roofline": roofline, "stages": per_stage,
-        "timing": ("the K steps replayed from one captured CUDA graph" if use_graph else
-                   "eager launches") + "; stage times from CUDA events between the stages of "
-                   "every timed step, on the launching stream",
+        "timing": ("the K steps replayed from one captured CUDA graph; stage times from CUDA "
+                   "events between the stages of every step of an instrumented replay of the "
+                   "same K steps right after, on the launching stream" if use_graph else
+                   "eager launches with CUDA events between the stages of every timed step"),
         "clocks": sampler.summary(),
         "gpu_launches": int(launches),
     }

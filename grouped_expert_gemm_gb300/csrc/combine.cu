@@ -25,6 +25,7 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
                const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
                const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
                uint32_t* __restrict__ dev_status) {
+  pdl_wait();
   constexpr int UNROLL = KMAX >= 8 ? 1 : (KMAX >= 4 ? 2 : 4);
   __shared__ int32_t s_row[KMAX];
   __shared__ float s_gate[KMAX];
@@ -90,6 +91,7 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
     }
     __syncthreads();
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -113,13 +115,11 @@ MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* 
   const int chunks = d / 8;
   cudaStream_t s = as_cuda(stream);
   const unsigned grid = static_cast<unsigned>(T < 152 * 24 ? T : 152 * 24);
-#define MOE_COMBINE_CASE(K)                                                                      \
-  combine_kernel<K><<<grid, kCombThreads, 0, s>>>(T, k, chunks,                                  \
-                                                  reinterpret_cast<const uint4*>(y), y_rows,     \
-                                                  route_to_row, gates,                           \
-                                                  reinterpret_cast<const uint4*>(shared_y),      \
-                                                  accumulate, reinterpret_cast<float4*>(out),    \
-                                                  dev_status)
+#define MOE_COMBINE_CASE(K)                                                                 \
+  launch(combine_kernel<K>, dim3(grid), dim3(kCombThreads), 0, s, T, k, chunks,               \
+         reinterpret_cast<const uint4*>(y), y_rows, route_to_row, gates,                      \
+         reinterpret_cast<const uint4*>(shared_y), static_cast<int>(accumulate),              \
+         reinterpret_cast<float4*>(out), dev_status)
   if (k <= 1) MOE_COMBINE_CASE(1);
   else if (k <= 2) MOE_COMBINE_CASE(2);
   else if (k <= 4) MOE_COMBINE_CASE(4);

@@ -507,6 +507,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b1)) : "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
+  pdl_wait();  // everything above is local; global data only from here on
   if (threadIdx.x >= 64)
     build_segment_table(args, kBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
   tc_fence_before();
@@ -628,6 +629,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     __syncwarp();
     tmem_dealloc(tmem_base, G::kTmemAlloc);
   }
+  pdl_trigger();
 }
 
 // ------------------------- CTA-pair kernel ----------------------------------
@@ -692,6 +694,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b1)) : "memory");
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(sm.tmem_slot), kTmemAlloc);
+  pdl_wait();  // everything above is local; global data only from here on
   if (threadIdx.x >= 64)
     build_segment_table(args, kPairBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start,
                         sm.warp_tot);
@@ -824,6 +827,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     __syncwarp();
     tmem_dealloc_pair(tmem_base, kTmemAlloc);
   }
+  pdl_trigger();
 }
 
 // ------------------------------ host side ----------------------------------
@@ -920,7 +924,7 @@ moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
     }
     n_sm = sms[dev];
   }
-  kern<<<n_sm, kThreads, G::kSmemBytes, s>>>(a, b0, b1, args);
+  launch(kern, dim3(n_sm), dim3(kThreads), G::kSmemBytes, s, a, b0, b1, args);
   return launch_status();
 }
 
@@ -954,7 +958,7 @@ moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const C
     }
     g = grid[dev];
   }
-  kern<<<g, kThreads, kPairSmemBytes, s>>>(a, b0, b1, args);
+  launch(kern, dim3(g), dim3(kThreads), kPairSmemBytes, s, a, b0, b1, args);
   return launch_status();
 }
 

@@ -10,6 +10,7 @@
 // Three launches, no host synchronisation and no inter-block waiting:
 //   1. permute_hist  one block per tile of consecutive routes (at most 128
 //                    tiles): per-tile expert histogram -> ws hist[tile][E].
+//                    Skipped when there is a single tile: its block counts itself.
 //   2. permute_rank  one block per tile.  Each block reads the whole (small)
 //                    histogram matrix with independent loads to get its tile's
 //                    first ordinal per expert and every expert's total, hence
@@ -51,6 +52,7 @@ permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
              int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  pdl_wait();
   __syncthreads();
   const int r0 = blockIdx.x * routes_per_tile;
   const int r1 = min(R, r0 + routes_per_tile);
@@ -63,6 +65,7 @@ permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
   __syncthreads();
   int32_t* out = hist + static_cast<int64_t>(blockIdx.x) * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = sh[e];
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kRankThreads)
@@ -70,7 +73,7 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
              const int32_t* __restrict__ ids, const int32_t* __restrict__ hist,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ n_dropped, int32_t* __restrict__ row_to_route,
-             int32_t* __restrict__ route_to_row) {
+             int32_t* __restrict__ route_to_row, uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kRankWarps][E]
   int32_t* off = cnt + kRankWarps * E;  // [E]
@@ -78,10 +81,27 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int tile = blockIdx.x;
 
+  const int r0 = tile * routes_per_tile;
+  const int r1 = min(R, r0 + routes_per_tile);
+  const int sub = (r1 - r0 + kRankWarps - 1) / kRankWarps;
+  const int s0 = r0 + w * sub, s1 = min(r1, s0 + sub);
+  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
+  pdl_wait();
+  __syncthreads();
+  // per-warp expert counts of the warp's contiguous sub-range
+  for (int r = s0 + lane; r < s1; r += 32) {
+    const int ee = __ldg(ids + r);
+    if (ee >= 0 && ee < E) atomicAdd(&cnt[w * E + ee], 1);
+  }
+  __syncthreads();
   // 1. this tile's first ordinal per expert, every expert's total, admitted counts
+  //    (from the histogram of all tiles, or, with no histogram (hist == nullptr,
+  //    a single tile), from this block's own counts)
   const int e = threadIdx.x;
   int32_t base = 0, total = 0;
-  if (e < E) {
+  if (e < E && hist == nullptr) {
+    for (int ww = 0; ww < kRankWarps; ++ww) total += cnt[ww * E + e];
+  } else if (e < E) {
     int t = 0;
     for (; t + 8 <= n_tiles; t += 8) {
       int32_t v[8];
@@ -108,7 +128,6 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
     if (lane >= o) incl += v;
   }
   if (lane == 31) warp_tot[w] = incl;
-  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   int32_t before = 0;
   for (int i = 0; i < w; ++i) before += warp_tot[i];
@@ -123,17 +142,7 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
       }
     }
   }
-  const int r0 = tile * routes_per_tile;
-  const int r1 = min(R, r0 + routes_per_tile);
-  const int sub = (r1 - r0 + kRankWarps - 1) / kRankWarps;
-  const int s0 = r0 + w * sub, s1 = min(r1, s0 + sub);
-  // 3. per-warp expert counts of the warp's contiguous sub-range
-  for (int r = s0 + lane; r < s1; r += 32) {
-    const int ee = __ldg(ids + r);
-    if (ee >= 0 && ee < E) atomicAdd(&cnt[w * E + ee], 1);
-  }
-  __syncthreads();
-  // 4. each warp's first ordinal per expert: tile base + earlier warps
+  // 3. each warp's first ordinal per expert: tile base + earlier warps
   if (e < E) {
     int32_t run = base;
     for (int ww = 0; ww < kRankWarps; ++ww) {
@@ -143,14 +152,17 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
     }
   }
   __syncthreads();
-  // 5. stable ranks, 32 routes at a time in route order
+  // 4. stable ranks, 32 routes at a time in route order
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int c0 = s0; c0 < s1; c0 += 32) {
     const int r = c0 + lane;
     int ee = -1;
     if (r < s1) {
       ee = __ldg(ids + r);
-      if (ee < 0 || ee >= E) ee = -2;  // invalid id: its own group, never admitted
+      if (ee < 0 || ee >= E) {  // invalid id: its own group, never admitted
+        ee = -2;
+        if (hist == nullptr) report(dev_status, MOE_DEV_BAD_EXPERT_ID);
+      }
     }
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, ee);
     int32_t ordinal = 0;
@@ -167,12 +179,14 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
       route_to_row[r] = row;
     }
   }
+  pdl_trigger();
 }
 
 // One warp per token: read the row once, store it to each admitted row.
 __global__ void __launch_bounds__(kCopyThreads)
 permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
              const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
@@ -196,6 +210,7 @@ permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
       }
     }
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -232,23 +247,24 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
   const size_t rank_smem = (static_cast<size_t>(kRankWarps) * E + E) * sizeof(int32_t);
   if (R == 0) {
     // No routes: one rank block with no tiles writes empty counts and offsets.
-    permute_rank<<<1, kRankThreads, rank_smem, s>>>(0, E, 1, 0, capacity, topk_ids, hist, counts,
-                                                    offsets, n_dropped, row_to_route,
-                                                    route_to_row);
+    launch(permute_rank, dim3(1), dim3(kRankThreads), rank_smem, s, 0, E, 1, 0, capacity,
+           topk_ids, static_cast<const int32_t*>(nullptr), counts, offsets, n_dropped,
+           row_to_route, route_to_row, dev_status);
     return launch_status();
   }
-  permute_hist<<<tl.n_tiles, kHistThreads, E * sizeof(int32_t), s>>>(R, E, tl.routes_per_tile,
-                                                                    topk_ids, hist, dev_status);
-  permute_rank<<<tl.n_tiles, kRankThreads, rank_smem, s>>>(R, E, tl.routes_per_tile, tl.n_tiles,
-                                                           capacity, topk_ids, hist, counts,
-                                                           offsets, n_dropped, row_to_route,
-                                                           route_to_row);
+  if (tl.n_tiles > 1)
+    launch(permute_hist, dim3(tl.n_tiles), dim3(kHistThreads), E * sizeof(int32_t), s, R, E,
+           tl.routes_per_tile, topk_ids, hist, dev_status);
+  launch(permute_rank, dim3(tl.n_tiles), dim3(kRankThreads), rank_smem, s, R, E,
+         tl.routes_per_tile, tl.n_tiles, capacity, topk_ids,
+         static_cast<const int32_t*>(tl.n_tiles > 1 ? hist : nullptr), counts, offsets, n_dropped,
+         row_to_route, route_to_row, dev_status);
   const int warps = kCopyThreads / 32;
   int64_t blocks = ceil_div(T, warps);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  permute_copy<<<static_cast<unsigned>(blocks), kCopyThreads, 0, s>>>(
-      T, k, d / 8, route_to_row, reinterpret_cast<const uint4*>(x),
-      reinterpret_cast<uint4*>(x_perm));
+  launch(permute_copy, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k, d / 8,
+         static_cast<const int32_t*>(route_to_row), reinterpret_cast<const uint4*>(x),
+         reinterpret_cast<uint4*>(x_perm));
   return launch_status();
 }
 

@@ -39,6 +39,7 @@ pack_hist(int R, int n_dest, int L, int items_per_tile, const int32_t* __restric
           int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];
   for (int i = threadIdx.x; i < n_dest; i += blockDim.x) sh[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int r0 = blockIdx.x * items_per_tile, r1 = min(R, r0 + items_per_tile);
   bool bad = false;
@@ -50,6 +51,7 @@ pack_hist(int R, int n_dest, int L, int items_per_tile, const int32_t* __restric
   __syncthreads();
   for (int i = threadIdx.x; i < n_dest; i += blockDim.x)
     hist[static_cast<int64_t>(blockIdx.x) * n_dest + i] = sh[i];
+  pdl_trigger();
 }
 
 __device__ __forceinline__ int block_sum_512(int v, int* scratch) {
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(512)
 pack_scan(int n_dest, int n_tiles, int n_waves, int pool_cap, int policy, int wave,
           int32_t* __restrict__ hist, int32_t* __restrict__ pool_fill,
           int32_t* __restrict__ sender_drops) {
+  pdl_wait();
   __shared__ int scratch[16];
   const int D = threadIdx.x;
   int32_t run = 0;
@@ -89,6 +92,7 @@ pack_scan(int n_dest, int n_tiles, int n_waves, int pool_cap, int policy, int wa
   if (D < n_dest) pool_fill[D] = fill;
   const int drops = block_sum_512(in_wave - fill, scratch);
   if (threadIdx.x == 0) *sender_drops = drops;
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -97,6 +101,7 @@ pack_scatter(int T, int d, int k, int n_dest, int L, int n_waves, int pool_cap, 
              const int32_t* __restrict__ tile_base, const int32_t* __restrict__ pool_fill,
              const uint4* __restrict__ x, uint4* __restrict__ pools,
              uint16_t* __restrict__ pools_u16, int32_t* __restrict__ route_to_poolrow) {
+  pdl_wait();
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kWarps][n_dest]
   int64_t* rows = reinterpret_cast<int64_t*>(cnt + ((kWarps * n_dest + 1) & ~1));  // [tile routes]
@@ -161,18 +166,32 @@ pack_scatter(int T, int d, int k, int n_dest, int L, int n_waves, int pool_cap, 
     }
   }
   __syncthreads();
+  // Token-major copy: each token row is read once (four 16-byte loads in flight
+  // per lane) and written to each of its rows placed in this wave.
   const int chunks = d >> 3;
   for (int t = t0 + w; t < t1; t += kWarps) {
-    const uint4* src = x + static_cast<int64_t>(t) * chunks;
     const int64_t* trow = rows + (t - t0) * k;
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 v = __ldg(src + c);
+    bool any = false;
+    for (int jj = 0; jj < k; ++jj) any |= trow[jj] >= 0;
+    if (!any) continue;
+    const uint4* src = x + static_cast<int64_t>(t) * chunks;
+    for (int cb = 0; cb < chunks; cb += 32 * 4) {
+      const int c = cb + lane;
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < chunks) v[u] = __ldg(src + c + 32 * u);
       for (int jj = 0; jj < k; ++jj) {
         const int64_t dst = trow[jj];
-        if (dst >= 0) pools[dst * chunks + c] = v;
+        if (dst < 0) continue;
+        uint4* o = pools + dst * chunks;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + 32 * u < chunks) o[c + 32 * u] = v[u];
       }
     }
   }
+  pdl_trigger();
 }
 
 // ------------------------------ receiver ----------------------------------
@@ -192,6 +211,7 @@ compact_hist(int64_t n_items, int pool_cap, int d, int n_local, int items_per_ti
              uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];
   for (int i = threadIdx.x; i < n_local; i += blockDim.x) sh[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * items_per_tile;
   const int64_t i1 = min(n_items, i0 + items_per_tile);
@@ -204,11 +224,13 @@ compact_hist(int64_t n_items, int pool_cap, int d, int n_local, int items_per_ti
   __syncthreads();
   for (int i = threadIdx.x; i < n_local; i += blockDim.x)
     hist[static_cast<int64_t>(blockIdx.x) * n_local + i] = sh[i];
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(512)
 compact_scan(int n_local, int n_tiles, int local_cap, int32_t* __restrict__ hist,
              int32_t* __restrict__ local_counts, int32_t* __restrict__ receiver_drops) {
+  pdl_wait();
   __shared__ int scratch[16];
   int drops_total = 0;
   for (int l0 = 0; l0 < n_local; l0 += blockDim.x) {
@@ -227,6 +249,7 @@ compact_scan(int n_local, int n_tiles, int local_cap, int32_t* __restrict__ hist
     __syncthreads();
   }
   if (threadIdx.x == 0) *receiver_drops = drops_total;
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -234,6 +257,7 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
                 int items_per_tile, const uint16_t* __restrict__ pools_u16,
                 const uint4* __restrict__ pools, const int32_t* __restrict__ tile_base,
                 uint4* __restrict__ compact, int32_t* __restrict__ poolrow_to_row) {
+  pdl_wait();
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kWarps][n_local]
   int32_t* rows = cnt + kWarps * n_local;  // [items in tile]
@@ -279,6 +303,7 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
     }
   }
   __syncthreads();
+  // Row copy, one warp per kept row, four 16-byte loads in flight per lane.
   const int chunks = d >> 3;
   for (int64_t i = i0 + w; i < i1; i += kWarps) {
     const int32_t row = rows[i - i0];
@@ -286,13 +311,24 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
     const int64_t s = i / pool_cap, r = i % pool_cap;
     const uint4* src = pools + (s * (pool_cap + 1) + 1 + r) * chunks;
     uint4* dst = compact + static_cast<int64_t>(row) * chunks;
-    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    for (int cb = 0; cb < chunks; cb += 32 * 4) {
+      const int c = cb + lane;
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < chunks) v[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < chunks) dst[c + 32 * u] = v[u];
+    }
   }
+  pdl_trigger();
 }
 
 __global__ void compose_kernel(int64_t n, const int32_t* __restrict__ a,
                                const int32_t* __restrict__ b, int64_t b_len,
                                int32_t* __restrict__ out, uint32_t* __restrict__ dev_status) {
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t v = __ldg(a + i);
@@ -302,6 +338,7 @@ __global__ void compose_kernel(int64_t n, const int32_t* __restrict__ a,
     }
     out[i] = r;
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -347,15 +384,16 @@ MOE_API moe_status moe_pool_pack(const moe_pool_params* p, int32_t T, int32_t d,
   const int n_tiles = T > 0 ? static_cast<int>(ceil_div(R, per)) : 0;
   int32_t* hist = static_cast<int32_t*>(ws);
   if (n_tiles > 0)
-    pack_hist<<<n_tiles, kThreads, p->n_dest * sizeof(int32_t), s>>>(
-        static_cast<int>(R), p->n_dest, p->local_per_dest, per, topk_ids, hist, dev_status);
-  pack_scan<<<1, 512, 0, s>>>(p->n_dest, n_tiles, p->n_waves, p->pool_cap, p->wave_policy, wave,
-                              hist, pool_fill, sender_drops);
+    launch(pack_hist, dim3(n_tiles), dim3(kThreads), p->n_dest * sizeof(int32_t), s,
+           static_cast<int>(R), p->n_dest, p->local_per_dest, per, topk_ids, hist, dev_status);
+  launch(pack_scan, dim3(1), dim3(512), 0, s, p->n_dest, n_tiles, p->n_waves, p->pool_cap,
+         p->wave_policy, wave, hist, pool_fill, sender_drops);
   const size_t smem = ((kWarps * p->n_dest + 1) & ~1) * sizeof(int32_t) + per * sizeof(int64_t);
-  pack_scatter<<<n_tiles > 0 ? n_tiles : 1, kThreads, smem, s>>>(
-      T, d, k, p->n_dest, p->local_per_dest, p->n_waves, p->pool_cap, p->wave_policy, wave,
-      per / k, topk_ids, hist, pool_fill, reinterpret_cast<const uint4*>(x),
-      reinterpret_cast<uint4*>(pools), reinterpret_cast<uint16_t*>(pools), route_to_poolrow);
+  launch(pack_scatter, dim3(n_tiles > 0 ? n_tiles : 1), dim3(kThreads), smem, s, T, d, k,
+         p->n_dest, p->local_per_dest, p->n_waves, p->pool_cap, p->wave_policy, wave, per / k,
+         topk_ids, static_cast<const int32_t*>(hist), static_cast<const int32_t*>(pool_fill),
+         reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(pools),
+         reinterpret_cast<uint16_t*>(pools), route_to_poolrow);
   return launch_status();
 }
 
@@ -391,14 +429,14 @@ MOE_API moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, 
   const int n_tiles = static_cast<int>(ceil_div(n_items, per));
   int32_t* hist = static_cast<int32_t*>(ws);
   const uint16_t* hdr = reinterpret_cast<const uint16_t*>(pools);
-  compact_hist<<<n_tiles, kThreads, n_local * sizeof(int32_t), s>>>(n_items, pool_cap, d, n_local,
-                                                                   per, hdr, hist, dev_status);
-  compact_scan<<<1, 512, 0, s>>>(n_local, n_tiles, local_cap, hist, local_counts, receiver_drops);
+  launch(compact_hist, dim3(n_tiles), dim3(kThreads), n_local * sizeof(int32_t), s, n_items,
+         pool_cap, d, n_local, per, hdr, hist, dev_status);
+  launch(compact_scan, dim3(1), dim3(512), 0, s, n_local, n_tiles, local_cap, hist, local_counts,
+         receiver_drops);
   const size_t smem = (static_cast<size_t>(kWarps) * n_local + per) * sizeof(int32_t);
-  compact_scatter<<<n_tiles, kThreads, smem, s>>>(n_items, pool_cap, d, n_local, local_cap, per,
-                                                  hdr, reinterpret_cast<const uint4*>(pools),
-                                                  hist, reinterpret_cast<uint4*>(compact),
-                                                  poolrow_to_row);
+  launch(compact_scatter, dim3(n_tiles), dim3(kThreads), smem, s, n_items, pool_cap, d, n_local,
+         local_cap, per, hdr, reinterpret_cast<const uint4*>(pools),
+         static_cast<const int32_t*>(hist), reinterpret_cast<uint4*>(compact), poolrow_to_row);
   return launch_status();
 }
 
@@ -408,7 +446,7 @@ MOE_API moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b
   if (n == 0) return MOE_OK;
   if (a == nullptr || out == nullptr || (b == nullptr && b_len > 0)) return MOE_ERR_INVALID_ARG;
   const int64_t blocks = ceil_div(n, 256);
-  compose_kernel<<<static_cast<unsigned>(blocks < 152 * 32 ? blocks : 152 * 32), 256, 0,
-                   as_cuda(stream)>>>(n, a, b, b_len, out, dev_status);
+  launch(compose_kernel, dim3(static_cast<unsigned>(blocks < 152 * 32 ? blocks : 152 * 32)),
+         dim3(256), 0, as_cuda(stream), n, a, b, b_len, out, dev_status);
   return launch_status();
 }

@@ -59,13 +59,14 @@ __device__ __forceinline__ int key_expert(uint64_t key) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
 }
 
+// Warp maximum of 64-bit keys with two 32-bit reductions: the high words first,
+// then the low words of the lanes that hold the maximal high word.
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
+  const uint32_t hi = static_cast<uint32_t>(v >> 32);
+  const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  const uint32_t lo = hi == mhi ? static_cast<uint32_t>(v) : 0u;
+  const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lo);
+  return (static_cast<uint64_t>(mhi) << 32) | mlo;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -82,6 +83,7 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
              const float* __restrict__ logits, const float* __restrict__ sel_bias,
              int32_t* __restrict__ topk_ids, float* __restrict__ gates,
              uint32_t* __restrict__ dev_status) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTokensPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -190,6 +192,7 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
     topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
     gates[static_cast<int64_t>(t) * k + lane] = g;
   }
+  pdl_trigger();
 }
 
 template <bool GROUPED>
@@ -198,10 +201,9 @@ moe_status launch_route(const moe_route_params* p, const float* logits, const fl
   const int vpl = static_cast<int>(ceil_div(p->E, 32));
   const dim3 grid(static_cast<unsigned>(ceil_div(p->T, kTokensPerBlock)));
   const dim3 block(kTokensPerBlock * 32);
-#define MOE_ROUTE_CASE(V)                                                                     \
-  route_kernel<V, GROUPED><<<grid, block, 0, s>>>(p->T, p->E, p->k, p->n_group, p->topk_group, \
-                                                  p->route_scale, logits, sel_bias, ids,      \
-                                                  gates, st)
+#define MOE_ROUTE_CASE(V)                                                                \
+  launch(route_kernel<V, GROUPED>, grid, block, 0, s, p->T, p->E, p->k, p->n_group,        \
+         p->topk_group, p->route_scale, logits, sel_bias, ids, gates, st)
   if (vpl <= 1) MOE_ROUTE_CASE(1);
   else if (vpl <= 2) MOE_ROUTE_CASE(2);
   else if (vpl <= 4) MOE_ROUTE_CASE(4);
@@ -213,9 +215,11 @@ moe_status launch_route(const moe_route_params* p, const float* logits, const fl
 }
 
 __global__ void sigmoid_det_kernel(int64_t n, const float* __restrict__ z, float* __restrict__ s) {
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     s[i] = sigmoid_det(z[i]);
+  pdl_trigger();
 }
 
 }  // namespace
@@ -248,7 +252,7 @@ MOE_API moe_status moe_sigmoid_det(int64_t n, const float* z, float* s, moe_stre
   if (n < 0 || (n > 0 && (z == nullptr || s == nullptr))) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
   const int64_t blocks = ceil_div(n, 256);
-  sigmoid_det_kernel<<<static_cast<unsigned>(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0,
-                       as_cuda(stream)>>>(n, z, s);
+  launch(sigmoid_det_kernel, dim3(static_cast<unsigned>(blocks < 152 * 64 ? blocks : 152 * 64)),
+         dim3(256), 0, as_cuda(stream), n, z, s);
   return launch_status();
 }
