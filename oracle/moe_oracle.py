@@ -455,3 +455,85 @@ def drop_rates(total: int, sender: int, receiver: int):
     return dict(sender=sender / total, receiver=receiver / total,
                 total=(sender + receiver) / total,
                 receiver_conditional=(receiver / (total - sender)) if total > sender else 0.0)
+
+
+# ----------------------------------------------------------------------------
+# Backward of the transpose  ([M6.2] 0x03D "Backward Is The Reverse Semantic
+# Transpose": Zbar_r = g_r * Ybar_origin(r), gbar_r = <Ybar_origin(r), Z_r>, and
+# route-input gradients summed by origin token through the saved inverse)
+# ----------------------------------------------------------------------------
+
+def combine_backward(dout_f64: np.ndarray, y_rows_f64: np.ndarray, route_to_row: np.ndarray,
+                     gates: np.ndarray, T: int, k: int):
+    """Gradients of out[t] = sum_j g[t,j] * y[row(t,j)] for upstream dout [T, d].
+
+    Returns (dy float64 [n_rows, d] -- g[t,j] * dout[t] on the row of every accepted
+    route, zero elsewhere -- and dgates float64 [T, k] -- <dout[t], y[row(t,j)]>,
+    zero for dropped routes).
+    """
+    r2r = np.asarray(route_to_row).reshape(T, k)
+    g = np.asarray(gates, dtype=np.float64).reshape(T, k)
+    dout = np.asarray(dout_f64, dtype=np.float64)
+    dy = np.zeros_like(np.asarray(y_rows_f64, dtype=np.float64))
+    dg = np.zeros((T, k))
+    for j in range(k):
+        rows = r2r[:, j]
+        ok = rows >= 0
+        dy[rows[ok]] = g[ok, j:j + 1] * dout[ok]
+        dg[ok, j] = np.sum(dout[ok] * y_rows_f64[rows[ok]], axis=1)
+    return dy, dg
+
+
+def unpermute_grad(dx_perm_f64: np.ndarray, route_to_row: np.ndarray, T: int, k: int):
+    """Token gradients: dx[t] = sum over the token's accepted routes of dx_perm[row(t,j)]."""
+    r2r = np.asarray(route_to_row).reshape(T, k)
+    d = dx_perm_f64.shape[1]
+    dx = np.zeros((T, d))
+    for j in range(k):
+        rows = r2r[:, j]
+        ok = rows >= 0
+        dx[ok] += dx_perm_f64[rows[ok]]
+    return dx
+
+
+# ----------------------------------------------------------------------------
+# Load telemetry and the loss-free bias step  ([M6.2] 0x01I skew summaries,
+# 0x06E "The Bias Is A Delayed Controller State", 0x06J1-0x06J3)
+# ----------------------------------------------------------------------------
+
+def load_stats(counts) -> dict:
+    """Skew summaries of a nonnegative count vector n over U units.
+
+    mu = R / U; CV^2 = mean((n - mu)^2) / mu^2; rho_max = max(n) / mu;
+    q = n / R with 0 log 0 = 0; H_norm = -sum q log q / log U; E_eff = exp(-sum q log q);
+    MaxVio = (max(n) - mu) / mu.  Reading: an all-zero vector (R = 0) has all
+    summaries 0, and H_norm is 0 when U = 1.
+    """
+    n = np.asarray(counts, dtype=np.float64)
+    U = n.size
+    R = n.sum()
+    if U == 0 or R == 0:
+        return dict(cv2=0.0, rho_max=0.0, h_norm=0.0, e_eff=0.0, max_vio=0.0, total=0)
+    mu = R / U
+    q = n / R
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ent = -np.sum(np.where(q > 0, q * np.log(np.where(q > 0, q, 1.0)), 0.0))
+    return dict(cv2=float(np.mean((n - mu) ** 2) / mu ** 2), rho_max=float(n.max() / mu),
+                h_norm=float(ent / np.log(U)) if U > 1 else 0.0, e_eff=float(np.exp(ent)),
+                max_vio=float((n.max() - mu) / mu), total=int(R))
+
+
+def bias_update(bias, counts, u: float, rule: str = "sign") -> np.ndarray:
+    """One delayed controller step on the fp32 selection bias.
+
+    sign:         b_e <- b_e + u * sign(mean(c) - c_e)
+    proportional: b_e <- b_e + u * (mean(c) - c_e)
+    Reading: the increment is formed in float64 and rounded to fp32 once, then
+    added to the fp32 bias with one fp32 rounding.
+    """
+    b = np.asarray(bias, dtype=np.float32)
+    c = np.asarray(counts, dtype=np.float64)
+    err = c.mean() - c
+    step = np.sign(err) if rule == "sign" else err
+    inc = (np.float64(np.float32(u)) * step).astype(np.float32)
+    return (b + inc).astype(np.float32)

@@ -530,3 +530,94 @@ def test_compose_map_brute_force():
     out = oracle.compose_map(a, b)
     for i in range(50):
         assert out[i] == (-1 if a[i] < 0 else b[a[i]])
+
+
+# ----------------------------------------------------------------------------
+# Backward of the transpose, load telemetry and the bias controller
+# ----------------------------------------------------------------------------
+
+def test_m62_loop9_backward_of_the_transpose():
+    """[M6.2] 0x03D: all-ones upstream gradient on the Loop 9 fixture."""
+    fx = load("m62_loop9_permute_combine.json")
+    k, E = fx["k"], fx["E"]
+    ids = np.array(fx["expert_of_route"]).reshape(-1, k)
+    hidden = np.array(fx["hidden"], dtype=np.float64)
+    gates = np.array(fx["gate_of_route"])
+    p = oracle.permute(ids, E, -1)
+    x_perm = hidden[p["row_to_route"] // k]
+    scale = np.array(fx["scalar_expert"], dtype=np.float64)
+    row_expert = ids.reshape(-1)[p["row_to_route"]]
+    z = scale[row_expert][:, None] * x_perm
+    dy, dg = oracle.combine_backward(np.ones((4, 3)), z, p["route_to_row"], gates, 4, k)
+    assert np.allclose(dg.reshape(-1), fx["backward_all_ones"]["gate_grad_by_route"], atol=1e-12)
+    # scalar experts: dL/ds_e = sum over its rows of <dy_row, x_row>
+    ds = [float(np.sum(dy[row_expert == e] * x_perm[row_expert == e])) for e in range(E)]
+    np.testing.assert_allclose(ds, [15, 17.25, 10.2, 35.55], atol=1e-12)
+    # route-input gradients s_e * dy, summed back to tokens through the inverse
+    dx = oracle.unpermute_grad(scale[row_expert][:, None] * dy, p["route_to_row"], 4, k)
+    np.testing.assert_allclose(dx, np.array([2.4, 2.4, 2.35, 3.5])[:, None] * np.ones((4, 3)),
+                               atol=1e-12)
+
+
+def test_combine_backward_is_the_adjoint_of_combine():
+    """<combine(y), dout> = <y, dy> + sum_g dgates * gates-derivative (linearity checks)."""
+    rng = np.random.default_rng(12)
+    T, k, d, rows = 7, 3, 5, 25
+    y = rng.standard_normal((rows, d))
+    r2r = rng.permutation(rows)[: T * k]
+    r2r[[2, 9]] = -1
+    g = rng.uniform(0, 1, T * k)
+    dout = rng.standard_normal((T, d))
+    dy, dg = oracle.combine_backward(dout, y, r2r, g, T, k)
+    out = oracle.combine(y, r2r, g, T, k)
+    # out is linear in y: <out, dout> == <y, dy>
+    assert abs(np.sum(out * dout) - np.sum(y * dy)) < 1e-10
+    # and linear in the gates: <out, dout> == <g, dgates>
+    assert abs(np.sum(out * dout) - np.sum(g.reshape(T, k) * dg)) < 1e-10
+    # finite difference in one gate
+    eps = 1e-6
+    g2 = g.copy()
+    g2[4] += eps
+    fd = (np.sum(oracle.combine(y, r2r, g2, T, k) * dout) - np.sum(out * dout)) / eps
+    assert abs(fd - dg.reshape(-1)[4]) < 1e-5
+
+
+def test_unpermute_grad_is_the_adjoint_of_the_gather():
+    rng = np.random.default_rng(13)
+    T, k, d, E = 9, 2, 4, 5
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    p = oracle.permute(ids, E, 2)
+    x = rng.standard_normal((T, d))
+    xp = x[p["row_to_route"] // k]
+    dxp = rng.standard_normal(xp.shape)
+    dx = oracle.unpermute_grad(dxp, p["route_to_row"], T, k)
+    assert abs(np.sum(xp * dxp) - np.sum(x * dx)) < 1e-10
+
+
+def test_m62_skew_summaries_fixture():
+    fx = load("m62_load_and_controller.json")
+    for axis, (counts, cv2) in fx["cv2_by_axis"].items():
+        assert abs(oracle.load_stats(counts)["cv2"] - cv2) < 1e-12, axis
+    mv = fx["maxvio_toy"]
+    assert abs(oracle.load_stats(mv["counts"])["max_vio"] - mv["max_vio"]) < 1e-12
+    # closed forms: uniform counts and a single occupied unit
+    u = oracle.load_stats([5] * 8)
+    assert abs(u["h_norm"] - 1) < 1e-12 and abs(u["e_eff"] - 8) < 1e-9 and u["cv2"] == 0
+    one = oracle.load_stats([0, 0, 7, 0])
+    assert one["h_norm"] == 0 and abs(one["e_eff"] - 1) < 1e-12 and one["rho_max"] == 4
+    assert oracle.load_stats([0, 0, 0])["total"] == 0
+
+
+def test_m62_controller_step_fixture():
+    fx = load("m62_load_and_controller.json")["controller"]
+    c = np.array(fx["counts"])
+    assert abs(c.mean() - fx["mean"]) < 1e-15
+    b0 = np.zeros(c.size, np.float32)
+    b1 = oracle.bias_update(b0, c, fx["gamma"], "sign")
+    for e in fx["decrease"]:
+        assert b1[e] == np.float32(-0.001)
+    for e in fx["increase_zero_load"]:
+        assert b1[e] == np.float32(0.001)
+    assert np.all(np.sign(b1) == np.sign(c.mean() - c))
+    bp = oracle.bias_update(b0, c, 0.01, "proportional")
+    np.testing.assert_allclose(bp, 0.01 * (c.mean() - c), rtol=1e-6)
