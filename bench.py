@@ -48,6 +48,9 @@ def parse_args():
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
                          "a smaller T for short profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--extras", action="store_true",
+                    help="also time the backward of the transpose and the telemetry/bias calls "
+                         "on this workload's buffers")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -433,7 +436,56 @@ def run_ours(args, dist, w):
     }
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph)
+    if args.extras:
+        result["extras"] = run_extras(args, w, layer, stream, steps)
     return result, layer, logits, sel_bias, x
+
+
+def run_extras(args, w, layer, stream, steps):
+    """Time the calls beyond the forward path on this workload's buffers (events on the
+    launching stream, eager launches): combine backward, token-gradient unpermute,
+    load telemetry and the bias step.  Not part of the step or of `value`."""
+    from grouped_expert_gemm_gb300 import abi
+    if w.pooled:
+        return None
+    hbm, _, _, _ = load_peaks()
+    T, k, d = w.T, w.k, w.d
+    R = max(T * k, 1)
+    acc = int(layer.offsets[-1].item())
+    dev = layer.out.device
+    dout = torch.randn((T, d), device=dev, dtype=torch.float32)
+    dy = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
+    dg = torch.empty((R,), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, d), dtype=torch.float32, device=dev)
+    stats = torch.empty(5, dtype=torch.float64, device=dev)
+    bias = torch.zeros(w.E, dtype=torch.float32, device=dev)
+    calls = {
+        "combine_backward": (lambda: abi.moe_combine_backward(
+            T, k, d, dout, layer.y, R, layer.route_to_row, layer.gates, dy, dg, layer.dev_status,
+            stream), T * d * 4 + 2 * acc * d * 2 + T * k * 8),
+        "unpermute_grad": (lambda: abi.moe_unpermute_grad(
+            T, k, d, dy, R, layer.route_to_row, dx, 0, layer.dev_status, stream),
+            acc * d * 2 + T * d * 4 + T * k * 4),
+        "load_stats": (lambda: abi.moe_load_stats(w.E, layer.counts, stats, stream), w.E * 4),
+        "bias_update": (lambda: abi.moe_bias_update(w.E, layer.counts, bias, 1e-3,
+                                                     abi.MOE_BIAS_SIGN, stream), w.E * 12),
+    }
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        stream.synchronize()
+        ms = a.elapsed_time(b) / steps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms_per_launch": round(ms, 5), "alg_bytes": int(nbytes),
+                     "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+    return out
 
 
 def config_dict(w, layer):

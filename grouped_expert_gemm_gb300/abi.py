@@ -33,6 +33,8 @@ MOE_SCORE_SIGMOID_GROUP = 1
 MOE_WAVE_STRIPE = 0
 MOE_WAVE_DESTMOD = 1
 MOE_POOL_EMPTY = 0xFFFF
+MOE_BIAS_SIGN = 0
+MOE_BIAS_PROPORTIONAL = 1
 
 EXPORTED = [
     "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
@@ -40,6 +42,7 @@ EXPORTED = [
     "moe_grouped_swiglu_workspace_size",
     "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
+    "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
 ]
 
 
@@ -90,6 +93,10 @@ _SIGS = {
     "moe_pool_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                 _P]),
     "moe_compose_map": (_I32, [_I64, _P, _P, _I64, _P, _P, _P]),
+    "moe_combine_backward": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
+    "moe_unpermute_grad": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
+    "moe_load_stats": (_I32, [_I32, _P, _P, _P]),
+    "moe_bias_update": (_I32, [_I32, _P, _P, ctypes.c_float, _I32, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -262,3 +269,30 @@ def moe_compose_map(n, a, b, b_len, out, dev_status=None, stream=None):
     _check("moe_compose_map", lib().moe_compose_map(n, _ptr(a), _ptr(b), b_len, _ptr(out),
                                                     _ptr(dev_status), _stream(stream)))
     _count(1 if n > 0 else 0)
+
+
+def moe_combine_backward(T, k, d, dout, y, y_rows, route_to_row, gates, dy, dgates,
+                         dev_status=None, stream=None):
+    _check("moe_combine_backward", lib().moe_combine_backward(
+        T, k, d, _ptr(dout), _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates), _ptr(dy),
+        _ptr(dgates), _ptr(dev_status), _stream(stream)))
+    _count(1 if T > 0 else 0)
+
+
+def moe_unpermute_grad(T, k, d, dx_perm, rows, route_to_row, dx, accumulate=0, dev_status=None,
+                       stream=None):
+    _check("moe_unpermute_grad", lib().moe_unpermute_grad(
+        T, k, d, _ptr(dx_perm), rows, _ptr(route_to_row), _ptr(dx), int(accumulate),
+        _ptr(dev_status), _stream(stream)))
+    _count(1 if T > 0 else 0)
+
+
+def moe_load_stats(U, counts, stats, stream=None):
+    _check("moe_load_stats", lib().moe_load_stats(U, _ptr(counts), _ptr(stats), _stream(stream)))
+    _count(1)
+
+
+def moe_bias_update(E, counts, bias, u, rule=MOE_BIAS_SIGN, stream=None):
+    _check("moe_bias_update", lib().moe_bias_update(E, _ptr(counts), _ptr(bias), float(u), rule,
+                                                    _stream(stream)))
+    _count(1)

@@ -35,7 +35,7 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
       float g = 0.0f;
       if (threadIdx.x < k) {
         r = __ldg(route_to_row + t * k + threadIdx.x);
-        g = __ldg(gates + t * k + threadIdx.x);
+        g = gates != nullptr ? __ldg(gates + t * k + threadIdx.x) : 1.0f;
         if (r >= 0 && r >= y_rows) {
           report(dev_status, MOE_DEV_BAD_ROW);
           r = -1;
@@ -99,15 +99,37 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
 
 using namespace moe;
 
+// Shared by moe_combine (gates given) and moe_unpermute_grad (unit gates).
+static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
+                               const int32_t* route_to_row, const float* gates,
+                               const moe_bf16* shared_y, int32_t accumulate, float* out,
+                               uint32_t* dev_status, moe_stream_t stream);
+
 MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
+                               const int32_t* route_to_row, const float* gates,
+                               const moe_bf16* shared_y, int32_t accumulate, float* out,
+                               uint32_t* dev_status, moe_stream_t stream) {
+  if (T > 0 && gates == nullptr) return MOE_ERR_INVALID_ARG;
+  return combine_impl(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, out,
+                      dev_status, stream);
+}
+
+MOE_API moe_status moe_unpermute_grad(int32_t T, int32_t k, int32_t d, const moe_bf16* dx_perm,
+                                      int64_t rows, const int32_t* route_to_row, float* dx,
+                                      int32_t accumulate, uint32_t* dev_status,
+                                      moe_stream_t stream) {
+  return combine_impl(T, k, d, dx_perm, rows, route_to_row, nullptr, nullptr, accumulate, dx,
+                      dev_status, stream);
+}
+
+static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
                                const int32_t* route_to_row, const float* gates,
                                const moe_bf16* shared_y, int32_t accumulate, float* out,
                                uint32_t* dev_status, moe_stream_t stream) {
   if (T < 0 || k <= 0 || d <= 0 || y_rows < 0) return MOE_ERR_INVALID_ARG;
   if (k > 16 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (out == nullptr || route_to_row == nullptr || gates == nullptr ||
-      (y == nullptr && y_rows > 0))
+  if (out == nullptr || route_to_row == nullptr || (y == nullptr && y_rows > 0))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(out) || (y != nullptr && !aligned16(y)) ||
       (shared_y != nullptr && !aligned16(shared_y)))

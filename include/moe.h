@@ -287,6 +287,55 @@ moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t 
 moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b, int64_t b_len,
                            int32_t* out, uint32_t* dev_status, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Backward of the transpose                                                */
+/* ------------------------------------------------------------------------ */
+/* [M6.2] 0x03D "Backward Is The Reverse Semantic Transpose".  For the combine
+ * out[t] = sum_j g[t,j] * y[row(t,j)] and upstream gradient dout [T,d] fp32:
+ *   dy[row(t,j)] = bf16(g[t,j] * dout[t])   for every accepted route (the
+ *                  expert-output gradient, in the expert-major row space of y;
+ *                  rows of no accepted route are left untouched),
+ *   dgates[t,j]  = <dout[t], y[row(t,j)]>  fp32 (0 for dropped routes).
+ * y and dy are [y_rows, d] bf16.  Limits: d % 8 == 0, k <= 16, 16-byte aligned
+ * dout / y / dy.  Rows >= y_rows set MOE_DEV_BAD_ROW and are skipped.        */
+moe_status moe_combine_backward(int32_t T, int32_t k, int32_t d, const float* dout,
+                                const moe_bf16* y, int64_t y_rows, const int32_t* route_to_row,
+                                const float* gates, moe_bf16* dy, float* dgates,
+                                uint32_t* dev_status, moe_stream_t stream);
+
+/* Route-input gradients back to their tokens through the saved inverse map
+ * ([M6.2] 0x03D, "the inverse ownership path then sums route-input gradients
+ * by origin token"): dx[t] = (accumulate ? dx[t] : 0) + sum over the token's
+ * accepted routes of dx_perm[route_to_row[t*k+j]], fp32, slot order.  dx_perm
+ * is [rows, d] bf16, dx [T,d] fp32.  Limits and errors as moe_combine.       */
+moe_status moe_unpermute_grad(int32_t T, int32_t k, int32_t d, const moe_bf16* dx_perm,
+                              int64_t rows, const int32_t* route_to_row, float* dx,
+                              int32_t accumulate, uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Load telemetry and the delayed bias controller                          */
+/* ------------------------------------------------------------------------ */
+/* [M6.2] 0x01I skew summaries of a count vector n[U] (int32, e.g. the per-expert
+ * counts written by moe_permute): with mu = R/U, R = sum n, q = n/R, 0 log 0 = 0,
+ *   stats[0] = CV^2 = mean((n - mu)^2) / mu^2      stats[1] = rho_max = max n / mu
+ *   stats[2] = H_norm = -sum q log q / log U      stats[3] = E_eff = exp(-sum q log q)
+ *   stats[4] = MaxVio = (max n - mu) / mu         ([M6.2] 0x06J2)
+ * in fp64 (device array of 5 doubles).  All five are 0 when R = 0; H_norm is 0
+ * when U = 1.  Negative counts are read as 0.                                */
+moe_status moe_load_stats(int32_t U, const int32_t* counts, double* stats, moe_stream_t stream);
+
+enum { MOE_BIAS_SIGN = 0, MOE_BIAS_PROPORTIONAL = 1 };
+
+/* One step of the loss-free selection-bias controller ([M6.2] 0x06E, 0x06J1,
+ * 0x06J3) after a batch routed with the current bias: with c = counts[E] and
+ * cbar = mean(c),
+ *   MOE_BIAS_SIGN:         bias[e] += u * sign(cbar - c[e])
+ *   MOE_BIAS_PROPORTIONAL: bias[e] += u * (cbar - c[e])
+ * in place on the fp32 bias [E]; the increment is formed in fp64 and rounded to
+ * fp32 once, then added with one fp32 rounding.                              */
+moe_status moe_bias_update(int32_t E, const int32_t* counts, float* bias, float u, int32_t rule,
+                           moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
