@@ -48,6 +48,9 @@ def parse_args():
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
                          "a smaller T for short profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bucket", type=int, default=0,
+                    help="decode: replay one captured graph over a fixed bucket of this many "
+                         "token slots, serving --tokens real tokens per step")
     ap.add_argument("--extras", action="store_true",
                     help="also time the backward of the transpose and the telemetry/bias calls "
                          "on this workload's buffers")
@@ -441,6 +444,55 @@ def run_ours(args, dist, w):
     return result, layer, logits, sel_bias, x
 
 
+def run_bucket(args, dist, w):
+    """Decode steps served from a fixed token bucket (one captured graph, device-side
+    valid count; each step copies its inputs into the stable buffers and replays)."""
+    import grouped_expert_gemm_gb300 as g
+    from grouped_expert_gemm_gb300 import build
+    build.build()
+    device = torch.device(f"cuda:{dist.local}")
+    torch.cuda.set_device(device)
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
+    B = args.bucket
+    wb = workloads.scaled(w, T=B)
+    wg, wu, wd = workloads.make_expert_weights(wb, device)
+    bucket = g.DecodeBucket(B, w.d, w.E, w.k, w.I, wg, wu, wd, device=device)
+    stream = torch.cuda.Stream(device)
+    bucket.capture(stream)
+    logits, _ = workloads.make_router_inputs(w, device)
+    x = workloads.make_activations(w, device)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            out, path = bucket.forward(logits, x, stream=stream)
+    stream.synchronize()
+    assert path == "replay", path
+    sampler = ClockSampler(dist.local)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    with sampler:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                bucket.forward(logits, x, stream=stream)
+        b.record(stream)
+        stream.synchronize()
+    dist.barrier()
+    ms = dist.max(a.elapsed_time(b))
+    if int(bucket.layer.dev_status.item()) != 0:
+        raise RuntimeError("device status after bucket steps")
+    return {"metric": METRIC, "value": round(dist.world * w.T * steps / (ms / 1e3), 2),
+            "unit": "tokens/s", "n_gpus": dist.world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / steps, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "T": w.T, "bucket": B, "d": w.d, "E": w.E,
+                       "top_k": w.k, "I": w.I,
+                       "path": "graph replay over the bucket, device-side valid count"},
+            "timing": "each step: input copies into the stable buffers, valid-count write, "
+                      "graph replay", "clocks": sampler.summary()}
+
+
 def run_extras(args, w, layer, stream, steps):
     """Time the calls beyond the forward path on this workload's buffers (events on the
     launching stream, eager launches): combine backward, token-gradient unpermute,
@@ -689,6 +741,11 @@ def main():
         if args.impl == "reference":
             res = run_reference(args, dist, w)
             if res is not None:
+                print(json.dumps(res), flush=True)
+            return
+        if args.bucket:
+            res = run_bucket(args, dist, w)
+            if dist.rank == 0:
                 print(json.dumps(res), flush=True)
             return
         res, layer, logits, sel_bias, x = run_ours(args, dist, w)

@@ -33,6 +33,7 @@ MOE_SCORE_SIGMOID_GROUP = 1
 MOE_WAVE_STRIPE = 0
 MOE_WAVE_DESTMOD = 1
 MOE_POOL_EMPTY = 0xFFFF
+MOE_ROUTE_MASKED = -1
 MOE_BIAS_SIGN = 0
 MOE_BIAS_PROPORTIONAL = 1
 
@@ -43,6 +44,7 @@ EXPORTED = [
     "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
+    "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
 ]
 
 
@@ -96,6 +98,10 @@ _SIGS = {
     "moe_combine_backward": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_grad": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
     "moe_load_stats": (_I32, [_I32, _P, _P, _P]),
+    "moe_route_bucket": (_I32, [ctypes.POINTER(RouteParams), _P, _P, _P, _P, _P, _P, _P]),
+    "moe_permute_bucket": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  _P, _SZ, _P, _P]),
+    "moe_combine_bucket": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_bias_update": (_I32, [_I32, _P, _P, ctypes.c_float, _I32, _P]),
 }
 
@@ -178,6 +184,15 @@ def moe_sigmoid_det(n: int, z, s, stream=None):
     _count(1 if n > 0 else 0)
 
 
+def _permute_launches(T: int, k: int) -> int:
+    """Kernels one permute call launches: the tile histogram runs only with several tiles."""
+    R = T * k
+    if R <= 0:
+        return 1
+    per_tile = max(2048, -(-R // 128))
+    return 3 if -(-R // per_tile) > 1 else 2
+
+
 def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
     return lib().moe_permute_workspace_size(T, k, E)
 
@@ -188,7 +203,7 @@ def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
-    _count(3 if T > 0 else 1)
+    _count(_permute_launches(T, k))
 
 
 def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
@@ -200,7 +215,7 @@ def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offse
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(dev_status),
         _stream(stream)))
-    _count(3 if T > 0 else 1)
+    _count(_permute_launches(T, k))
 
 
 def moe_grouped_swiglu_workspace_size(max_rows: int, I: int) -> int:
@@ -296,3 +311,29 @@ def moe_bias_update(E, counts, bias, u, rule=MOE_BIAS_SIGN, stream=None):
     _check("moe_bias_update", lib().moe_bias_update(E, _ptr(counts), _ptr(bias), float(u), rule,
                                                     _stream(stream)))
     _count(1)
+
+
+def moe_route_bucket(p: RouteParams, valid_tokens, logits, sel_bias, topk_ids, gates,
+                     dev_status=None, stream=None):
+    _check("moe_route_bucket", lib().moe_route_bucket(
+        ctypes.byref(p), _ptr(valid_tokens), _ptr(logits), _ptr(sel_bias), _ptr(topk_ids),
+        _ptr(gates), _ptr(dev_status), _stream(stream)))
+    _count(1 if p.T > 0 else 0)
+
+
+def moe_permute_bucket(T, d, E, k, capacity, valid_tokens, topk_ids, x, x_perm, counts, offsets,
+                       row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status=None,
+                       stream=None):
+    _check("moe_permute_bucket", lib().moe_permute_bucket(
+        T, d, E, k, capacity, _ptr(valid_tokens), _ptr(topk_ids), _ptr(x), _ptr(x_perm),
+        _ptr(counts), _ptr(offsets), _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped),
+        _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+    _count(_permute_launches(T, k))
+
+
+def moe_combine_bucket(T, k, d, valid_tokens, y, y_rows, route_to_row, gates, shared_y,
+                       accumulate, out, dev_status=None, stream=None):
+    _check("moe_combine_bucket", lib().moe_combine_bucket(
+        T, k, d, _ptr(valid_tokens), _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates),
+        _ptr(shared_y), int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
+    _count(1 if T > 0 else 0)

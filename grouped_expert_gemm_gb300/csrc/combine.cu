@@ -24,12 +24,23 @@ __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
                const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
-               uint32_t* __restrict__ dev_status) {
+               uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid) {
   pdl_wait();
   constexpr int UNROLL = KMAX >= 8 ? 1 : (KMAX >= 4 ? 2 : 4);
   __shared__ int32_t s_row[KMAX];
   __shared__ float s_gate[KMAX];
-  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+  const int64_t T_live = valid == nullptr ? T : min(static_cast<int64_t>(T),
+                                                    static_cast<int64_t>(max(__ldg(valid), 0)));
+  // Padding slots of a fixed token bucket get a zero output (left as they are
+  // when accumulating): they never receive a routed contribution.
+  for (int64_t t = T_live + blockIdx.x; t < T; t += gridDim.x) {
+    if (accumulate) break;
+    for (int c = threadIdx.x; c < chunks; c += kCombThreads) {
+      out[(t * chunks + c) * 2] = make_float4(0.f, 0.f, 0.f, 0.f);
+      out[(t * chunks + c) * 2 + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  for (int64_t t = blockIdx.x; t < T_live; t += gridDim.x) {
     if (threadIdx.x < KMAX) {
       int32_t r = -1;
       float g = 0.0f;
@@ -103,7 +114,8 @@ using namespace moe;
 static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
                                const int32_t* route_to_row, const float* gates,
                                const moe_bf16* shared_y, int32_t accumulate, float* out,
-                               uint32_t* dev_status, moe_stream_t stream);
+                               uint32_t* dev_status, moe_stream_t stream,
+                               const int32_t* valid = nullptr);
 
 MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
                                const int32_t* route_to_row, const float* gates,
@@ -112,6 +124,16 @@ MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* 
   if (T > 0 && gates == nullptr) return MOE_ERR_INVALID_ARG;
   return combine_impl(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, out,
                       dev_status, stream);
+}
+
+MOE_API moe_status moe_combine_bucket(int32_t T, int32_t k, int32_t d, const int32_t* valid_tokens,
+                                      const moe_bf16* y, int64_t y_rows,
+                                      const int32_t* route_to_row, const float* gates,
+                                      const moe_bf16* shared_y, int32_t accumulate, float* out,
+                                      uint32_t* dev_status, moe_stream_t stream) {
+  if (valid_tokens == nullptr || (T > 0 && gates == nullptr)) return MOE_ERR_INVALID_ARG;
+  return combine_impl(T, k, d, y, y_rows, route_to_row, gates, shared_y, accumulate, out,
+                      dev_status, stream, valid_tokens);
 }
 
 MOE_API moe_status moe_unpermute_grad(int32_t T, int32_t k, int32_t d, const moe_bf16* dx_perm,
@@ -125,7 +147,7 @@ MOE_API moe_status moe_unpermute_grad(int32_t T, int32_t k, int32_t d, const moe
 static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64_t y_rows,
                                const int32_t* route_to_row, const float* gates,
                                const moe_bf16* shared_y, int32_t accumulate, float* out,
-                               uint32_t* dev_status, moe_stream_t stream) {
+                               uint32_t* dev_status, moe_stream_t stream, const int32_t* valid) {
   if (T < 0 || k <= 0 || d <= 0 || y_rows < 0) return MOE_ERR_INVALID_ARG;
   if (k > 16 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
@@ -141,7 +163,7 @@ static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* 
   launch(combine_kernel<K>, dim3(grid), dim3(kCombThreads), 0, s, T, k, chunks,               \
          reinterpret_cast<const uint4*>(y), y_rows, route_to_row, gates,                      \
          reinterpret_cast<const uint4*>(shared_y), static_cast<int>(accumulate),              \
-         reinterpret_cast<float4*>(out), dev_status)
+         reinterpret_cast<float4*>(out), dev_status, valid)
   if (k <= 1) MOE_COMBINE_CASE(1);
   else if (k <= 2) MOE_COMBINE_CASE(2);
   else if (k <= 4) MOE_COMBINE_CASE(4);

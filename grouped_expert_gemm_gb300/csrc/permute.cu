@@ -33,6 +33,13 @@ constexpr int kMinTileRoutes = 2048;
 constexpr int kMaxTiles = 128;
 constexpr int kCopyThreads = 256;
 
+// Routes of the first min(*valid, T) tokens (all T*k routes without a valid count).
+__device__ __forceinline__ int valid_routes(int R, int k, const int32_t* __restrict__ valid) {
+  if (valid == nullptr) return R;
+  const int v = __ldg(valid);
+  return v <= 0 ? 0 : min(R, v * k);
+}
+
 struct PermTiling {
   int routes_per_tile;
   int n_tiles;
@@ -48,14 +55,16 @@ PermTiling permute_tiling(int64_t R) {
 }
 
 __global__ void __launch_bounds__(kHistThreads)
-permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
-             int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status) {
+permute_hist(int R, int E, int k, int routes_per_tile, const int32_t* __restrict__ ids,
+             int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status,
+             const int32_t* __restrict__ valid) {
   extern __shared__ int32_t sh[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   pdl_wait();
   __syncthreads();
+  const int R_live = valid_routes(R, k, valid);
   const int r0 = blockIdx.x * routes_per_tile;
-  const int r1 = min(R, r0 + routes_per_tile);
+  const int r1 = min(R_live, r0 + routes_per_tile);
   bool bad = false;
   for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
     const int e = __ldg(ids + r);
@@ -69,11 +78,12 @@ permute_hist(int R, int E, int routes_per_tile, const int32_t* __restrict__ ids,
 }
 
 __global__ void __launch_bounds__(kRankThreads)
-permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
+permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity,
              const int32_t* __restrict__ ids, const int32_t* __restrict__ hist,
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ n_dropped, int32_t* __restrict__ row_to_route,
-             int32_t* __restrict__ route_to_row, uint32_t* __restrict__ dev_status) {
+             int32_t* __restrict__ route_to_row, uint32_t* __restrict__ dev_status,
+             const int32_t* __restrict__ valid) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kRankWarps][E]
   int32_t* off = cnt + kRankWarps * E;  // [E]
@@ -81,13 +91,18 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int tile = blockIdx.x;
 
-  const int r0 = tile * routes_per_tile;
-  const int r1 = min(R, r0 + routes_per_tile);
-  const int sub = (r1 - r0 + kRankWarps - 1) / kRankWarps;
-  const int s0 = r0 + w * sub, s1 = min(r1, s0 + sub);
   for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
   pdl_wait();
   __syncthreads();
+  // Routes at or past R_live belong to masked padding tokens of a fixed bucket:
+  // they are neither counted, admitted nor dropped, and map to row -1.
+  const int R_live = valid_routes(R, k, valid);
+  const int r0 = tile * routes_per_tile;
+  const int r1 = min(R_live, r0 + routes_per_tile);
+  const int sub = (max(r1 - r0, 0) + kRankWarps - 1) / kRankWarps;
+  const int s0 = r0 + w * sub, s1 = min(r1, s0 + sub);
+  for (int r = max(r0, R_live) + threadIdx.x; r < min(R, r0 + routes_per_tile); r += blockDim.x)
+    route_to_row[r] = -1;
   // per-warp expert counts of the warp's contiguous sub-range
   for (int r = s0 + lane; r < s1; r += 32) {
     const int ee = __ldg(ids + r);
@@ -138,7 +153,7 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
       offsets[e] = before + incl - c;
       if (e == E - 1) {
         offsets[E] = before + incl;
-        *n_dropped = R - (before + incl);
+        *n_dropped = R_live - (before + incl);
       }
     }
   }
@@ -185,11 +200,13 @@ permute_rank(int R, int E, int routes_per_tile, int n_tiles, int capacity,
 // One warp per token: read the row once, store it to each admitted row.
 __global__ void __launch_bounds__(kCopyThreads)
 permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
-             const uint4* __restrict__ x, uint4* __restrict__ x_perm) {
+             const uint4* __restrict__ x, uint4* __restrict__ x_perm,
+             const int32_t* __restrict__ valid) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
-  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+  const int T_live = valid_routes(T, 1, valid);
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T_live; t += gridDim.x * warps) {
     const int32_t my_row = lane < k ? __ldg(route_to_row + static_cast<int64_t>(t) * k + lane) : -1;
     const uint4* src = x + static_cast<int64_t>(t) * chunks;
     // The chunk loop runs uniformly over the warp (lanes past the row end only
@@ -226,11 +243,12 @@ MOE_API size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E) {
   return c.off + 256;
 }
 
-MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
-                               const int32_t* topk_ids, const moe_bf16* x, moe_bf16* x_perm,
-                               int32_t* counts, int32_t* offsets, int32_t* row_to_route,
-                               int32_t* route_to_row, int32_t* n_dropped, void* ws,
-                               size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream) {
+static moe_status permute_impl(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                               const int32_t* valid, const int32_t* topk_ids, const moe_bf16* x,
+                               moe_bf16* x_perm, int32_t* counts, int32_t* offsets,
+                               int32_t* row_to_route, int32_t* route_to_row, int32_t* n_dropped,
+                               void* ws, size_t ws_bytes, uint32_t* dev_status,
+                               moe_stream_t stream) {
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
   if (E > 512 || k > 16 || d % 8 != 0 || static_cast<int64_t>(T) * k >= (int64_t(1) << 31))
     return MOE_ERR_UNSUPPORTED;
@@ -247,25 +265,46 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
   const size_t rank_smem = (static_cast<size_t>(kRankWarps) * E + E) * sizeof(int32_t);
   if (R == 0) {
     // No routes: one rank block with no tiles writes empty counts and offsets.
-    launch(permute_rank, dim3(1), dim3(kRankThreads), rank_smem, s, 0, E, 1, 0, capacity,
+    launch(permute_rank, dim3(1), dim3(kRankThreads), rank_smem, s, 0, E, k, 1, 0, capacity,
            topk_ids, static_cast<const int32_t*>(nullptr), counts, offsets, n_dropped,
-           row_to_route, route_to_row, dev_status);
+           row_to_route, route_to_row, dev_status, static_cast<const int32_t*>(nullptr));
     return launch_status();
   }
   if (tl.n_tiles > 1)
-    launch(permute_hist, dim3(tl.n_tiles), dim3(kHistThreads), E * sizeof(int32_t), s, R, E,
-           tl.routes_per_tile, topk_ids, hist, dev_status);
-  launch(permute_rank, dim3(tl.n_tiles), dim3(kRankThreads), rank_smem, s, R, E,
+    launch(permute_hist, dim3(tl.n_tiles), dim3(kHistThreads), E * sizeof(int32_t), s, R, E, k,
+           tl.routes_per_tile, topk_ids, hist, dev_status, valid);
+  launch(permute_rank, dim3(tl.n_tiles), dim3(kRankThreads), rank_smem, s, R, E, k,
          tl.routes_per_tile, tl.n_tiles, capacity, topk_ids,
          static_cast<const int32_t*>(tl.n_tiles > 1 ? hist : nullptr), counts, offsets, n_dropped,
-         row_to_route, route_to_row, dev_status);
+         row_to_route, route_to_row, dev_status, valid);
   const int warps = kCopyThreads / 32;
   int64_t blocks = ceil_div(T, warps);
   if (blocks > 152 * 16) blocks = 152 * 16;
   launch(permute_copy, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k, d / 8,
          static_cast<const int32_t*>(route_to_row), reinterpret_cast<const uint4*>(x),
-         reinterpret_cast<uint4*>(x_perm));
+         reinterpret_cast<uint4*>(x_perm), valid);
   return launch_status();
+}
+
+MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                               const int32_t* topk_ids, const moe_bf16* x, moe_bf16* x_perm,
+                               int32_t* counts, int32_t* offsets, int32_t* row_to_route,
+                               int32_t* route_to_row, int32_t* n_dropped, void* ws,
+                               size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream) {
+  return permute_impl(T, d, E, k, capacity, nullptr, topk_ids, x, x_perm, counts, offsets,
+                      row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status, stream);
+}
+
+MOE_API moe_status moe_permute_bucket(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                                      const int32_t* valid_tokens, const int32_t* topk_ids,
+                                      const moe_bf16* x, moe_bf16* x_perm, int32_t* counts,
+                                      int32_t* offsets, int32_t* row_to_route,
+                                      int32_t* route_to_row, int32_t* n_dropped, void* ws,
+                                      size_t ws_bytes, uint32_t* dev_status,
+                                      moe_stream_t stream) {
+  if (valid_tokens == nullptr) return MOE_ERR_INVALID_ARG;
+  return permute_impl(T, d, E, k, capacity, valid_tokens, topk_ids, x, x_perm, counts, offsets,
+                      row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -82,11 +82,19 @@ __global__ void __launch_bounds__(kTokensPerBlock * 32)
 route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale,
              const float* __restrict__ logits, const float* __restrict__ sel_bias,
              int32_t* __restrict__ topk_ids, float* __restrict__ gates,
-             uint32_t* __restrict__ dev_status) {
+             uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTokensPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
+  if (valid != nullptr && t >= __ldg(valid)) {
+    // padding slot of a fixed token bucket: no expert identity, zero gate
+    if (lane < k) {
+      topk_ids[static_cast<int64_t>(t) * k + lane] = MOE_ROUTE_MASKED;
+      gates[static_cast<int64_t>(t) * k + lane] = 0.0f;
+    }
+    return;
+  }
   const float* row = logits + static_cast<int64_t>(t) * E;
 
   float sel[VPL];  // selection score: the logit, or the corrected sigmoid s~
@@ -197,13 +205,14 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
 
 template <bool GROUPED>
 moe_status launch_route(const moe_route_params* p, const float* logits, const float* sel_bias,
-                        int32_t* ids, float* gates, uint32_t* st, cudaStream_t s) {
+                        int32_t* ids, float* gates, uint32_t* st, cudaStream_t s,
+                        const int32_t* valid) {
   const int vpl = static_cast<int>(ceil_div(p->E, 32));
   const dim3 grid(static_cast<unsigned>(ceil_div(p->T, kTokensPerBlock)));
   const dim3 block(kTokensPerBlock * 32);
 #define MOE_ROUTE_CASE(V)                                                                \
   launch(route_kernel<V, GROUPED>, grid, block, 0, s, p->T, p->E, p->k, p->n_group,        \
-         p->topk_group, p->route_scale, logits, sel_bias, ids, gates, st)
+         p->topk_group, p->route_scale, logits, sel_bias, ids, gates, st, valid)
   if (vpl <= 1) MOE_ROUTE_CASE(1);
   else if (vpl <= 2) MOE_ROUTE_CASE(2);
   else if (vpl <= 4) MOE_ROUTE_CASE(4);
@@ -227,7 +236,7 @@ __global__ void sigmoid_det_kernel(int64_t n, const float* __restrict__ z, float
 
 using namespace moe;
 
-MOE_API moe_status moe_route(const moe_route_params* p, const float* logits,
+static moe_status route_impl(const moe_route_params* p, const int32_t* valid, const float* logits,
                              const float* sel_bias, int32_t* topk_ids, float* gates,
                              uint32_t* dev_status, moe_stream_t stream) {
   if (p == nullptr || logits == nullptr || topk_ids == nullptr || gates == nullptr)
@@ -237,7 +246,8 @@ MOE_API moe_status moe_route(const moe_route_params* p, const float* logits,
   if (p->T == 0) return MOE_OK;
   if (p->score_fn == MOE_SCORE_SOFTMAX) {
     if (sel_bias != nullptr) return MOE_ERR_INVALID_ARG;
-    return launch_route<false>(p, logits, nullptr, topk_ids, gates, dev_status, as_cuda(stream));
+    return launch_route<false>(p, logits, nullptr, topk_ids, gates, dev_status, as_cuda(stream),
+                               valid);
   }
   if (p->score_fn != MOE_SCORE_SIGMOID_GROUP) return MOE_ERR_INVALID_ARG;
   if (p->n_group <= 0 || p->topk_group <= 0 || p->topk_group > p->n_group ||
@@ -245,7 +255,22 @@ MOE_API moe_status moe_route(const moe_route_params* p, const float* logits,
     return MOE_ERR_INVALID_ARG;
   if (p->n_group > 32 || p->E / p->n_group < 2 || p->topk_group * (p->E / p->n_group) < p->k)
     return MOE_ERR_UNSUPPORTED;
-  return launch_route<true>(p, logits, sel_bias, topk_ids, gates, dev_status, as_cuda(stream));
+  return launch_route<true>(p, logits, sel_bias, topk_ids, gates, dev_status, as_cuda(stream),
+                            valid);
+}
+
+MOE_API moe_status moe_route(const moe_route_params* p, const float* logits,
+                             const float* sel_bias, int32_t* topk_ids, float* gates,
+                             uint32_t* dev_status, moe_stream_t stream) {
+  return route_impl(p, nullptr, logits, sel_bias, topk_ids, gates, dev_status, stream);
+}
+
+MOE_API moe_status moe_route_bucket(const moe_route_params* p, const int32_t* valid_tokens,
+                                    const float* logits, const float* sel_bias,
+                                    int32_t* topk_ids, float* gates, uint32_t* dev_status,
+                                    moe_stream_t stream) {
+  if (valid_tokens == nullptr) return MOE_ERR_INVALID_ARG;
+  return route_impl(p, valid_tokens, logits, sel_bias, topk_ids, gates, dev_status, stream);
 }
 
 MOE_API moe_status moe_sigmoid_det(int64_t n, const float* z, float* s, moe_stream_t stream) {

@@ -3,6 +3,9 @@
 ``MoELayer``       route -> permute (capacity or dropless) -> grouped SwiGLU over
                    the expert segments (+ an optional always-on shared expert)
                    -> gate-weighted fp32 combine.
+``DecodeBucket``   a fixed token bucket for decode steps: stable buffers, one
+                   captured CUDA graph of the bucketed layer, a device-side
+                   valid-token count, exact admission and an eager fallback.
 ``PooledMoELayer`` route -> for each wave: pool pack (sender) -> pool compact
                    (receiver; the pools are read in place, there is no
                    communication) -> grouped SwiGLU over the local-expert
@@ -243,3 +246,99 @@ class PooledMoELayer:
         return self.out
 
     forward_host = MoELayer.forward_host
+
+
+class DecodeBucket:
+    """Decode steps replayed from one CUDA graph over a fixed bucket of B token slots.
+
+    [M6.6] 0x05C-0x05F: the graph keeps stable buffers (logits, hidden rows, routes,
+    gates, expert rows, output) for B slots; the real token count lives in a device
+    int32 that changes each step, and padding slots are masked before they get an
+    expert identity (moe_route_bucket / moe_permute_bucket / moe_combine_bucket).
+    A step replays the graph only when an exact predicate holds: decode phase, the
+    same immutable key (shapes, dtypes, capacity, router, weight and bias
+    addresses), 1 <= T <= B and a captured graph; otherwise it runs the eager layer
+    on exactly its T tokens.  Either way the real tokens get the same result.
+    """
+
+    def __init__(self, B: int, d: int, E: int, k: int, I: int, w_gate, w_up, w_down,
+                 capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
+                 topk_group: int = 1, route_scale: float = 1.0, sel_bias=None, device="cuda"):
+        self.B, self.d, self.E, self.k, self.I = B, d, E, k, I
+        self.cfg = dict(d=d, E=E, k=k, I=I, w_gate=w_gate, w_up=w_up, w_down=w_down,
+                        capacity=capacity, score_fn=score_fn, n_group=n_group,
+                        topk_group=topk_group, route_scale=route_scale, sel_bias=sel_bias,
+                        device=device)
+        self.layer = MoELayer(B, **self.cfg)
+        dev = torch.device(device)
+        self.logits = torch.zeros((B, E), dtype=torch.float32, device=dev)
+        self.x = torch.zeros((B, d), dtype=torch.bfloat16, device=dev)
+        self.valid = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.key = self.make_key(d, E, k, I, capacity, score_fn, n_group, topk_group,
+                                 route_scale, w_gate, w_up, w_down, sel_bias)
+        self.graph = None
+        self._eager = {}
+
+    @staticmethod
+    def make_key(d, E, k, I, capacity, score_fn, n_group, topk_group, route_scale, w_gate, w_up,
+                 w_down, sel_bias=None):
+        """The immutable part of a step: a replay is valid only for an equal key."""
+        ptr = lambda t: None if t is None else (t.data_ptr(), tuple(t.shape), str(t.dtype))
+        return (d, E, k, I, capacity, score_fn, n_group, topk_group, float(route_scale),
+                ptr(w_gate), ptr(w_up), ptr(w_down), ptr(sel_bias))
+
+    def step(self, stream=None):
+        """The bucketed layer on the stable buffers (what the graph holds)."""
+        L = self.layer
+        R = self.B * self.k
+        abi.moe_route_bucket(L.params, self.valid, self.logits, L.sel_bias, L.topk_ids, L.gates,
+                             L.dev_status, stream)
+        abi.moe_permute_bucket(self.B, self.d, self.E, self.k, L.capacity, self.valid,
+                               L.topk_ids, self.x, L.x_perm, L.counts, L.offsets, L.row_to_route,
+                               L.route_to_row, L.n_dropped, L.perm_ws, L.perm_ws_bytes,
+                               L.dev_status, stream)
+        L.experts_gate_up(stream)
+        L.experts_down(stream)
+        abi.moe_combine_bucket(self.B, self.k, self.d, self.valid, L.y, R, L.route_to_row,
+                               L.gates, None, 0, L.out, L.dev_status, stream)
+
+    def capture(self, stream=None):
+        """Warm the calls once on the stable buffers, then capture the step (on `stream`,
+        or on a side stream of its own: graphs cannot be captured on the default stream)."""
+        s = torch.cuda.Stream(self.layer.out.device) if stream is None else stream
+        with torch.cuda.stream(s):
+            self.valid.fill_(self.B)
+            self.step(s)
+        s.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            self.step(None)
+        return self.graph
+
+    def admit(self, T: int, phase: str = "decode", key=None):
+        """Exact admission predicate: (True, "replay") or (False, reason)."""
+        if phase != "decode":
+            return False, "phase_not_decode"
+        if key is not None and key != self.key:
+            return False, "graph_key_mismatch"
+        if T < 1 or T > self.B:
+            return False, "token_capacity_exceeded" if T > self.B else "empty_step"
+        if self.graph is None:
+            return False, "graph_not_captured"
+        return True, "replay"
+
+    def forward(self, logits, x, phase: str = "decode", key=None, stream=None):
+        """One step on T = logits.shape[0] tokens; returns (out [T, d] fp32, path)."""
+        T = int(logits.shape[0])
+        ok, why = self.admit(T, phase, key)
+        s = torch.cuda.current_stream() if stream is None else stream
+        if ok:
+            with torch.cuda.stream(s):
+                self.logits[:T].copy_(logits, non_blocking=True)
+                self.x[:T].copy_(x, non_blocking=True)
+                self.valid.fill_(T)
+                self.graph.replay()
+            return self.layer.out[:T], "replay"
+        if T not in self._eager:
+            self._eager[T] = MoELayer(T, **self.cfg)
+        return self._eager[T].forward(logits, x, s), why

@@ -61,6 +61,7 @@ enum {
 };
 
 #define MOE_POOL_EMPTY 0xFFFFu /* header element of an unused pool row */
+#define MOE_ROUTE_MASKED (-1)  /* topk_ids of a masked padding slot of a token bucket */
 
 /* Library version (major*10000 + minor*100 + patch) and a status message. */
 int32_t moe_version(void);
@@ -286,6 +287,39 @@ moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t 
  * MOE_DEV_BAD_ROW and give -1.                                               */
 moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b, int64_t b_len,
                            int32_t* out, uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fixed token bucket (decode graphs)                                       */
+/* ------------------------------------------------------------------------ */
+/* [M6.6] 0x05C-0x05F: a decode graph keeps stable buffers for a bucket of T
+ * token slots while the number of real tokens changes on the device each step.
+ * These calls are moe_route / moe_permute / moe_combine with T = the bucket
+ * capacity and one more argument, valid_tokens: a DEVICE int32 read by the
+ * kernels, so a captured graph can be replayed with a new count.  Slots
+ * t >= *valid_tokens (clamped to [0, T]) are padding and are masked before
+ * they acquire an expert identity:
+ *   moe_route_bucket    writes topk_ids = MOE_ROUTE_MASKED and gates = 0 there;
+ *   moe_permute_bucket  never reads their ids, neither counts, admits nor drops
+ *                       their routes (n_dropped counts real routes only) and
+ *                       maps them to row -1; the real routes get exactly the
+ *                       rows an unbucketed moe_permute of the real tokens gives;
+ *   moe_combine_bucket  writes zero output rows for them (leaves them as they
+ *                       are when accumulating).
+ * The capacity argument of moe_permute_bucket is fixed at capture (it is part
+ * of the graph's key).  Everything else as the unbucketed calls.            */
+moe_status moe_route_bucket(const moe_route_params* p, const int32_t* valid_tokens,
+                            const float* logits, const float* sel_bias, int32_t* topk_ids,
+                            float* gates, uint32_t* dev_status, moe_stream_t stream);
+moe_status moe_permute_bucket(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                              const int32_t* valid_tokens, const int32_t* topk_ids,
+                              const moe_bf16* x, moe_bf16* x_perm, int32_t* counts,
+                              int32_t* offsets, int32_t* row_to_route, int32_t* route_to_row,
+                              int32_t* n_dropped, void* ws, size_t ws_bytes, uint32_t* dev_status,
+                              moe_stream_t stream);
+moe_status moe_combine_bucket(int32_t T, int32_t k, int32_t d, const int32_t* valid_tokens,
+                              const moe_bf16* y, int64_t y_rows, const int32_t* route_to_row,
+                              const float* gates, const moe_bf16* shared_y, int32_t accumulate,
+                              float* out, uint32_t* dev_status, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Backward of the transpose                                                */

@@ -1,0 +1,113 @@
+"""Decode graphs over a fixed token bucket ([M6.6] 0x05C-0x05F): padding slots are
+masked before they get expert identities, a replay gives the real tokens exactly
+the eager layer's result, and the exact admission predicate falls back to the
+eager layer without changing the result."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from moe_check import bits, host
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from grouped_expert_gemm_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def bucket():
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.decode(128)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    b = g.DecodeBucket(128, w.d, w.E, w.k, w.I, wg, wu, wd, device=DEV)
+    b.capture()
+    return b
+
+
+def _inputs(T, seed, E=128, d=2048):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    logits = torch.randn((T, E), generator=gen, device=DEV)
+    x = torch.randn((T, d), generator=gen, device=DEV).to(torch.bfloat16)
+    return logits, x
+
+
+@pytest.mark.parametrize("T", [1, 37, 128, 5])
+def test_replay_equals_eager_on_the_real_tokens(bucket, T):
+    import grouped_expert_gemm_gb300 as g
+    logits, x = _inputs(T, seed=T)
+    out, path = bucket.forward(logits, x)
+    torch.cuda.synchronize()
+    assert path == "replay"
+    L = bucket.layer
+    assert int(L.dev_status.item()) == 0
+    eager = g.MoELayer(T, **bucket.cfg)
+    ref = eager.forward(logits, x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)  # same routes, rows, tiles: identical bits
+    # padding slots never acquired expert identities or output
+    k = bucket.k
+    assert torch.all(L.topk_ids[T:] == g.MOE_ROUTE_MASKED)
+    assert torch.all(L.gates[T:] == 0)
+    assert torch.all(L.route_to_row[T * k:] == -1)
+    assert int(L.counts.sum().item()) == T * k == int(L.offsets[-1].item())
+    assert int(L.n_dropped.item()) == 0
+    assert torch.all(L.out[T:] == 0)
+    assert torch.equal(L.route_to_row[: T * k], eager.route_to_row[: T * k])
+
+
+def test_exact_admission_and_fallback(bucket):
+    import grouped_expert_gemm_gb300 as g
+    logits, x = _inputs(129, seed=9)
+    out, path = bucket.forward(logits, x)
+    assert path == "token_capacity_exceeded"
+    ref = g.MoELayer(129, **bucket.cfg).forward(logits, x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    small_l, small_x = _inputs(16, seed=10)
+    assert bucket.forward(small_l, small_x, phase="prefill")[1] == "phase_not_decode"
+    other = bucket.key[:4] + (bucket.key[4] + 1,) + bucket.key[5:]
+    assert bucket.forward(small_l, small_x, key=other)[1] == "graph_key_mismatch"
+    assert bucket.forward(small_l, small_x, key=bucket.key)[1] == "replay"
+
+
+@pytest.mark.parametrize("cap", [-1, 3])
+def test_permute_bucket_parity(cap):
+    import grouped_expert_gemm_gb300 as g
+    T, valid, d, E, k = 300, 211, 64, 32, 4
+    rng = np.random.default_rng(cap + 5)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[valid:] = 99999  # padding ids are garbage and must never be read
+    x = torch.randn((T, d), device=DEV).to(torch.bfloat16)
+    R = T * k
+    outs = dict(x_perm=torch.zeros((R, d), dtype=torch.bfloat16, device=DEV),
+                counts=torch.empty(E, dtype=torch.int32, device=DEV),
+                offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV),
+                r2r=torch.full((R,), -5, dtype=torch.int32, device=DEV),
+                inv=torch.full((R,), -5, dtype=torch.int32, device=DEV),
+                nd=torch.zeros(1, dtype=torch.int32, device=DEV))
+    wsb = g.moe_permute_workspace_size(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    vt = torch.tensor([valid], dtype=torch.int32, device=DEV)
+    g.moe_permute_bucket(T, d, E, k, cap, vt, torch.from_numpy(ids).to(DEV), x, outs["x_perm"],
+                         outs["counts"], outs["offsets"], outs["r2r"], outs["inv"], outs["nd"],
+                         ws, wsb, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0  # the garbage ids were never read
+    ref = oracle.permute(ids[:valid], E, cap)
+    acc = int(ref["offsets"][-1])
+    assert host(outs["counts"]).tolist() == ref["counts"].tolist()
+    assert host(outs["offsets"]).tolist() == ref["offsets"].tolist()
+    assert np.array_equal(host(outs["r2r"])[:acc], ref["row_to_route"])
+    inv = host(outs["inv"])
+    assert np.array_equal(inv[: valid * k], ref["route_to_row"])
+    assert np.all(inv[valid * k:] == -1)
+    assert int(outs["nd"].item()) == ref["n_dropped"]
+    assert np.array_equal(bits(outs["x_perm"])[:acc],
+                          oracle.gather_rows(bits(x), ref["row_to_route"], k))
