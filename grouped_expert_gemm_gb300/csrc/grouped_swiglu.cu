@@ -53,7 +53,6 @@ namespace {
 constexpr int kBM = 128;          // rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kMaxSeg = 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress = broken pipeline
@@ -70,10 +69,12 @@ template <int N_ATOMS>
 struct Geometry {
   static constexpr int kN = 64 * N_ATOMS;                  // MMA N
   static constexpr int kStageBytes = kABytes + N_ATOMS * kAtomBytes;
+  // As many stages as fit the same ~192 KB: narrower tiles keep more loads in flight.
+  static constexpr int kStages = N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8);
   static constexpr int kTmemCols = 2 * kN;                 // two accumulator buffers
   static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + 256 /*barriers*/ +
-                                    (3 * kMaxSeg + 16) * 4;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes +
+                                    (2 * kStages + 5) * 8 /*barriers*/ + (3 * kMaxSeg + 16) * 4;
 };
 
 struct GemmArgs {
@@ -466,6 +467,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b0,
                     const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
   using G = Geometry<N_ATOMS>;
+  constexpr int kStages = G::kStages;
   constexpr int kN = G::kN;
   constexpr int kBnOut = SWIGLU ? kN / 2 : kN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -1046,6 +1048,8 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
              dev_status, choose_m_outer(n_seg, max_rows, I, d)};
   cudaStream_t s = as_cuda(stream);
+  // The widest output tile the width allows (narrower tiles for one-token decode were
+  // measured slower: the few tiles there are bound by pipeline latency, not SM count).
   if (d % 256 == 0) {
     return pair_shape(n_seg, max_rows) ? launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s)
                                        : launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);

@@ -309,6 +309,12 @@ def test_grouped_swiglu_large_segments_row_block_outer_order(d, I):
     _gemm_case(2, d, I, [8191, 8193], sample=300)
 
 
+def test_grouped_swiglu_many_experts_few_rows():
+    # decode-like: 64 experts of a few rows each (single-CTA kernel, 2x128 gate/up tiles)
+    rng = np.random.default_rng(21)
+    _gemm_case(64, 128, 768, rng.integers(0, 20, size=64))
+
+
 def test_grouped_swiglu_gapped_segments():
     # segments with gaps between them (the pooled layout's fixed-stride arrays)
     _gemm_case(3, 128, 128, [100, 0, 250], begins=[0, 300, 600], max_rows=900)
