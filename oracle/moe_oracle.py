@@ -537,3 +537,107 @@ def bias_update(bias, counts, u: float, rule: str = "sign") -> np.ndarray:
     step = np.sign(err) if rule == "sign" else err
     inc = (np.float64(np.float32(u)) * step).astype(np.float32)
     return (b + inc).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# FP8 dispatch payload with fp32 scales  ([M6.6] 0x0AB "Deriving BF16 And FP8
+# Payloads", 0x0AC "Scale Tensor Ownership And Row Trace", 0x0AE "Router, Gate,
+# Combine, And Accumulation Dtypes")
+#
+# Readings (the pages name "FP8" and fp32 scales, one per row or one per 128
+# values of a row, but fix neither the FP8 format nor how a scale is chosen):
+#   * format: E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+#     infinities; S.1111.111 is NaN; largest finite value 448);
+#   * scale of a group: s = fp32(amax / 448), amax the largest |x| of the group
+#     (exact), s = 1 for an all-zero group; groups are the whole row, or 128
+#     consecutive values with a shorter last group when 128 does not divide d;
+#   * code: q = E4M3(fp32(x / s)), rounded to nearest with ties to even and
+#     saturated to +-448; the quotient is rounded to fp32 first, as a device
+#     computes it;
+#   * dequantized operand: xhat = bf16(fp32(decode(q) * s)), one fp32 rounding
+#     of the exact product, then one bf16 rounding: the expert arithmetic that
+#     follows is the bf16 path's.
+# ----------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+E4M3_NAN = 0x7F
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 codes (uint8) -> float64, from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    exp = (c >> 3) & 0xF
+    man = (c & 0x7).astype(np.float64)
+    mag = np.where(exp == 0, man / 8.0 * 2.0 ** -6, (1.0 + man / 8.0) * np.exp2(exp - 7.0))
+    mag = np.where((exp == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+# the 127 finite non-negative E4M3 values in code order (code i has value _E4M3_POS[i])
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """float values -> E4M3 codes: nearest finite value, ties to the even code,
+    magnitudes above 448 saturate to 448, NaN -> 0x7F (sign kept), sign of zero kept."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.abs(v)
+    sat = np.minimum(mag, E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, sat, side="left"), 0, 0x7E)  # first value >= sat
+    lo = np.maximum(hi - 1, 0)
+    d_lo = sat - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - sat
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(np.isnan(v), E4M3_NAN, code)
+    neg = np.signbit(v)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def n_scale_groups(d: int, group: int) -> int:
+    """Scales per row: 1 for a whole-row scale (group 0), ceil(d / group) otherwise."""
+    return 1 if group == 0 else -(-d // group)
+
+
+def quantize_fp8(x_bits: np.ndarray, group: int):
+    """bf16 rows [n, d] -> (E4M3 codes uint8 [n, d], fp32 scales [n, G]).
+
+    group 0: one scale per row; group 128: one scale per 128 values of a row.
+    """
+    x = bf16_to_f64(np.asarray(x_bits)).astype(np.float32)  # exact
+    n, d = x.shape
+    g = d if group == 0 else group
+    G = n_scale_groups(d, group)
+    codes = np.empty((n, d), dtype=np.uint8)
+    scales = np.empty((n, G), dtype=np.float32)
+    for j in range(G):
+        blk = x[:, j * g:(j + 1) * g]
+        amax = np.abs(blk).max(axis=1) if blk.shape[1] else np.zeros(n, np.float32)
+        s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        scales[:, j] = s
+        quot = (blk / s[:, None]).astype(np.float32)  # IEEE fp32 division
+        codes[:, j * g:(j + 1) * g] = e4m3_encode(quot)
+    return codes, scales
+
+
+def dequantize_fp8(codes: np.ndarray, scales: np.ndarray, group: int) -> np.ndarray:
+    """(E4M3 codes [n, d], fp32 scales [n, G]) -> bf16 bits [n, d] of the dequantized rows."""
+    c = np.asarray(codes)
+    n, d = c.shape
+    g = d if group == 0 else group
+    s_full = np.repeat(np.asarray(scales, dtype=np.float64), g, axis=1)[:, :d]
+    prod = e4m3_decode(c) * s_full          # exact in float64 (4 x 24 significant bits)
+    return f64_to_bf16(prod.astype(np.float32).astype(np.float64))
+
+
+def payload_bytes(rows: int, d: int, mode: str, group: int = 128) -> int:
+    """Logical dispatch payload of `rows` routed rows of width d ([M6.6] 0x0AB):
+    bf16: rows*d*2; fp8_row: rows*d + rows*4; fp8_block: rows*d + rows*ceil(d/group)*4."""
+    if mode == "bf16":
+        return rows * d * 2
+    if mode == "fp8_row":
+        return rows * d + rows * 4
+    if mode == "fp8_block":
+        return rows * d + rows * (-(-d // group)) * 4
+    raise ValueError(mode)

@@ -621,3 +621,150 @@ def test_m62_controller_step_fixture():
     assert np.all(np.sign(b1) == np.sign(c.mean() - c))
     bp = oracle.bias_update(b0, c, 0.01, "proportional")
     np.testing.assert_allclose(bp, 0.01 * (c.mean() - c), rtol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# FP8 dispatch payload ([M6.6] 0x0AB-0x0AF)
+# ----------------------------------------------------------------------------
+
+def test_m66_payload_ledger_table():
+    fx = load("m66_fp8_payload_ledger.json")
+    for row in fx["table"]:
+        for mode in ("bf16", "fp8_row", "fp8_block"):
+            assert oracle.payload_bytes(fx["rows"], row["d"], mode, fx["group"]) == row[mode], (row, mode)
+    # the d = 3 row: fp8 plus scales is larger than bf16
+    assert oracle.payload_bytes(6, 3, "fp8_row") > oracle.payload_bytes(6, 3, "bf16")
+
+
+def _torch_e4m3_decode(codes):
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_matches_library_format_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = om.e4m3_decode(codes)
+    lib = _torch_e4m3_decode(codes)
+    assert np.array_equal(np.isnan(mine), np.isnan(lib))
+    fin = ~np.isnan(lib)
+    assert np.array_equal(mine[fin], lib[fin])
+    assert np.array_equal(np.signbit(mine[fin]), np.signbit(lib[fin]))
+    # format landmarks: 2 NaN codes, 254 finite, largest 448, smallest normal 2^-6, subnormal 2^-9
+    assert np.isnan(mine).sum() == 2 and np.nanmax(mine) == 448.0
+    assert mine[0x08] == 2.0 ** -6 and mine[0x01] == 2.0 ** -9 and mine[0x38] == 1.0
+
+
+def test_e4m3_encode_matches_library_rounding_in_range():
+    """Nearest-even rounding against the library conversion on every code value,
+    every midpoint (the ties), one fp32 ulp either side of each midpoint and random
+    values; the library does not saturate, so only |v| < 464 is compared there."""
+    pos = om.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (pos[:-1] + pos[1:]) / 2
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)  # midpoints are fp32-exact
+    up = np.nextafter(mids32, np.float32(np.inf))
+    dn = np.nextafter(mids32, np.float32(0))
+    rng = np.random.default_rng(0)
+    rnd = np.concatenate([rng.uniform(0, 463, 20000), rng.uniform(0, 2 ** -5, 5000)]).astype(np.float32)
+    v = np.concatenate([pos, mids32, up, dn, rnd, [463.99]]).astype(np.float32)
+    v = np.concatenate([v, -v])
+    mine = om.e4m3_encode(v)
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, lib)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    v = np.array([448.0, 464.0, 465.0, 1e6, 3e38, -1e9, np.nan], np.float32)
+    assert om.e4m3_encode(v).tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7F]
+
+
+def _bf16_rows(rng, n, d, scale=1.0):
+    return oracle.f64_to_bf16(rng.standard_normal((n, d)) * scale)
+
+
+@pytest.mark.parametrize("group,d", [(0, 64), (128, 256), (128, 200), (0, 3), (128, 3)])
+def test_quantize_invariants(group, d):
+    rng = np.random.default_rng(d + group)
+    xb = _bf16_rows(rng, 9, d)
+    xb[3] = 0  # an all-zero row
+    xb[4, : min(d, 100)] = oracle.f64_to_bf16(rng.standard_normal(min(d, 100)) * 1e-3)
+    q, s = oracle.quantize_fp8(xb, group)
+    G = oracle.n_scale_groups(d, group)
+    assert s.shape == (9, G) and q.shape == (9, d)
+    g = d if group == 0 else group
+    x = oracle.bf16_to_f64(xb)
+    dec = om.e4m3_decode(q)
+    for i in range(9):
+        for j in range(G):
+            blk = x[i, j * g:(j + 1) * g]
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert s[i, j] == 1.0 and np.all(q[i, j * g:(j + 1) * g] & 0x7F == 0)
+                continue
+            # the scale maps the group's largest magnitude onto the largest code
+            assert abs(float(s[i, j]) * 448 - amax) <= amax * 2 ** -23
+            big = np.argmax(np.abs(blk))
+            assert q[i, j * g + big] & 0x7F == 0x7E
+            # every code is the nearest E4M3 value to x / s (brute force over all codes)
+            ratio = blk / float(s[i, j])
+            allv = om.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+            dist = np.abs(np.abs(ratio)[:, None] - allv[None, :]).min(axis=1)
+            got = np.abs(np.abs(ratio) - np.abs(dec[i, j * g:(j + 1) * g]))
+            assert np.all(got <= dist + 1e-6 * np.abs(ratio))
+            assert np.all(np.sign(dec[i, j * g:(j + 1) * g]) * np.sign(blk) >= 0)
+
+
+def test_quantize_exact_on_representable_rows():
+    """A row whose values are E4M3 values times a power of two, with its largest
+    magnitude 448 * 2^-7, quantizes to exactly those codes and dequantizes to x."""
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 0x7F, (5, 128)).astype(np.uint8)
+    codes[rng.random((5, 128)) < 0.5] |= 0x80
+    codes[:, 7] = 0x7E
+    x = om.e4m3_decode(codes) * 2.0 ** -7
+    xb = oracle.f64_to_bf16(x)
+    assert np.array_equal(oracle.bf16_to_f64(xb), x)
+    q, s = oracle.quantize_fp8(xb, 128)
+    assert np.all(s == 2.0 ** -7)
+    assert np.array_equal(om.e4m3_decode(q), om.e4m3_decode(codes))
+    assert np.array_equal(oracle.dequantize_fp8(q, s, 128), xb)
+
+
+def test_dequantize_matches_library_steps():
+    """decode -> fp32 multiply -> bf16, the same three steps through the library."""
+    rng = np.random.default_rng(4)
+    xb = _bf16_rows(rng, 17, 384, 3.0)
+    for group in (0, 128):
+        q, s = oracle.quantize_fp8(xb, group)
+        g = 384 if group == 0 else 128
+        qf = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float32)
+        sf = torch.from_numpy(s).repeat_interleave(g, dim=1)
+        lib = (qf * sf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(oracle.dequantize_fp8(q, s, group), lib)
+        # quantisation error of the round trip: half an E4M3 step of the group's scale
+        err = np.abs(oracle.bf16_to_f64(oracle.dequantize_fp8(q, s, group)) - oracle.bf16_to_f64(xb))
+        x = np.abs(oracle.bf16_to_f64(xb))
+        smax = np.repeat(s.astype(np.float64), g, axis=1)
+        assert np.all(err <= np.maximum(x * 2 ** -4, smax * 2 ** -10) * (1 + 2 ** -7) + x * 2 ** -8)
+
+
+def test_scales_must_follow_the_row_permutation():
+    """[M6.6] 0x0AC / 0x0AF: permuting the fp8 rows and their scales with the same
+    map reproduces the dequantized token rows at every route row; scales left in
+    token order give finite but wrong rows."""
+    rng = np.random.default_rng(5)
+    T, d, E, k = 12, 256, 4, 2
+    xb = _bf16_rows(rng, T, d)
+    xb = oracle.f64_to_bf16(oracle.bf16_to_f64(xb) * rng.uniform(0.1, 10, (T, 1)))
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    p = oracle.permute(ids, E, -1)
+    for group in (0, 128):
+        q, s = oracle.quantize_fp8(xb, group)
+        q_perm = oracle.gather_rows(q, p["row_to_route"], k)
+        s_perm = oracle.gather_rows(s, p["row_to_route"], k)
+        want = oracle.gather_rows(oracle.dequantize_fp8(q, s, group), p["row_to_route"], k)
+        assert np.array_equal(oracle.dequantize_fp8(q_perm, s_perm, group), want)
+        # the hazard: scales kept in route (token-major) order next to expert-major rows
+        s_route_order = np.repeat(s, k, axis=0)[: q_perm.shape[0]]
+        wrong = oracle.dequantize_fp8(q_perm, s_route_order, group)
+        assert np.all(np.isfinite(oracle.bf16_to_f64(wrong)))
+        assert not np.array_equal(wrong, want)
