@@ -56,6 +56,8 @@ def parse_args():
                          "on this workload's buffers")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of CUDA-graph replays of the step")
+    ap.add_argument("--payload", default="bf16", choices=["bf16", "fp8_row", "fp8_block128"],
+                    help="dispatch payload of the expert input rows (not for --config pooled)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -186,12 +188,18 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
     row: each such token row is read once) and kept (rows compacted)."""
     T, k, E = w.T, w.k, w.E
     touched = int((counts > 0).sum())
+    # bytes of one dispatched row: bf16 data, or E4M3 data plus its fp32 scales
+    row_b = d * 2
+    if getattr(layer, "payload", "bf16") != "bf16":
+        row_b = d + layer.xs.shape[1] * 4
     if name == "route":
         return T * E * 4 + T * k * 8, 0
+    if name == "quantize":
+        return T * d * 2 + T * row_b, 0
     if name == "permute":
-        return T * k * 4 + T * d * 2 + acc_rows * d * 2 + 2 * T * k * 4 + (2 * E + 1) * 4, 0
+        return T * k * 4 + T * row_b + acc_rows * row_b + 2 * T * k * 4 + (2 * E + 1) * 4, 0
     if name == "gate_up":
-        return touched * 2 * d * I * 2 + acc_rows * d * 2 + acc_rows * I * 2, 4 * acc_rows * d * I
+        return touched * 2 * d * I * 2 + acc_rows * row_b + acc_rows * I * 2, 4 * acc_rows * d * I
     if name == "down":
         return touched * I * d * 2 + acc_rows * I * 2 + acc_rows * d * 2, 2 * acc_rows * I * d
     if name == "shared_expert":
@@ -226,6 +234,7 @@ def load_peaks():
 def kernel_source_sha(name):
     src = {"gate_up": "grouped_swiglu.cu", "down": "grouped_swiglu.cu",
            "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
+           "quantize": "fp8.cu",
            "combine": "combine.cu", "pool_pack": "pool.cu", "pool_compact": "pool.cu"}[name]
     with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", src), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -255,8 +264,10 @@ def lookup_traffic(stage, workload_name):
 # our arm
 # ----------------------------------------------------------------------------
 
-def build_layer(w, device):
+def build_layer(w, device, payload="bf16"):
     import grouped_expert_gemm_gb300 as g
+    if w.pooled and payload != "bf16":
+        raise SystemExit("--payload applies to the routed (non-pooled) workloads")
     logits, sel_bias = workloads.make_router_inputs(w, device)
     x = workloads.make_activations(w, device)
     wg, wu, wd = workloads.make_expert_weights(w, device)
@@ -271,7 +282,7 @@ def build_layer(w, device):
         layer = g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                            n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                            sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
-                           device=device)
+                           payload=payload, device=device)
     return layer, logits, sel_bias, x
 
 
@@ -297,7 +308,7 @@ def run_ours(args, dist, w):
     device = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
-    layer, logits, sel_bias, x = build_layer(w, device)
+    layer, logits, sel_bias, x = build_layer(w, device, args.payload)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _ in stages]
@@ -420,7 +431,7 @@ def run_ours(args, dist, w):
     ds = per_stage[dom]
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                 "peak": tf_peak if ds["bound"] == "tensor" else hbm, "unit": ds["unit"],
-                "frac": ds["frac"], "traffic": lookup_traffic(dom, w.name),
+                "frac": ds["frac"], "traffic": lookup_traffic(dom, traffic_key(w, layer)),
                 "peak_source": f"{peak_src} ({'sustained' if long_region and ds['bound'] == 'tensor' else 'burst'})"}
 
     result = {
@@ -540,9 +551,19 @@ def run_extras(args, w, layer, stream, steps):
     return out
 
 
+def traffic_key(w, layer):
+    """Workload name under which profiles/ records a stage's DRAM traffic."""
+    p = getattr(layer, "payload", "bf16")
+    return w.name if p == "bf16" else f"{w.name}+{p}"
+
+
 def config_dict(w, layer):
     c = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I,
          "router": w.score_fn, "parallelism": "replicas only (no data-path collective)"}
+    if not w.pooled:
+        c["payload"] = layer.payload
+        if layer.payload != "bf16":
+            c["payload_bytes_per_row"] = w.d + layer.xs.shape[1] * 4
     if w.capacity_factor is not None:
         c["capacity_factor"] = w.capacity_factor
         c["capacity"] = layer.capacity
@@ -607,7 +628,7 @@ def oracle_step(w, host_inputs, tokens):
     """One oracle pass over the workload for the sampled `tokens` (routing, admission and
     permutation over all tokens, expert math and combine for the sample)."""
     import oracle
-    logits, sel_bias, xb, weights_of, shared = host_inputs
+    logits, sel_bias, xb, weights_of, shared, scale_group = host_inputs
     if w.score_fn == "softmax":
         ids, gates = oracle.route_softmax(logits, w.k)
     else:
@@ -640,7 +661,10 @@ def oracle_step(w, host_inputs, tokens):
     y = {}
     for e, routes in need.items():
         wg, wu, wd = weights_of(e)
-        _, ye = oracle.swiglu(oracle.bf16_to_f64(xb[np.array(routes) // k]), oracle.bf16_to_f64(wg),
+        xr = xb[np.array(routes) // k]
+        if scale_group is not None:  # FP8 payload: the experts see the dequantized rows
+            xr = oracle.dequantize_fp8(*oracle.quantize_fp8(xr, scale_group), scale_group)
+        _, ye = oracle.swiglu(oracle.bf16_to_f64(xr), oracle.bf16_to_f64(wg),
                               oracle.bf16_to_f64(wu), oracle.bf16_to_f64(wd))
         for i, r in enumerate(routes):
             y[int(perm["route_to_row"][r])] = ye[i]
@@ -666,7 +690,7 @@ def host_inputs_of(w, logits, sel_bias, x, layer):
     if getattr(layer, "shared", None) is not None:
         shared = tuple(workloads.bf16_bits(t) for t in layer.shared)
     return (logits.cpu().numpy(), None if sel_bias is None else sel_bias.cpu().numpy(),
-            workloads.bf16_bits(x), weights_of, shared)
+            workloads.bf16_bits(x), weights_of, shared, getattr(layer, "scale_group", None))
 
 
 def cpu_sample_tokens(w, budget_s, host_inputs, rng):

@@ -27,6 +27,7 @@ MOE_DEV_BAD_EXPERT_ID = 2
 MOE_DEV_BAD_HEADER_ID = 4
 MOE_DEV_BAD_ROW = 8
 MOE_DEV_TIMEOUT = 16
+MOE_DEV_NONFINITE_INPUT = 32
 
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID_GROUP = 1
@@ -36,6 +37,11 @@ MOE_POOL_EMPTY = 0xFFFF
 MOE_ROUTE_MASKED = -1
 MOE_BIAS_SIGN = 0
 MOE_BIAS_PROPORTIONAL = 1
+MOE_SCALE_ROW = 0
+MOE_SCALE_BLOCK128 = 128
+MOE_PAYLOAD_BF16 = 0
+MOE_PAYLOAD_FP8_ROW = 1
+MOE_PAYLOAD_FP8_BLOCK128 = 2
 
 EXPORTED = [
     "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
@@ -45,6 +51,8 @@ EXPORTED = [
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
     "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
+    "moe_payload_bytes", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
+    "moe_grouped_gate_up_fp8",
 ]
 
 
@@ -103,6 +111,13 @@ _SIGS = {
                                   _P, _SZ, _P, _P]),
     "moe_combine_bucket": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_bias_update": (_I32, [_I32, _P, _P, ctypes.c_float, _I32, _P]),
+    "moe_payload_bytes": (_I64, [_I64, _I32, _I32]),
+    "moe_quantize_fp8": (_I32, [_I64, _I32, _I32, _P, _P, _P, _P, _P]),
+    "moe_dequantize_fp8": (_I32, [_I64, _I32, _I32, _P, _P, _P, _P]),
+    "moe_permute_fp8": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                               _P, _P, _P, _SZ, _P, _P]),
+    "moe_grouped_gate_up_fp8": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -235,6 +250,45 @@ def moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, 
     _check("moe_grouped_gate_up", lib().moe_grouped_gate_up(
         n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
         _ptr(w_up), _ptr(h), _ptr(dev_status), _stream(stream)))
+    _count(1 if max_rows > 0 else 0)
+
+
+def moe_payload_bytes(rows: int, d: int, payload: int) -> int:
+    return lib().moe_payload_bytes(rows, d, payload)
+
+
+def fp8_scale_groups(d: int, group: int) -> int:
+    """Scales per row for a scale group setting (MOE_SCALE_ROW or MOE_SCALE_BLOCK128)."""
+    return 1 if group == MOE_SCALE_ROW else -(-d // 128)
+
+
+def moe_quantize_fp8(n, d, group, x, q, scales, dev_status=None, stream=None):
+    _check("moe_quantize_fp8", lib().moe_quantize_fp8(
+        n, d, group, _ptr(x), _ptr(q), _ptr(scales), _ptr(dev_status), _stream(stream)))
+    _count(1 if n > 0 else 0)
+
+
+def moe_dequantize_fp8(n, d, group, q, scales, x, stream=None):
+    _check("moe_dequantize_fp8", lib().moe_dequantize_fp8(
+        n, d, group, _ptr(q), _ptr(scales), _ptr(x), _stream(stream)))
+    _count(1 if n > 0 else 0)
+
+
+def moe_permute_fp8(T, d, E, k, capacity, group, topk_ids, q, scales, q_perm, scales_perm, counts,
+                    offsets, row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status=None,
+                    stream=None):
+    _check("moe_permute_fp8", lib().moe_permute_fp8(
+        T, d, E, k, capacity, group, _ptr(topk_ids), _ptr(q), _ptr(scales), _ptr(q_perm),
+        _ptr(scales_perm), _ptr(counts), _ptr(offsets), _ptr(row_to_route), _ptr(route_to_row),
+        _ptr(n_dropped), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+    _count(_permute_launches(T, k))
+
+
+def moe_grouped_gate_up_fp8(n_seg, d, I, max_rows, group, xq, scales, seg_begin, seg_count,
+                            w_gate, w_up, h, dev_status=None, stream=None):
+    _check("moe_grouped_gate_up_fp8", lib().moe_grouped_gate_up_fp8(
+        n_seg, d, I, max_rows, group, _ptr(xq), _ptr(scales), _ptr(seg_begin), _ptr(seg_count),
+        _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(dev_status), _stream(stream)))
     _count(1 if max_rows > 0 else 0)
 
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include <utility>
@@ -88,6 +89,38 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// E4M3 decoding by bit placement: a code's 7 magnitude bits moved to fp32 bits
+// 20..26 (its 4 exponent bits become the low bits of the fp32 exponent field,
+// its 3 mantissa bits the top of the fp32 mantissa) and its sign to bit 31 give
+// exactly decode(code) * 2^-120 -- for subnormal codes too, since both formats
+// continue their smallest binade linearly.  Multiplying by 2^120 is then exact,
+// and the multiply by the scale is the one rounding of decode(code) * s to fp32.
+// (NaN codes 0x7F / 0xFF, which moe_quantize_fp8 produces only from non-finite
+// input, come out as +-480 * s.)  Four codes of one word at a time, two fp32
+// lanes per multiply.
+__device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& bf01, uint32_t& bf23) {
+  const float2 two120 = make_float2(0x1p120f, 0x1p120f);
+  const float2 sc = make_float2(s, s);
+  float2 a, b;
+  a.x = __uint_as_float(((w << 24) & 0x80000000u) | ((w << 20) & 0x07F00000u));
+  a.y = __uint_as_float(((w << 16) & 0x80000000u) | ((w << 12) & 0x07F00000u));
+  b.x = __uint_as_float(((w << 8) & 0x80000000u) | ((w << 4) & 0x07F00000u));
+  b.y = __uint_as_float((w & 0x80000000u) | ((w >> 4) & 0x07F00000u));
+  a = __fmul2_rn(__fmul2_rn(a, two120), sc);
+  b = __fmul2_rn(__fmul2_rn(b, two120), sc);
+  bf01 = pack_bf16x2(a.x, a.y);
+  bf23 = pack_bf16x2(b.x, b.y);
+}
+
+// 16 E4M3 codes (one uint4, element order = byte order) -> 16 bf16 in two uint4,
+// each bf16(fp32(decode(code) * s)).
+__device__ __forceinline__ void dequant16(const uint4& v, float s, uint4& lo, uint4& hi) {
+  dequant4(v.x, s, lo.x, lo.y);
+  dequant4(v.y, s, lo.z, lo.w);
+  dequant4(v.z, s, hi.x, hi.y);
+  dequant4(v.w, s, hi.z, hi.w);
 }
 
 }  // namespace moe

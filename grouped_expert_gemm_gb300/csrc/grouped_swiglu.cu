@@ -32,6 +32,12 @@
 //               bf16 stores of the rows that belong to the segment.
 // Two accumulator buffers let the epilogue of tile i overlap the MMAs of tile i+1.
 //
+// FP8 dispatch payload ([M6.6] 0x0AB-0x0AC): with an E4M3 A operand (gate/up
+// pass only) TMA stages the [128 x 64] E4M3 tile (8 KB instead of 16 KB) and
+// four more warps (6..9, 320 threads) dequantize it with each row's fp32 scale
+// into the bf16 A tile the MMA reads, so the expert input never exists as bf16
+// in HBM.
+//
 // Tiles are enumerated per segment (n-block outer, m-block inner) from the
 // device-resident segment table, so no host synchronisation is needed and
 // consecutive tiles on neighbouring SMs share the same weight columns in L2.
@@ -53,28 +59,77 @@ namespace {
 constexpr int kBM = 128;          // rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int kThreads = 192;
 constexpr int kMaxSeg = 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress = broken pipeline
 
 constexpr int kABytes = kBM * kBK * 2;        // 16 KB
 constexpr int kAtomBytes = kBK * 64 * 2;      // 8 KB: [64 K rows][64 N cols]
+constexpr int kRawBytes = kBM * kBK;          // 8 KB: [128 rows][64 E4M3 codes]
 
-constexpr int kStagesPair = 6;
 constexpr int kPairAtoms = 2;                     // B atoms per CTA in the pair kernel
-constexpr int kPairStageBytes = kABytes + kPairAtoms * kAtomBytes;  // 32 KB
-constexpr int kPairSmemBytes = 1024 + kStagesPair * kPairStageBytes + 256 + (3 * kMaxSeg + 16) * 4;
 
-template <int N_ATOMS>
+// Stage (TMA slot) layout.  bf16 A operand: [A tile 16 KB][N_ATOMS B atoms].
+// E4M3 A operand: [N_ATOMS B atoms][E4M3 A tile 8 KB]; the converter warps write
+// the bf16 A operand into tensor memory -- kASlots slots of 32 columns after the
+// accumulators -- where the MMA reads it, so it costs no shared-memory traffic.
+// Where the A slots do not fit beside two accumulator buffers (N = 256) there is
+// one.  With an E4M3 operand both ring sizes are even: stage n, TMA slot
+// n % kStages and A slot n % kASlots then always belong to converter group
+// n % 2, so every barrier a converter group waits on is one whose phases only
+// that group observes, in order (a parity wait cannot tell a phase from the one
+// two phases later).
+constexpr int kTmemCols = 512;
+constexpr int kASlotCols = kBK / 2;  // 64 bf16 of a row = 32 columns
+
+template <int N_ATOMS, bool FP8A = false>
 struct Geometry {
   static constexpr int kN = 64 * N_ATOMS;                  // MMA N
-  static constexpr int kStageBytes = kABytes + N_ATOMS * kAtomBytes;
-  // As many stages as fit the same ~192 KB: narrower tiles keep more loads in flight.
-  static constexpr int kStages = N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8);
-  static constexpr int kTmemCols = 2 * kN;                 // two accumulator buffers
-  static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
+  static constexpr int kBOff = FP8A ? 0 : kABytes;         // B atoms in a TMA slot
+  static constexpr int kRawOff = N_ATOMS * kAtomBytes;     // E4M3 tile in a TMA slot
+  static constexpr int kStageBytes = N_ATOMS * kAtomBytes + (FP8A ? kRawBytes : kABytes);
+  static constexpr int kTxBytes = kStageBytes;             // all of a TMA slot comes by TMA
+  // As many stages as fit the shared memory: narrower tiles keep more loads in flight.
+  static constexpr int kStages = FP8A ? (N_ATOMS >= 4 ? 4 : 8)
+                                      : (N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8));
+  static constexpr int kASlots = FP8A ? 8 : 0;
+  static constexpr int kAccBufs = 2 * kN + kASlots * kASlotCols <= kTmemCols ? 2 : 1;
+  static constexpr int kACol = kAccBufs * kN;              // first column of the A slots
+  static constexpr int kTmemUsed = kACol + kASlots * kASlotCols;
+  static constexpr int kTmemAlloc = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
+  // full[S], empty[S], tfull[2], tempty[2], drain, (FP8A) afull[A], aempty[A]
+  static constexpr int kBars = 2 * kStages + 5 + 2 * kASlots;
+  static constexpr int kThreads = FP8A ? 448 : 192;        // + 8 converter warps
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes +
-                                    (2 * kStages + 5) * 8 /*barriers*/ + (3 * kMaxSeg + 16) * 4;
+                                    kBars * 8 /*barriers*/ + (3 * kMaxSeg + 16) * 4;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kTmemUsed <= kTmemCols, "tensor memory");
+  static_assert(!FP8A || (kStages % 2 == 0 && kASlots % 2 == 0), "even rings");
+  static_assert(kRawOff % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
+};
+
+// Pair kernel, per CTA: TMA slot [A bf16 tile 16 KB][2 B atoms 16 KB], or with an
+// E4M3 A operand [2 B atoms 16 KB][E4M3 A tile 8 KB] and A slots in tensor memory
+// after a single accumulator buffer.
+template <bool FP8A = false>
+struct PairGeometry {
+  static constexpr int kN = 2 * kPairAtoms * 64;           // 256 accumulator columns
+  static constexpr int kBOff = FP8A ? 0 : kABytes;
+  static constexpr int kRawOff = kPairAtoms * kAtomBytes;
+  static constexpr int kStageBytes = kPairAtoms * kAtomBytes + (FP8A ? kRawBytes : kABytes);
+  static constexpr int kStages = FP8A ? 8 : 6;
+  static constexpr int kASlots = FP8A ? 8 : 0;
+  static constexpr int kAccBufs = FP8A ? 1 : 2;
+  static constexpr int kACol = kAccBufs * kN;
+  static constexpr int kTmemAlloc = 512;
+  // full, empty, tfull[2], tempty[2], drain, (FP8A) raw[S], afull[A], aempty[A]
+  static constexpr int kBars = 2 * kStages + 5 + (FP8A ? kStages + 2 * kASlots : 0);
+  static constexpr int kThreads = FP8A ? 448 : 192;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBars * 8 +
+                                    (3 * kMaxSeg + 16) * 4;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kACol + kASlots * kASlotCols <= kTmemAlloc, "tensor memory");
+  static_assert(!FP8A || (kStages % 2 == 0 && kASlots % 2 == 0), "even rings");
+  static_assert(kRawOff % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
 };
 
 struct GemmArgs {
@@ -87,6 +142,11 @@ struct GemmArgs {
   uint16_t* out; // [max_rows, N] bf16 bits
   uint32_t* dev_status;
   int m_outer;   // tile order inside a segment: 0 = n-block outer, 1 = m-block outer
+  // E4M3 A operand only: fp32 scales [max_rows, n_groups], one per group_k
+  // consecutive K values of a row.
+  const float* scales;
+  int n_groups;
+  int group_k;
 };
 
 // ------------------------------ PTX wrappers -------------------------------
@@ -114,26 +174,40 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope (the phase was completed by a release of
+// another CTA of the cluster whose prior writes this thread relies on).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Bounded wait for the phase of `parity` to complete.  Returns false when the
 // CTA is aborting (another role gave up) or when this wait itself times out.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              uint32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if (*abort_flag) return false;
     if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -208,6 +282,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// This thread's TMEM lane, 32 consecutive 32-bit columns from `taddr` (the
+// warp's lane quadrant is in the address).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D (+)= A B with the A operand in tensor memory (rows = lanes, two K-consecutive
+// bf16 per 32-bit column) and B in shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -266,6 +371,16 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -459,22 +574,142 @@ __device__ __forceinline__ Smem carve(uint8_t* after_stages, int n_bars) {
   return m;
 }
 
+// E4M3 A operand.  Two groups of four converter warps take the stages in turn
+// (stage n goes to group n % 2), so the hand-over of one stage overlaps the
+// conversion of the next.  Thread lane of converter warp w converts row
+// r = 32 (w % 4) + lane -- the tensor-memory lane its warp may access -- of the
+// staged [128 x 64] E4M3 tile (TMA layout with 64-byte swizzle: 16-byte chunk c
+// of row r at chunk c ^ ((r >> 1) & 3)): each value becomes
+// bf16(fp32(decode(code) * scale of its row and group)), two K-consecutive
+// values per 32-bit column of the row's lane in A slot n % kASlots.  Per stage:
+// wait for the E4M3 tile (raw barrier n % kStages) and for the MMA to have
+// released the A slot, convert, store to tensor memory, wait for the stores,
+// then one arrival per warp on the slot's afull barrier.  Scales are loaded one
+// own stage ahead (the first one of a tile during the previous tile).
+constexpr int kConvGroups = 2;
+
+template <int kStages, int kStageBytes, int kRawOff, int kASlots>
+__device__ __forceinline__ void convert_a_tiles(uint8_t* stage_base, uint32_t tmem_a0, int ct,
+                                                int lane, int t0, int t_step, int total_tiles,
+                                                int k_steps, int bm, int row_off,
+                                                const GemmArgs& args, const Smem& sm,
+                                                int n_blocks, int bn_out, uint32_t raw_bar0,
+                                                uint32_t afull_bar0, uint32_t aempty_bar0,
+                                                volatile int* abort_flag) {
+  const int quad = (ct >> 5) & 3;  // converter warps start at warp 6: (6 + i) & 3 == (2 + i) & 3
+  const int r = ((quad + 2) & 3) * 32 + lane;  // = 32 * (warp % 4) + lane
+  const int grp = ct >> 7;         // converter group
+  const uint32_t tmem_row = tmem_a0 + (static_cast<uint32_t>(r & ~31) << 16);
+  const int ng = args.n_groups;
+  auto scale_row = [&](int t) {
+    const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, args.n_seg, bm, bn_out,
+                            n_blocks, args.m_outer);
+    // rows past the tensor (zero-filled by TMA) read the last row's scale: unused
+    const int row = min(tl.row0 + row_off + r, args.max_rows - 1);
+    return args.scales + static_cast<int64_t>(row) * ng;
+  };
+  auto scale_at = [&](const float* row, int ks) { return __ldg(row + (ks * kBK) / args.group_k); };
+  // first k-step of a tile that belongs to this group, given the tile's first stage index
+  auto first_own = [&](int n_base) {
+    const int k0 = (grp - n_base) % kConvGroups;
+    return k0 < 0 ? k0 + kConvGroups : k0;
+  };
+  const int swz_in = (r >> 1) & 3;
+  int n_base = 0;  // stage index (over all of this CTA's tiles) of the tile's k-step 0
+  int t = t0;
+  const float* next_row = nullptr;
+  float next_first = 1.0f;
+  if (t < total_tiles) {
+    next_row = scale_row(t);
+    if (first_own(0) < k_steps) next_first = scale_at(next_row, first_own(0));
+  }
+  for (; t < total_tiles; t += t_step, n_base += k_steps) {
+    const float* srow = next_row;
+    float sc = next_first;
+    if (t + t_step < total_tiles) {
+      next_row = scale_row(t + t_step);
+      const int k0 = first_own(n_base + k_steps);
+      if (k0 < k_steps) next_first = scale_at(next_row, k0);
+    }
+    for (int ks = first_own(n_base); ks < k_steps; ks += kConvGroups) {
+      const int n = n_base + ks;
+      const int s = n % kStages, a = n % kASlots;
+      const float sc_next = ks + kConvGroups < k_steps ? scale_at(srow, ks + kConvGroups) : 0.0f;
+      // every exit is warp-uniform: the tensor-memory stores below are .sync.aligned
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(raw_bar0 + 8 * s,
+                                                static_cast<uint32_t>(n / kStages) & 1u,
+                                                abort_flag, args.dev_status)))
+        return;
+      const uint8_t* raw = stage_base + s * kStageBytes + kRawOff + r * 64;
+      uint32_t col[kASlotCols];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz_in) << 4));
+        uint4 lo, hi;
+        dequant16(v, sc, lo, hi);
+        col[8 * c + 0] = lo.x; col[8 * c + 1] = lo.y; col[8 * c + 2] = lo.z; col[8 * c + 3] = lo.w;
+        col[8 * c + 4] = hi.x; col[8 * c + 5] = hi.y; col[8 * c + 6] = hi.z; col[8 * c + 7] = hi.w;
+      }
+      // the MMAs that read this slot's previous contents must have completed
+      if (!__all_sync(0xFFFFFFFFu,
+                      wait_bounded(aempty_bar0 + 8 * a, (static_cast<uint32_t>(n / kASlots) & 1u) ^ 1u,
+                                   abort_flag, args.dev_status)))
+        return;
+      tc_fence_after();
+      tmem_st32(tmem_row + static_cast<uint32_t>(a * kASlotCols), col);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull_bar0 + 8 * a);
+      sc = sc_next;
+    }
+  }
+}
+
+// Pair kernel, rank 1: one thread forwards each completed local afull[a] phase
+// to the leader's afull[a] barrier, whose thread issues the MMAs that read this
+// rank's A slot.  The arrival is relaxed: by the time this thread has acquired
+// the local phase, every converter warp has waited for its tensor-memory stores
+// to complete (tcgen05.wait::st) and fenced them before its release, so the
+// slot's contents are in place before the signal leaves this CTA.  (A release
+// at cluster scope per stage measured about 1,500 cycles and paced the whole
+// pipeline.)
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ bool forward_conversions(int n_stages_total, int slots,
+                                                    uint32_t local_bar0, volatile int* abort_flag,
+                                                    uint32_t* dev_status) {
+  for (int n = 0; n < n_stages_total; ++n) {
+    const int a = n % slots;
+    if (!wait_bounded(local_bar0 + 8 * a, static_cast<uint32_t>(n / slots) & 1u, abort_flag,
+                      dev_status))
+      return false;
+    mbar_arrive_remote_relaxed(map_to_rank(local_bar0 + 8 * a, 0));
+  }
+  return true;
+}
+
 // ------------------------- single-CTA kernel --------------------------------
 
-template <int N_ATOMS, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int N_ATOMS, bool SWIGLU, bool FP8A>
+__global__ void __launch_bounds__(Geometry<N_ATOMS, FP8A>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b0,
                     const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
-  using G = Geometry<N_ATOMS>;
+  using G = Geometry<N_ATOMS, FP8A>;
   constexpr int kStages = G::kStages;
+  constexpr int kASlots = G::kASlots;
+  constexpr int kAccBufs = G::kAccBufs;
   constexpr int kN = G::kN;
   constexpr int kBnOut = SWIGLU ? kN / 2 : kN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  const Smem sm = carve(stage_base + kStages * G::kStageBytes, 2 * kStages + 5);
+  // bars: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, (FP8A) afull[A], aempty[A]
+  const Smem sm = carve(stage_base + kStages * G::kStageBytes, G::kBars);
   uint64_t* bars = sm.bars;
   volatile int* abort_flag = sm.abort_flag;
 
@@ -488,11 +723,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+  auto afull_bar = [&](int a) { return smem_u32(bars + 2 * kStages + 5 + a); };
+  auto aempty_bar = [&](int a) { return smem_u32(bars + 2 * kStages + 5 + kASlots + a); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      mbar_init(afull_bar(a), 4);  // one arrival per warp of the converting group
+      mbar_init(aempty_bar(a), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -510,7 +751,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   }
   if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
   pdl_wait();  // everything above is local; global data only from here on
-  if (threadIdx.x >= 64)
+  if (threadIdx.x >= 64 && threadIdx.x < 192)
     build_segment_table(args, kBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
   tc_fence_before();
   __syncthreads();
@@ -531,11 +772,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
           const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
-          mbar_arrive_expect_tx(full_bar(s), G::kStageBytes);
-          tma_load_2d(st, &tmap_a, full_bar(s), ks * kBK, tl.row0);
+          mbar_arrive_expect_tx(full_bar(s), G::kTxBytes);
+          // A: the bf16 tile, or the E4M3 tile for the converter warps
+          tma_load_2d(FP8A ? st + G::kRawOff : st, &tmap_a, full_bar(s), ks * kBK, tl.row0);
 #pragma unroll
           for (int a = 0; a < N_ATOMS; ++a) {
-            const uint32_t dst = st + kABytes + a * kAtomBytes;
+            const uint32_t dst = st + G::kBOff + a * kAtomBytes;
             if constexpr (SWIGLU) {
               const int half = N_ATOMS / 2;
               const CUtensorMap* m = a < half ? &tmap_b0 : &tmap_b1;
@@ -563,8 +805,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ======================= MMA issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, kN);
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
       int buf = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
@@ -575,25 +817,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kN);
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, args.dev_status)) { ok = false; break; }
+          if (FP8A && !wait_bounded(afull_bar(a), aph, abort_flag, args.dev_status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_base + s * G::kStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+          const uint32_t b_addr = st + G::kBOff;
 #pragma unroll
           for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-            // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
-            const uint64_t ad = smem_desc_sw128(a_addr + kk * kUmmaK * 2, 16, 1024);
             // B: N-major, advance 16 K rows = 2048 bytes; atoms of 64 columns
             // are kAtomBytes apart (LBO), 8-row K groups 1024 bytes apart (SBO).
             const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 128, kAtomBytes, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (FP8A) {
+              // A in tensor memory: 16 K values = 8 columns of slot a
+              const uint32_t ta = tmem_base + static_cast<uint32_t>(G::kACol + a * kASlotCols + kk * (kUmmaK / 2));
+              mma_bf16_ta(d_tmem, ta, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
+              const uint64_t ad = smem_desc_sw128(st + kk * kUmmaK * 2, 16, 1024);
+              mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           issued_any = true;
           mma_commit(empty_bar(s));  // frees this stage once its MMAs have read it
           if (++s == kStages) { s = 0; ph ^= 1u; }
+          if constexpr (FP8A) {
+            mma_commit(aempty_bar(a));  // and the converted A slot
+            if (++a == kASlots) { a = 0; aph ^= 1u; }
+          }
         }
         if (!ok) break;
         mma_commit(tfull_bar(buf));  // accumulator ready for the epilogue
-        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+        if (++buf == kAccBufs) { buf = 0; acc_ph ^= 1u; }
       }
       if (!ok && issued_any) {
         // All MMAs issued so far must finish before tensor memory is freed.
@@ -601,7 +854,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         wait_drain(drain_bar, 0);
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ======================= epilogue (warps 2..5) =======================
     const int quad = warp & 3;            // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;       // accumulator row owned by this thread
@@ -610,7 +863,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut, n_blocks,
                               args.m_outer);
-      if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
+      // warp-uniform exit: the tensor-memory loads below are .sync.aligned
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)))
+        break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(buf * kN);
@@ -619,8 +874,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       epilogue_row<kBnOut, SWIGLU>(taddr, live, orow);
       tc_fence_before();
       mbar_arrive(tempty_bar(buf));
-      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      if (++buf == kAccBufs) { buf = 0; acc_ph ^= 1u; }
     }
+  } else if constexpr (FP8A) {
+    // ================ E4M3 -> bf16 converter (warps 6..13) ================
+    convert_a_tiles<kStages, G::kStageBytes, G::kRawOff, kASlots>(
+        stage_base, tmem_base + G::kACol, threadIdx.x - 192, lane, blockIdx.x, gridDim.x,
+        total_tiles, k_steps, kBM, 0, args, sm, n_blocks, kBnOut, full_bar(0), afull_bar(0),
+        aempty_bar(0), abort_flag);
   }
 
   // ---- teardown ----
@@ -642,23 +903,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 // gate/up pass rank 0 holds the 128 gate columns and rank 1 the 128 up columns,
 // so the accumulator of either rank is [G | U] for its own 128 rows.  Barriers:
 //   full[s]      leader only: the leader's expect_tx covers both ranks' bytes,
-//                and each rank's TMA completes its bytes on the leader's barrier;
+//                and each rank's TMA completes its bytes on the leader's barrier
+//                (with an E4M3 A operand: the B bytes only);
 //   empty[s]     both ranks: the leader's commit is multicast to both;
+//   raw[s]       E4M3 A only, both ranks: the rank's own E4M3 tile has landed;
+//   afull[a]     E4M3 A only: the rank's bf16 A slot a is written (4 converter
+//                warps); the leader's also counts one arrival forwarded by rank 1;
+//   aempty[a]    E4M3 A only, both ranks: multicast commit, slot a free again;
 //   tfull[b]     both ranks: multicast commit after a tile's last MMA;
 //   tempty[b]    leader only: one arrival per epilogue warp of both ranks (8).
-template <bool SWIGLU>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool SWIGLU, bool FP8A>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeometry<FP8A>::kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b0,
                          const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
-  constexpr int kN = 2 * kPairAtoms * 64;        // 256 accumulator columns
+  using PG = PairGeometry<FP8A>;
+  constexpr int kStagesPair = PG::kStages;
+  constexpr int kPairStageBytes = PG::kStageBytes;
+  constexpr int kASlots = PG::kASlots;
+  constexpr int kAccBufs = PG::kAccBufs;
+  constexpr int kN = PG::kN;                     // 256 accumulator columns
   constexpr int kBnOut = SWIGLU ? kN / 2 : kN;   // output columns per tile
   constexpr int kPairBM = 2 * kBM;               // rows per tile
-  constexpr int kTmemAlloc = 2 * kN;             // two accumulator buffers = 512
+  constexpr int kTmemAlloc = PG::kTmemAlloc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Smem sm = carve(stage_base + kStagesPair * kPairStageBytes, 2 * kStagesPair + 5);
+  const Smem sm = carve(stage_base + kStagesPair * kPairStageBytes, PG::kBars);
   uint64_t* bars = sm.bars;
   volatile int* abort_flag = sm.abort_flag;
 
@@ -675,11 +946,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStagesPair + b); };
   auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStagesPair + 2 + b); };
   const uint32_t drain_bar = smem_u32(bars + 2 * kStagesPair + 4);
+  auto raw_bar = [&](int s) { return smem_u32(bars + 2 * kStagesPair + 5 + s); };
+  auto afull_bar = [&](int a) { return smem_u32(bars + 3 * kStagesPair + 5 + a); };
+  auto aempty_bar = [&](int a) { return smem_u32(bars + 3 * kStagesPair + 5 + kASlots + a); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesPair; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      if (FP8A) mbar_init(raw_bar(s), 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      // leader: its own 4 converter arrivals + 1 forwarded from rank 1; rank 1: 4
+      mbar_init(afull_bar(a), leader ? 5 : 4);
+      mbar_init(aempty_bar(a), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -697,7 +977,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(sm.tmem_slot), kTmemAlloc);
   pdl_wait();  // everything above is local; global data only from here on
-  if (threadIdx.x >= 64)
+  if (threadIdx.x >= 64 && threadIdx.x < 192)
     build_segment_table(args, kPairBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start,
                         sm.warp_tot);
   // Both ranks' barriers are initialised and their tensor memory allocated
@@ -723,12 +1003,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
           const uint32_t full_leader = map_to_rank(full_bar(s), 0);
-          if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kPairStageBytes);
           const uint32_t st = smem_u32(stage_base + s * kPairStageBytes);
-          tma_load_2d_pair(st, &tmap_a, full_leader, ks * kBK, tl.row0 + static_cast<int>(rank) * kBM);
+          if constexpr (FP8A) {
+            // this rank's E4M3 rows land on its own raw barrier; B on the leader's
+            if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kPairAtoms * kAtomBytes);
+            mbar_arrive_expect_tx(raw_bar(s), kRawBytes);
+            tma_load_2d(st + PG::kRawOff, &tmap_a, raw_bar(s), ks * kBK,
+                        tl.row0 + static_cast<int>(rank) * kBM);
+          } else {
+            if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kPairStageBytes);
+            tma_load_2d_pair(st, &tmap_a, full_leader, ks * kBK,
+                             tl.row0 + static_cast<int>(rank) * kBM);
+          }
 #pragma unroll
           for (int a = 0; a < kPairAtoms; ++a) {
-            const uint32_t dst = st + kABytes + a * kAtomBytes;
+            const uint32_t dst = st + PG::kBOff + a * kAtomBytes;
             if constexpr (SWIGLU) {
               tma_load_2d_pair(dst, leader ? &tmap_b0 : &tmap_b1, full_leader, tl.n0 + a * 64,
                                b_row0 + ks * kBK);
@@ -743,6 +1032,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
       }
       if (!ok && issued_any) {
+        if (FP8A) {  // this rank's own E4M3 copies
+          int ss = s;
+          uint32_t pp = ph;
+          for (int i = 0; i < kStagesPair; ++i) {
+            if (--ss < 0) { ss = kStagesPair - 1; pp ^= 1u; }
+            wait_drain(raw_bar(ss), pp);
+          }
+        }
         if (leader) {
           int ss = s;
           uint32_t pp = ph;
@@ -761,8 +1058,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ======================= MMA issuer (leader only) =======================
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16(kPairBM, kN);
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
       int buf = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
@@ -773,29 +1070,44 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kN);
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(full_bar(s), ph, abort_flag, args.dev_status)) { ok = false; break; }
+          if (FP8A && !wait_bounded<true>(afull_bar(a), aph, abort_flag, args.dev_status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_base + s * kPairStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t st = smem_u32(stage_base + s * kPairStageBytes);
+          const uint32_t b_addr = st + PG::kBOff;
 #pragma unroll
           for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a_addr + kk * kUmmaK * 2, 16, 1024);
             const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 128, kAtomBytes, 1024);
-            mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (FP8A) {
+              // A in tensor memory, each rank's 128 rows in its own lanes
+              const uint32_t ta = tmem_base + static_cast<uint32_t>(PG::kACol + a * kASlotCols + kk * (kUmmaK / 2));
+              mma_bf16_pair_ta(d_tmem, ta, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              const uint64_t ad = smem_desc_sw128(st + kk * kUmmaK * 2, 16, 1024);
+              mma_bf16_pair(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           issued_any = true;
           mma_commit_pair(empty_bar(s), 0x3);  // frees stage s in both ranks
           if (++s == kStagesPair) { s = 0; ph ^= 1u; }
+          if constexpr (FP8A) {
+            mma_commit_pair(aempty_bar(a), 0x3);  // and A slot a in both ranks
+            if (++a == kASlots) { a = 0; aph ^= 1u; }
+          }
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar(buf), 0x3);  // both ranks' accumulators ready
-        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+        if (++buf == kAccBufs) { buf = 0; acc_ph ^= 1u; }
       }
       if (!ok && issued_any) {
         mma_commit_pair(drain_bar, 0x1);
         wait_drain(drain_bar, 0);
       }
+    } else if (FP8A && lane == 0) {
+      // rank 1: forward its converted A slots to the leader
+      const int my_tiles = cid < total_tiles ? (total_tiles - cid + n_clusters - 1) / n_clusters : 0;
+      forward_conversions(my_tiles * k_steps, kASlots, afull_bar(0), abort_flag, args.dev_status);
     }
-  } else {
+  } else if (warp < 6) {
     // ======================= epilogue (warps 2..5, both ranks) ===============
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                        // row within this rank's half
@@ -805,7 +1117,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     for (int t = cid; t < total_tiles; t += n_clusters) {
       const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM, kBnOut,
                               n_blocks, args.m_outer);
-      if (!wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)) break;
+      // warp-uniform exit: the tensor-memory loads below are .sync.aligned
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)))
+        break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(buf * kN);
@@ -816,8 +1130,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(buf), 0));
-      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      if (++buf == kAccBufs) { buf = 0; acc_ph ^= 1u; }
     }
+  } else if constexpr (FP8A) {
+    // ============ E4M3 -> bf16 converter (warps 6..13, both ranks) ============
+    convert_a_tiles<kStagesPair, kPairStageBytes, PG::kRawOff, kASlots>(
+        stage_base, tmem_base + PG::kACol, threadIdx.x - 192, lane, cid, n_clusters, total_tiles,
+        k_steps, kPairBM, static_cast<int>(rank) * kBM, args, sm, n_blocks, kBnOut, raw_bar(0),
+        afull_bar(0), aempty_bar(0), abort_flag);
   }
 
   // ---- teardown: no rank leaves while the other may still touch its memory ----
@@ -854,15 +1174,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128B swizzle.
-// An encoded map depends only on (address, rows, cols, box rows), so encodings
-// are kept in a small cache keyed by exactly those values: a hit is always a
-// valid map, whatever the caller did with the memory in between.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D tensor [rows, cols] (cols contiguous) with a box of [box_rows, 64]
+// elements: bf16 with 128-byte swizzle, or (fp8) bytes with 64-byte swizzle.
+// An encoded map depends only on (address, rows, cols, box rows, element type),
+// so encodings are kept in a small cache keyed by exactly those values: a hit is
+// always a valid map, whatever the caller did with the memory in between.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              bool fp8 = false) {
   struct Entry {
     const void* base;
     uint64_t rows, cols;
     uint32_t box_rows;
+    bool fp8;
     CUtensorMap map;
   };
   constexpr int kCache = 64;
@@ -873,7 +1196,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i) {
       const Entry& e = cache[i];
-      if (e.base == base && e.rows == rows && e.cols == cols && e.box_rows == box_rows) {
+      if (e.base == base && e.rows == rows && e.cols == cols && e.box_rows == box_rows &&
+          e.fp8 == fp8) {
         *m = e.map;
         return true;
       }
@@ -882,16 +1206,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {cols * (fp8 ? 1 : 2)};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  if (fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   std::lock_guard<std::mutex> lock(mu);
   Entry& e = cache[next];
-  e = Entry{base, rows, cols, box_rows, *m};
+  e = Entry{base, rows, cols, box_rows, fp8, *m};
   next = (next + 1) % kCache;
   if (used < kCache) ++used;
   return true;
@@ -904,11 +1229,11 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int N_ATOMS, bool SWIGLU>
+template <int N_ATOMS, bool SWIGLU, bool FP8A = false>
 moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                        const GemmArgs& args, cudaStream_t s) {
-  using G = Geometry<N_ATOMS>;
-  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU>;
+  using G = Geometry<N_ATOMS, FP8A>;
+  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU, FP8A>;
   // The shared-memory opt-in and the SM count are per device: set/read once.
   constexpr int kMaxDev = 64;
   static int sms[kMaxDev] = {};
@@ -926,16 +1251,17 @@ moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
     }
     n_sm = sms[dev];
   }
-  launch(kern, dim3(n_sm), dim3(kThreads), G::kSmemBytes, s, a, b0, b1, args);
+  launch(kern, dim3(n_sm), dim3(G::kThreads), G::kSmemBytes, s, a, b0, b1, args);
   return launch_status();
 }
 
 // The pair kernel runs as many two-CTA clusters as can be resident at once
 // (queried once per device), each looping over its share of the tiles.
-template <bool SWIGLU>
+template <bool SWIGLU, bool FP8A = false>
 moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                             const GemmArgs& args, cudaStream_t s) {
-  auto kern = grouped_gemm_pair_kernel<SWIGLU>;
+  using PG = PairGeometry<FP8A>;
+  auto kern = grouped_gemm_pair_kernel<SWIGLU, FP8A>;
   constexpr int kMaxDev = 64;
   static int grid[kMaxDev] = {};
   static std::mutex mu;
@@ -946,12 +1272,12 @@ moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const C
     std::lock_guard<std::mutex> lock(mu);
     if (grid[dev] == 0) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kPairSmemBytes) != cudaSuccess)
+                               PG::kSmemBytes) != cudaSuccess)
         return MOE_ERR_CUDA;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(num_sms() & ~1));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = kPairSmemBytes;
+      cfg.blockDim = dim3(PG::kThreads);
+      cfg.dynamicSmemBytes = PG::kSmemBytes;
       int clusters = 0;
       if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
         clusters = num_sms() / 2;
@@ -960,7 +1286,7 @@ moe_status launch_gemm_pair(const CUtensorMap& a, const CUtensorMap& b0, const C
     }
     g = grid[dev];
   }
-  launch(kern, dim3(g), dim3(kThreads), kPairSmemBytes, s, a, b0, b1, args);
+  launch(kern, dim3(g), dim3(PG::kThreads), PG::kSmemBytes, s, a, b0, b1, args);
   return launch_status();
 }
 
@@ -1023,13 +1349,48 @@ MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int3
       !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
-             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I))};
+             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
+             nullptr, 0, 0};
   cudaStream_t s = as_cuda(stream);
   if (I % 128 == 0) {
     return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s)
                                        : launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
   }
   return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+}
+
+MOE_API moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                                           int32_t group, const moe_fp8* xq, const float* scales,
+                                           const int32_t* seg_begin, const int32_t* seg_count,
+                                           const moe_bf16* w_gate, const moe_bf16* w_up,
+                                           moe_bf16* h, uint32_t* dev_status,
+                                           moe_stream_t stream) {
+  moe_status st = check_common(n_seg, d, I, max_rows);
+  if (st != MOE_OK) return st;
+  if (group != MOE_SCALE_ROW && group != MOE_SCALE_BLOCK128) return MOE_ERR_INVALID_ARG;
+  if (max_rows == 0) return MOE_OK;
+  if (xq == nullptr || scales == nullptr || seg_begin == nullptr || seg_count == nullptr ||
+      w_gate == nullptr || w_up == nullptr || h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return MOE_ERR_UNSUPPORTED;
+  CUtensorMap m_x, m_wg, m_wu;
+  if (!make_map(&m_x, xq, max_rows, d, kBM, true) ||
+      !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
+      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
+    return MOE_ERR_CUDA;
+  const int n_groups = group == MOE_SCALE_ROW ? 1 : static_cast<int>(ceil_div(d, 128));
+  GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
+             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
+             scales, n_groups, group == MOE_SCALE_ROW ? d : 128};
+  cudaStream_t s = as_cuda(stream);
+  // the same kernel shapes as the bf16 operand
+  if (I % 128 == 0) {
+    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true, true>(m_x, m_wg, m_wu, a, s)
+                                       : launch_gemm<4, true, true>(m_x, m_wg, m_wu, a, s);
+  }
+  return launch_gemm<2, true, true>(m_x, m_wg, m_wu, a, s);
 }
 
 MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
@@ -1046,7 +1407,7 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   if (!make_map(&m_h, h, max_rows, I, kBM) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
-             dev_status, choose_m_outer(n_seg, max_rows, I, d)};
+             dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0};
   cudaStream_t s = as_cuda(stream);
   // The widest output tile the width allows (narrower tiles for one-token decode were
   // measured slower: the few tiles there are bound by pipeline latency, not SM count).

@@ -197,11 +197,14 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
   pdl_trigger();
 }
 
-// One warp per token: read the row once, store it to each admitted row.
+// One warp per token: read the row once, store it to each admitted row (and,
+// with SCALES, the row's G fp32 scales to the same rows of scales_perm).
+template <bool SCALES>
 __global__ void __launch_bounds__(kCopyThreads)
 permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
              const uint4* __restrict__ x, uint4* __restrict__ x_perm,
-             const int32_t* __restrict__ valid) {
+             const int32_t* __restrict__ valid, int G, const float* __restrict__ scales,
+             float* __restrict__ scales_perm) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
@@ -226,6 +229,15 @@ permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
           if (c + 32 * u < chunks) dst[c + 32 * u] = v[u];
       }
     }
+    if constexpr (SCALES) {
+      const float* src_s = scales + static_cast<int64_t>(t) * G;
+      for (int j = 0; j < k; ++j) {
+        const int32_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+        if (row < 0) continue;
+        for (int g = lane; g < G; g += 32)
+          scales_perm[static_cast<int64_t>(row) * G + g] = __ldg(src_s + g);
+      }
+    }
   }
   pdl_trigger();
 }
@@ -243,15 +255,20 @@ MOE_API size_t moe_permute_workspace_size(int32_t T, int32_t k, int32_t E) {
   return c.off + 256;
 }
 
-static moe_status permute_impl(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
-                               const int32_t* valid, const int32_t* topk_ids, const moe_bf16* x,
-                               moe_bf16* x_perm, int32_t* counts, int32_t* offsets,
+// Payload rows are row_bytes long (a multiple of 16); with scales != nullptr each
+// row also carries G fp32 scales, copied to the same rows of scales_perm.
+static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t k,
+                               int32_t capacity, const int32_t* valid, const int32_t* topk_ids,
+                               const void* x, void* x_perm, int32_t G, const float* scales,
+                               float* scales_perm, int32_t* counts, int32_t* offsets,
                                int32_t* row_to_route, int32_t* route_to_row, int32_t* n_dropped,
                                void* ws, size_t ws_bytes, uint32_t* dev_status,
                                moe_stream_t stream) {
-  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
-  if (E > 512 || k > 16 || d % 8 != 0 || static_cast<int64_t>(T) * k >= (int64_t(1) << 31))
+  if (T < 0 || row_bytes <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 512 || k > 16 || row_bytes % 16 != 0 || row_bytes > (int64_t(1) << 24) ||
+      static_cast<int64_t>(T) * k >= (int64_t(1) << 31))
     return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && G > 0 && (scales == nullptr || scales_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || offsets == nullptr || n_dropped == nullptr) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (topk_ids == nullptr || x == nullptr || x_perm == nullptr ||
                 row_to_route == nullptr || route_to_row == nullptr || ws == nullptr))
@@ -280,9 +297,15 @@ static moe_status permute_impl(int32_t T, int32_t d, int32_t E, int32_t k, int32
   const int warps = kCopyThreads / 32;
   int64_t blocks = ceil_div(T, warps);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  launch(permute_copy, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k, d / 8,
-         static_cast<const int32_t*>(route_to_row), reinterpret_cast<const uint4*>(x),
-         reinterpret_cast<uint4*>(x_perm), valid);
+  const int chunks = static_cast<int>(row_bytes / 16);
+  if (scales == nullptr)
+    launch(permute_copy<false>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T,
+           k, chunks, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
+           static_cast<uint4*>(x_perm), valid, 0, scales, scales_perm);
+  else
+    launch(permute_copy<true>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k,
+           chunks, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
+           static_cast<uint4*>(x_perm), valid, G, scales, scales_perm);
   return launch_status();
 }
 
@@ -291,8 +314,27 @@ MOE_API moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32
                                int32_t* counts, int32_t* offsets, int32_t* row_to_route,
                                int32_t* route_to_row, int32_t* n_dropped, void* ws,
                                size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream) {
-  return permute_impl(T, d, E, k, capacity, nullptr, topk_ids, x, x_perm, counts, offsets,
-                      row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status, stream);
+  if (d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  return permute_impl(T, int64_t(d) * 2, E, k, capacity, nullptr, topk_ids, x, x_perm, 0, nullptr,
+                      nullptr, counts, offsets, row_to_route, route_to_row, n_dropped, ws,
+                      ws_bytes, dev_status, stream);
+}
+
+MOE_API moe_status moe_permute_fp8(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                                   int32_t group, const int32_t* topk_ids, const moe_fp8* q,
+                                   const float* scales, moe_fp8* q_perm, float* scales_perm,
+                                   int32_t* counts, int32_t* offsets, int32_t* row_to_route,
+                                   int32_t* route_to_row, int32_t* n_dropped, void* ws,
+                                   size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream) {
+  if (d <= 0 || (group != MOE_SCALE_ROW && group != MOE_SCALE_BLOCK128)) return MOE_ERR_INVALID_ARG;
+  if (d % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (reinterpret_cast<uintptr_t>(scales) & 3u || reinterpret_cast<uintptr_t>(scales_perm) & 3u))
+    return MOE_ERR_UNSUPPORTED;
+  const int32_t G = group == MOE_SCALE_ROW ? 1 : static_cast<int32_t>(ceil_div(d, 128));
+  return permute_impl(T, d, E, k, capacity, nullptr, topk_ids, q, q_perm, G, scales, scales_perm,
+                      counts, offsets, row_to_route, route_to_row, n_dropped, ws, ws_bytes,
+                      dev_status, stream);
 }
 
 MOE_API moe_status moe_permute_bucket(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
@@ -302,9 +344,11 @@ MOE_API moe_status moe_permute_bucket(int32_t T, int32_t d, int32_t E, int32_t k
                                       int32_t* route_to_row, int32_t* n_dropped, void* ws,
                                       size_t ws_bytes, uint32_t* dev_status,
                                       moe_stream_t stream) {
-  if (valid_tokens == nullptr) return MOE_ERR_INVALID_ARG;
-  return permute_impl(T, d, E, k, capacity, valid_tokens, topk_ids, x, x_perm, counts, offsets,
-                      row_to_route, route_to_row, n_dropped, ws, ws_bytes, dev_status, stream);
+  if (valid_tokens == nullptr || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  return permute_impl(T, int64_t(d) * 2, E, k, capacity, valid_tokens, topk_ids, x, x_perm, 0,
+                      nullptr, nullptr, counts, offsets, row_to_route, route_to_row, n_dropped, ws,
+                      ws_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -2,7 +2,10 @@
 
 ``MoELayer``       route -> permute (capacity or dropless) -> grouped SwiGLU over
                    the expert segments (+ an optional always-on shared expert)
-                   -> gate-weighted fp32 combine.
+                   -> gate-weighted fp32 combine.  With an FP8 payload the token
+                   rows are quantized to E4M3 + fp32 scales first, the pair is
+                   permuted together and the gate/up GEMM dequantizes in its
+                   loader.
 ``DecodeBucket``   a fixed token bucket for decode steps: stable buffers, one
                    captured CUDA graph of the bucketed layer, a device-side
                    valid-token count, exact admission and an eager fallback.
@@ -32,6 +35,10 @@ def capacity_from_factor(cf: float, assignments: int, slots: int) -> int:
     return abi.moe_capacity(fr.numerator, fr.denominator, assignments, slots)
 
 
+# dispatch payload of the expert input rows -> scale group of the FP8 forms
+PAYLOADS = {"bf16": None, "fp8_row": abi.MOE_SCALE_ROW, "fp8_block128": abi.MOE_SCALE_BLOCK128}
+
+
 def _u8(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
@@ -40,8 +47,12 @@ class MoELayer:
     def __init__(self, T: int, d: int, E: int, k: int, I: int, w_gate, w_up, w_down,
                  capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
                  topk_group: int = 1, route_scale: float = 1.0, sel_bias=None,
-                 shared_weights=None, device="cuda"):
+                 shared_weights=None, payload: str = "bf16", device="cuda"):
         self.T, self.d, self.E, self.k, self.I = T, d, E, k, I
+        if payload not in PAYLOADS:
+            raise ValueError(f"payload must be one of {sorted(PAYLOADS)}")
+        self.payload = payload
+        self.scale_group = PAYLOADS[payload]
         self.capacity = capacity
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
         self.sel_bias = sel_bias
@@ -51,7 +62,14 @@ class MoELayer:
         i32 = dict(dtype=torch.int32, device=dev)
         self.topk_ids = torch.empty((T, k), **i32)
         self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
-        self.x_perm = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
+        if payload == "bf16":
+            self.x_perm = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
+        else:
+            G = abi.fp8_scale_groups(d, self.scale_group)
+            self.xq = torch.empty((max(T, 1), d), dtype=torch.uint8, device=dev)
+            self.xs = torch.empty((max(T, 1), G), dtype=torch.float32, device=dev)
+            self.xq_perm = torch.empty((max(R, 1), d), dtype=torch.uint8, device=dev)
+            self.xs_perm = torch.empty((max(R, 1), G), dtype=torch.float32, device=dev)
         self.counts = torch.empty((E,), **i32)
         self.offsets = torch.empty((E + 1,), **i32)
         self.row_to_route = torch.empty((max(R, 1),), **i32)
@@ -84,7 +102,18 @@ class MoELayer:
         abi.moe_route(self.params, logits, self.sel_bias, self.topk_ids, self.gates,
                       self.dev_status, stream)
 
+    def quantize(self, x, stream=None):
+        abi.moe_quantize_fp8(self.T, self.d, self.scale_group, x, self.xq, self.xs,
+                             self.dev_status, stream)
+
     def permute(self, x, stream=None):
+        if self.payload != "bf16":
+            abi.moe_permute_fp8(self.T, self.d, self.E, self.k, self.capacity, self.scale_group,
+                                self.topk_ids, self.xq, self.xs, self.xq_perm, self.xs_perm,
+                                self.counts, self.offsets, self.row_to_route, self.route_to_row,
+                                self.n_dropped, self.perm_ws, self.perm_ws_bytes,
+                                self.dev_status, stream)
+            return
         abi.moe_permute(self.T, self.d, self.E, self.k, self.capacity, self.topk_ids, x,
                         self.x_perm, self.counts, self.offsets, self.row_to_route,
                         self.route_to_row, self.n_dropped, self.perm_ws, self.perm_ws_bytes,
@@ -92,6 +121,11 @@ class MoELayer:
 
     def experts_gate_up(self, stream=None):
         R = max(self.T * self.k, 1)
+        if self.payload != "bf16":
+            abi.moe_grouped_gate_up_fp8(self.E, self.d, self.I, R, self.scale_group, self.xq_perm,
+                                        self.xs_perm, self.offsets, self.counts, self.w_gate,
+                                        self.w_up, self.H, self.dev_status, stream)
+            return
         abi.moe_grouped_gate_up(self.E, self.d, self.I, R, self.x_perm, self.offsets, self.counts,
                                 self.w_gate, self.w_up, self.H, self.dev_status, stream)
 
@@ -118,8 +152,10 @@ class MoELayer:
 
     def stages(self, logits, x):
         """The layer as (name, callable(stream)) steps, in launch order."""
-        st = [("route", lambda s: self.route(logits, s)),
-              ("permute", lambda s: self.permute(x, s)),
+        st = [("route", lambda s: self.route(logits, s))]
+        if self.payload != "bf16":
+            st.append(("quantize", lambda s: self.quantize(x, s)))
+        st += [("permute", lambda s: self.permute(x, s)),
               ("gate_up", self.experts_gate_up),
               ("down", self.experts_down)]
         if self.shared is not None:

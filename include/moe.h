@@ -57,7 +57,8 @@ enum {
   MOE_DEV_BAD_EXPERT_ID = 2u,   /* an expert id outside [0,E); the route was skipped */
   MOE_DEV_BAD_HEADER_ID = 4u,   /* a pool header id >= n_local that is not EMPTY     */
   MOE_DEV_BAD_ROW = 8u,         /* a map entry outside the row space; skipped        */
-  MOE_DEV_TIMEOUT = 16u         /* a bounded pipeline wait gave up; output invalid   */
+  MOE_DEV_TIMEOUT = 16u,        /* a bounded pipeline wait gave up; output invalid   */
+  MOE_DEV_NONFINITE_INPUT = 32u /* a NaN/Inf activation met by moe_quantize_fp8      */
 };
 
 #define MOE_POOL_EMPTY 0xFFFFu /* header element of an unused pool row */
@@ -369,6 +370,77 @@ enum { MOE_BIAS_SIGN = 0, MOE_BIAS_PROPORTIONAL = 1 };
  * fp32 once, then added with one fp32 rounding.                              */
 moe_status moe_bias_update(int32_t E, const int32_t* counts, float* bias, float u, int32_t rule,
                            moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* FP8 dispatch payload with fp32 scales                                    */
+/* ------------------------------------------------------------------------ */
+/* [M6.6] 0x0AB-0x0AF: a dispatched activation row may travel as FP8 data plus
+ * fp32 scale metadata.  The pair belongs together: the scales are permuted with
+ * their rows (same route row) and the expert dequantizes each row with its own
+ * scale; scales left in token order next to expert-major rows would give finite
+ * but wrong expert inputs.
+ *   Format: E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ *   infinities; 0x7F / 0xFF are NaN; largest finite value 448).
+ *   Scale groups: group = MOE_SCALE_ROW (0): one scale per row, G = 1;
+ *   group = MOE_SCALE_BLOCK128 (128): one scale per 128 consecutive values of a
+ *   row, G = ceil(d / 128), the last group shorter when 128 does not divide d.
+ *   Scales are fp32 [rows, G], row-major.
+ *   Quantization of a group with largest magnitude amax: s = fp32(amax / 448)
+ *   (s = 1 for an all-zero group) and code = E4M3(fp32(x / s)), to nearest with
+ *   ties to even, saturated to +-448.
+ *   Dequantization: xhat = bf16(fp32(decode(code) * s)), the bf16 operand of the
+ *   expert GEMM (one fp32 rounding of the exact product, one bf16 rounding).
+ *   The NaN codes, which moe_quantize_fp8 emits only for non-finite input, are
+ *   outside the contract: they dequantize to +-480 * s.                      */
+typedef uint8_t moe_fp8; /* raw E4M3 byte */
+
+enum { MOE_SCALE_ROW = 0, MOE_SCALE_BLOCK128 = 128 };
+enum { MOE_PAYLOAD_BF16 = 0, MOE_PAYLOAD_FP8_ROW = 1, MOE_PAYLOAD_FP8_BLOCK128 = 2 };
+
+/* Logical payload bytes of `rows` dispatched rows of width d ([M6.6] 0x0AB):
+ * BF16 rows*d*2; FP8_ROW rows*d + rows*4; FP8_BLOCK128 rows*d + rows*ceil(d/128)*4.
+ * Alignment, metadata, headers and packetization are not included.  Host
+ * function; returns -1 for rows < 0, d < 1 or an unknown payload.           */
+int64_t moe_payload_bytes(int64_t rows, int32_t d, int32_t payload);
+
+/* Quantize bf16 rows x [n,d] to E4M3 codes q [n,d] and fp32 scales [n,G] as
+ * above.  Limits: d % 16 == 0, 16-byte aligned x and q, group 0 or 128.  A
+ * non-finite input sets MOE_DEV_NONFINITE_INPUT; that group's codes and scale
+ * are then unspecified.                                                      */
+moe_status moe_quantize_fp8(int64_t n, int32_t d, int32_t group, const moe_bf16* x, moe_fp8* q,
+                            float* scales, uint32_t* dev_status, moe_stream_t stream);
+
+/* x[i] = bf16(fp32(decode(q[i]) * s)) over rows [n,d]: the operand that
+ * moe_grouped_gate_up_fp8 builds in shared memory, written out.  Limits as
+ * moe_quantize_fp8 (x and q 16-byte aligned).                                */
+moe_status moe_dequantize_fp8(int64_t n, int32_t d, int32_t group, const moe_fp8* q,
+                              const float* scales, moe_bf16* x, moe_stream_t stream);
+
+/* moe_permute with an FP8 payload ([M6.6] 0x0AC row trace): the same admission,
+ * counts, offsets, row_to_route, route_to_row and n_dropped as moe_permute,
+ * and for every accepted route q_perm[row] = q[token] (d bytes) and
+ * scales_perm[row] = scales[token] (G floats): the payload and its scales move
+ * together.  q [T,d], scales [T,G], q_perm [T*k,d], scales_perm [T*k,G]; rows
+ * >= offsets[E] are left untouched.  Workspace: moe_permute_workspace_size.
+ * Limits as moe_permute with d % 16 == 0 and 16-byte aligned q / q_perm.     */
+moe_status moe_permute_fp8(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capacity,
+                           int32_t group, const int32_t* topk_ids, const moe_fp8* q,
+                           const float* scales, moe_fp8* q_perm, float* scales_perm,
+                           int32_t* counts, int32_t* offsets, int32_t* row_to_route,
+                           int32_t* route_to_row, int32_t* n_dropped, void* ws, size_t ws_bytes,
+                           uint32_t* dev_status, moe_stream_t stream);
+
+/* moe_grouped_gate_up with an FP8 A operand: the expert input rows arrive as
+ * E4M3 codes xq [max_rows, d] with fp32 scales [max_rows, G]; the kernel's
+ * loader dequantizes every staged tile with the scale of its own row (and
+ * 128-value group) into the bf16 operand moe_dequantize_fp8 defines, so h is
+ * bit-identical to moe_grouped_gate_up on moe_dequantize_fp8's output.  Limits
+ * and errors as moe_grouped_gate_up; scales 4-byte aligned.                  */
+moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                                   int32_t group, const moe_fp8* xq, const float* scales,
+                                   const int32_t* seg_begin, const int32_t* seg_count,
+                                   const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* h,
+                                   uint32_t* dev_status, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -74,11 +74,15 @@ def oracle_capacity(w):
     return oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
 
 
-def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, weights_of, shared=None):
+def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, weights_of, shared=None,
+                         shared_x_bits=None):
     """Oracle combined output rows for `tokens` (float64 [n, d]) and their y rows by row.
 
     Each sampled route's expert output is computed from the token row and that
-    expert's weights; ``weights_of(e)`` returns expert e's (Wg, Wu, Wd) bf16 bits."""
+    expert's weights; ``weights_of(e)`` returns expert e's (Wg, Wu, Wd) bf16 bits.
+    The shared expert reads ``shared_x_bits`` (default: the routed experts' rows)."""
+    if shared_x_bits is None:
+        shared_x_bits = x_bits
     k = w.k
     need = {}
     for t in tokens:
@@ -97,7 +101,7 @@ def oracle_token_outputs(w, tokens, x_bits, ids, gates, perm, weights_of, shared
     sh = None
     if shared is not None:
         sg, su, sd = shared
-        _, sh = oracle.swiglu(oracle.bf16_to_f64(x_bits[np.array(tokens)]),
+        _, sh = oracle.swiglu(oracle.bf16_to_f64(shared_x_bits[np.array(tokens)]),
                               oracle.bf16_to_f64(sg[0]), oracle.bf16_to_f64(su[0]),
                               oracle.bf16_to_f64(sd[0]))
     outs = []

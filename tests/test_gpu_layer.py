@@ -25,21 +25,24 @@ def built():
     build.build()
 
 
-def make_layer(w, wg, wu, wd, sel_bias=None, shared=None):
+def make_layer(w, wg, wu, wd, sel_bias=None, shared=None, payload="bf16"):
     import grouped_expert_gemm_gb300 as g
     cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
     score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
     return g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                       n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
-                      sel_bias=sel_bias, shared_weights=shared, device=DEV)
+                      sel_bias=sel_bias, shared_weights=shared, payload=payload, device=DEV)
 
 
-def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None):
+SCALE_GROUP = {"fp8_row": 0, "fp8_block128": 128}
+
+
+def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, payload="bf16"):
     logits, sel_bias = workloads.make_router_inputs(w, DEV)
     x = workloads.make_activations(w, DEV)
     wg, wu, wd = weights if weights is not None else workloads.make_expert_weights(w, DEV)
     shared = workloads.make_shared_weights(w, DEV)
-    layer = make_layer(w, wg, wu, wd, sel_bias, shared)
+    layer = make_layer(w, wg, wu, wd, sel_bias, shared, payload)
     out = layer.forward(logits, x)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
@@ -60,15 +63,30 @@ def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None):
     xb = bits(x)
     rng = np.random.default_rng(seed)
     rows = np.arange(acc) if acc <= sample_rows else np.sort(rng.choice(acc, sample_rows, False))
-    # permuted payload rows: bit copies
-    assert np.array_equal(bits(layer.x_perm[torch.from_numpy(rows).to(DEV)]),
-                          xb[perm["row_to_route"][rows] // w.k])
+    rows_dev = torch.from_numpy(rows).to(DEV)
+    tok_of_row = perm["row_to_route"][rows] // w.k
+    x_expert = xb  # the bf16 rows the experts see (token order)
+    if payload == "bf16":
+        # permuted payload rows: bit copies
+        assert np.array_equal(bits(layer.x_perm[rows_dev]), xb[tok_of_row])
+    else:
+        # E4M3 codes and scales of every token, bit-exact; permuted together
+        grp = SCALE_GROUP[payload]
+        q, sc = oracle.quantize_fp8(xb, grp)
+        assert np.array_equal(host(layer.xq), q)
+        assert np.array_equal(host(layer.xs).view(np.uint32), sc.view(np.uint32))
+        assert np.array_equal(host(layer.xq_perm[rows_dev]), q[tok_of_row])
+        assert np.array_equal(host(layer.xs_perm[rows_dev]).view(np.uint32),
+                              sc[tok_of_row].view(np.uint32))
+        x_expert = oracle.dequantize_fp8(q, sc, grp)
+    shared_x = xb
 
     tokens = np.arange(w.T) if sample_tokens is None else np.sort(
         rng.choice(w.T, min(sample_tokens, w.T), replace=False))
     shared_bits = None if shared is None else tuple(bits(s) for s in shared)
-    ref_out, y_of_row = oracle_token_outputs(w, tokens, xb, ids, gates, perm,
-                                             weights_fetcher(wg, wu, wd), shared_bits)
+    ref_out, y_of_row = oracle_token_outputs(w, tokens, x_expert, ids, gates, perm,
+                                             weights_fetcher(wg, wu, wd), shared_bits,
+                                             shared_x_bits=shared_x)
     if y_of_row:
         yrows = np.array(sorted(y_of_row))
         got_y = oracle.bf16_to_f64(bits(layer.y[torch.from_numpy(yrows).to(DEV)]))
@@ -110,6 +128,37 @@ def test_v3_full_size_sampled():
 def test_v3_small_full():
     w = workloads.scaled(workloads.v3(), T=64, d=256, I=256, shared_I=128)
     run_and_check(w, sample_rows=10**6)
+
+
+# ----------------------------------------------------------------------------
+# FP8 dispatch payload ([M6.6] 0x0AB-0x0AC): E4M3 rows + fp32 scales permuted
+# together, dequantized in the gate/up GEMM's loader
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
+def test_tiny_full_fp8(payload):
+    run_and_check(workloads.tiny(), payload=payload)
+
+
+@pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
+def test_decode_T128_full_fp8(payload, decode_weights):
+    run_and_check(workloads.decode(128), weights=decode_weights, sample_rows=4096, payload=payload)
+
+
+@pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
+def test_v3_small_full_fp8(payload):
+    w = workloads.scaled(workloads.v3(), T=64, d=384, I=256, shared_I=128)
+    run_and_check(w, sample_rows=10**6, payload=payload)
+
+
+@pytest.mark.slow
+def test_v3_full_size_sampled_fp8():
+    run_and_check(workloads.v3(), sample_tokens=6, sample_rows=256, seed=5, payload="fp8_block128")
+
+
+@pytest.mark.slow
+def test_prefill_full_size_sampled_fp8():
+    run_and_check(workloads.prefill(), sample_tokens=8, sample_rows=256, seed=6, payload="fp8_row")
 
 
 # ----------------------------------------------------------------------------
