@@ -426,7 +426,8 @@ def run_ours(args, dist, w):
                         "share": round(stage_ms[n] / sum(stage_ms.values()), 4),
                         "bound": bound, "achieved": round(achieved, 2),
                         "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
-                        "frac": round(frac, 4), "alg_bytes": int(b), "alg_flops": int(f)}
+                        "frac": round(frac, 4), "alg_bytes": int(b), "alg_flops": int(f),
+                        "traffic": lookup_traffic(n, traffic_key(w, layer))}
     dom = max(stage_ms, key=lambda n: stage_ms[n])
     ds = per_stage[dom]
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
