@@ -125,13 +125,16 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
   if (GROUPED) {
     // Group score: sum of the two largest corrected scores of each contiguous group.
     const int gs = E / n_group;
+    int grp[VPL];  // group of each of this lane's experts (one division each)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) grp[i] = (i * 32 + lane) / gs;
     float my_gscore = -INFINITY;
     for (int g = 0; g < n_group; ++g) {
       float b1 = -INFINITY, b2 = -INFINITY;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = i * 32 + lane;
-        if (e < E && e / gs == g) {
+        if (e < E && grp[i] == g) {
           const float v = sel[i];
           if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
         }
@@ -158,30 +161,36 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = i * 32 + lane;
-      if (e < E && !((keep >> (e / gs)) & 1u)) taken |= 1u << i;
+      if (e < E && !((keep >> grp[i]) & 1u)) taken |= 1u << i;
     }
   }
 
-  // k rounds of warp arg-max; lane j keeps the j-th winner.
+  // k rounds of warp arg-max over keys built once; lane j keeps the j-th winner.
+  // A taken expert's key is 0, below every live key (a live key's high word is
+  // the orderable score, never 0 for a number or -inf).
+  uint64_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) key[i] = ((taken >> i) & 1u) ? 0ull : make_key(sel[i], i * 32 + lane);
   int my_id = 0;
   float my_sel = 0.0f, my_aff = 0.0f, top_sel = 0.0f;
   for (int j = 0; j < k; ++j) {
-    uint64_t local = 0ull;
+    uint64_t local = key[0];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if (!((taken >> i) & 1u)) {
-        const uint64_t key = make_key(sel[i], i * 32 + lane);
-        local = key > local ? key : local;
-      }
-    }
+    for (int i = 1; i < VPL; ++i) local = key[i] > local ? key[i] : local;
     const uint64_t best = warp_max_u64(local);
     const int e = key_expert(best);
+    const int owner = e & 31, slot = e >> 5;
     float a = 0.0f;
+    if (lane == owner) {
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if (i * 32 + lane == e) { taken |= 1u << i; a = aff[i]; }
+      for (int i = 0; i < VPL; ++i) {
+        if (i == slot) {
+          key[i] = 0ull;
+          if (GROUPED) a = aff[i];
+        }
+      }
     }
-    a = __shfl_sync(0xFFFFFFFFu, a, e & 31);
+    if (GROUPED) a = __shfl_sync(0xFFFFFFFFu, a, owner);
     const float v = ord_to_float(static_cast<uint32_t>(best >> 32));
     if (j == 0) top_sel = v;
     if (lane == j) { my_id = e; my_sel = v; my_aff = a; }
