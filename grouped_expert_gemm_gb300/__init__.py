@@ -5,6 +5,6 @@ composes the calls into one layer forward.
 """
 from . import abi  # noqa: F401
 from .abi import *  # noqa: F401,F403
-from .layer import DecodeBucket, MoELayer, PooledMoELayer, capacity_from_factor  # noqa: F401
+from .layer import DecodeBucket, HostPipeline, MoELayer, PooledMoELayer, capacity_from_factor  # noqa: F401
 
-__all__ = ["abi", "MoELayer", "PooledMoELayer", "DecodeBucket", "capacity_from_factor"] + abi.EXPORTED
+__all__ = ["abi", "MoELayer", "PooledMoELayer", "DecodeBucket", "HostPipeline", "capacity_from_factor"] + abi.EXPORTED

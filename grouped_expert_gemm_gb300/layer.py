@@ -144,14 +144,15 @@ class MoELayer:
                                self.shared_count, sg, su, sd, self.shared_y, self.shared_ws,
                                self.shared_ws_bytes, self.dev_status, stream)
 
-    def combine(self, stream=None):
+    def combine(self, stream=None, out=None):
         R = max(self.T * self.k, 1)
         abi.moe_combine(self.T, self.k, self.d, self.y, R, self.route_to_row, self.gates,
-                        self.shared_y if self.shared is not None else None, 0, self.out,
-                        self.dev_status, stream)
+                        self.shared_y if self.shared is not None else None, 0,
+                        self.out if out is None else out, self.dev_status, stream)
 
-    def stages(self, logits, x):
-        """The layer as (name, callable(stream)) steps, in launch order."""
+    def stages(self, logits, x, out=None):
+        """The layer as (name, callable(stream)) steps, in launch order; the fp32 result
+        goes to `out` (default: the layer's own buffer)."""
         st = [("route", lambda s: self.route(logits, s))]
         if self.payload != "bf16":
             st.append(("quantize", lambda s: self.quantize(x, s)))
@@ -160,14 +161,15 @@ class MoELayer:
               ("down", self.experts_down)]
         if self.shared is not None:
             st.append(("shared_expert", lambda s: self.shared_expert(x, s)))
-        st.append(("combine", self.combine))
+        st.append(("combine", lambda s: self.combine(s, out)))
         return st
 
-    def forward(self, logits, x, stream=None) -> torch.Tensor:
-        """Enqueue the whole layer on `stream`; returns the fp32 output buffer [T, d]."""
-        for _, fn in self.stages(logits, x):
+    def forward(self, logits, x, stream=None, out=None) -> torch.Tensor:
+        """Enqueue the whole layer on `stream`; returns the fp32 output buffer [T, d]
+        (`out` if given, else the layer's own)."""
+        for _, fn in self.stages(logits, x, out):
             fn(stream)
-        return self.out
+        return self.out if out is None else out
 
     def forward_host(self, logits_host, x_host, out_host, stream=None):
         """Layer forward for host-resident inputs: copies logits and x from (pinned) host
@@ -246,12 +248,13 @@ class PooledMoELayer:
                                self.local_counts, self.w_gate, self.w_up, self.w_down, self.y,
                                self.gemm_ws, self.gemm_ws_bytes, self.dev_status, stream)
 
-    def combine_wave(self, wave, stream=None):
+    def combine_wave(self, wave, stream=None, out=None):
         abi.moe_compose_map(self.T * self.k, self.route_to_poolrow, self.poolrow_to_row,
                             self.n_dest * self.pool_cap, self.route_to_row, self.dev_status,
                             stream)
         abi.moe_combine(self.T, self.k, self.d, self.y, self.rows, self.route_to_row, self.gates,
-                        None, 1 if wave > 0 else 0, self.out, self.dev_status, stream)
+                        None, 1 if wave > 0 else 0, self.out if out is None else out,
+                        self.dev_status, stream)
 
     def experts_gate_up(self, stream=None):
         abi.moe_grouped_gate_up(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,
@@ -266,22 +269,91 @@ class PooledMoELayer:
     def H(self) -> torch.Tensor:
         return self.gemm_ws[: self.rows * self.I * 2].view(torch.bfloat16).view(self.rows, self.I)
 
-    def stages(self, logits, x):
+    def stages(self, logits, x, out=None):
         st = [("route", lambda s: self.route(logits, s))]
         for w in range(self.n_waves):
             st += [("pool_pack", lambda s, w=w: self.pack(x, w, s)),
                    ("pool_compact", lambda s, w=w: self.compact_wave(w, s)),
                    ("gate_up", self.experts_gate_up),
                    ("down", self.experts_down),
-                   ("combine", lambda s, w=w: self.combine_wave(w, s))]
+                   ("combine", lambda s, w=w: self.combine_wave(w, s, out))]
         return st
 
-    def forward(self, logits, x, stream=None) -> torch.Tensor:
-        for _, fn in self.stages(logits, x):
+    def forward(self, logits, x, stream=None, out=None) -> torch.Tensor:
+        for _, fn in self.stages(logits, x, out):
             fn(stream)
-        return self.out
+        return self.out if out is None else out
 
     forward_host = MoELayer.forward_host
+
+
+class HostPipeline:
+    """Layer steps served from host-resident (pinned) inputs with the copies overlapped.
+
+    Each step copies its logits and token rows host->device on an upload stream, runs
+    the layer on the caller's stream and copies the fp32 result device->host on a
+    download stream.  Device inputs and outputs are double-buffered, so step i's
+    upload overlaps step i-1's layer and step i's download overlaps step i+1's layer;
+    every copy of every step still happens, in step order on its stream.  Usage:
+
+        pipe.begin(stream); for each step: pipe.submit(logits_h, x_h, out_h); pipe.end(stream)
+
+    `begin` makes the copy streams wait for work already on `stream`, `end` makes
+    `stream` wait for every submitted copy, so the whole sequence can be captured into
+    one CUDA graph or timed with events on `stream`.  Nothing synchronises the host.
+    """
+
+    def __init__(self, layer):
+        self.layer = layer
+        dev = layer.out.device
+        self.up = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        self.outs = [layer.out, torch.empty_like(layer.out)]
+        self.ins = None
+        self.ev = {name: [torch.cuda.Event(), torch.cuda.Event()]
+                   for name in ("uploaded", "in_free", "computed", "out_free")}
+
+    def _inputs(self, logits_host, x_host):
+        if self.ins is None:
+            dev = self.layer.out.device
+            self.ins = [(torch.empty(logits_host.shape, dtype=logits_host.dtype, device=dev),
+                         torch.empty(x_host.shape, dtype=x_host.dtype, device=dev))
+                        for _ in range(2)]
+        return self.ins
+
+    def begin(self, stream=None):
+        self.stream = torch.cuda.current_stream() if stream is None else stream
+        self.up.wait_stream(self.stream)
+        self.down.wait_stream(self.stream)
+        self.i = 0
+
+    def submit(self, logits_host, x_host, out_host):
+        ins = self._inputs(logits_host, x_host)
+        b = self.i % 2
+        ev = self.ev
+        if self.i >= 2:
+            self.up.wait_event(ev["in_free"][b])  # the layer is done reading inputs b
+        with torch.cuda.stream(self.up):
+            ins[b][0].copy_(logits_host, non_blocking=True)
+            ins[b][1].copy_(x_host, non_blocking=True)
+            ev["uploaded"][b].record(self.up)
+        self.stream.wait_event(ev["uploaded"][b])
+        if self.i >= 2:
+            self.stream.wait_event(ev["out_free"][b])  # output b has been read back
+        with torch.cuda.stream(self.stream):
+            self.layer.forward(ins[b][0], ins[b][1], self.stream, out=self.outs[b])
+            ev["in_free"][b].record(self.stream)
+            ev["computed"][b].record(self.stream)
+        self.down.wait_event(ev["computed"][b])
+        with torch.cuda.stream(self.down):
+            out_host.copy_(self.outs[b], non_blocking=True)
+            ev["out_free"][b].record(self.down)
+        self.i += 1
+
+    def end(self, stream=None):
+        s = self.stream if stream is None else stream
+        s.wait_stream(self.up)
+        s.wait_stream(self.down)
 
 
 class DecodeBucket:

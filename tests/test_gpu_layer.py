@@ -251,3 +251,83 @@ def test_pooled_full_size_sampled():
     totals = pooled_check(workloads.pooled(), 0, sample_tokens=8, sample_rows=256, seed=4)
     rates = oracle.drop_rates(65536 * 8, totals["sender"], totals["receiver"])
     assert 0 < rates["total"] < 0.5
+
+
+# ----------------------------------------------------------------------------
+# host-buffer pipeline: copies overlapped with the neighbouring steps' layer
+# ----------------------------------------------------------------------------
+
+def _host_steps(w, n, seed):
+    out = []
+    for i in range(n):
+        wi = workloads.scaled(w, seed=seed + i)
+        logits, _ = workloads.make_router_inputs(wi, DEV)
+        x = workloads.make_activations(wi, DEV)
+        out.append((logits.cpu().pin_memory(), x.cpu().pin_memory()))
+    return out
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_host_pipeline_equals_forward(use_graph):
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.tiny()
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    layer = make_layer(w, wg, wu, wd)
+    steps = _host_steps(w, 5, seed=40)
+    outs = [torch.empty((w.T, w.d), dtype=torch.float32).pin_memory() for _ in steps]
+    pipe = g.HostPipeline(layer)
+    stream = torch.cuda.Stream(DEV)
+
+    def run():
+        pipe.begin(stream)
+        for (lh, xh), oh in zip(steps, outs):
+            pipe.submit(lh, xh, oh)
+        pipe.end(stream)
+
+    with torch.cuda.stream(stream):
+        if use_graph:
+            run()  # warm-up outside capture
+            stream.synchronize()
+            for o in outs:
+                o.zero_()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                run()
+            graph.replay()
+        else:
+            run()
+    stream.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    ref_layer = make_layer(w, wg, wu, wd)
+    for (lh, xh), oh in zip(steps, outs):
+        ref = ref_layer.forward(lh.to(DEV), xh.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref.cpu())
+
+
+def test_host_pipeline_pooled_layer():
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.scaled(workloads.pooled(), T=1024, d=256, I=256, n_dest=32, E=32 * 6)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    pool_cap = g.capacity_from_factor(w.sender_cf, w.R, w.n_dest * w.n_waves)
+    local_cap = g.capacity_from_factor(w.receiver_cf, w.R, w.local_per_dest * w.n_waves)
+
+    def mk():
+        return g.PooledMoELayer(w.T, w.d, w.k, w.I, w.n_dest, w.local_per_dest, w.n_waves,
+                                pool_cap, local_cap, wg, wu, wd, device=DEV)
+    layer = mk()
+    steps = _host_steps(w, 3, seed=50)
+    outs = [torch.empty((w.T, w.d), dtype=torch.float32).pin_memory() for _ in steps]
+    pipe = g.HostPipeline(layer)
+    stream = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(stream):
+        pipe.begin(stream)
+        for (lh, xh), oh in zip(steps, outs):
+            pipe.submit(lh, xh, oh)
+        pipe.end(stream)
+    stream.synchronize()
+    ref_layer = mk()
+    for (lh, xh), oh in zip(steps, outs):
+        ref = ref_layer.forward(lh.to(DEV), xh.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref.cpu())
