@@ -87,7 +87,6 @@ struct Geometry {
   static constexpr int kBOff = FP8A ? 0 : kABytes;         // B atoms in a TMA slot
   static constexpr int kRawOff = N_ATOMS * kAtomBytes;     // E4M3 tile in a TMA slot
   static constexpr int kStageBytes = N_ATOMS * kAtomBytes + (FP8A ? kRawBytes : kABytes);
-  static constexpr int kTxBytes = kStageBytes;             // all of a TMA slot comes by TMA
   // As many stages as fit the shared memory: narrower tiles keep more loads in flight.
   static constexpr int kStages = FP8A ? (N_ATOMS >= 4 ? 4 : 8)
                                       : (N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8));
@@ -147,6 +146,11 @@ struct GemmArgs {
   const float* scales;
   int n_groups;
   int group_k;
+  // Single-CTA kernel: rows per tile (the height of the A box TMA stages: 128, or
+  // 16..64 when experts hold few rows; the MMA still runs M = 128 and the rows
+  // past the box are never stored) and the A bytes one stage's TMA delivers.
+  int bm;
+  int a_box_bytes;
 };
 
 // ------------------------------ PTX wrappers -------------------------------
@@ -752,7 +756,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
   pdl_wait();  // everything above is local; global data only from here on
   if (threadIdx.x >= 64 && threadIdx.x < 192)
-    build_segment_table(args, kBM, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
+    build_segment_table(args, args.bm, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -766,13 +770,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       uint32_t ph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut, n_blocks,
-                              args.m_outer);
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, args.bm, kBnOut,
+                                n_blocks, args.m_outer);
         const int b_row0 = tl.seg * args.K;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
           const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
-          mbar_arrive_expect_tx(full_bar(s), G::kTxBytes);
+          mbar_arrive_expect_tx(full_bar(s), args.a_box_bytes + N_ATOMS * kAtomBytes);
           // A: the bf16 tile, or the E4M3 tile for the converter warps
           tma_load_2d(FP8A ? st + G::kRawOff : st, &tmap_a, full_bar(s), ks * kBK, tl.row0);
 #pragma unroll
@@ -861,8 +865,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     int buf = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kBM, kBnOut, n_blocks,
-                              args.m_outer);
+      const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, args.bm, kBnOut,
+                              n_blocks, args.m_outer);
       // warp-uniform exit: the tensor-memory loads below are .sync.aligned
       if (!__all_sync(0xFFFFFFFFu, wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)))
         break;
@@ -880,7 +884,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ================ E4M3 -> bf16 converter (warps 6..13) ================
     convert_a_tiles<kStages, G::kStageBytes, G::kRawOff, kASlots>(
         stage_base, tmem_base + G::kACol, threadIdx.x - 192, lane, blockIdx.x, gridDim.x,
-        total_tiles, k_steps, kBM, 0, args, sm, n_blocks, kBnOut, full_bar(0), afull_bar(0),
+        total_tiles, k_steps, args.bm, 0, args, sm, n_blocks, kBnOut, full_bar(0), afull_bar(0),
         aempty_bar(0), abort_flag);
   }
 
@@ -1308,6 +1312,27 @@ int choose_m_outer(int32_t n_seg, int32_t max_rows, int32_t K, int64_t b_cols_pe
   return (a_seg > kL2Budget && b_seg <= kL2Budget) ? 1 : 0;
 }
 
+// Rows per single-CTA tile.  Decode-sized batches leave most of a 128-row A box
+// empty (one token touches k experts with one row each), and staging it costs
+// L2 traffic and TMA time beside the weights being streamed: the box height
+// follows four times the average rows per segment, at least 16.
+int choose_bm(int32_t n_seg, int32_t max_rows) {
+  const int64_t four_avg = 4 * static_cast<int64_t>(max_rows) / (n_seg > 0 ? n_seg : 1);
+  return four_avg <= 16 ? 16 : four_avg <= 32 ? 32 : four_avg <= 64 ? 64 : kBM;
+}
+
+// Single-CTA gate/up tiles of 2 x 128 columns unless even one tile per touched
+// expert and n-block (at most min(n_seg, max_rows) experts hold rows) leaves SMs
+// without work -- one-token decode -- then 2 x 64 (with small-M boxes measured
+// 20.5 -> 18.4 us for the gate/up pass at T = 1; the down pass is better off wide).
+bool wide_gate_up(int32_t n_seg, int32_t max_rows, int32_t I) {
+  if (I % 128 != 0) return false;
+  static int sms = 0;
+  if (sms == 0) sms = num_sms();
+  const int64_t touched = n_seg < max_rows ? n_seg : max_rows;
+  return touched * (I / 128) >= sms;
+}
+
 bool pair_shape(int32_t n_seg, int32_t max_rows) {
   return static_cast<int64_t>(max_rows) >= static_cast<int64_t>(kBM) * n_seg;
 }
@@ -1344,18 +1369,18 @@ MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int3
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up))
     return MOE_ERR_UNSUPPORTED;
+  const bool pair = I % 128 == 0 && pair_shape(n_seg, max_rows);
+  const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
   CUtensorMap m_x, m_wg, m_wu;
-  if (!make_map(&m_x, x, max_rows, d, kBM) || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
+  if (!make_map(&m_x, x, max_rows, d, bm) || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
       !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
              dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
-             nullptr, 0, 0};
+             nullptr, 0, 0, bm, bm * kBK * 2};
   cudaStream_t s = as_cuda(stream);
-  if (I % 128 == 0) {
-    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s)
-                                       : launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
-  }
+  if (pair) return launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s);
+  if (wide_gate_up(n_seg, max_rows, I)) return launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
   return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
 }
 
@@ -1375,21 +1400,21 @@ MOE_API moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, 
   if (!aligned16(xq) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up) ||
       (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
     return MOE_ERR_UNSUPPORTED;
+  // the same kernel shapes and tile heights as the bf16 operand
+  const bool pair = I % 128 == 0 && pair_shape(n_seg, max_rows);
+  const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
   CUtensorMap m_x, m_wg, m_wu;
-  if (!make_map(&m_x, xq, max_rows, d, kBM, true) ||
+  if (!make_map(&m_x, xq, max_rows, d, bm, true) ||
       !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
       !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
     return MOE_ERR_CUDA;
   const int n_groups = group == MOE_SCALE_ROW ? 1 : static_cast<int>(ceil_div(d, 128));
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
              dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
-             scales, n_groups, group == MOE_SCALE_ROW ? d : 128};
+             scales, n_groups, group == MOE_SCALE_ROW ? d : 128, bm, bm * kBK};
   cudaStream_t s = as_cuda(stream);
-  // the same kernel shapes as the bf16 operand
-  if (I % 128 == 0) {
-    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<true, true>(m_x, m_wg, m_wu, a, s)
-                                       : launch_gemm<4, true, true>(m_x, m_wg, m_wu, a, s);
-  }
+  if (pair) return launch_gemm_pair<true, true>(m_x, m_wg, m_wu, a, s);
+  if (wide_gate_up(n_seg, max_rows, I)) return launch_gemm<4, true, true>(m_x, m_wg, m_wu, a, s);
   return launch_gemm<2, true, true>(m_x, m_wg, m_wu, a, s);
 }
 
@@ -1403,18 +1428,18 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
       y == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(y) || !aligned16(w_down)) return MOE_ERR_UNSUPPORTED;
+  const bool pair = d % 256 == 0 && pair_shape(n_seg, max_rows);
+  const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
   CUtensorMap m_h, m_wd;
-  if (!make_map(&m_h, h, max_rows, I, kBM) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
+  if (!make_map(&m_h, h, max_rows, I, bm) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
-             dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0};
+             dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0, bm, bm * kBK * 2};
   cudaStream_t s = as_cuda(stream);
-  // The widest output tile the width allows (narrower tiles for one-token decode were
-  // measured slower: the few tiles there are bound by pipeline latency, not SM count).
-  if (d % 256 == 0) {
-    return pair_shape(n_seg, max_rows) ? launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s)
-                                       : launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
-  }
+  // The widest output tile the width allows (narrower 128-row tiles for one-token
+  // decode were measured slower: the few tiles there are bound by pipeline latency).
+  if (pair) return launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s);
+  if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
   if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
   return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
 }
