@@ -190,6 +190,7 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
     touched = int((counts > 0).sum())
     # bytes of one dispatched row: bf16 data, or E4M3 data plus its fp32 scales
     row_b = d * 2
+    fused = getattr(layer, "fused_fp8", False)
     if getattr(layer, "payload", "bf16") != "bf16":
         row_b = d + layer.xs.shape[1] * 4
     if name == "route":
@@ -198,8 +199,11 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
         return T * d * 2 + T * row_b, 0
     if name == "permute":
         return T * k * 4 + T * row_b + acc_rows * row_b + 2 * T * k * 4 + (2 * E + 1) * 4, 0
+    if name == "dequantize":
+        return acc_rows * row_b + acc_rows * d * 2, 0
     if name == "gate_up":
-        return touched * 2 * d * I * 2 + acc_rows * row_b + acc_rows * I * 2, 4 * acc_rows * d * I
+        a_row = row_b if fused else d * 2  # the unfused FP8 path reads the dequantized bf16 rows
+        return touched * 2 * d * I * 2 + acc_rows * a_row + acc_rows * I * 2, 4 * acc_rows * d * I
     if name == "down":
         return touched * I * d * 2 + acc_rows * I * 2 + acc_rows * d * 2, 2 * acc_rows * I * d
     if name == "shared_expert":
@@ -234,7 +238,7 @@ def load_peaks():
 def kernel_source_sha(name):
     src = {"gate_up": "grouped_swiglu.cu", "down": "grouped_swiglu.cu",
            "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
-           "quantize": "fp8.cu",
+           "quantize": "fp8.cu", "dequantize": "fp8.cu",
            "combine": "combine.cu", "pool_pack": "pool.cu", "pool_compact": "pool.cu"}[name]
     with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", src), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]

@@ -17,6 +17,7 @@ namespace moe {
 namespace {
 
 constexpr int kQThreads = 256;
+constexpr int kQUnroll = 4;  // 16-byte loads in flight per lane
 constexpr float kE4M3Max = 448.0f;
 constexpr uint32_t kAbsInf = 0x7F800000u;
 
@@ -63,26 +64,56 @@ quantize_kernel(int64_t n, int d, int G, const uint4* __restrict__ x, uint2* __r
     const uint4* xr = x + row * chunks;
     uint2* qr = q + row * chunks;
     if constexpr (ROW) {
+      // largest magnitude first (four 16-byte loads in flight per lane), then the codes
       uint32_t m = 0;
-      for (int c = lane; c < chunks; c += 32) m = max(m, amax_bits8(__ldg(xr + c)));
+      for (int cb = 0; cb < chunks; cb += 32 * kQUnroll) {
+        uint4 v[kQUnroll];
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int c = cb + u * 32 + lane;
+          v[u] = c < chunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) m = max(m, amax_bits8(v[u]));
+      }
       m = __reduce_max_sync(0xFFFFFFFFu, m);
       if (m >= kAbsInf) bad = true;
       const float s = scale_of(m);
       if (lane == 0) scales[row] = s;
-      for (int c = lane; c < chunks; c += 32) qr[c] = quant8(__ldg(xr + c), s);
-    } else {
-      // Half-warp h of iteration `it` owns group 2*it + h (chunks 16g .. 16g+15).
-      for (int cb = 0; cb < chunks; cb += 32) {
-        const int c = cb + lane;
-        const bool live = c < chunks;
-        const uint4 v = live ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-        uint32_t m = amax_bits8(v);
+      for (int cb = 0; cb < chunks; cb += 32 * kQUnroll) {
+        uint4 v[kQUnroll];
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (m >= kAbsInf && live) bad = true;
-        const float s = scale_of(m);
-        if (live && (c & 15) == 0) scales[row * G + (c >> 4)] = s;
-        if (live) qr[c] = quant8(v, s);
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int c = cb + u * 32 + lane;
+          if (c < chunks) v[u] = __ldg(xr + c);
+        }
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int c = cb + u * 32 + lane;
+          if (c < chunks) qr[c] = quant8(v[u], s);
+        }
+      }
+    } else {
+      // Half-warp h of sub-iteration u owns group 2*(cb/32 + u) + h (chunks 16g .. 16g+15).
+      for (int cb = 0; cb < chunks; cb += 32 * kQUnroll) {
+        uint4 v[kQUnroll];
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int c = cb + u * 32 + lane;
+          v[u] = c < chunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kQUnroll; ++u) {
+          const int c = cb + u * 32 + lane;
+          const bool live = c < chunks;
+          uint32_t m = amax_bits8(v[u]);
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          if (m >= kAbsInf && live) bad = true;
+          const float s = scale_of(m);
+          if (live && (c & 15) == 0) scales[row * G + (c >> 4)] = s;
+          if (live) qr[c] = quant8(v[u], s);
+        }
       }
     }
   }
@@ -90,22 +121,44 @@ quantize_kernel(int64_t n, int d, int G, const uint4* __restrict__ x, uint2* __r
   pdl_trigger();
 }
 
-// One thread per 16 codes.
+// One warp per row, kDqUnroll 16-code chunks in flight per lane.  A chunk's
+// scale is the row's (one group) or that of its 128-value group (chunk c / 8).
+constexpr int kDqUnroll = 4;
+
 __global__ void __launch_bounds__(kQThreads)
-dequantize_kernel(int64_t n, int d, int G, int group_elems, const uint4* __restrict__ q,
+dequantize_kernel(int64_t n, int d, int G, const uint4* __restrict__ q,
                   const float* __restrict__ scales, uint4* __restrict__ x) {
   pdl_wait();
-  const int per_row = d / 16;
-  const int64_t total = n * per_row;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = i / per_row;
-    const int col = static_cast<int>(i - row * per_row) * 16;
-    const float s = __ldg(scales + row * G + col / group_elems);
-    uint4 lo, hi;
-    dequant16(__ldg(q + i), s, lo, hi);
-    x[2 * i] = lo;
-    x[2 * i + 1] = hi;
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int per_row = d / 16;  // 16 codes per chunk
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); row < n;
+       row += static_cast<int64_t>(gridDim.x) * warps) {
+    const uint4* qr = q + row * per_row;
+    uint4* xr = x + row * per_row * 2;
+    const float* sr = scales + row * G;
+    for (int cb = 0; cb < per_row; cb += 32 * kDqUnroll) {
+      uint4 v[kDqUnroll];
+      float sc[kDqUnroll];
+#pragma unroll
+      for (int u = 0; u < kDqUnroll; ++u) {
+        const int c = cb + u * 32 + lane;
+        if (c < per_row) {
+          v[u] = __ldg(qr + c);
+          sc[u] = __ldg(sr + (G == 1 ? 0 : (c >> 3)));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kDqUnroll; ++u) {
+        const int c = cb + u * 32 + lane;
+        if (c < per_row) {
+          uint4 lo, hi;
+          dequant16(v[u], sc[u], lo, hi);
+          xr[2 * c] = lo;
+          xr[2 * c + 1] = hi;
+        }
+      }
+    }
   }
   pdl_trigger();
 }
@@ -168,9 +221,7 @@ MOE_API moe_status moe_dequantize_fp8(int64_t n, int32_t d, int32_t group, const
   if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
     return MOE_ERR_UNSUPPORTED;
   const int G = static_cast<int>(n_groups(d, group));
-  const int64_t items = n * (d / 16);
-  launch(dequantize_kernel, dim3(grid_for(items, kQThreads)), dim3(kQThreads), 0, as_cuda(stream),
-         n, d, G, group == 0 ? d : 128, reinterpret_cast<const uint4*>(q), scales,
-         reinterpret_cast<uint4*>(x));
+  launch(dequantize_kernel, dim3(grid_for(n, kQThreads / 32)), dim3(kQThreads), 0, as_cuda(stream),
+         n, d, G, reinterpret_cast<const uint4*>(q), scales, reinterpret_cast<uint4*>(x));
   return launch_status();
 }

@@ -62,9 +62,15 @@ class MoELayer:
         i32 = dict(dtype=torch.int32, device=dev)
         self.topk_ids = torch.empty((T, k), **i32)
         self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
-        if payload == "bf16":
+        # FP8 payload: where experts hold many rows each (>= 128 on average, the
+        # tensor-bound shapes) the permuted rows are dequantized once into bf16 and
+        # the bf16 pass runs -- the fused loader would convert every row block once
+        # per output-column block (measured 1.5x slower on prefill); with few rows per
+        # expert the gate/up pass dequantizes in its loader.  Both give the same bits.
+        self.fused_fp8 = payload != "bf16" and R < 128 * E
+        if payload == "bf16" or not self.fused_fp8:
             self.x_perm = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
-        else:
+        if payload != "bf16":
             G = abi.fp8_scale_groups(d, self.scale_group)
             self.xq = torch.empty((max(T, 1), d), dtype=torch.uint8, device=dev)
             self.xs = torch.empty((max(T, 1), G), dtype=torch.float32, device=dev)
@@ -119,9 +125,15 @@ class MoELayer:
                         self.route_to_row, self.n_dropped, self.perm_ws, self.perm_ws_bytes,
                         self.dev_status, stream)
 
+    def dequantize(self, stream=None):
+        """FP8 payload, unfused: the permuted E4M3 rows and their scales -> bf16 x_perm."""
+        R = max(self.T * self.k, 1)
+        abi.moe_dequantize_fp8(R, self.d, self.scale_group, self.xq_perm, self.xs_perm,
+                               self.x_perm, stream)
+
     def experts_gate_up(self, stream=None):
         R = max(self.T * self.k, 1)
-        if self.payload != "bf16":
+        if self.payload != "bf16" and self.fused_fp8:
             abi.moe_grouped_gate_up_fp8(self.E, self.d, self.I, R, self.scale_group, self.xq_perm,
                                         self.xs_perm, self.offsets, self.counts, self.w_gate,
                                         self.w_up, self.H, self.dev_status, stream)
@@ -156,9 +168,10 @@ class MoELayer:
         st = [("route", lambda s: self.route(logits, s))]
         if self.payload != "bf16":
             st.append(("quantize", lambda s: self.quantize(x, s)))
-        st += [("permute", lambda s: self.permute(x, s)),
-              ("gate_up", self.experts_gate_up),
-              ("down", self.experts_down)]
+        st.append(("permute", lambda s: self.permute(x, s)))
+        if self.payload != "bf16" and not self.fused_fp8:
+            st.append(("dequantize", self.dequantize))
+        st += [("gate_up", self.experts_gate_up), ("down", self.experts_down)]
         if self.shared is not None:
             st.append(("shared_expert", lambda s: self.shared_expert(x, s)))
         st.append(("combine", lambda s: self.combine(s, out)))

@@ -79,6 +79,8 @@ def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, p
         assert np.array_equal(host(layer.xs_perm[rows_dev]).view(np.uint32),
                               sc[tok_of_row].view(np.uint32))
         x_expert = oracle.dequantize_fp8(q, sc, grp)
+        if not layer.fused_fp8:  # dequantized once into bf16 rows before the gate/up pass
+            assert np.array_equal(bits(layer.x_perm[rows_dev]), x_expert[tok_of_row])
     shared_x = xb
 
     tokens = np.arange(w.T) if sample_tokens is None else np.sort(
