@@ -315,18 +315,32 @@ def run_ours(args, dist, w):
     layer, logits, sel_bias, x = build_layer(w, device, args.payload)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
-    names = [n for n, _ in stages]
+    names = [n for n, _, _ in stages]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            for _, fn in stages:
+            for _, fn, _ in stages:
                 fn(stream)
     stream.synchronize()
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after warm-up")
 
-    # An event after every stage of every step.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+    # Per step: an event at the start and one after every stage, on the stream the
+    # stage runs on; a stage on a side stream also gets an event before it there.
+    # A main-stream stage's time runs from the previous main-stream event.
+    def new_ev():
+        return torch.cuda.Event(enable_timing=True)
+    evs = [{"start": new_ev(), "after": [new_ev() for _ in stages],
+            "before": [new_ev() if side is not None else None for _, _, side in stages]}
            for _ in range(steps)]
+
+    def instrumented_step(s_idx, cur, record):
+        ev = evs[s_idx]
+        record(ev["start"], cur)
+        for i, (_, fn, side) in enumerate(stages):
+            if side is not None:
+                record(ev["before"][i], side)
+            fn(None if record is record_external else cur)
+            record(ev["after"][i], side if side is not None else cur)
     use_graph = not args.no_graph
     if use_graph:
         # The K timed steps as one CUDA graph (every call is asynchronous and
@@ -335,24 +349,21 @@ def run_ours(args, dist, w):
         # the step time comes from the plain graph and the kernel durations from the
         # instrumented one, replayed right after it.
         for row in evs:
-            for e in row:
+            for e in [row["start"]] + row["after"] + [b for b in row["before"] if b is not None]:
                 e.record(stream)  # creates the event objects
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         l0 = abi.launch_count()
         with torch.cuda.graph(graph, stream=stream):
             for s in range(steps):
-                for _, fn in stages:
+                for _, fn, _ in stages:
                     fn(None)
         graph_launches = abi.launch_count() - l0
         graph_inst = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_inst, stream=stream):
             cur = torch.cuda.current_stream()
             for s in range(steps):
-                record_external(evs[s][0], cur)
-                for i, (_, fn) in enumerate(stages):
-                    fn(None)
-                    record_external(evs[s][i + 1], cur)
+                instrumented_step(s, cur, record_external)
         with torch.cuda.stream(stream):
             graph.replay()  # warm replays (untimed)
             graph_inst.replay()
@@ -372,10 +383,7 @@ def run_ours(args, dist, w):
                 graph.replay()
             else:
                 for s in range(steps):
-                    evs[s][0].record(stream)
-                    for i, (_, fn) in enumerate(stages):
-                        fn(stream)
-                        evs[s][i + 1].record(stream)
+                    instrumented_step(s, stream, lambda e, st: e.record(st))
         t_end.record(stream)
         stream.synchronize()
         if use_graph:
@@ -392,8 +400,15 @@ def run_ours(args, dist, w):
 
     stage_ms = {}
     for s in range(steps):
-        for i, n in enumerate(names):
-            stage_ms[n] = stage_ms.get(n, 0.0) + evs[s][i].elapsed_time(evs[s][i + 1])
+        prev = evs[s]["start"]
+        for i, (n, _, side) in enumerate(stages):
+            if side is not None:
+                dt = evs[s]["before"][i].elapsed_time(evs[s]["after"][i])
+            else:
+                dt = prev.elapsed_time(evs[s]["after"][i])
+                prev = evs[s]["after"][i]
+            if not (n.endswith("_fork") or n.endswith("_join")):  # ordering steps, no kernels
+                stage_ms[n] = stage_ms.get(n, 0.0) + dt
     per_step = {n: names.count(n) for n in names}
     step_ms = max_ms / steps
     value = dist.world * w.T * steps / (max_ms / 1e3)
@@ -447,7 +462,8 @@ def run_ours(args, dist, w):
         "config": config_dict(w, layer),
         "roofline": roofline, "stages": per_stage,
         "timing": ("the K steps replayed from one captured CUDA graph; stage times from CUDA "
-                   "events between the stages of every step of an instrumented replay of the "
+                   "events between the stages of every step (on the stream each stage runs on) "
+                   "of an instrumented replay of the "
                    "same K steps right after, on the launching stream" if use_graph else
                    "eager launches with CUDA events between the stages of every timed step"),
         "clocks": sampler.summary(),

@@ -97,6 +97,10 @@ class MoELayer:
             self.shared_ws = _u8(self.shared_ws_bytes, dev)
             self.shared_begin = torch.zeros((1,), **i32)
             self.shared_count = torch.full((1,), T, **i32)
+            # The shared expert depends only on the token rows: it runs on a side
+            # stream from the start of the step, beside routing and permutation
+            # (which leave the tensor cores idle), and joins before the combine.
+            self.side = torch.cuda.Stream(dev)
 
     @property
     def H(self) -> torch.Tensor:
@@ -150,6 +154,12 @@ class MoELayer:
         self.experts_gate_up(stream)
         self.experts_down(stream)
 
+    def shared_fork(self, stream=None):
+        self.side.wait_stream(torch.cuda.current_stream() if stream is None else stream)
+
+    def shared_join(self, stream=None):
+        (torch.cuda.current_stream() if stream is None else stream).wait_stream(self.side)
+
     def shared_expert(self, x, stream=None):
         sg, su, sd = self.shared
         abi.moe_grouped_swiglu(1, self.d, self.I_shared, self.T, x, self.shared_begin,
@@ -163,24 +173,31 @@ class MoELayer:
                         self.out if out is None else out, self.dev_status, stream)
 
     def stages(self, logits, x, out=None):
-        """The layer as (name, callable(stream)) steps, in launch order; the fp32 result
-        goes to `out` (default: the layer's own buffer)."""
-        st = [("route", lambda s: self.route(logits, s))]
-        if self.payload != "bf16":
-            st.append(("quantize", lambda s: self.quantize(x, s)))
-        st.append(("permute", lambda s: self.permute(x, s)))
-        if self.payload != "bf16" and not self.fused_fp8:
-            st.append(("dequantize", self.dequantize))
-        st += [("gate_up", self.experts_gate_up), ("down", self.experts_down)]
+        """The layer as (name, callable(stream), side_stream) steps in launch order.  A
+        step with a side stream launches there whatever stream it is given (the fork
+        and join steps order it against the main stream); the others launch on the
+        stream they are given.  The fp32 result goes to `out` (default: the layer's
+        own buffer)."""
+        st = []
         if self.shared is not None:
-            st.append(("shared_expert", lambda s: self.shared_expert(x, s)))
-        st.append(("combine", lambda s: self.combine(s, out)))
+            st += [("shared_fork", self.shared_fork, None),
+                   ("shared_expert", lambda s: self.shared_expert(x, self.side), self.side)]
+        st.append(("route", lambda s: self.route(logits, s), None))
+        if self.payload != "bf16":
+            st.append(("quantize", lambda s: self.quantize(x, s), None))
+        st.append(("permute", lambda s: self.permute(x, s), None))
+        if self.payload != "bf16" and not self.fused_fp8:
+            st.append(("dequantize", self.dequantize, None))
+        st += [("gate_up", self.experts_gate_up, None), ("down", self.experts_down, None)]
+        if self.shared is not None:
+            st.append(("shared_join", self.shared_join, None))
+        st.append(("combine", lambda s: self.combine(s, out), None))
         return st
 
     def forward(self, logits, x, stream=None, out=None) -> torch.Tensor:
         """Enqueue the whole layer on `stream`; returns the fp32 output buffer [T, d]
         (`out` if given, else the layer's own)."""
-        for _, fn in self.stages(logits, x, out):
+        for _, fn, _ in self.stages(logits, x, out):
             fn(stream)
         return self.out if out is None else out
 
@@ -283,17 +300,18 @@ class PooledMoELayer:
         return self.gemm_ws[: self.rows * self.I * 2].view(torch.bfloat16).view(self.rows, self.I)
 
     def stages(self, logits, x, out=None):
-        st = [("route", lambda s: self.route(logits, s))]
+        """(name, callable(stream), side_stream=None) steps in launch order."""
+        st = [("route", lambda s: self.route(logits, s), None)]
         for w in range(self.n_waves):
-            st += [("pool_pack", lambda s, w=w: self.pack(x, w, s)),
-                   ("pool_compact", lambda s, w=w: self.compact_wave(w, s)),
-                   ("gate_up", self.experts_gate_up),
-                   ("down", self.experts_down),
-                   ("combine", lambda s, w=w: self.combine_wave(w, s, out))]
+            st += [("pool_pack", lambda s, w=w: self.pack(x, w, s), None),
+                   ("pool_compact", lambda s, w=w: self.compact_wave(w, s), None),
+                   ("gate_up", self.experts_gate_up, None),
+                   ("down", self.experts_down, None),
+                   ("combine", lambda s, w=w: self.combine_wave(w, s, out), None)]
         return st
 
     def forward(self, logits, x, stream=None, out=None) -> torch.Tensor:
-        for _, fn in self.stages(logits, x, out):
+        for _, fn, _ in self.stages(logits, x, out):
             fn(stream)
         return self.out if out is None else out
 
