@@ -479,7 +479,42 @@ def run_ours(args, dist, w):
         result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph)
     if args.extras:
         result["extras"] = run_extras(args, w, layer, stream, steps)
+    result["routing"] = routing_report(w, layer, stream)
     return result, layer, logits, sel_bias, x
+
+
+def routing_report(w, layer, stream):
+    """Route accounting of the timed batch, read after the timed region: T*k routes,
+    accepted, sender drops S and receiver drops R with the rates S/(T*k), R/(T*k) and
+    R/(T*k - S), and the per-expert demand before capacity with its skew summaries
+    (computed on the device by the library's demand and load-statistics calls)."""
+    from grouped_expert_gemm_gb300 import abi
+    routes = w.T * w.k
+    demand = layer.expert_demand(stream)
+    stats = torch.empty(5, dtype=torch.float64, device=demand.device)
+    abi.moe_load_stats(w.E, demand, stats, stream)
+    stream.synchronize()
+    if w.pooled:
+        S = int(layer.sender_drops.sum().item())
+        Rr = int(layer.receiver_drops.sum().item())
+    else:
+        S = int(layer.n_dropped.item())
+        Rr = 0
+    st = stats.cpu().tolist()
+    dem = demand.cpu().tolist()
+    rep = {"routes": routes, "accepted": routes - S - Rr, "sender_drops": S,
+           "receiver_drops": Rr,
+           "sender_drop_rate": round(S / routes, 6) if routes else 0.0,
+           "receiver_drop_rate": round(Rr / routes, 6) if routes else 0.0,
+           "receiver_drop_rate_given_sent": round(Rr / (routes - S), 6) if routes > S else 0.0,
+           "demand_summary": {"min": min(dem), "max": max(dem), "mean": routes / w.E,
+                              "cv2": round(st[0], 6), "rho_max": round(st[1], 6),
+                              "h_norm": round(st[2], 6), "e_eff": round(st[3], 3),
+                              "max_vio": round(st[4], 6)},
+           "demand_per_expert": dem}
+    if not w.pooled:
+        rep["admitted_per_expert"] = layer.counts.cpu().tolist()
+    return rep
 
 
 def run_bucket(args, dist, w):
@@ -534,7 +569,8 @@ def run_bucket(args, dist, w):
 def run_extras(args, w, layer, stream, steps):
     """Time the calls beyond the forward path on this workload's buffers (events on the
     launching stream, eager launches): combine backward, token-gradient unpermute,
-    load telemetry and the bias step.  Not part of the step or of `value`."""
+    the demand histogram, load telemetry and the bias step on that demand.  Not part
+    of the step or of `value`."""
     from grouped_expert_gemm_gb300 import abi
     if w.pooled:
         return None
@@ -556,8 +592,9 @@ def run_extras(args, w, layer, stream, steps):
         "unpermute_grad": (lambda: abi.moe_unpermute_grad(
             T, k, d, dy, R, layer.route_to_row, dx, 0, layer.dev_status, stream),
             acc * d * 2 + T * d * 4 + T * k * 4),
-        "load_stats": (lambda: abi.moe_load_stats(w.E, layer.counts, stats, stream), w.E * 4),
-        "bias_update": (lambda: abi.moe_bias_update(w.E, layer.counts, bias, 1e-3,
+        "expert_demand": (lambda: layer.expert_demand(stream), T * k * 4 + w.E * 4),
+        "load_stats": (lambda: abi.moe_load_stats(w.E, layer.demand, stats, stream), w.E * 4),
+        "bias_update": (lambda: abi.moe_bias_update(w.E, layer.demand, bias, 1e-3,
                                                      abi.MOE_BIAS_SIGN, stream), w.E * 12),
     }
     out = {}

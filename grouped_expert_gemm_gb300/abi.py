@@ -28,6 +28,7 @@ MOE_DEV_BAD_HEADER_ID = 4
 MOE_DEV_BAD_ROW = 8
 MOE_DEV_TIMEOUT = 16
 MOE_DEV_NONFINITE_INPUT = 32
+MOE_DEV_BAD_MAP = 64
 
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID_GROUP = 1
@@ -52,7 +53,9 @@ EXPORTED = [
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
     "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
     "moe_payload_bytes", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
-    "moe_grouped_gate_up_fp8",
+    "moe_grouped_gate_up_fp8", "moe_expert_demand", "moe_validate_permutation",
+    "moe_validate_pools_workspace_size", "moe_validate_pools",
+    "moe_validate_compact_workspace_size", "moe_validate_compact", "moe_debug_wait_timeout",
 ]
 
 
@@ -118,6 +121,15 @@ _SIGS = {
                                _P, _P, _P, _SZ, _P, _P]),
     "moe_grouped_gate_up_fp8": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P]),
+    "moe_expert_demand": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "moe_validate_permutation": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P]),
+    "moe_validate_pools_workspace_size": (_SZ, [ctypes.POINTER(PoolParams)]),
+    "moe_validate_pools": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _P, _P, _P, _P,
+                                  _P, _SZ, _P, _P]),
+    "moe_validate_compact_workspace_size": (_SZ, [_I32, _I32]),
+    "moe_validate_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_debug_wait_timeout": (_I32, [_I64, _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -391,3 +403,49 @@ def moe_combine_bucket(T, k, d, valid_tokens, y, y_rows, route_to_row, gates, sh
         T, k, d, _ptr(valid_tokens), _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates),
         _ptr(shared_y), int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
     _count(1 if T > 0 else 0)
+
+
+def moe_expert_demand(T, k, E, valid_tokens, topk_ids, demand, dev_status=None, stream=None):
+    _check("moe_expert_demand", lib().moe_expert_demand(
+        T, k, E, _ptr(valid_tokens), _ptr(topk_ids), _ptr(demand), _ptr(dev_status),
+        _stream(stream)))
+    _count(1 if T > 0 else 0)
+
+
+def moe_validate_permutation(T, E, k, capacity, valid_tokens, topk_ids, counts, offsets,
+                             row_to_route, route_to_row, n_dropped, dev_status, stream=None):
+    _check("moe_validate_permutation", lib().moe_validate_permutation(
+        T, E, k, capacity, _ptr(valid_tokens), _ptr(topk_ids), _ptr(counts), _ptr(offsets),
+        _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(dev_status),
+        _stream(stream)))
+    _count(2 if T > 0 else 1)
+
+
+def moe_validate_pools_workspace_size(p: PoolParams) -> int:
+    return lib().moe_validate_pools_workspace_size(ctypes.byref(p))
+
+
+def moe_validate_pools(p: PoolParams, T, d, k, topk_ids, pools, route_to_poolrow, pool_fill, ws,
+                       ws_bytes, dev_status, stream=None):
+    _check("moe_validate_pools", lib().moe_validate_pools(
+        ctypes.byref(p), T, d, k, _ptr(topk_ids), _ptr(pools), _ptr(route_to_poolrow),
+        _ptr(pool_fill), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+    _count(3)
+
+
+def moe_validate_compact_workspace_size(n_local: int, local_cap: int) -> int:
+    return lib().moe_validate_compact_workspace_size(n_local, local_cap)
+
+
+def moe_validate_compact(n_src, pool_cap, d, n_local, local_cap, pools, local_counts,
+                         poolrow_to_row, ws, ws_bytes, dev_status, stream=None):
+    _check("moe_validate_compact", lib().moe_validate_compact(
+        n_src, pool_cap, d, n_local, local_cap, _ptr(pools), _ptr(local_counts),
+        _ptr(poolrow_to_row), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+    _count(4)
+
+
+def moe_debug_wait_timeout(limit_ns, dev_status, stream=None):
+    _check("moe_debug_wait_timeout", lib().moe_debug_wait_timeout(
+        int(limit_ns), _ptr(dev_status), _stream(stream)))
+    _count(1)

@@ -207,13 +207,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // CTA is aborting (another role gave up) or when this wait itself times out.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint32_t* dev_status) {
+                                             uint32_t* dev_status,
+                                             uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       report(dev_status, MOE_DEV_TIMEOUT);
       return false;
@@ -1337,6 +1338,21 @@ bool pair_shape(int32_t n_seg, int32_t max_rows) {
   return static_cast<int64_t>(max_rows) >= static_cast<int64_t>(kBM) * n_seg;
 }
 
+// One warp; lane 0 waits, with the pipelines' bounded wait, on a barrier whose
+// phase never completes (nothing arrives), so the wait gives up after limit_ns.
+__global__ void __launch_bounds__(32) wait_timeout_selftest(uint64_t limit_ns, uint32_t* dev_status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) wait_bounded(smem_u32(&bar), 0, &abort_flag, dev_status, limit_ns);
+  __syncwarp();
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -1465,4 +1481,11 @@ MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32
   if (st != MOE_OK) return st;
   return moe_grouped_down(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status,
                           stream);
+}
+
+MOE_API moe_status moe_debug_wait_timeout(int64_t limit_ns, uint32_t* dev_status,
+                                          moe_stream_t stream) {
+  if (dev_status == nullptr || limit_ns < 1 || limit_ns > 1000000000ll) return MOE_ERR_INVALID_ARG;
+  wait_timeout_selftest<<<1, 32, 0, as_cuda(stream)>>>(static_cast<uint64_t>(limit_ns), dev_status);
+  return launch_status();
 }

@@ -4,6 +4,9 @@
 //   CV^2 = mean((n - mu)^2) / mu^2, rho_max = max n / mu, with q = n / R and
 //   0 log 0 = 0: H_norm = -sum q log q / log U, E_eff = exp(-sum q log q),
 //   MaxVio = (max n - mu) / mu (0x06J2).
+// [M6.2] 0x01I demand n_e (routes that chose expert e, before any capacity):
+//   a shared-memory histogram per block over a slice of the routes, merged with
+//   one global atomic per non-empty bin.
 // [M6.2] 0x06E and 0x06J1-0x06J3 (the controller acts on the counts of the
 // batch just routed): b_e <- b_e + u * sign(mean c - c_e), or with the
 // proportional rule b_e <- b_e + u * (mean c - c_e).
@@ -95,10 +98,57 @@ bias_update_kernel(int E, const int32_t* __restrict__ counts, float* __restrict_
   pdl_trigger();
 }
 
+constexpr int kDemandThreads = 256;
+constexpr int kDemandRoutesPerBlock = 2048;
+
+__global__ void __launch_bounds__(kDemandThreads)
+demand_kernel(int R, int E, int k, const int32_t* __restrict__ valid,
+              const int32_t* __restrict__ ids, int32_t* __restrict__ demand,
+              uint32_t* __restrict__ dev_status) {
+  __shared__ int32_t hist[512];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  pdl_wait();
+  __syncthreads();
+  int R_live = R;
+  if (valid != nullptr) {
+    const int v = __ldg(valid);
+    R_live = v <= 0 ? 0 : min(R, v * k);
+  }
+  bool bad = false;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kDemandRoutesPerBlock;
+  const int64_t r1 = min(static_cast<int64_t>(R_live), r0 + kDemandRoutesPerBlock);
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    const int e = __ldg(ids + r);
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else if (e != MOE_ROUTE_MASKED) bad = true;
+  }
+  if (bad) report(dev_status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist[e] != 0) atomicAdd(demand + e, hist[e]);
+  pdl_trigger();
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+MOE_API moe_status moe_expert_demand(int32_t T, int32_t k, int32_t E, const int32_t* valid_tokens,
+                                     const int32_t* topk_ids, int32_t* demand,
+                                     uint32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || k <= 0 || E <= 0 || demand == nullptr) return MOE_ERR_INVALID_ARG;
+  if (E > 512 || static_cast<int64_t>(T) * k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  const int R = T * k;
+  if (R > 0 && topk_ids == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_cuda(stream);
+  if (cudaMemsetAsync(demand, 0, static_cast<size_t>(E) * sizeof(int32_t), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (R == 0) return MOE_OK;
+  launch(demand_kernel, dim3(static_cast<unsigned>(ceil_div(R, kDemandRoutesPerBlock))),
+         dim3(kDemandThreads), 0, s, R, E, k, valid_tokens, topk_ids, demand, dev_status);
+  return launch_status();
+}
 
 MOE_API moe_status moe_load_stats(int32_t U, const int32_t* counts, double* stats,
                                   moe_stream_t stream) {

@@ -81,6 +81,7 @@ class MoELayer:
         self.row_to_route = torch.empty((max(R, 1),), **i32)
         self.route_to_row = torch.empty((max(R, 1),), **i32)
         self.n_dropped = torch.zeros((1,), **i32)
+        self.demand = torch.zeros((E,), **i32)
         self.perm_ws_bytes = abi.moe_permute_workspace_size(T, k, E)
         self.perm_ws = _u8(self.perm_ws_bytes, dev)
         self.y = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
@@ -111,6 +112,13 @@ class MoELayer:
     def route(self, logits, stream=None):
         abi.moe_route(self.params, logits, self.sel_bias, self.topk_ids, self.gates,
                       self.dev_status, stream)
+
+    def expert_demand(self, stream=None) -> torch.Tensor:
+        """Per-expert demand n_e of the last routed batch, before capacity, into
+        ``self.demand`` (the load the skew summaries and the bias controller read)."""
+        abi.moe_expert_demand(self.T, self.k, self.E, None, self.topk_ids, self.demand,
+                              self.dev_status, stream)
+        return self.demand
 
     def quantize(self, x, stream=None):
         abi.moe_quantize_fp8(self.T, self.d, self.scale_group, x, self.xq, self.xs,
@@ -240,6 +248,7 @@ class PooledMoELayer:
         self.route_to_poolrow = torch.empty((R,), **i32)
         self.pool_fill = torch.empty((n_dest,), **i32)
         self.sender_drops = torch.zeros((n_waves,), **i32)
+        self.demand = torch.zeros((self.E,), **i32)
         self.pack_ws_bytes = abi.moe_pool_pack_workspace_size(self.pool_params, T, k)
         self.pack_ws = _u8(self.pack_ws_bytes, dev)
         self.rows = local_per_dest * local_cap
@@ -260,6 +269,12 @@ class PooledMoELayer:
 
     def route(self, logits, stream=None):
         abi.moe_route(self.params, logits, None, self.topk_ids, self.gates, self.dev_status, stream)
+
+    def expert_demand(self, stream=None) -> torch.Tensor:
+        """Per-expert demand of the last routed batch (all E experts) into ``self.demand``."""
+        abi.moe_expert_demand(self.T, self.k, self.E, None, self.topk_ids, self.demand,
+                              self.dev_status, stream)
+        return self.demand
 
     def pack(self, x, wave, stream=None):
         abi.moe_pool_pack(self.pool_params, self.T, self.d, self.k, wave, self.topk_ids, x,

@@ -58,7 +58,8 @@ enum {
   MOE_DEV_BAD_HEADER_ID = 4u,   /* a pool header id >= n_local that is not EMPTY     */
   MOE_DEV_BAD_ROW = 8u,         /* a map entry outside the row space; skipped        */
   MOE_DEV_TIMEOUT = 16u,        /* a bounded pipeline wait gave up; output invalid   */
-  MOE_DEV_NONFINITE_INPUT = 32u /* a NaN/Inf activation met by moe_quantize_fp8      */
+  MOE_DEV_NONFINITE_INPUT = 32u, /* a NaN/Inf activation met by moe_quantize_fp8     */
+  MOE_DEV_BAD_MAP = 64u          /* a moe_validate_* call found a broken invariant    */
 };
 
 #define MOE_POOL_EMPTY 0xFFFFu /* header element of an unused pool row */
@@ -441,6 +442,83 @@ moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, int32_t 
                                    const int32_t* seg_begin, const int32_t* seg_count,
                                    const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* h,
                                    uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Expert demand and map validators                                         */
+/* ------------------------------------------------------------------------ */
+/* Per-expert demand before capacity ([M6.2] 0x01I: n_e, the count of routes
+ * that chose expert e, the quantity the skew summaries and the bias controller
+ * read; with a capacity C the admitted count is min(n_e, C)).  demand[E] int32
+ * is overwritten with the histogram of topk_ids[0 .. R_live), R_live = T*k, or
+ * min(*valid_tokens, T)*k when valid_tokens (a device int32) is not NULL.  Ids
+ * outside [0,E) -- including MOE_ROUTE_MASKED -- are not counted; ids other
+ * than MOE_ROUTE_MASKED outside [0,E) set MOE_DEV_BAD_EXPERT_ID.  Limits: 1 <=
+ * E <= 512, T*k < 2^31.                                                      */
+moe_status moe_expert_demand(int32_t T, int32_t k, int32_t E, const int32_t* valid_tokens,
+                             const int32_t* topk_ids, int32_t* demand, uint32_t* dev_status,
+                             moe_stream_t stream);
+
+/* Debug validators ([M6.6] 0x0CD "Route And Combine Assertions": accepted +
+ * dropped = routes, the counts sum to the accepted routes, one inverse entry
+ * per accepted route).  Each reads outputs of the calls named and sets
+ * MOE_DEV_BAD_MAP in *dev_status when an invariant below fails; nothing else is
+ * written (dev_status is never cleared; workspaces are scratch).  They are meant for tests
+ * and for checking a pipeline once, not for every step.
+ *
+ * moe_validate_permutation -- after moe_permute / moe_permute_bucket /
+ * moe_permute_fp8 with the same T, E, k, capacity and valid_tokens (NULL for
+ * the unbucketed calls).  [M6.2] 0x03B and [M6.6] 0x03B, 0x03C3: offsets[0] =
+ * 0 and offsets[e+1] - offsets[e] = counts[e] >= 0 (capacity >= 0: <=
+ * capacity); accepted + n_dropped = R_live (no drops when dropless); every row
+ * i < offsets[E] holds a live route r with route_to_row[r] = i, and every
+ * route r with route_to_row[r] = i >= 0 has row_to_route[i] = r inside its
+ * expert's segment (the two maps are inverse bijections between the accepted
+ * routes and [0, offsets[E])); route ids increase along a segment (stable
+ * order); a route is dropped (-1) only when its expert holds `capacity` rows,
+ * all of routes with smaller ids (admission in route id order); padding routes
+ * map to -1.  Routes with ids outside [0,E) are not checked against a segment.
+ *
+ * moe_validate_pools -- after moe_pool_pack of one wave.  [POOL] 02-05:
+ * 0 <= pool_fill[D] <= pool_cap; header element r of pool D is a local id <
+ * local_per_dest for r < pool_fill[D] and MOE_POOL_EMPTY otherwise; a placed
+ * route (route_to_poolrow >= 0) points at a filled row of destination
+ * topk_ids / local_per_dest whose header holds topk_ids % local_per_dest; every
+ * filled row is pointed at by exactly one route (conservation of placed rows).
+ * Workspace: moe_validate_pools_workspace_size(p) bytes.
+ *
+ * moe_validate_compact -- after moe_pool_compact of one wave.  [POOL] 03, 05:
+ * 0 <= local_counts[l] <= local_cap; a pool row whose header id l < n_local
+ * maps to -1 (a receiver drop) or to l*local_cap + slot with slot <
+ * local_counts[l]; every other pool row maps to -1; every compact row below its
+ * expert's count is the image of exactly one pool row; receiver drops happen
+ * only to experts that are full.  Workspace:
+ * moe_validate_compact_workspace_size(n_local, local_cap) bytes.
+ *
+ * Limits as the calls they check.                                           */
+moe_status moe_validate_permutation(int32_t T, int32_t E, int32_t k, int32_t capacity,
+                                    const int32_t* valid_tokens, const int32_t* topk_ids,
+                                    const int32_t* counts, const int32_t* offsets,
+                                    const int32_t* row_to_route, const int32_t* route_to_row,
+                                    const int32_t* n_dropped, uint32_t* dev_status,
+                                    moe_stream_t stream);
+size_t moe_validate_pools_workspace_size(const moe_pool_params* p);
+moe_status moe_validate_pools(const moe_pool_params* p, int32_t T, int32_t d, int32_t k,
+                              const int32_t* topk_ids, const moe_bf16* pools,
+                              const int32_t* route_to_poolrow, const int32_t* pool_fill, void* ws,
+                              size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
+size_t moe_validate_compact_workspace_size(int32_t n_local, int32_t local_cap);
+moe_status moe_validate_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
+                                int32_t local_cap, const moe_bf16* pools,
+                                const int32_t* local_counts, const int32_t* poolrow_to_row,
+                                void* ws, size_t ws_bytes, uint32_t* dev_status,
+                                moe_stream_t stream);
+
+/* Self-test of the bounded pipeline wait used by the tensor-core kernels: one
+ * CTA initialises an mbarrier that nothing arrives at and waits on it with the
+ * same bounded-wait routine, giving up after limit_ns nanoseconds of global
+ * time (1 <= limit_ns <= 10^9); it then sets MOE_DEV_TIMEOUT and returns.  The
+ * kernel never traps and leaves the context usable.                          */
+moe_status moe_debug_wait_timeout(int64_t limit_ns, uint32_t* dev_status, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -450,6 +450,176 @@ def compose_map(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return out
 
 
+# ----------------------------------------------------------------------------
+# Invariant checks of the maps  ([M6.6] 0x0CD "Route And Combine Assertions":
+# accepted + dropped = routes, sum of counts = accepted, one inverse entry per
+# accepted route; [M6.2] 0x03B stable order and inverse; [POOL] 02-05 headers,
+# fills and one route per filled pool row).  Plain loops over every entry; they
+# name each broken invariant so a one-field mutation can be traced to its check.
+# ----------------------------------------------------------------------------
+
+def expert_demand(ids: np.ndarray, E: int, live_routes: int = -1) -> np.ndarray:
+    """n_e: routes among the first ``live_routes`` (all when < 0) that chose expert
+    e, before any capacity ([M6.2] 0x01I).  Ids outside [0, E) are not counted."""
+    e = np.asarray(ids, dtype=np.int64).reshape(-1)
+    if live_routes >= 0:
+        e = e[:live_routes]
+    n = np.zeros(E, dtype=np.int64)
+    for v in e:
+        if 0 <= v < E:
+            n[v] += 1
+    return n
+
+
+def permutation_violations(ids, E: int, cap: int, counts, offsets, row_to_route, route_to_row,
+                           n_dropped: int, live_routes: int = -1) -> list:
+    """Names of the permutation invariants that the given maps break ([] if none).
+
+    row_to_route holds at least offsets[E] entries; route_to_row one per route.
+    Routes at or past ``live_routes`` (padding slots of a token bucket) must map
+    to -1.  Checked: offsets start at 0 and step by counts; counts are
+    non-negative and (cap >= 0) at most cap; accepted + dropped = live routes and
+    nothing is dropped when dropless; each accepted row points at a live route
+    that points back, inside that route's expert segment; route ids increase
+    along a segment; a dropped route's expert is full with routes of smaller id.
+    """
+    e = np.asarray(ids, dtype=np.int64).reshape(-1)
+    R = e.size
+    R_live = R if live_routes < 0 else min(R, max(live_routes, 0))
+    counts = [int(v) for v in counts]
+    offsets = [int(v) for v in offsets]
+    r2r = [int(v) for v in route_to_row]
+    row2 = [int(v) for v in row_to_route]
+    bad = set()
+    if offsets[0] != 0:
+        bad.add("offsets[0]")
+    for x in range(E):
+        if counts[x] < 0 or offsets[x + 1] - offsets[x] != counts[x]:
+            bad.add("offsets-counts")
+        if cap >= 0 and counts[x] > cap:
+            bad.add("capacity")
+    acc = offsets[E]
+    if acc < 0 or acc > R_live or acc + int(n_dropped) != R_live:
+        bad.add("conservation")
+    if cap < 0 and int(n_dropped) != 0:
+        bad.add("dropless-drop")
+    if acc < 0 or acc > R_live:
+        return sorted(bad)
+    for r in range(R):
+        row = r2r[r]
+        if r >= R_live:
+            if row != -1:
+                bad.add("padding-mapped")
+            continue
+        known = 0 <= e[r] < E
+        if row >= 0:
+            if not known or row >= acc or row2[row] != r or \
+                    not offsets[e[r]] <= row < offsets[e[r] + 1]:
+                bad.add("route-to-row")
+        elif row == -1:
+            if known:
+                c, o = counts[e[r]], offsets[e[r] + 1]
+                if cap < 0 or c != cap or (c > 0 and (o < 1 or o > acc or row2[o - 1] > r)):
+                    bad.add("drop-admission")
+        else:
+            bad.add("route-to-row")
+    for i in range(acc):
+        r = row2[i]
+        if not 0 <= r < R_live or r2r[r] != i:
+            bad.add("row-to-route")
+        elif i + 1 < acc and 0 <= e[r] < E and i + 1 < offsets[e[r] + 1] and row2[i + 1] <= r:
+            bad.add("stable-order")
+    return sorted(bad)
+
+
+def pool_violations(ids, n_dest: int, local_per_dest: int, pool_cap: int, headers,
+                    route_to_poolrow, fill) -> list:
+    """Invariants of one wave's sender pools; headers is [n_dest, d] (pool row 0).
+
+    Checked: 0 <= fill <= pool_cap; header element r < fill holds a local id,
+    every other element EMPTY_HEADER; a placed route points at a filled row of
+    its destination whose header holds its local id; every filled row has exactly
+    one route, and the routes of a pool increase along its rows.
+    """
+    e = np.asarray(ids, dtype=np.int64).reshape(-1)
+    hdr = np.asarray(headers).astype(np.int64)
+    fill = [int(v) for v in fill]
+    L = local_per_dest
+    bad = set()
+    for D in range(n_dest):
+        f = fill[D]
+        if not 0 <= f <= pool_cap:
+            bad.add("fill")
+            continue
+        for r in range(hdr.shape[1]):
+            if (r < f and not hdr[D, r] < L) or (r >= f and hdr[D, r] != EMPTY_HEADER):
+                bad.add("header")
+    owner = {}
+    for r, p in enumerate(int(v) for v in route_to_poolrow):
+        if p < 0:
+            if p != -1:
+                bad.add("route-to-poolrow")
+            continue
+        D, row = divmod(p, pool_cap)
+        if not 0 <= e[r] < n_dest * L or D != e[r] // L or row >= fill[D] or \
+                hdr[D, row] != e[r] % L or p in owner:
+            bad.add("route-to-poolrow")
+        owner.setdefault(p, r)
+    for D in range(n_dest):
+        f = min(fill[D], pool_cap)
+        for row in range(pool_cap):
+            p = D * pool_cap + row
+            if row >= f:
+                if p in owner:
+                    bad.add("pool-row-owner")
+            elif p not in owner or (row + 1 < f and owner.get(p + 1, -1) <= owner[p]):
+                bad.add("pool-row-owner")
+    return sorted(bad)
+
+
+def compact_violations(headers, pool_cap: int, n_local: int, local_cap: int, local_counts,
+                       poolrow_to_row) -> list:
+    """Invariants of one wave's receiver compact; headers is [n_src, >= pool_cap].
+
+    Checked: 0 <= count <= local_cap; a pool row with a valid header l maps to
+    -1 or to a slot of l below its count, any other row to -1; every slot below
+    a count is the image of exactly one pool row and images keep (source, row)
+    order; a receiver drop's expert is full with rows that came earlier.
+    """
+    hdr = np.asarray(headers)[:, :pool_cap].astype(np.int64).reshape(-1)
+    cnt = [int(v) for v in local_counts]
+    q_of = [int(v) for v in poolrow_to_row]
+    bad = set()
+    for l in range(n_local):
+        if not 0 <= cnt[l] <= local_cap:
+            bad.add("local-count")
+    owner = {}
+    for i, q in enumerate(q_of):
+        h = hdr[i]
+        if q == -1:
+            continue
+        if not h < n_local or q < 0 or q // local_cap != h or q % local_cap >= cnt[h] or \
+                q in owner:
+            bad.add("poolrow-to-row")
+        owner.setdefault(q, i)
+    for i, q in enumerate(q_of):
+        h = hdr[i]
+        if h < n_local and q == -1:
+            c = cnt[h]
+            if c != local_cap or (c > 0 and owner.get(h * local_cap + c - 1, -1) > i):
+                bad.add("receiver-drop")
+    for l in range(n_local):
+        f = min(cnt[l], local_cap)
+        for slot in range(local_cap):
+            q = l * local_cap + slot
+            if slot >= f:
+                if q in owner:
+                    bad.add("slot-owner")
+            elif q not in owner or (slot + 1 < f and owner.get(q + 1, -1) <= owner[q]):
+                bad.add("slot-owner")
+    return sorted(bad)
+
+
 def drop_rates(total: int, sender: int, receiver: int):
     """[POOL] 05 'Report both receiver rates': S/T, R/T (additive) and R/(T-S)."""
     return dict(sender=sender / total, receiver=receiver / total,

@@ -88,6 +88,29 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_pool_compact(4, 100, 64, 2, 8, 16, 16, 16, 16, 16, 16, 1 << 20, None,
                                 None) == abi.MOE_ERR_UNSUPPORTED
     assert lib.moe_compose_map(-1, 16, 16, 4, 16, None, None) == abi.MOE_ERR_INVALID_ARG
+    # demand: E beyond the router's limit, missing output
+    assert lib.moe_expert_demand(4, 2, 1024, None, 16, 16, None, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_demand(4, 2, 8, None, 16, None, None, None) == abi.MOE_ERR_INVALID_ARG
+    # validators: bad sizes, a missing status word, too small a workspace, header too wide
+    assert lib.moe_validate_permutation(4, 8, 9, -1, None, 16, 16, 16, 16, 16, 16, 16,
+                                        None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_validate_permutation(4, 8, 2, -1, None, 16, 16, 16, 16, 16, 16, None,
+                                        None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_validate_permutation(4, 600, 2, -1, None, 16, 16, 16, 16, 16, 16, 16,
+                                        None) == abi.MOE_ERR_UNSUPPORTED
+    pp = abi.PoolParams(4, 2, 3, 8, 0)
+    assert lib.moe_validate_pools(pp, 4, 64, 2, 16, 16, 16, 16, 16, 8, 16,
+                                  None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_validate_pools(abi.PoolParams(4, 2, 3, 100, 0), 4, 64, 2, 16, 16, 16, 16, 16,
+                                  1 << 20, 16, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_validate_compact(4, 8, 64, 2, 10, 16, 16, 16, 16, 79, 16,
+                                    None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_validate_compact(4, 100, 64, 2, 10, 16, 16, 16, 16, 1 << 20, 16,
+                                    None) == abi.MOE_ERR_UNSUPPORTED
+    # the wait self-test: limit outside (0, 1 s], missing status word
+    assert lib.moe_debug_wait_timeout(0, 16, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_wait_timeout(2000000000, 16, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_wait_timeout(1000, None, None) == abi.MOE_ERR_INVALID_ARG
 
 
 def test_workspace_sizes_are_monotone(lib):
@@ -97,6 +120,8 @@ def test_workspace_sizes_are_monotone(lib):
     pp = abi.PoolParams(64, 6, 3, 3004, 0)
     assert abi.moe_pool_pack_workspace_size(pp, 65536, 8) >= 64 * 4
     assert abi.moe_pool_compact_workspace_size(64, 3004, 6) >= 6 * 4
+    assert abi.moe_validate_pools_workspace_size(pp) == 64 * 3004 * 4
+    assert abi.moe_validate_compact_workspace_size(6, 33497) == 6 * 33497 * 4
 
 
 def test_status_strings(lib):
