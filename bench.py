@@ -58,6 +58,9 @@ def parse_args():
                     help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--payload", default="bf16", choices=["bf16", "fp8_row", "fp8_block128"],
                     help="dispatch payload of the expert input rows (not for --config pooled)")
+    ap.add_argument("--gather", action="store_true",
+                    help="bf16 payload: permute the maps only and gather the expert rows in the "
+                         "gate/up loader instead of copying them in the permute")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -197,11 +200,16 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
         return T * E * 4 + T * k * 8, 0
     if name == "quantize":
         return T * d * 2 + T * row_b, 0
+    gather = getattr(layer, "gather", False)
     if name == "permute":
+        if gather:  # the maps only: the gate/up loader gathers the rows itself
+            return T * k * 4 + 2 * T * k * 4 + (2 * E + 1) * 4, 0
         return T * k * 4 + T * row_b + acc_rows * row_b + 2 * T * k * 4 + (2 * E + 1) * 4, 0
     if name == "dequantize":
         return acc_rows * row_b + acc_rows * d * 2, 0
     if name == "gate_up":
+        if gather:  # every token row at least once (the k copies of a row come from L2)
+            return touched * 2 * d * I * 2 + T * d * 2 + acc_rows * I * 2, 4 * acc_rows * d * I
         a_row = row_b if fused else d * 2  # the unfused FP8 path reads the dequantized bf16 rows
         return touched * 2 * d * I * 2 + acc_rows * a_row + acc_rows * I * 2, 4 * acc_rows * d * I
     if name == "down":
@@ -268,7 +276,7 @@ def lookup_traffic(stage, workload_name):
 # our arm
 # ----------------------------------------------------------------------------
 
-def build_layer(w, device, payload="bf16"):
+def build_layer(w, device, payload="bf16", gather=False):
     import grouped_expert_gemm_gb300 as g
     if w.pooled and payload != "bf16":
         raise SystemExit("--payload applies to the routed (non-pooled) workloads")
@@ -286,7 +294,7 @@ def build_layer(w, device, payload="bf16"):
         layer = g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                            n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                            sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
-                           payload=payload, device=device)
+                           payload=payload, gather=gather, device=device)
     return layer, logits, sel_bias, x
 
 
@@ -312,7 +320,7 @@ def run_ours(args, dist, w):
     device = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
-    layer, logits, sel_bias, x = build_layer(w, device, args.payload)
+    layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _, _ in stages]
@@ -448,6 +456,10 @@ def run_ours(args, dist, w):
                         "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                         "frac": round(frac, 4), "alg_bytes": int(b), "alg_flops": int(f),
                         "traffic": lookup_traffic(n, traffic_key(w, layer))}
+        if n == "permute" and getattr(layer, "gather", False):
+            per_stage[n]["note"] = ("maps only (counts, offsets, both maps): the gate/up loader "
+                                    "gathers the expert rows from token order, so no row is "
+                                    "copied here; --extras times the copying permute")
         if n in side_names:
             per_stage[n]["timing"] = ("side stream, overlapping the main-stream stages: the "
                                       "figure is the wall-clock span of its work, not a kernel "
@@ -478,7 +490,7 @@ def run_ours(args, dist, w):
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph)
     if args.extras:
-        result["extras"] = run_extras(args, w, layer, stream, steps)
+        result["extras"] = run_extras(args, w, layer, stream, steps, x)
     result["routing"] = routing_report(w, layer, stream)
     return result, layer, logits, sel_bias, x
 
@@ -566,11 +578,12 @@ def run_bucket(args, dist, w):
                       "graph replay", "clocks": sampler.summary()}
 
 
-def run_extras(args, w, layer, stream, steps):
+def run_extras(args, w, layer, stream, steps, layer_x=None):
     """Time the calls beyond the forward path on this workload's buffers (events on the
-    launching stream, eager launches): combine backward, token-gradient unpermute,
-    the demand histogram, load telemetry and the bias step on that demand.  Not part
-    of the step or of `value`."""
+    launching stream, eager launches): the copying permute (when the step gathers its
+    rows instead), combine backward, token-gradient unpermute, the demand histogram,
+    load telemetry and the bias step on that demand.  Not part of the step or of
+    `value`."""
     from grouped_expert_gemm_gb300 import abi
     if w.pooled:
         return None
@@ -585,7 +598,16 @@ def run_extras(args, w, layer, stream, steps):
     dx = torch.empty((T, d), dtype=torch.float32, device=dev)
     stats = torch.empty(5, dtype=torch.float64, device=dev)
     bias = torch.zeros(w.E, dtype=torch.float32, device=dev)
-    calls = {
+    calls = {}
+    if getattr(layer, "gather", False):
+        # the dispatch as a standalone copy (what the gathered gate/up pass replaces)
+        xp = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
+        calls["permute_with_copy"] = (lambda: abi.moe_permute(
+            T, d, w.E, k, layer.capacity, layer.topk_ids, layer_x, xp, layer.counts,
+            layer.offsets, layer.row_to_route, layer.route_to_row, layer.n_dropped,
+            layer.perm_ws, layer.perm_ws_bytes, layer.dev_status, stream),
+            T * k * 4 + T * d * 2 + acc * d * 2 + 2 * T * k * 4 + (2 * w.E + 1) * 4)
+    calls.update({
         "combine_backward": (lambda: abi.moe_combine_backward(
             T, k, d, dout, layer.y, R, layer.route_to_row, layer.gates, dy, dg, layer.dev_status,
             stream), T * d * 4 + 2 * acc * d * 2 + T * k * 8),
@@ -596,7 +618,7 @@ def run_extras(args, w, layer, stream, steps):
         "load_stats": (lambda: abi.moe_load_stats(w.E, layer.demand, stats, stream), w.E * 4),
         "bias_update": (lambda: abi.moe_bias_update(w.E, layer.demand, bias, 1e-3,
                                                      abi.MOE_BIAS_SIGN, stream), w.E * 12),
-    }
+    })
     out = {}
     for name, (fn, nbytes) in calls.items():
         for _ in range(3):
@@ -618,7 +640,10 @@ def run_extras(args, w, layer, stream, steps):
 def traffic_key(w, layer):
     """Workload name under which profiles/ records a stage's DRAM traffic."""
     p = getattr(layer, "payload", "bf16")
-    return w.name if p == "bf16" else f"{w.name}+{p}"
+    key = w.name if p == "bf16" else f"{w.name}+{p}"
+    if getattr(layer, "gather", False):
+        key += "+gather"
+    return key
 
 
 def config_dict(w, layer):
@@ -626,6 +651,9 @@ def config_dict(w, layer):
          "router": w.score_fn, "parallelism": "replicas only (no data-path collective)"}
     if not w.pooled:
         c["payload"] = layer.payload
+        if layer.payload == "bf16":
+            c["expert_rows"] = ("gathered from token order by the gate/up loader"
+                                if layer.gather else "permuted copy written by the permute")
         if layer.payload != "bf16":
             c["payload_bytes_per_row"] = w.d + layer.xs.shape[1] * 4
     if w.capacity_factor is not None:

@@ -53,7 +53,7 @@ EXPORTED = [
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
     "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
     "moe_payload_bytes", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
-    "moe_grouped_gate_up_fp8", "moe_expert_demand", "moe_validate_permutation",
+    "moe_grouped_gate_up_fp8", "moe_grouped_gate_up_gather", "moe_expert_demand", "moe_validate_permutation",
     "moe_validate_pools_workspace_size", "moe_validate_pools",
     "moe_validate_compact_workspace_size", "moe_validate_compact", "moe_debug_wait_timeout",
 ]
@@ -121,6 +121,8 @@ _SIGS = {
                                _P, _P, _P, _SZ, _P, _P]),
     "moe_grouped_gate_up_fp8": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P]),
+    "moe_grouped_gate_up_gather": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
+                                          _P, _P, _P, _P]),
     "moe_expert_demand": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "moe_validate_permutation": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P]),
@@ -211,13 +213,14 @@ def moe_sigmoid_det(n: int, z, s, stream=None):
     _count(1 if n > 0 else 0)
 
 
-def _permute_launches(T: int, k: int) -> int:
-    """Kernels one permute call launches: the tile histogram runs only with several tiles."""
+def _permute_launches(T: int, k: int, copy: bool = True) -> int:
+    """Kernels one permute call launches: the tile histogram runs only with several tiles,
+    the row copy only when rows are copied (not for the maps-only form)."""
     R = T * k
     if R <= 0:
         return 1
     per_tile = max(2048, -(-R // 128))
-    return 3 if -(-R // per_tile) > 1 else 2
+    return (3 if -(-R // per_tile) > 1 else 2) - (0 if copy else 1)
 
 
 def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
@@ -230,7 +233,7 @@ def moe_permute(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(ws), ws_bytes,
         _ptr(dev_status), _stream(stream)))
-    _count(_permute_launches(T, k))
+    _count(_permute_launches(T, k, x is not None))
 
 
 def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offsets, row_to_route,
@@ -242,7 +245,7 @@ def moe_permute_noalloc(T, d, E, k, capacity, topk_ids, x, x_perm, counts, offse
         T, d, E, k, capacity, _ptr(topk_ids), _ptr(x), _ptr(x_perm), _ptr(counts), _ptr(offsets),
         _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped), _ptr(dev_status),
         _stream(stream)))
-    _count(_permute_launches(T, k))
+    _count(_permute_launches(T, k, x is not None))
 
 
 def moe_grouped_swiglu_workspace_size(max_rows: int, I: int) -> int:
@@ -294,6 +297,14 @@ def moe_permute_fp8(T, d, E, k, capacity, group, topk_ids, q, scales, q_perm, sc
         _ptr(scales_perm), _ptr(counts), _ptr(offsets), _ptr(row_to_route), _ptr(route_to_row),
         _ptr(n_dropped), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
     _count(_permute_launches(T, k))
+
+
+def moe_grouped_gate_up_gather(n_seg, d, I, max_rows, T, k, x, row_to_route, seg_begin,
+                               seg_count, w_gate, w_up, h, dev_status=None, stream=None):
+    _check("moe_grouped_gate_up_gather", lib().moe_grouped_gate_up_gather(
+        n_seg, d, I, max_rows, T, k, _ptr(x), _ptr(row_to_route), _ptr(seg_begin),
+        _ptr(seg_count), _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(dev_status), _stream(stream)))
+    _count(1 if max_rows > 0 else 0)
 
 
 def moe_grouped_gate_up_fp8(n_seg, d, I, max_rows, group, xq, scales, seg_begin, seg_count,
@@ -394,7 +405,7 @@ def moe_permute_bucket(T, d, E, k, capacity, valid_tokens, topk_ids, x, x_perm, 
         T, d, E, k, capacity, _ptr(valid_tokens), _ptr(topk_ids), _ptr(x), _ptr(x_perm),
         _ptr(counts), _ptr(offsets), _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped),
         _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
-    _count(_permute_launches(T, k))
+    _count(_permute_launches(T, k, x is not None))
 
 
 def moe_combine_bucket(T, k, d, valid_tokens, y, y_rows, route_to_row, gates, shared_y,

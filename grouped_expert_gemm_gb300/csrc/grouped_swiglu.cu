@@ -151,6 +151,12 @@ struct GemmArgs {
   // past the box are never stored) and the A bytes one stage's TMA delivers.
   int bm;
   int a_box_bytes;
+  // Gathered A rows (bf16 gate/up only; nullptr otherwise): row i of the expert
+  // row space is token row gather[i] / gather_k of the [gather_T, K] tensor the A
+  // map describes (one-row boxes), loaded four rows per TMA gather.
+  const int32_t* gather;
+  int gather_k;
+  int gather_T;
 };
 
 // ------------------------------ PTX wrappers -------------------------------
@@ -411,6 +417,29 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Four rows (r0..r3) x 64 columns from column c_inner of a map with one-row boxes,
+// landing as four consecutive 128-byte rows at dst (with the map's swizzle).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c_inner, const int (&r)[4]) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(r[0]), "r"(r[1]),
+      "r"(r[2]), "r"(r[3])
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c_inner,
+                                                 const int (&r)[4]) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c_inner), "r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3])
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
@@ -454,6 +483,27 @@ __device__ __forceinline__ Tile tile_of(int t, const int* tile_start, const int*
   tl.rows = min(bm, s_count[q] - mb * bm);
   tl.n0 = nb * bn_out;
   return tl;
+}
+
+// Token rows of the four A rows 4*lane .. 4*lane+3 of a gathered box whose first
+// row is `row0` of the expert row space and whose first `live` rows belong to the
+// segment.  Rows past `live` (the ragged tail) load token 0: they are computed
+// but never stored.  A map entry outside the routes is reported and reads token 0.
+__device__ __forceinline__ void gather_tokens(const GemmArgs& a, int row0, int live, int lane,
+                                              int (&tok)[4]) {
+  const int n_routes = a.gather_T * a.gather_k;
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = 4 * lane + j;
+    int t = 0;
+    if (i < live) {
+      const int r = __ldg(a.gather + row0 + i);
+      if (r >= 0 && r < n_routes) t = r / a.gather_k; else bad = true;
+    }
+    tok[j] = t;
+  }
+  if (bad) report(a.dev_status, MOE_DEV_BAD_ROW);
 }
 
 // Segment table in shared memory, built by threads 64..191 (each owns a run of
@@ -764,7 +814,53 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const uint32_t tmem_base = *sm.tmem_slot;
   const int total_tiles = sm.s_tile_start[n_seg];
 
-  if (warp == 0) {
+  bool gathered = false;
+  if constexpr (SWIGLU && !FP8A) gathered = args.gather != nullptr;
+  if (warp == 0 && gathered) {
+    // ============ TMA producer, A rows gathered from token order ============
+    // The whole warp: lane 0 waits and arms the stage, lanes 0 .. bm/4-1 each
+    // gather four A rows (512 bytes at offset 512 * lane of the A tile), lane 0
+    // loads the B atoms.
+    if constexpr (SWIGLU && !FP8A) {
+      const int lanes_a = args.bm / 4;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, args.bm,
+                                kBnOut, n_blocks, args.m_outer);
+        int tok[4];
+        gather_tokens(args, tl.row0, tl.rows, lane, tok);
+        const int b_row0 = tl.seg * args.K;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          bool w = true;
+          if (lane == 0) w = wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status);
+          if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+          const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+          if (lane == 0)
+            mbar_arrive_expect_tx(full_bar(s), args.a_box_bytes + N_ATOMS * kAtomBytes);
+          __syncwarp();
+          if (lane < lanes_a) tma_gather4(st + lane * 512, &tmap_a, full_bar(s), ks * kBK, tok);
+          if (lane == 0) {
+            constexpr int half = N_ATOMS / 2;
+#pragma unroll
+            for (int a = 0; a < N_ATOMS; ++a)
+              tma_load_2d(st + G::kBOff + a * kAtomBytes, a < half ? &tmap_b0 : &tmap_b1,
+                          full_bar(s), tl.n0 + (a % half) * 64, b_row0 + ks * kBK);
+          }
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && lane == 0) {
+        int ss = s;
+        uint32_t pp = ph;
+        for (int i = 0; i < kStages; ++i) {
+          if (--ss < 0) { ss = kStages - 1; pp ^= 1u; }
+          wait_drain(full_bar(ss), pp);
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       int s = 0;
@@ -994,7 +1090,59 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const uint32_t tmem_base = *sm.tmem_slot;
   const int total_tiles = sm.s_tile_start[n_seg];
 
-  if (warp == 0) {
+  bool gathered = false;
+  if constexpr (SWIGLU && !FP8A) gathered = args.gather != nullptr;
+  if (warp == 0 && gathered) {
+    // ==== TMA producer (both ranks), A rows gathered from token order ====
+    // Every lane gathers four of this rank's 128 A rows (512 bytes at offset
+    // 512 * lane of its A tile); lane 0 waits, the leader's lane 0 arms the stage
+    // for both ranks' bytes, and lane 0 loads this rank's B atoms.
+    if constexpr (SWIGLU && !FP8A) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cid; t < total_tiles && ok; t += n_clusters) {
+        const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, kPairBM,
+                                kBnOut, n_blocks, args.m_outer);
+        const int my_row0 = tl.row0 + static_cast<int>(rank) * kBM;
+        const int my_live = min(max(tl.rows - static_cast<int>(rank) * kBM, 0), kBM);
+        int tok[4];
+        gather_tokens(args, my_row0, my_live, lane, tok);
+        const int b_row0 = tl.seg * args.K;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          bool w = true;
+          if (lane == 0) w = wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status);
+          if (!__shfl_sync(0xFFFFFFFFu, w, 0)) { ok = false; break; }
+          const uint32_t full_leader = map_to_rank(full_bar(s), 0);
+          const uint32_t st = smem_u32(stage_base + s * kPairStageBytes);
+          if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(s), 2 * kPairStageBytes);
+          __syncwarp();
+          tma_gather4_pair(st + lane * 512, &tmap_a, full_leader, ks * kBK, tok);
+          if (lane == 0) {
+#pragma unroll
+            for (int a = 0; a < kPairAtoms; ++a)
+              tma_load_2d_pair(st + PG::kBOff + a * kAtomBytes, leader ? &tmap_b0 : &tmap_b1,
+                               full_leader, tl.n0 + a * 64, b_row0 + ks * kBK);
+          }
+          issued_any = true;
+          if (++s == kStagesPair) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && issued_any && lane == 0) {
+        if (leader) {
+          int ss = s;
+          uint32_t pp = ph;
+          for (int i = 0; i < kStagesPair; ++i) {
+            if (--ss < 0) { ss = kStagesPair - 1; pp ^= 1u; }
+            wait_drain(full_bar(ss), pp);
+          }
+        } else {
+          spin_ns(2000000ull);  // this rank's copies complete on the leader's barriers
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ======================= TMA producer (both ranks) =======================
     if (lane == 0) {
       int s = 0;
@@ -1373,6 +1521,30 @@ static moe_status check_common(int32_t n_seg, int32_t K, int32_t N, int32_t max_
   return MOE_OK;
 }
 
+// The bf16 gate/up pass.  With gather == nullptr the A rows are rows [0, max_rows)
+// of x; otherwise row i is x[gather[i] / k] of the token rows x [T, d].
+static moe_status gate_up_impl(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                               const moe_bf16* x, int32_t T, int32_t k, const int32_t* gather,
+                               const int32_t* seg_begin, const int32_t* seg_count,
+                               const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* h,
+                               uint32_t* dev_status, moe_stream_t stream) {
+  const bool pair = I % 128 == 0 && pair_shape(n_seg, max_rows);
+  const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
+  CUtensorMap m_x, m_wg, m_wu;
+  const bool x_ok = gather == nullptr ? make_map(&m_x, x, max_rows, d, bm)
+                                      : make_map(&m_x, x, T, d, 1);  // one-row boxes
+  if (!x_ok || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
+      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
+    return MOE_ERR_CUDA;
+  GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
+             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
+             nullptr, 0, 0, bm, bm * kBK * 2, gather, k, T};
+  cudaStream_t s = as_cuda(stream);
+  if (pair) return launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s);
+  if (wide_gate_up(n_seg, max_rows, I)) return launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
+  return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+}
+
 MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
                                        const moe_bf16* x, const int32_t* seg_begin,
                                        const int32_t* seg_count, const moe_bf16* w_gate,
@@ -1385,19 +1557,29 @@ MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int3
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up))
     return MOE_ERR_UNSUPPORTED;
-  const bool pair = I % 128 == 0 && pair_shape(n_seg, max_rows);
-  const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
-  CUtensorMap m_x, m_wg, m_wu;
-  if (!make_map(&m_x, x, max_rows, d, bm) || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
-      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
-    return MOE_ERR_CUDA;
-  GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
-             dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
-             nullptr, 0, 0, bm, bm * kBK * 2};
-  cudaStream_t s = as_cuda(stream);
-  if (pair) return launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s);
-  if (wide_gate_up(n_seg, max_rows, I)) return launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
-  return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+  return gate_up_impl(n_seg, d, I, max_rows, x, 0, 1, nullptr, seg_begin, seg_count, w_gate,
+                      w_up, h, dev_status, stream);
+}
+
+MOE_API moe_status moe_grouped_gate_up_gather(int32_t n_seg, int32_t d, int32_t I,
+                                              int32_t max_rows, int32_t T, int32_t k,
+                                              const moe_bf16* x, const int32_t* row_to_route,
+                                              const int32_t* seg_begin, const int32_t* seg_count,
+                                              const moe_bf16* w_gate, const moe_bf16* w_up,
+                                              moe_bf16* h, uint32_t* dev_status,
+                                              moe_stream_t stream) {
+  moe_status st = check_common(n_seg, d, I, max_rows);
+  if (st != MOE_OK) return st;
+  if (T < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (max_rows == 0) return MOE_OK;
+  if (T == 0 || x == nullptr || row_to_route == nullptr || seg_begin == nullptr ||
+      seg_count == nullptr || w_gate == nullptr || w_up == nullptr || h == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(h) || !aligned16(w_gate) || !aligned16(w_up))
+    return MOE_ERR_UNSUPPORTED;
+  return gate_up_impl(n_seg, d, I, max_rows, x, T, k, row_to_route, seg_begin, seg_count, w_gate,
+                      w_up, h, dev_status, stream);
 }
 
 MOE_API moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,

@@ -20,7 +20,8 @@
 //                    its ordinal, its row and both maps.
 //   3. permute_copy  token-major row copy over many blocks: every token row is
 //                    read once and written to its admitted rows with 16-byte
-//                    accesses.
+//                    accesses.  Skipped when the caller wants the maps only (the
+//                    gate/up pass can gather the rows itself).
 #include "common.cuh"
 
 namespace moe {
@@ -270,10 +271,12 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
     return MOE_ERR_UNSUPPORTED;
   if (T > 0 && G > 0 && (scales == nullptr || scales_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || offsets == nullptr || n_dropped == nullptr) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (topk_ids == nullptr || x == nullptr || x_perm == nullptr ||
-                row_to_route == nullptr || route_to_row == nullptr || ws == nullptr))
+  // x and x_perm both NULL (no scales): the maps only, no row copy
+  const bool maps_only = x == nullptr && x_perm == nullptr && G == 0;
+  if (T > 0 && (topk_ids == nullptr || row_to_route == nullptr || route_to_row == nullptr ||
+                ws == nullptr || (!maps_only && (x == nullptr || x_perm == nullptr))))
     return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && !maps_only && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_UNSUPPORTED;
   if (ws_bytes < moe_permute_workspace_size(T, k, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = as_cuda(stream);
   const int R = T * k;
@@ -294,6 +297,7 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
          tl.routes_per_tile, tl.n_tiles, capacity, topk_ids,
          static_cast<const int32_t*>(tl.n_tiles > 1 ? hist : nullptr), counts, offsets, n_dropped,
          row_to_route, route_to_row, dev_status, valid);
+  if (maps_only) return launch_status();
   const int warps = kCopyThreads / 32;
   int64_t blocks = ceil_div(T, warps);
   if (blocks > 152 * 16) blocks = 152 * 16;

@@ -47,7 +47,8 @@ class MoELayer:
     def __init__(self, T: int, d: int, E: int, k: int, I: int, w_gate, w_up, w_down,
                  capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
                  topk_group: int = 1, route_scale: float = 1.0, sel_bias=None,
-                 shared_weights=None, payload: str = "bf16", device="cuda"):
+                 shared_weights=None, payload: str = "bf16", gather: bool = False,
+                 device="cuda"):
         self.T, self.d, self.E, self.k, self.I = T, d, E, k, I
         if payload not in PAYLOADS:
             raise ValueError(f"payload must be one of {sorted(PAYLOADS)}")
@@ -68,7 +69,14 @@ class MoELayer:
         # per output-column block (measured 1.5x slower on prefill); with few rows per
         # expert the gate/up pass dequantizes in its loader.  Both give the same bits.
         self.fused_fp8 = payload != "bf16" and R < 128 * E
-        if payload == "bf16" or not self.fused_fp8:
+        # bf16 payload, gather=True: the permute writes the maps only and the gate/up
+        # pass gathers each expert row from token order (moe_grouped_gate_up_gather).
+        # Off by default: one TMA gather moves four 128-byte rows, and at that
+        # granularity the copy engine's instruction rate, not HBM, bounds the A
+        # operand (gate/up measured 1.22 -> 4.16 ms on the 4096 x 4096 prefill shape,
+        # 120 -> 127 us on decode), while the separate copy runs at 75-83 % of HBM.
+        self.gather = gather and payload == "bf16"
+        if (payload == "bf16" and not self.gather) or (payload != "bf16" and not self.fused_fp8):
             self.x_perm = torch.empty((max(R, 1), d), dtype=torch.bfloat16, device=dev)
         if payload != "bf16":
             G = abi.fp8_scale_groups(d, self.scale_group)
@@ -132,10 +140,10 @@ class MoELayer:
                                 self.n_dropped, self.perm_ws, self.perm_ws_bytes,
                                 self.dev_status, stream)
             return
-        abi.moe_permute(self.T, self.d, self.E, self.k, self.capacity, self.topk_ids, x,
-                        self.x_perm, self.counts, self.offsets, self.row_to_route,
-                        self.route_to_row, self.n_dropped, self.perm_ws, self.perm_ws_bytes,
-                        self.dev_status, stream)
+        abi.moe_permute(self.T, self.d, self.E, self.k, self.capacity, self.topk_ids,
+                        None if self.gather else x, None if self.gather else self.x_perm,
+                        self.counts, self.offsets, self.row_to_route, self.route_to_row,
+                        self.n_dropped, self.perm_ws, self.perm_ws_bytes, self.dev_status, stream)
 
     def dequantize(self, stream=None):
         """FP8 payload, unfused: the permuted E4M3 rows and their scales -> bf16 x_perm."""
@@ -143,8 +151,14 @@ class MoELayer:
         abi.moe_dequantize_fp8(R, self.d, self.scale_group, self.xq_perm, self.xs_perm,
                                self.x_perm, stream)
 
-    def experts_gate_up(self, stream=None):
+    def experts_gate_up(self, stream=None, x=None):
+        """The gate/up pass; `x` (the token rows) is needed when the rows are gathered."""
         R = max(self.T * self.k, 1)
+        if self.gather:
+            abi.moe_grouped_gate_up_gather(self.E, self.d, self.I, R, self.T, self.k, x,
+                                           self.row_to_route, self.offsets, self.counts,
+                                           self.w_gate, self.w_up, self.H, self.dev_status, stream)
+            return
         if self.payload != "bf16" and self.fused_fp8:
             abi.moe_grouped_gate_up_fp8(self.E, self.d, self.I, R, self.scale_group, self.xq_perm,
                                         self.xs_perm, self.offsets, self.counts, self.w_gate,
@@ -158,8 +172,8 @@ class MoELayer:
         abi.moe_grouped_down(self.E, self.I, self.d, R, self.H, self.offsets, self.counts,
                              self.w_down, self.y, self.dev_status, stream)
 
-    def experts(self, stream=None):
-        self.experts_gate_up(stream)
+    def experts(self, stream=None, x=None):
+        self.experts_gate_up(stream, x)
         self.experts_down(stream)
 
     def shared_fork(self, stream=None):
@@ -196,7 +210,8 @@ class MoELayer:
         st.append(("permute", lambda s: self.permute(x, s), None))
         if self.payload != "bf16" and not self.fused_fp8:
             st.append(("dequantize", self.dequantize, None))
-        st += [("gate_up", self.experts_gate_up, None), ("down", self.experts_down, None)]
+        st += [("gate_up", lambda s: self.experts_gate_up(s, x), None),
+               ("down", self.experts_down, None)]
         if self.shared is not None:
             st.append(("shared_join", self.shared_join, None))
         st.append(("combine", lambda s: self.combine(s, out), None))
@@ -448,10 +463,11 @@ class DecodeBucket:
         abi.moe_route_bucket(L.params, self.valid, self.logits, L.sel_bias, L.topk_ids, L.gates,
                              L.dev_status, stream)
         abi.moe_permute_bucket(self.B, self.d, self.E, self.k, L.capacity, self.valid,
-                               L.topk_ids, self.x, L.x_perm, L.counts, L.offsets, L.row_to_route,
-                               L.route_to_row, L.n_dropped, L.perm_ws, L.perm_ws_bytes,
-                               L.dev_status, stream)
-        L.experts_gate_up(stream)
+                               L.topk_ids, None if L.gather else self.x,
+                               None if L.gather else L.x_perm, L.counts, L.offsets,
+                               L.row_to_route, L.route_to_row, L.n_dropped, L.perm_ws,
+                               L.perm_ws_bytes, L.dev_status, stream)
+        L.experts_gate_up(stream, self.x)
         L.experts_down(stream)
         abi.moe_combine_bucket(self.B, self.k, self.d, self.valid, L.y, R, L.route_to_row,
                                L.gates, None, 0, L.out, L.dev_status, stream)

@@ -136,7 +136,10 @@ moe_status moe_sigmoid_det(int64_t n, const float* z, float* s, moe_stream_t str
  *   n_dropped[1]       R - accepted,
  *   x_perm[R,d]        x_perm[row] = x[token of row_to_route[row]] (bit copy);
  *                      rows >= offsets[E] are left untouched.
- * x is [T,d].  Workspace: moe_permute_workspace_size(T,k,E) bytes.
+ * x is [T,d].  x and x_perm may both be NULL: then only the maps, counts,
+ * offsets and n_dropped are produced and no row is copied (for
+ * moe_grouped_gate_up_gather, which reads the rows from token order itself).
+ * Workspace: moe_permute_workspace_size(T,k,E) bytes.
  * Limits: 1 <= E <= 512, 1 <= k <= 16, 0 <= T, T*k < 2^31, d % 8 == 0,
  * 16-byte aligned x / x_perm.  Out-of-range ids set MOE_DEV_BAD_EXPERT_ID and
  * the route is treated as dropped.                                          */
@@ -211,6 +214,23 @@ moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int32_t max_
                                const int32_t* seg_count, const moe_bf16* w_gate,
                                const moe_bf16* w_up, moe_bf16* h, uint32_t* dev_status,
                                moe_stream_t stream);
+/* moe_grouped_gate_up whose A rows are gathered from token order inside the
+ * pass instead of read from a permuted copy: row i of the expert row space is
+ * x[row_to_route[i] / k] of the token rows x [T, d] -- exactly the row
+ * moe_permute copies to x_perm[i] -- so with moe_permute's row_to_route, counts
+ * and offsets as the segment table h is bit-identical to moe_grouped_gate_up on
+ * moe_permute's x_perm, and the permuted rows are never written to or read back
+ * from HBM.  The loader issues one TMA gather per four rows: the permutation
+ * of [M6.6] 0x03B is applied as a map of rows inside the pass rather than as a
+ * copy.  Only row_to_route entries of rows inside segments are read; one
+ * outside [0, T*k) sets MOE_DEV_BAD_ROW and that row reads token 0.  Limits
+ * and errors as moe_grouped_gate_up, plus T*k < 2^31.                        */
+moe_status moe_grouped_gate_up_gather(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                                      int32_t T, int32_t k, const moe_bf16* x,
+                                      const int32_t* row_to_route, const int32_t* seg_begin,
+                                      const int32_t* seg_count, const moe_bf16* w_gate,
+                                      const moe_bf16* w_up, moe_bf16* h, uint32_t* dev_status,
+                                      moe_stream_t stream);
 moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
                             const moe_bf16* h, const int32_t* seg_begin, const int32_t* seg_count,
                             const moe_bf16* w_down, moe_bf16* y, uint32_t* dev_status,

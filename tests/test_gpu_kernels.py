@@ -342,6 +342,104 @@ def test_grouped_swiglu_bad_segment_is_reported():
     assert int(host(st)[0]) & g.MOE_DEV_BAD_ROW
 
 
+def _gather_case(T, d, E, k, I, cap=-1, seed=0, alpha=1.0):
+    """gate/up with rows gathered from token order vs the same pass on moe_permute's
+    copy: H bit-identical on every segment row, other rows untouched."""
+    g = G()
+    rng = np.random.default_rng(seed)
+    p = rng.dirichlet(np.ones(E) * alpha)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    gen = torch.Generator(device=DEV).manual_seed(seed + 1)
+    x = torch.randn((T, d), generator=gen, device=DEV).to(torch.bfloat16)
+    w = workloads.scaled(workloads.tiny(), d=d, I=I, E=E, seed=seed)
+    wg, wu, _ = workloads.make_expert_weights(w, DEV, n_experts=E)
+    R = T * k
+    got = _permute(T, d, E, k, cap, ids_np, x)  # maps and the copied rows
+    i32 = dict(dtype=torch.int32, device=DEV)
+    counts, offsets = torch.from_numpy(got["counts"]).to(DEV), torch.from_numpy(got["offsets"]).to(DEV)
+    r2r = torch.from_numpy(got["row_to_route"]).to(DEV)
+    xp = torch.from_numpy(got["x_perm"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    h_copy = torch.full((R, I), 3.0, dtype=torch.bfloat16, device=DEV)
+    h_gath = torch.full((R, I), 3.0, dtype=torch.bfloat16, device=DEV)
+    st = status0()
+    g.moe_grouped_gate_up(E, d, I, R, xp, offsets, counts, wg, wu, h_copy, st)
+    g.moe_grouped_gate_up_gather(E, d, I, R, T, k, x, r2r, offsets, counts, wg, wu, h_gath, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(h_copy.view(torch.int16), h_gath.view(torch.int16))
+    acc = int(got["offsets"][-1])
+    assert torch.all(h_gath[acc:] == 3.0)
+    # and H against the oracle on a few rows
+    if acc:
+        rows = np.sort(rng.choice(acc, min(acc, 24), replace=False))
+        xb = bits(x)
+        for r in rows:
+            e = int(np.searchsorted(got["offsets"], r, side="right") - 1)
+            xr = oracle.bf16_to_f64(xb[got["row_to_route"][r] // k][None])
+            gg = xr @ oracle.bf16_to_f64(bits(wg[e]))
+            uu = xr @ oracle.bf16_to_f64(bits(wu[e]))
+            ref = oracle.bf16_to_f64(oracle.f64_to_bf16(oracle.silu(gg) * uu))
+            assert_float_parity(oracle.bf16_to_f64(bits(h_gath[r:r + 1])), ref, f"H row {r}")
+
+
+@pytest.mark.parametrize("T,d,E,k,I,cap", [
+    (1, 2048, 128, 8, 768, -1),    # one token: 16-row boxes, 2 x 64-column tiles
+    (8, 2048, 128, 8, 768, -1),
+    (128, 256, 128, 8, 768, -1),   # decode T=128 shape class: 32-row boxes, wide tiles
+    (300, 256, 32, 4, 192, -1),    # I not a multiple of 128
+    (1000, 128, 8, 2, 256, 200),   # capacity with drops
+    (4096, 512, 8, 2, 256, -1),    # CTA-pair kernel (segments average >= 128 rows)
+    (2000, 256, 16, 4, 384, 480),  # pair kernel with ragged tails and drops
+])
+def test_gate_up_gather_equals_copy_path(T, d, E, k, I, cap):
+    _gather_case(T, d, E, k, I, cap, seed=T + E)
+
+
+@pytest.mark.parametrize("T,E,k,cap", [(300, 32, 4, 40), (5000, 128, 8, -1), (1, 8, 2, -1)])
+def test_permute_maps_only_equals_the_copying_call(T, E, k, cap):
+    """x = x_perm = NULL: the same maps, counts, offsets and drops, one launch fewer."""
+    g = G()
+    rng = np.random.default_rng(T)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    x = torch.randn((T, 64), device=DEV).to(torch.bfloat16)
+    full = _permute(T, 64, E, k, cap, ids_np, x)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    r2r, inv = torch.full((T * k,), -7, **i32), torch.full((T * k,), -7, **i32)
+    nd = torch.zeros(1, **i32)
+    wsb = g.moe_permute_workspace_size(T, k, E)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    n0 = g.launch_count()
+    g.moe_permute(T, 64, E, k, cap, ids, None, None, counts, offsets, r2r, inv, nd, ws, wsb, st)
+    assert g.launch_count() - n0 == g.abi._permute_launches(T, k) - 1
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    acc = int(full["offsets"][-1])
+    assert np.array_equal(host(counts), full["counts"])
+    assert np.array_equal(host(offsets), full["offsets"])
+    assert np.array_equal(host(r2r)[:acc], full["row_to_route"][:acc])
+    assert np.array_equal(host(inv), full["route_to_row"][:T * k])
+    assert int(nd.item()) == full["n_dropped"]
+
+
+def test_gate_up_gather_bad_map_entry_is_reported():
+    g = G()
+    T, d, E, k, I = 16, 64, 4, 2, 128
+    x = torch.randn((T, d), device=DEV).to(torch.bfloat16)
+    wg = torch.zeros((E, d, I), dtype=torch.bfloat16, device=DEV)
+    r2r = torch.arange(T * k, dtype=torch.int32, device=DEV)
+    r2r[5] = T * k + 3  # outside the routes
+    counts = torch.full((E,), T * k // E, dtype=torch.int32, device=DEV)
+    offsets = torch.arange(E + 1, dtype=torch.int32, device=DEV) * (T * k // E)
+    h = torch.zeros((T * k, I), dtype=torch.bfloat16, device=DEV)
+    st = status0()
+    g.moe_grouped_gate_up_gather(E, d, I, T * k, T, k, x, r2r, offsets, counts, wg, wg, h, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & g.MOE_DEV_BAD_ROW
+
+
 # ----------------------------------------------------------------------------
 # Pooled layout
 # ----------------------------------------------------------------------------

@@ -25,24 +25,26 @@ def built():
     build.build()
 
 
-def make_layer(w, wg, wu, wd, sel_bias=None, shared=None, payload="bf16"):
+def make_layer(w, wg, wu, wd, sel_bias=None, shared=None, payload="bf16", gather=False):
     import grouped_expert_gemm_gb300 as g
     cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
     score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
     return g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                       n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
-                      sel_bias=sel_bias, shared_weights=shared, payload=payload, device=DEV)
+                      sel_bias=sel_bias, shared_weights=shared, payload=payload, gather=gather,
+                      device=DEV)
 
 
 SCALE_GROUP = {"fp8_row": 0, "fp8_block128": 128}
 
 
-def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, payload="bf16"):
+def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, payload="bf16",
+                  gather=False):
     logits, sel_bias = workloads.make_router_inputs(w, DEV)
     x = workloads.make_activations(w, DEV)
     wg, wu, wd = weights if weights is not None else workloads.make_expert_weights(w, DEV)
     shared = workloads.make_shared_weights(w, DEV)
-    layer = make_layer(w, wg, wu, wd, sel_bias, shared, payload)
+    layer = make_layer(w, wg, wu, wd, sel_bias, shared, payload, gather)
     out = layer.forward(logits, x)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
@@ -66,7 +68,10 @@ def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, p
     rows_dev = torch.from_numpy(rows).to(DEV)
     tok_of_row = perm["row_to_route"][rows] // w.k
     x_expert = xb  # the bf16 rows the experts see (token order)
-    if payload == "bf16":
+    if payload == "bf16" and layer.gather:
+        # no permuted copy: the gate/up pass gathers the rows (checked through H and y)
+        assert not hasattr(layer, "x_perm")
+    elif payload == "bf16":
         # permuted payload rows: bit copies
         assert np.array_equal(bits(layer.x_perm[rows_dev]), xb[tok_of_row])
     else:
@@ -112,6 +117,21 @@ def decode_weights():
 @pytest.mark.parametrize("T", [1, 8, 32, 128])
 def test_decode_sweep_full(T, decode_weights):
     run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096)
+
+
+def test_tiny_full_gathered_rows():
+    """The maps-only permute with the gathering gate/up loader gives the same checks."""
+    run_and_check(workloads.tiny(), gather=True)
+
+
+@pytest.mark.parametrize("T", [1, 32])
+def test_decode_gathered_rows(T, decode_weights):
+    run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096, gather=True)
+
+
+def test_v3_small_full_gathered_rows():
+    w = workloads.scaled(workloads.v3(), T=64, d=256, I=256, shared_I=128)
+    run_and_check(w, sample_rows=10**6, gather=True)
 
 
 @pytest.mark.slow
