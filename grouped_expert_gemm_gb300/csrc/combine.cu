@@ -6,8 +6,9 @@
 // bf16 returned rows.  [POOL] 03: waves add into one fp32 accumulator
 // (accumulate != 0).
 //
-// One block owns one token at a time (grid-stride over tokens).  The token's k
-// row indices and gates are staged once in shared memory; each thread then
+// One block owns one token at a time (grid-stride over tokens; with few tokens,
+// one column part of a token).  The token's k row indices and gates are staged
+// once in shared memory; each thread then
 // handles 16-byte column chunks, issuing all k (up to KMAX) independent 16-byte
 // loads of y for UNROLL chunks before using them, sums in fp32 in slot order,
 // and writes two 16-byte fp32 stores per chunk.  No atomics: each output element
@@ -21,7 +22,7 @@ constexpr int kCombThreads = 128;
 
 template <int KMAX>
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_rows,
+combine_kernel(int T, int k, int chunks, int parts, const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
                const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
                uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid) {
@@ -40,7 +41,12 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
       out[(t * chunks + c) * 2 + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  for (int64_t t = blockIdx.x; t < T_live; t += gridDim.x) {
+  // A block owns one (token, column part) unit at a time; parts > 1 only when
+  // there are too few tokens to give every SM work.
+  const int per = (chunks + parts - 1) / parts;
+  for (int64_t u0 = blockIdx.x; u0 < T_live * parts; u0 += gridDim.x) {
+    const int64_t t = u0 / parts;
+    const int c_lo = static_cast<int>(u0 % parts) * per, c_hi = min(chunks, c_lo + per);
     if (threadIdx.x < KMAX) {
       int32_t r = -1;
       float g = 0.0f;
@@ -56,20 +62,20 @@ combine_kernel(int T, int k, int chunks, const uint4* __restrict__ y, int64_t y_
       s_gate[threadIdx.x] = g;
     }
     __syncthreads();
-    for (int c0 = threadIdx.x; c0 < chunks; c0 += kCombThreads * UNROLL) {
+    for (int c0 = c_lo + threadIdx.x; c0 < c_hi; c0 += kCombThreads * UNROLL) {
       uint4 v[UNROLL][KMAX];
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         const int c = c0 + u * kCombThreads;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
-          if (c < chunks && s_row[j] >= 0)
+          if (c < c_hi && s_row[j] >= 0)
             v[u][j] = __ldg(y + static_cast<int64_t>(s_row[j]) * chunks + c);
       }
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         const int c = c0 + u * kCombThreads;
-        if (c >= chunks) continue;
+        if (c >= c_hi) continue;
         float acc[8];
         float4* o = out + (t * chunks + c) * 2;
         if (accumulate) {
@@ -158,9 +164,15 @@ static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* 
     return MOE_ERR_UNSUPPORTED;
   const int chunks = d / 8;
   cudaStream_t s = as_cuda(stream);
-  const unsigned grid = static_cast<unsigned>(T < 152 * 24 ? T : 152 * 24);
+  // Column parts while that still leaves a chunk per thread and fewer than two
+  // blocks per SM would otherwise have work (decode).
+  int parts = 1;
+  while (static_cast<int64_t>(T) * parts * 2 <= 152 * 2 && chunks / (parts * 2) >= kCombThreads)
+    parts *= 2;
+  const int64_t units = static_cast<int64_t>(T) * parts;
+  const unsigned grid = static_cast<unsigned>(units < 152 * 24 ? units : 152 * 24);
 #define MOE_COMBINE_CASE(K)                                                                 \
-  launch(combine_kernel<K>, dim3(grid), dim3(kCombThreads), 0, s, T, k, chunks,               \
+  launch(combine_kernel<K>, dim3(grid), dim3(kCombThreads), 0, s, T, k, chunks, parts,        \
          reinterpret_cast<const uint4*>(y), y_rows, route_to_row, gates,                      \
          reinterpret_cast<const uint4*>(shared_y), static_cast<int>(accumulate),              \
          reinterpret_cast<float4*>(out), dev_status, valid)

@@ -198,11 +198,13 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
   pdl_trigger();
 }
 
-// One warp per token: read the row once, store it to each admitted row (and,
-// with SCALES, the row's G fp32 scales to the same rows of scales_perm).
+// One warp per (token, column part): read the part of the row once, store it to
+// each admitted row (and, with SCALES, part 0 copies the row's G fp32 scales to
+// the same rows of scales_perm).  `parts` > 1 splits rows into column ranges
+// when there are too few tokens to give every SM work (decode).
 template <bool SCALES>
 __global__ void __launch_bounds__(kCopyThreads)
-permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
+permute_copy(int T, int k, int chunks, int parts, const int32_t* __restrict__ route_to_row,
              const uint4* __restrict__ x, uint4* __restrict__ x_perm,
              const int32_t* __restrict__ valid, int G, const float* __restrict__ scales,
              float* __restrict__ scales_perm) {
@@ -210,27 +212,33 @@ permute_copy(int T, int k, int chunks, const int32_t* __restrict__ route_to_row,
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int T_live = valid_routes(T, 1, valid);
-  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T_live; t += gridDim.x * warps) {
+  const int per = (chunks + parts - 1) / parts;
+  const int64_t units = static_cast<int64_t>(T_live) * parts;
+  for (int64_t u0 = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); u0 < units;
+       u0 += static_cast<int64_t>(gridDim.x) * warps) {
+    const int t = static_cast<int>(u0 / parts), part = static_cast<int>(u0 % parts);
+    const int c_lo = part * per, c_hi = min(chunks, c_lo + per);
     const int32_t my_row = lane < k ? __ldg(route_to_row + static_cast<int64_t>(t) * k + lane) : -1;
     const uint4* src = x + static_cast<int64_t>(t) * chunks;
-    // The chunk loop runs uniformly over the warp (lanes past the row end only
+    // The chunk loop runs uniformly over the warp (lanes past the range end only
     // skip their accesses) because its body broadcasts rows with __shfl_sync.
-    for (int cb = 0; cb < chunks; cb += 32 * 4) {
+    for (int cb = c_lo; cb < c_hi; cb += 32 * 4) {
       const int c = cb + lane;
       uint4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (c + 32 * u < chunks) v[u] = __ldg(src + c + 32 * u);
+        if (c + 32 * u < c_hi) v[u] = __ldg(src + c + 32 * u);
       for (int j = 0; j < k; ++j) {
         const int32_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
         if (row < 0) continue;
         uint4* dst = x_perm + static_cast<int64_t>(row) * chunks;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (c + 32 * u < chunks) dst[c + 32 * u] = v[u];
+          if (c + 32 * u < c_hi) dst[c + 32 * u] = v[u];
       }
     }
     if constexpr (SCALES) {
+      if (part != 0) continue;
       const float* src_s = scales + static_cast<int64_t>(t) * G;
       for (int j = 0; j < k; ++j) {
         const int32_t row = __shfl_sync(0xFFFFFFFFu, my_row, j);
@@ -299,16 +307,22 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
          row_to_route, route_to_row, dev_status, valid);
   if (maps_only) return launch_status();
   const int warps = kCopyThreads / 32;
-  int64_t blocks = ceil_div(T, warps);
-  if (blocks > 152 * 16) blocks = 152 * 16;
   const int chunks = static_cast<int>(row_bytes / 16);
+  // Column parts: enough warps for every SM when tokens are few, at least 64
+  // chunks (1 KB) per part.
+  int parts = 1;
+  while (static_cast<int64_t>(T) * parts * 2 <= 152 * warps && chunks / (parts * 2) >= 64)
+    parts *= 2;
+  int64_t blocks = ceil_div(static_cast<int64_t>(T) * parts, warps);
+  if (blocks > 152 * 16) blocks = 152 * 16;
   if (scales == nullptr)
     launch(permute_copy<false>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T,
-           k, chunks, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
-           static_cast<uint4*>(x_perm), valid, 0, scales, scales_perm);
+           k, chunks, parts, static_cast<const int32_t*>(route_to_row),
+           static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), valid, 0, scales,
+           scales_perm);
   else
     launch(permute_copy<true>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k,
-           chunks, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
+           chunks, parts, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
            static_cast<uint4*>(x_perm), valid, G, scales, scales_perm);
   return launch_status();
 }
