@@ -81,15 +81,25 @@ constexpr int kPairAtoms = 2;                     // B atoms per CTA in the pair
 constexpr int kTmemCols = 512;
 constexpr int kASlotCols = kBK / 2;  // 64 bf16 of a row = 32 columns
 
-template <int N_ATOMS, bool FP8A = false>
+// SMALLA (bf16 A, boxes of at most 32 rows): the A slot holds only the 32 rows
+// TMA stages (4 KB), so more stages fit; the MMA still reads 128 rows from the
+// slot's start, the rows past 32 falling on the same stage's B atoms -- finite
+// data whose accumulator rows are never stored.
+constexpr int kSmallABytes = 32 * kBK * 2;  // 4 KB
+constexpr int kFixedSmem = 1024 + (3 * kMaxSeg + 16) * 4 + 64 * 8;  // alignment, tables, barriers
+
+template <int N_ATOMS, bool FP8A = false, bool SMALLA = false>
 struct Geometry {
   static constexpr int kN = 64 * N_ATOMS;                  // MMA N
-  static constexpr int kBOff = FP8A ? 0 : kABytes;         // B atoms in a TMA slot
+  static constexpr int kASlotBytes = SMALLA ? kSmallABytes : kABytes;
+  static constexpr int kBOff = FP8A ? 0 : kASlotBytes;     // B atoms in a TMA slot
   static constexpr int kRawOff = N_ATOMS * kAtomBytes;     // E4M3 tile in a TMA slot
-  static constexpr int kStageBytes = N_ATOMS * kAtomBytes + (FP8A ? kRawBytes : kABytes);
+  static constexpr int kStageBytes = N_ATOMS * kAtomBytes + (FP8A ? kRawBytes : kASlotBytes);
   // As many stages as fit the shared memory: narrower tiles keep more loads in flight.
-  static constexpr int kStages = FP8A ? (N_ATOMS >= 4 ? 4 : 8)
-                                      : (N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8));
+  static constexpr int kSmallAStages = (227 * 1024 - kFixedSmem) / kStageBytes;
+  static constexpr int kStages = SMALLA ? (kSmallAStages > 12 ? 12 : kSmallAStages)
+                                 : FP8A ? (N_ATOMS >= 4 ? 4 : 8)
+                                        : (N_ATOMS >= 4 ? 4 : (N_ATOMS == 2 ? 6 : 8));
   static constexpr int kASlots = FP8A ? 8 : 0;
   static constexpr int kAccBufs = 2 * kN + kASlots * kASlotCols <= kTmemCols ? 2 : 1;
   static constexpr int kACol = kAccBufs * kN;              // first column of the A slots
@@ -104,6 +114,8 @@ struct Geometry {
   static_assert(kTmemUsed <= kTmemCols, "tensor memory");
   static_assert(!FP8A || (kStages % 2 == 0 && kASlots % 2 == 0), "even rings");
   static_assert(kRawOff % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
+  static_assert(!(FP8A && SMALLA), "the E4M3 loader has its own slot layout");
+  static_assert(!SMALLA || kStageBytes >= kABytes, "the MMA's 128 A rows stay inside the stage");
 };
 
 // Pair kernel, per CTA: TMA slot [A bf16 tile 16 KB][2 B atoms 16 KB], or with an
@@ -749,12 +761,12 @@ __device__ __forceinline__ bool forward_conversions(int n_stages_total, int slot
 
 // ------------------------- single-CTA kernel --------------------------------
 
-template <int N_ATOMS, bool SWIGLU, bool FP8A>
-__global__ void __launch_bounds__(Geometry<N_ATOMS, FP8A>::kThreads, 1)
+template <int N_ATOMS, bool SWIGLU, bool FP8A, bool SMALLA>
+__global__ void __launch_bounds__(Geometry<N_ATOMS, FP8A, SMALLA>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b0,
                     const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
-  using G = Geometry<N_ATOMS, FP8A>;
+  using G = Geometry<N_ATOMS, FP8A, SMALLA>;
   constexpr int kStages = G::kStages;
   constexpr int kASlots = G::kASlots;
   constexpr int kAccBufs = G::kAccBufs;
@@ -1382,11 +1394,11 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int N_ATOMS, bool SWIGLU, bool FP8A = false>
-moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                       const GemmArgs& args, cudaStream_t s) {
-  using G = Geometry<N_ATOMS, FP8A>;
-  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU, FP8A>;
+template <int N_ATOMS, bool SWIGLU, bool FP8A = false, bool SMALLA = false>
+moe_status launch_gemm_shape(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                             const GemmArgs& args, cudaStream_t s) {
+  using G = Geometry<N_ATOMS, FP8A, SMALLA>;
+  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU, FP8A, SMALLA>;
   // The shared-memory opt-in and the SM count are per device: set/read once.
   constexpr int kMaxDev = 64;
   static int sms[kMaxDev] = {};
@@ -1406,6 +1418,18 @@ moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   }
   launch(kern, dim3(n_sm), dim3(G::kThreads), G::kSmemBytes, s, a, b0, b1, args);
   return launch_status();
+}
+
+// Single-CTA launch: the small-A slot layout (deeper pipeline) when the row
+// boxes hold at most 32 rows, the A operand is bf16 and a stage (at least two B
+// atoms) covers the 128 rows the MMA reads.
+template <int N_ATOMS, bool SWIGLU, bool FP8A = false>
+moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                       const GemmArgs& args, cudaStream_t s) {
+  if constexpr (!FP8A && N_ATOMS >= 2) {
+    if (args.bm <= 32) return launch_gemm_shape<N_ATOMS, SWIGLU, false, true>(a, b0, b1, args, s);
+  }
+  return launch_gemm_shape<N_ATOMS, SWIGLU, FP8A, false>(a, b0, b1, args, s);
 }
 
 // The pair kernel runs as many two-CTA clusters as can be resident at once
