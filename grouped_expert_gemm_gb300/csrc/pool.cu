@@ -65,22 +65,71 @@ __device__ __forceinline__ int block_sum_512(int v, int* scratch) {
   return tot;
 }
 
+// In-place exclusive scan down the columns of hist [n_tiles][n_cols] (row-major),
+// column totals to tot[n_cols] (shared memory); every thread of the block calls it.
+// G threads (a power of two, at most a warp) share a column: each sums its slice of
+// the tiles with batched independent loads, the group scans the slice sums with
+// shuffles, and each thread rewrites its slice -- a chain of n_tiles / G loads
+// instead of n_tiles dependent ones.
+constexpr int kScanBatch = 8;
+
+__device__ void scan_columns(int n_cols, int n_tiles, int32_t* __restrict__ hist, int32_t* tot) {
+  const int nthr = blockDim.x;
+  int G = 1;
+  while (G < 32 && n_cols * G * 2 <= nthr) G *= 2;
+  const int per_pass = nthr / G;
+  const int m = threadIdx.x % G, cl = threadIdx.x / G;
+  const int t0 = static_cast<int>(static_cast<int64_t>(n_tiles) * m / G);
+  const int t1 = static_cast<int>(static_cast<int64_t>(n_tiles) * (m + 1) / G);
+  for (int c0 = 0; c0 < n_cols; c0 += per_pass) {
+    const int c = c0 + cl;
+    const bool live = c < n_cols;
+    int sum = 0;
+    if (live) {
+      for (int t = t0; t < t1; t += kScanBatch) {
+        int32_t v[kScanBatch];
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j)
+          v[j] = t + j < t1 ? hist[static_cast<int64_t>(t + j) * n_cols + c] : 0;
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) sum += v[j];
+      }
+    }
+    int incl = sum;
+    for (int o = 1; o < G; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o, G);
+      if (m >= o) incl += n;
+    }
+    const int total = __shfl_sync(0xFFFFFFFFu, incl, G - 1, G);
+    if (live) {
+      int run = incl - sum;
+      for (int t = t0; t < t1; t += kScanBatch) {
+        int32_t v[kScanBatch];
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j)
+          v[j] = t + j < t1 ? hist[static_cast<int64_t>(t + j) * n_cols + c] : 0;
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+          if (t + j < t1) hist[static_cast<int64_t>(t + j) * n_cols + c] = run;
+          run += v[j];
+        }
+      }
+      if (m == 0) tot[c] = total;
+    }
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(512)
 pack_scan(int n_dest, int n_tiles, int n_waves, int pool_cap, int policy, int wave,
           int32_t* __restrict__ hist, int32_t* __restrict__ pool_fill,
           int32_t* __restrict__ sender_drops) {
   pdl_wait();
   __shared__ int scratch[16];
+  __shared__ int32_t tot[512];  // n_dest <= 512
+  scan_columns(n_dest, n_tiles, hist, tot);
   const int D = threadIdx.x;
-  int32_t run = 0;
-  if (D < n_dest) {
-    for (int t = 0; t < n_tiles; ++t) {
-      const int64_t b = static_cast<int64_t>(t) * n_dest + D;
-      const int32_t v = hist[b];
-      hist[b] = run;
-      run += v;
-    }
-  }
+  const int32_t run = D < n_dest ? tot[D] : 0;
   int in_wave = 0;
   if (D < n_dest) {
     if (policy == MOE_WAVE_STRIPE)
@@ -232,19 +281,13 @@ compact_scan(int n_local, int n_tiles, int local_cap, int32_t* __restrict__ hist
              int32_t* __restrict__ local_counts, int32_t* __restrict__ receiver_drops) {
   pdl_wait();
   __shared__ int scratch[16];
+  extern __shared__ int32_t tot[];  // [n_local]
+  scan_columns(n_local, n_tiles, hist, tot);
   int drops_total = 0;
   for (int l0 = 0; l0 < n_local; l0 += blockDim.x) {
     const int l = l0 + threadIdx.x;
-    int32_t run = 0;
-    if (l < n_local) {
-      for (int t = 0; t < n_tiles; ++t) {
-        const int64_t b = static_cast<int64_t>(t) * n_local + l;
-        const int32_t v = hist[b];
-        hist[b] = run;
-        run += v;
-      }
-      local_counts[l] = min(run, local_cap);
-    }
+    const int32_t run = l < n_local ? tot[l] : 0;
+    if (l < n_local) local_counts[l] = min(run, local_cap);
     drops_total += block_sum_512(l < n_local ? run - min(run, local_cap) : 0, scratch);
     __syncthreads();
   }
@@ -431,8 +474,8 @@ MOE_API moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, 
   const uint16_t* hdr = reinterpret_cast<const uint16_t*>(pools);
   launch(compact_hist, dim3(n_tiles), dim3(kThreads), n_local * sizeof(int32_t), s, n_items,
          pool_cap, d, n_local, per, hdr, hist, dev_status);
-  launch(compact_scan, dim3(1), dim3(512), 0, s, n_local, n_tiles, local_cap, hist, local_counts,
-         receiver_drops);
+  launch(compact_scan, dim3(1), dim3(512), n_local * sizeof(int32_t), s, n_local, n_tiles,
+         local_cap, hist, local_counts, receiver_drops);
   const size_t smem = (static_cast<size_t>(kWarps) * n_local + per) * sizeof(int32_t);
   launch(compact_scatter, dim3(n_tiles), dim3(kThreads), smem, s, n_items, pool_cap, d, n_local,
          local_cap, per, hdr, reinterpret_cast<const uint4*>(pools),
