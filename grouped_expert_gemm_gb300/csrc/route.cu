@@ -165,33 +165,44 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
     }
   }
 
-  // k rounds of warp arg-max over keys built once; lane j keeps the j-th winner.
-  // A taken expert's key is 0, below every live key (a live key's high word is
-  // the orderable score, never 0 for a number or -inf).
-  uint64_t key[VPL];
+  // k rounds of warp arg-max over orderable 32-bit scores built once; lane j keeps
+  // the j-th winner.  A round takes the lane maxima by a tree, the warp maximum,
+  // then the lowest expert index holding it (a lane's experts i*32 + lane grow
+  // with i, so its first slot at the maximum is its lowest): the order is score
+  // descending, ties to the lower expert.  A taken expert's score is 0, below
+  // every live score (the orderable bits of a number or -inf are never 0).
+  uint32_t ob[VPL];
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) key[i] = ((taken >> i) & 1u) ? 0ull : make_key(sel[i], i * 32 + lane);
+  for (int i = 0; i < VPL; ++i) ob[i] = ((taken >> i) & 1u) ? 0u : ord_bits(sel[i]);
   int my_id = 0;
   float my_sel = 0.0f, my_aff = 0.0f, top_sel = 0.0f;
   for (int j = 0; j < k; ++j) {
-    uint64_t local = key[0];
+    uint32_t t[VPL];
 #pragma unroll
-    for (int i = 1; i < VPL; ++i) local = key[i] > local ? key[i] : local;
-    const uint64_t best = warp_max_u64(local);
-    const int e = key_expert(best);
+    for (int i = 0; i < VPL; ++i) t[i] = ob[i];
+#pragma unroll
+    for (int w = 1; w < VPL; w <<= 1)
+#pragma unroll
+      for (int i = 0; i + w < VPL; i += 2 * w) t[i] = max(t[i], t[i + w]);
+    const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, t[0]);
+    uint32_t cand = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = VPL - 1; i >= 0; --i)
+      if (ob[i] == gm) cand = static_cast<uint32_t>(i * 32 + lane);
+    const int e = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
     const int owner = e & 31, slot = e >> 5;
     float a = 0.0f;
     if (lane == owner) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         if (i == slot) {
-          key[i] = 0ull;
+          ob[i] = 0u;
           if (GROUPED) a = aff[i];
         }
       }
     }
     if (GROUPED) a = __shfl_sync(0xFFFFFFFFu, a, owner);
-    const float v = ord_to_float(static_cast<uint32_t>(best >> 32));
+    const float v = ord_to_float(gm);
     if (j == 0) top_sel = v;
     if (lane == j) { my_id = e; my_sel = v; my_aff = a; }
   }
