@@ -326,6 +326,13 @@ def test_grouped_swiglu_many_small_segments():
     _gemm_case(256, 64, 128, counts)
 
 
+def test_grouped_swiglu_max_segments():
+    """1024 segments, the limit: the device segment table (8 segments per thread) and
+    the tile scheduler over many empty and tiny segments."""
+    rng = np.random.default_rng(1024)
+    _gemm_case(1024, 64, 128, rng.integers(0, 4, size=1024), sample=256)
+
+
 def test_grouped_swiglu_bad_segment_is_reported():
     g = G()
     d, I = 64, 128
