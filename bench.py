@@ -18,6 +18,7 @@ import hashlib
 import json
 import os
 import re
+import subprocess
 import statistics
 import sys
 import threading
@@ -929,12 +930,31 @@ def cores():
         return os.cpu_count()
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def run_cpu_baseline(args, w, layer, logits, sel_bias, x):
     hi = host_inputs_of(w, logits, sel_bias, x, layer)
     rng = np.random.default_rng(0)
     toks, dt = cpu_sample_tokens(w, args.cpu_budget, hi, rng)
     return {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": cores(),
-            "kind": "oracle",
+            "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{len(toks)} of {w.T} tokens of {w.name} (routing/admission over all "
                       f"tokens, expert math + combine for the sample), one pass, {dt:.1f} s"}
 
@@ -968,7 +988,7 @@ def run_reference(args, dist, w):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I},
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores(),
-                             "kind": "oracle", "sample": sample},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
