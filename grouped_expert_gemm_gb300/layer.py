@@ -128,6 +128,17 @@ class MoELayer:
                               self.dev_status, stream)
         return self.demand
 
+    def bias_step(self, u: float, rule: int = abi.MOE_BIAS_SIGN, stream=None) -> torch.Tensor:
+        """One step of the loss-free selection-bias controller ([M6.2] 0x06E) after the
+        batch just routed: the demand of this batch, then sel_bias[e] += u * sign(mean - n_e)
+        (or u * (mean - n_e)) in place on the device.  Needs a selection bias (the
+        group-limited sigmoid router's correction term)."""
+        if self.sel_bias is None:
+            raise ValueError("bias_step needs the layer's selection bias (sel_bias)")
+        self.expert_demand(stream)
+        abi.moe_bias_update(self.E, self.demand, self.sel_bias, u, rule, stream)
+        return self.sel_bias
+
     def quantize(self, x, stream=None):
         abi.moe_quantize_fp8(self.T, self.d, self.scale_group, x, self.xq, self.xs,
                              self.dev_status, stream)

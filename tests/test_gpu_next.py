@@ -165,3 +165,29 @@ def test_bias_update_page_fixture():
     b = host(bias)
     assert all(b[e] == np.float32(-0.001) for e in fx["decrease"])
     assert all(b[e] == np.float32(0.001) for e in fx["increase_zero_load"])
+
+
+@pytest.mark.parametrize("rule", [0, 1])
+def test_layer_bias_step_on_v3_routing(rule):
+    """MoELayer.bias_step after a V3-routed batch: the demand of that batch (before the
+    capacity of 1.0) and the controller step on the layer's selection bias, bit-exact."""
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.scaled(workloads.v3(), T=512, d=256, I=256, shared_I=0)
+    logits, sel_bias = workloads.make_router_inputs(w, DEV)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    cap = g.capacity_from_factor(w.capacity_factor, w.R, w.E)
+    layer = g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap,
+                       score_fn=g.MOE_SCORE_SIGMOID_GROUP, n_group=w.n_group,
+                       topk_group=w.topk_group, route_scale=w.route_scale, sel_bias=sel_bias,
+                       device=DEV)
+    b0 = host(sel_bias).copy()
+    layer.route(logits)
+    u = 1e-3 if rule == 0 else 2e-4
+    layer.bias_step(u, rule)
+    torch.cuda.synchronize()
+    ids = host(layer.topk_ids)
+    demand = oracle.expert_demand(ids, w.E)
+    assert host(layer.demand).tolist() == demand.tolist()
+    assert demand.max() > cap  # the capped counts would hide the overload
+    ref = oracle.bias_update(b0, demand, u, "sign" if rule == 0 else "proportional")
+    assert np.array_equal(host(layer.sel_bias).view(np.uint32), ref.view(np.uint32))
