@@ -49,7 +49,8 @@ EXPORTED = [
     "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
     "moe_grouped_swiglu_workspace_size",
     "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
-    "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_compose_map",
+    "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_pool_compact_rotated",
+    "moe_compose_map",
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
     "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
     "moe_payload_bytes", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
@@ -105,6 +106,8 @@ _SIGS = {
     "moe_pool_compact_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "moe_pool_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P,
                                 _P]),
+    "moe_pool_compact_rotated": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                        _SZ, _P, _P]),
     "moe_compose_map": (_I32, [_I64, _P, _P, _I64, _P, _P, _P]),
     "moe_combine_backward": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_grad": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
@@ -130,7 +133,8 @@ _SIGS = {
     "moe_validate_pools": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _P, _P, _P, _P,
                                   _P, _SZ, _P, _P]),
     "moe_validate_compact_workspace_size": (_SZ, [_I32, _I32]),
-    "moe_validate_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_validate_compact": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P,
+                                    _P]),
     "moe_debug_wait_timeout": (_I32, [_I64, _P, _P]),
 }
 
@@ -357,6 +361,16 @@ def moe_pool_compact(n_src, pool_cap, d, n_local, local_cap, pools, compact, loc
     _count(3)
 
 
+def moe_pool_compact_rotated(n_src, pool_cap, d, n_local, local_cap, first_source, pools, compact,
+                             local_counts, poolrow_to_row, receiver_drops, ws, ws_bytes,
+                             dev_status=None, stream=None):
+    _check("moe_pool_compact_rotated", lib().moe_pool_compact_rotated(
+        n_src, pool_cap, d, n_local, local_cap, first_source, _ptr(pools), _ptr(compact),
+        _ptr(local_counts), _ptr(poolrow_to_row), _ptr(receiver_drops), _ptr(ws), ws_bytes,
+        _ptr(dev_status), _stream(stream)))
+    _count(3)
+
+
 def moe_compose_map(n, a, b, b_len, out, dev_status=None, stream=None):
     _check("moe_compose_map", lib().moe_compose_map(n, _ptr(a), _ptr(b), b_len, _ptr(out),
                                                     _ptr(dev_status), _stream(stream)))
@@ -449,9 +463,9 @@ def moe_validate_compact_workspace_size(n_local: int, local_cap: int) -> int:
 
 
 def moe_validate_compact(n_src, pool_cap, d, n_local, local_cap, pools, local_counts,
-                         poolrow_to_row, ws, ws_bytes, dev_status, stream=None):
+                         poolrow_to_row, ws, ws_bytes, dev_status, stream=None, first_source=0):
     _check("moe_validate_compact", lib().moe_validate_compact(
-        n_src, pool_cap, d, n_local, local_cap, _ptr(pools), _ptr(local_counts),
+        n_src, pool_cap, d, n_local, local_cap, first_source, _ptr(pools), _ptr(local_counts),
         _ptr(poolrow_to_row), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
     _count(4)
 

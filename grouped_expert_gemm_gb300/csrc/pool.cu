@@ -245,6 +245,13 @@ pack_scatter(int T, int d, int k, int n_dest, int L, int n_waves, int pool_cap, 
 
 // ------------------------------ receiver ----------------------------------
 
+// Visit position i of the receiver -> pool row (source * pool_cap + row): sources
+// from `first` on (the per-receiver rotation; 0 = fixed source order), rows up.
+__device__ __forceinline__ int64_t visit_to_poolrow(int64_t i, int pool_cap, int n_src, int first) {
+  const int64_t s = i / pool_cap + first;
+  return (s >= n_src ? s - n_src : s) * pool_cap + i % pool_cap;
+}
+
 __device__ __forceinline__ int header_key(const uint16_t* __restrict__ pools_u16, int64_t i,
                                           int pool_cap, int d, int n_local, bool* bad) {
   const int64_t s = i / pool_cap, r = i % pool_cap;
@@ -255,8 +262,8 @@ __device__ __forceinline__ int header_key(const uint16_t* __restrict__ pools_u16
 }
 
 __global__ void __launch_bounds__(kThreads)
-compact_hist(int64_t n_items, int pool_cap, int d, int n_local, int items_per_tile,
-             const uint16_t* __restrict__ pools_u16, int32_t* __restrict__ hist,
+compact_hist(int64_t n_items, int pool_cap, int d, int n_local, int items_per_tile, int n_src,
+             int first, const uint16_t* __restrict__ pools_u16, int32_t* __restrict__ hist,
              uint32_t* __restrict__ dev_status) {
   extern __shared__ int32_t sh[];
   for (int i = threadIdx.x; i < n_local; i += blockDim.x) sh[i] = 0;
@@ -266,7 +273,8 @@ compact_hist(int64_t n_items, int pool_cap, int d, int n_local, int items_per_ti
   const int64_t i1 = min(n_items, i0 + items_per_tile);
   bool bad = false;
   for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    const int l = header_key(pools_u16, i, pool_cap, d, n_local, &bad);
+    const int l = header_key(pools_u16, visit_to_poolrow(i, pool_cap, n_src, first), pool_cap, d,
+                             n_local, &bad);
     if (l >= 0) atomicAdd(&sh[l], 1);
   }
   if (bad) report(dev_status, MOE_DEV_BAD_HEADER_ID);
@@ -297,7 +305,7 @@ compact_scan(int n_local, int n_tiles, int local_cap, int32_t* __restrict__ hist
 
 __global__ void __launch_bounds__(kThreads)
 compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap,
-                int items_per_tile, const uint16_t* __restrict__ pools_u16,
+                int items_per_tile, int n_src, int first, const uint16_t* __restrict__ pools_u16,
                 const uint4* __restrict__ pools, const int32_t* __restrict__ tile_base,
                 uint4* __restrict__ compact, int32_t* __restrict__ poolrow_to_row) {
   pdl_wait();
@@ -314,7 +322,8 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
   __syncthreads();
   bool bad = false;
   for (int64_t i = s0 + lane; i < s1; i += 32) {
-    const int l = header_key(pools_u16, i, pool_cap, d, n_local, &bad);
+    const int l = header_key(pools_u16, visit_to_poolrow(i, pool_cap, n_src, first), pool_cap, d,
+                             n_local, &bad);
     if (l >= 0) atomicAdd(&cnt[w * n_local + l], 1);
   }
   __syncthreads();
@@ -331,8 +340,9 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
   const uint32_t lt = (1u << lane) - 1u;
   for (int64_t c0 = s0; c0 < s1; c0 += 32) {
     const int64_t i = c0 + lane;
+    const int64_t pr = visit_to_poolrow(i, pool_cap, n_src, first);
     int l = -2;
-    if (i < s1) l = header_key(pools_u16, i, pool_cap, d, n_local, &bad);
+    if (i < s1) l = header_key(pools_u16, pr, pool_cap, d, n_local, &bad);
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, l);
     int32_t o = 0;
     if (l >= 0) o = cnt[w * n_local + l] + __popc(peers & lt);
@@ -341,7 +351,7 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
     __syncwarp();
     if (i < s1) {
       const int32_t row = (l >= 0 && o < local_cap) ? l * local_cap + o : -1;
-      poolrow_to_row[i] = row;
+      poolrow_to_row[pr] = row;
       rows[i - i0] = row;
     }
   }
@@ -351,7 +361,8 @@ compact_scatter(int64_t n_items, int pool_cap, int d, int n_local, int local_cap
   for (int64_t i = i0 + w; i < i1; i += kWarps) {
     const int32_t row = rows[i - i0];
     if (row < 0) continue;
-    const int64_t s = i / pool_cap, r = i % pool_cap;
+    const int64_t pr = visit_to_poolrow(i, pool_cap, n_src, first);
+    const int64_t s = pr / pool_cap, r = pr % pool_cap;
     const uint4* src = pools + (s * (pool_cap + 1) + 1 + r) * chunks;
     uint4* dst = compact + static_cast<int64_t>(row) * chunks;
     for (int cb = 0; cb < chunks; cb += 32 * 4) {
@@ -449,12 +460,15 @@ MOE_API size_t moe_pool_compact_workspace_size(int32_t n_src, int32_t pool_cap, 
   return c.off + 256;
 }
 
-MOE_API moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
-                                    int32_t local_cap, const moe_bf16* pools, moe_bf16* compact,
-                                    int32_t* local_counts, int32_t* poolrow_to_row,
-                                    int32_t* receiver_drops, void* ws, size_t ws_bytes,
-                                    uint32_t* dev_status, moe_stream_t stream) {
-  if (n_src <= 0 || pool_cap <= 0 || d <= 0 || n_local <= 0 || local_cap < 0)
+MOE_API moe_status moe_pool_compact_rotated(int32_t n_src, int32_t pool_cap, int32_t d,
+                                            int32_t n_local, int32_t local_cap,
+                                            int32_t first_source, const moe_bf16* pools,
+                                            moe_bf16* compact, int32_t* local_counts,
+                                            int32_t* poolrow_to_row, int32_t* receiver_drops,
+                                            void* ws, size_t ws_bytes, uint32_t* dev_status,
+                                            moe_stream_t stream) {
+  if (n_src <= 0 || pool_cap <= 0 || d <= 0 || n_local <= 0 || local_cap < 0 ||
+      first_source < 0 || first_source >= n_src)
     return MOE_ERR_INVALID_ARG;
   if (d % 8 != 0 || pool_cap > d || n_local > 65534 || n_local > 4096 ||
       static_cast<int64_t>(n_src) * pool_cap >= (int64_t(1) << 31) ||
@@ -473,14 +487,24 @@ MOE_API moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, 
   int32_t* hist = static_cast<int32_t*>(ws);
   const uint16_t* hdr = reinterpret_cast<const uint16_t*>(pools);
   launch(compact_hist, dim3(n_tiles), dim3(kThreads), n_local * sizeof(int32_t), s, n_items,
-         pool_cap, d, n_local, per, hdr, hist, dev_status);
+         pool_cap, d, n_local, per, n_src, first_source, hdr, hist, dev_status);
   launch(compact_scan, dim3(1), dim3(512), n_local * sizeof(int32_t), s, n_local, n_tiles,
          local_cap, hist, local_counts, receiver_drops);
   const size_t smem = (static_cast<size_t>(kWarps) * n_local + per) * sizeof(int32_t);
   launch(compact_scatter, dim3(n_tiles), dim3(kThreads), smem, s, n_items, pool_cap, d, n_local,
-         local_cap, per, hdr, reinterpret_cast<const uint4*>(pools),
+         local_cap, per, n_src, first_source, hdr, reinterpret_cast<const uint4*>(pools),
          static_cast<const int32_t*>(hist), reinterpret_cast<uint4*>(compact), poolrow_to_row);
   return launch_status();
+}
+
+MOE_API moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
+                                    int32_t local_cap, const moe_bf16* pools, moe_bf16* compact,
+                                    int32_t* local_counts, int32_t* poolrow_to_row,
+                                    int32_t* receiver_drops, void* ws, size_t ws_bytes,
+                                    uint32_t* dev_status, moe_stream_t stream) {
+  return moe_pool_compact_rotated(n_src, pool_cap, d, n_local, local_cap, 0, pools, compact,
+                                  local_counts, poolrow_to_row, receiver_drops, ws, ws_bytes,
+                                  dev_status, stream);
 }
 
 MOE_API moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b, int64_t b_len,

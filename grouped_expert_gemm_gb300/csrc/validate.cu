@@ -175,8 +175,15 @@ validate_pack_kernel(int R, int n_dest, int L, int pool_cap, int d,
 
 // ---- pooled layout: receiver compact of one wave ----------------------------
 
+// Visit position of pool row i (source s = i / pool_cap) for a receiver whose
+// visit starts at source `first`: the order in which compact rows are assigned.
+__device__ __forceinline__ int visit_pos(int i, int pool_cap, int n_src, int first) {
+  const int s = i / pool_cap - first;
+  return (s < 0 ? s + n_src : s) * pool_cap + i % pool_cap;
+}
+
 __global__ void __launch_bounds__(kValThreads)
-validate_compact_kernel(int n_src, int pool_cap, int d, int n_local, int local_cap,
+validate_compact_kernel(int n_src, int pool_cap, int d, int n_local, int local_cap, int first,
                         const uint16_t* __restrict__ pools, const int32_t* __restrict__ counts,
                         const int32_t* __restrict__ poolrow_to_row, int32_t* inv,
                         uint32_t* __restrict__ st) {
@@ -193,7 +200,7 @@ validate_compact_kernel(int n_src, int pool_cap, int d, int n_local, int local_c
     const int q = __ldg(poolrow_to_row + i);
     if (q == -1) continue;  // empty, invalid header or receiver drop: checked below
     if (h >= n_local || q < 0 || q / local_cap != h || q % local_cap >= __ldg(counts + h) ||
-        !claim(inv, q, i))
+        !claim(inv, q, visit_pos(i, pool_cap, n_src, first)))
       bad = true;
   }
   flag_if(bad, st);
@@ -201,9 +208,9 @@ validate_compact_kernel(int n_src, int pool_cap, int d, int n_local, int local_c
 }
 
 // A receiver drop (a row with a valid header mapped to -1) needs its expert full
-// with rows that came earlier in (source, row) order.
+// with rows that came earlier in the receiver's visiting order.
 __global__ void __launch_bounds__(kValThreads)
-validate_compact_drops_kernel(int n_src, int pool_cap, int d, int n_local, int local_cap,
+validate_compact_drops_kernel(int n_src, int pool_cap, int d, int n_local, int local_cap, int first,
                               const uint16_t* __restrict__ pools,
                               const int32_t* __restrict__ counts,
                               const int32_t* __restrict__ poolrow_to_row, const int32_t* inv,
@@ -215,7 +222,8 @@ validate_compact_drops_kernel(int n_src, int pool_cap, int d, int n_local, int l
     const uint16_t h = header_at(pools, pool_cap, d, i / pool_cap, i % pool_cap);
     if (h >= n_local || __ldg(poolrow_to_row + i) != -1) continue;
     const int c = __ldg(counts + h);
-    if (c != local_cap || (c > 0 && inv[static_cast<int64_t>(h) * local_cap + c - 1] > i))
+    if (c != local_cap ||
+        (c > 0 && inv[static_cast<int64_t>(h) * local_cap + c - 1] > visit_pos(i, pool_cap, n_src, first)))
       bad = true;
   }
   flag_if(bad, st);
@@ -310,11 +318,12 @@ MOE_API size_t moe_validate_compact_workspace_size(int32_t n_local, int32_t loca
 }
 
 MOE_API moe_status moe_validate_compact(int32_t n_src, int32_t pool_cap, int32_t d,
-                                        int32_t n_local, int32_t local_cap,
+                                        int32_t n_local, int32_t local_cap, int32_t first_source,
                                         const moe_bf16* pools, const int32_t* local_counts,
                                         const int32_t* poolrow_to_row, void* ws, size_t ws_bytes,
                                         uint32_t* dev_status, moe_stream_t stream) {
-  if (n_src <= 0 || pool_cap <= 0 || d <= 0 || n_local <= 0 || local_cap <= 0)
+  if (n_src <= 0 || pool_cap <= 0 || d <= 0 || n_local <= 0 || local_cap <= 0 ||
+      first_source < 0 || first_source >= n_src)
     return MOE_ERR_INVALID_ARG;
   if (pool_cap > d || n_local > 65534 ||
       static_cast<int64_t>(n_src) * pool_cap >= (int64_t(1) << 31) ||
@@ -332,10 +341,10 @@ MOE_API moe_status moe_validate_compact(int32_t n_src, int32_t pool_cap, int32_t
   const uint16_t* pl = reinterpret_cast<const uint16_t*>(pools);
   launch(fill_minus_one, dim3(grid_of(n_targets)), dim3(kValThreads), 0, s, n_targets, inv);
   launch(validate_compact_kernel, dim3(grid_of(n_rows > n_local ? n_rows : n_local)),
-         dim3(kValThreads), 0, s, n_src, pool_cap, d, n_local, local_cap, pl, local_counts,
-         poolrow_to_row, inv, dev_status);
+         dim3(kValThreads), 0, s, n_src, pool_cap, d, n_local, local_cap, first_source, pl,
+         local_counts, poolrow_to_row, inv, dev_status);
   launch(validate_compact_drops_kernel, dim3(grid_of(n_rows)), dim3(kValThreads), 0, s, n_src,
-         pool_cap, d, n_local, local_cap, pl, local_counts, poolrow_to_row,
+         pool_cap, d, n_local, local_cap, first_source, pl, local_counts, poolrow_to_row,
          static_cast<const int32_t*>(inv), dev_status);
   launch(validate_targets_kernel, dim3(grid_of(n_targets)), dim3(kValThreads), 0, s, n_targets,
          local_cap, local_counts, static_cast<const int32_t*>(inv), dev_status);

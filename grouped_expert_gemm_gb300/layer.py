@@ -257,11 +257,14 @@ class PooledMoELayer:
 
     def __init__(self, T: int, d: int, k: int, I: int, n_dest: int, local_per_dest: int,
                  n_waves: int, pool_cap: int, local_cap: int, w_gate, w_up, w_down,
-                 wave_policy: int = abi.MOE_WAVE_STRIPE, device="cuda"):
+                 wave_policy: int = abi.MOE_WAVE_STRIPE, first_source: int = 0, device="cuda"):
         self.T, self.d, self.k, self.I = T, d, k, I
         self.E = n_dest * local_per_dest
         self.n_dest, self.L, self.n_waves = n_dest, local_per_dest, n_waves
         self.pool_cap, self.local_cap = pool_cap, local_cap
+        # the receiver's first source pool (0: fixed source order; r: the per-receiver
+        # rotation, so overflow does not always fall on the same last sources)
+        self.first_source = first_source
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
         self.params = abi.RouteParams(T, self.E, k, abi.MOE_SCORE_SOFTMAX, 1, 1, 1.0)
         self.pool_params = abi.PoolParams(n_dest, local_per_dest, n_waves, pool_cap, wave_policy)
@@ -309,10 +312,11 @@ class PooledMoELayer:
                           self.dev_status, stream)
 
     def compact_wave(self, wave, stream=None):
-        abi.moe_pool_compact(self.n_dest, self.pool_cap, self.d, self.L, self.local_cap,
-                             self.pools, self.compact, self.local_counts, self.poolrow_to_row,
-                             self.receiver_drops[wave:wave + 1], self.compact_ws,
-                             self.compact_ws_bytes, self.dev_status, stream)
+        abi.moe_pool_compact_rotated(self.n_dest, self.pool_cap, self.d, self.L, self.local_cap,
+                                     self.first_source, self.pools, self.compact,
+                                     self.local_counts, self.poolrow_to_row,
+                                     self.receiver_drops[wave:wave + 1], self.compact_ws,
+                                     self.compact_ws_bytes, self.dev_status, stream)
 
     def experts(self, stream=None):
         abi.moe_grouped_swiglu(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,

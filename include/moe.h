@@ -304,6 +304,19 @@ moe_status moe_pool_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t 
                             int32_t* receiver_drops, void* ws, size_t ws_bytes,
                             uint32_t* dev_status, moe_stream_t stream);
 
+/* moe_pool_compact with a per-receiver rotation of the source order ([POOL] 07
+ * names it as a proposal, so that overflow does not always fall on the same
+ * last sources): sources are visited first_source, first_source + 1, ...,
+ * n_src - 1, 0, ..., first_source - 1, each from row 0 up; 0 <= first_source
+ * < n_src.  poolrow_to_row stays indexed by source * pool_cap + row.
+ * first_source = 0 is moe_pool_compact.                                     */
+moe_status moe_pool_compact_rotated(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
+                                    int32_t local_cap, int32_t first_source,
+                                    const moe_bf16* pools, moe_bf16* compact,
+                                    int32_t* local_counts, int32_t* poolrow_to_row,
+                                    int32_t* receiver_drops, void* ws, size_t ws_bytes,
+                                    uint32_t* dev_status, moe_stream_t stream);
+
 /* out[i] = a[i] < 0 ? -1 : b[a[i]] for i < n (route -> pool row -> compact row;
  * the inverse composition of [M6.6] 0x03C3).  Entries a[i] >= b_len set
  * MOE_DEV_BAD_ROW and give -1.                                               */
@@ -506,12 +519,14 @@ moe_status moe_expert_demand(int32_t T, int32_t k, int32_t E, const int32_t* val
  * filled row is pointed at by exactly one route (conservation of placed rows).
  * Workspace: moe_validate_pools_workspace_size(p) bytes.
  *
- * moe_validate_compact -- after moe_pool_compact of one wave.  [POOL] 03, 05:
- * 0 <= local_counts[l] <= local_cap; a pool row whose header id l < n_local
- * maps to -1 (a receiver drop) or to l*local_cap + slot with slot <
- * local_counts[l]; every other pool row maps to -1; every compact row below its
- * expert's count is the image of exactly one pool row; receiver drops happen
- * only to experts that are full.  Workspace:
+ * moe_validate_compact -- after moe_pool_compact(_rotated) of one wave with the
+ * same first_source (0 for moe_pool_compact).  [POOL] 03, 05: 0 <=
+ * local_counts[l] <= local_cap; a pool row whose header id l < n_local maps to
+ * -1 (a receiver drop) or to l*local_cap + slot with slot < local_counts[l];
+ * every other pool row maps to -1; every compact row below its expert's count
+ * is the image of exactly one pool row, slots in the receiver's visiting order;
+ * receiver drops happen only to experts that are full of rows visited earlier.
+ * Workspace:
  * moe_validate_compact_workspace_size(n_local, local_cap) bytes.
  *
  * Limits as the calls they check.                                           */
@@ -528,7 +543,7 @@ moe_status moe_validate_pools(const moe_pool_params* p, int32_t T, int32_t d, in
                               size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
 size_t moe_validate_compact_workspace_size(int32_t n_local, int32_t local_cap);
 moe_status moe_validate_compact(int32_t n_src, int32_t pool_cap, int32_t d, int32_t n_local,
-                                int32_t local_cap, const moe_bf16* pools,
+                                int32_t local_cap, int32_t first_source, const moe_bf16* pools,
                                 const int32_t* local_counts, const int32_t* poolrow_to_row,
                                 void* ws, size_t ws_bytes, uint32_t* dev_status,
                                 moe_stream_t stream);

@@ -404,7 +404,8 @@ def pool_pack(ids: np.ndarray, x_bits: np.ndarray, n_dest: int, local_per_dest: 
                 sender_drops=int((in_wave & ~placed).sum()), in_wave=in_wave)
 
 
-def pool_compact(pools: np.ndarray, pool_cap: int, n_local: int, local_cap: int):
+def pool_compact(pools: np.ndarray, pool_cap: int, n_local: int, local_cap: int,
+                 first_source: int = 0):
     """Receiver side of one wave: group pooled rows into fixed per-local-expert arrays.
 
     Rows are visited in fixed source order (source pool ascending, then row);
@@ -412,12 +413,24 @@ def pool_compact(pools: np.ndarray, pool_cap: int, n_local: int, local_cap: int)
     receiver drop once that expert already holds local_cap rows.  Header ids
     that are neither < n_local nor EMPTY_HEADER are invalid and skipped.
 
+    first_source > 0 is the per-receiver rotation [POOL] 07 mentions as a proposal
+    (so overflow does not always fall on the same last sources).  Reading: the
+    receiver visits sources first_source, first_source + 1, ..., n_src - 1, 0, ...,
+    first_source - 1, each from row 0 up.
+
     Returns dict(compact uint16 [n_local, local_cap, d] (unfilled rows zero, not
     part of the contract), local_counts [n_local], poolrow_to_row int64
-    [n_src*pool_cap] (l*local_cap + slot or -1), receiver_drops, bad_headers).
+    [n_src*pool_cap] (l*local_cap + slot or -1, indexed by source*pool_cap + row),
+    receiver_drops, bad_headers).
     """
     n_src, _, d = pools.shape
-    hdr = pools[:, 0, :pool_cap].astype(np.int64).reshape(-1)  # [n_src*pool_cap], src-major
+    if not 0 <= first_source < n_src:
+        raise ValueError("first_source out of range")
+    # visit position -> pool row (source * pool_cap + row)
+    visit = (np.arange(n_src * pool_cap) // pool_cap + first_source) % n_src * pool_cap \
+        + np.arange(n_src * pool_cap) % pool_cap
+    flat = pools[:, 0, :pool_cap].astype(np.int64).reshape(-1)  # [n_src*pool_cap], src-major
+    hdr = flat[visit]                                               # in visit order
     valid = hdr < n_local
     bad = int(((hdr != EMPTY_HEADER) & ~valid).sum())
     ordinal = np.full(hdr.size, -1, dtype=np.int64)
@@ -431,10 +444,10 @@ def pool_compact(pools: np.ndarray, pool_cap: int, n_local: int, local_cap: int)
     ordinal[vi] = ov
     keep = valid & (ordinal < local_cap) & (ordinal >= 0)
     poolrow_to_row = np.full(hdr.size, -1, dtype=np.int64)
-    poolrow_to_row[keep] = hdr[keep] * local_cap + ordinal[keep]
+    poolrow_to_row[visit[keep]] = hdr[keep] * local_cap + ordinal[keep]
     compact = np.zeros((n_local, local_cap, d), dtype=np.uint16)
     ki = np.nonzero(keep)[0]
-    src, r = ki // pool_cap, ki % pool_cap
+    src, r = visit[ki] // pool_cap, visit[ki] % pool_cap
     compact[hdr[ki], ordinal[ki]] = pools[src, 1 + r]
     counts = np.minimum(np.bincount(hdr[vi], minlength=n_local), local_cap)
     return dict(compact=compact, local_counts=counts, poolrow_to_row=poolrow_to_row,
@@ -578,17 +591,22 @@ def pool_violations(ids, n_dest: int, local_per_dest: int, pool_cap: int, header
 
 
 def compact_violations(headers, pool_cap: int, n_local: int, local_cap: int, local_counts,
-                       poolrow_to_row) -> list:
+                       poolrow_to_row, first_source: int = 0) -> list:
     """Invariants of one wave's receiver compact; headers is [n_src, >= pool_cap].
 
     Checked: 0 <= count <= local_cap; a pool row with a valid header l maps to
     -1 or to a slot of l below its count, any other row to -1; every slot below
-    a count is the image of exactly one pool row and images keep (source, row)
-    order; a receiver drop's expert is full with rows that came earlier.
+    a count is the image of exactly one pool row and images keep the visiting
+    order (sources from first_source on, rows ascending); a receiver drop's
+    expert is full with rows that came earlier.
     """
-    hdr = np.asarray(headers)[:, :pool_cap].astype(np.int64).reshape(-1)
+    n_src = np.asarray(headers).shape[0]
+    visit = (np.arange(n_src * pool_cap) // pool_cap + first_source) % n_src * pool_cap \
+        + np.arange(n_src * pool_cap) % pool_cap
+    flat_hdr = np.asarray(headers)[:, :pool_cap].astype(np.int64).reshape(-1)
+    hdr = flat_hdr[visit]                              # in visit order
     cnt = [int(v) for v in local_counts]
-    q_of = [int(v) for v in poolrow_to_row]
+    q_of = [int(v) for v in np.asarray(poolrow_to_row)[visit]]
     bad = set()
     for l in range(n_local):
         if not 0 <= cnt[l] <= local_cap:

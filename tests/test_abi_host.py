@@ -103,10 +103,14 @@ def test_host_validation_rejects_before_launch(lib):
                                   None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
     assert lib.moe_validate_pools(abi.PoolParams(4, 2, 3, 100, 0), 4, 64, 2, 16, 16, 16, 16, 16,
                                   1 << 20, 16, None) == abi.MOE_ERR_UNSUPPORTED
-    assert lib.moe_validate_compact(4, 8, 64, 2, 10, 16, 16, 16, 16, 79, 16,
+    assert lib.moe_validate_compact(4, 8, 64, 2, 10, 0, 16, 16, 16, 16, 79, 16,
                                     None) == abi.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert lib.moe_validate_compact(4, 100, 64, 2, 10, 16, 16, 16, 16, 1 << 20, 16,
+    assert lib.moe_validate_compact(4, 100, 64, 2, 10, 0, 16, 16, 16, 16, 1 << 20, 16,
                                     None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_validate_compact(4, 8, 64, 2, 10, 4, 16, 16, 16, 16, 1 << 20, 16,
+                                    None) == abi.MOE_ERR_INVALID_ARG  # first_source >= n_src
+    assert lib.moe_pool_compact_rotated(4, 8, 64, 2, 10, -1, 16, 16, 16, 16, 16, 16, 1 << 20,
+                                        None, None) == abi.MOE_ERR_INVALID_ARG
     # the wait self-test: limit outside (0, 1 s], missing status word
     assert lib.moe_debug_wait_timeout(0, 16, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_wait_timeout(2000000000, 16, None) == abi.MOE_ERR_INVALID_ARG

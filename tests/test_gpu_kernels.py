@@ -519,6 +519,48 @@ def test_pool_pack_compact_parity(policy, T, d, k, n_dest, L, n_waves, pool_cap,
     _pool_case(T, d, k, n_dest, L, n_waves, pool_cap, local_cap, policy)
 
 
+@pytest.mark.parametrize("first", [1, 5, 7])
+def test_pool_compact_rotated_parity(first):
+    """The per-receiver rotation of the source order: same maps, counts and drops as the
+    oracle visiting sources from `first` on; the overflow falls on other sources."""
+    g = G()
+    T, d, k, n_dest, L, pool_cap, local_cap = 600, 64, 4, 8, 3, 40, 40
+    rng = np.random.default_rng(first)
+    E = n_dest * L
+    p = rng.dirichlet(np.ones(E) * 0.5)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    x = torch.randn((T, d), device=DEV).to(torch.bfloat16)
+    pp = g.PoolParams(n_dest, L, 1, pool_cap, g.MOE_WAVE_STRIPE)
+    pools = torch.zeros((n_dest, pool_cap + 1, d), dtype=torch.bfloat16, device=DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    r2p, fill, sdrop = torch.empty(T * k, **i32), torch.empty(n_dest, **i32), torch.zeros(1, **i32)
+    pwsb = g.moe_pool_pack_workspace_size(pp, T, k)
+    pws = torch.empty(pwsb, dtype=torch.uint8, device=DEV)
+    st = status0()
+    g.moe_pool_pack(pp, T, d, k, 0, torch.from_numpy(ids_np).to(DEV), x, pools, r2p, fill, sdrop,
+                    pws, pwsb, st)
+    compact = torch.zeros((L * local_cap, d), dtype=torch.bfloat16, device=DEV)
+    lcounts, p2r, rdrop = torch.empty(L, **i32), torch.empty(n_dest * pool_cap, **i32), torch.zeros(1, **i32)
+    cwsb = g.moe_pool_compact_workspace_size(n_dest, pool_cap, L)
+    cws = torch.empty(cwsb, dtype=torch.uint8, device=DEV)
+    g.moe_pool_compact_rotated(n_dest, pool_cap, d, L, local_cap, first, pools, compact, lcounts,
+                               p2r, rdrop, cws, cwsb, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    pb = bits(pools)
+    rc = oracle.pool_compact(pb, pool_cap, L, local_cap, first)
+    assert rc["receiver_drops"] > 0  # the case overflows
+    assert np.array_equal(host(p2r), rc["poolrow_to_row"])
+    assert np.array_equal(host(lcounts), rc["local_counts"])
+    assert int(rdrop.item()) == rc["receiver_drops"]
+    cb = bits(compact).reshape(L, local_cap, d)
+    for l in range(L):
+        c = int(rc["local_counts"][l])
+        assert np.array_equal(cb[l, :c], rc["compact"][l, :c])
+    base = oracle.pool_compact(pb, pool_cap, L, local_cap)
+    assert not np.array_equal(base["poolrow_to_row"], rc["poolrow_to_row"])
+
+
 def test_pool_compact_bad_header_is_reported():
     g = G()
     d, cap = 16, 4

@@ -279,3 +279,40 @@ def test_bounded_wait_gives_up_with_timeout_status_and_context_survives():
     rng = np.random.default_rng(0)
     m = _permute(64, 64, 8, 2, -1, _skewed_ids(rng, 64, 8, 2))
     assert _validate_perm(64, 8, 2, -1, None, m) == 0
+
+
+def test_compact_validator_follows_the_rotation():
+    """The compact validator checks slots in the receiver's visiting order: it passes the
+    rotated compact's maps with the same first source and flags them read in fixed
+    source order, as the oracle's checks do."""
+    g = G()
+    rng = np.random.default_rng(5)
+    n_src, pool_cap, d, L, local_cap = 6, 16, 64, 2, 12
+    pools = torch.zeros((n_src, pool_cap + 1, d), dtype=torch.bfloat16, device=DEV)
+    hdr = np.full((n_src, d), 0xFFFF, np.int64)
+    for s_ in range(n_src):
+        f = int(rng.integers(4, pool_cap + 1))
+        hdr[s_, :f] = rng.integers(0, L, f)
+    pools.view(torch.int16)[:, 0, :] = torch.from_numpy(hdr.astype(np.uint16).view(np.int16)).to(DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    compact = torch.zeros((L * local_cap, d), dtype=torch.bfloat16, device=DEV)
+    lcounts, p2r, rdrop = torch.empty(L, **i32), torch.empty(n_src * pool_cap, **i32), torch.zeros(1, **i32)
+    cwsb = g.moe_pool_compact_workspace_size(n_src, pool_cap, L)
+    cws = torch.empty(cwsb, dtype=torch.uint8, device=DEV)
+    vcb = g.moe_validate_compact_workspace_size(L, local_cap)
+    vc = torch.empty(vcb, dtype=torch.uint8, device=DEV)
+    first = 3
+    st = status0()
+    g.moe_pool_compact_rotated(n_src, pool_cap, d, L, local_cap, first, pools, compact, lcounts,
+                               p2r, rdrop, cws, cwsb, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for f_check in (first, 0):
+        ora = oracle.compact_violations(hdr, pool_cap, L, local_cap, host(lcounts), host(p2r),
+                                        f_check)
+        st = status0()
+        g.moe_validate_compact(n_src, pool_cap, d, L, local_cap, pools, lcounts, p2r, vc, vcb,
+                               st, first_source=f_check)
+        torch.cuda.synchronize()
+        assert (ora == []) == (int(st.item()) == 0), (f_check, ora)
+        assert (ora == []) == (f_check == first)

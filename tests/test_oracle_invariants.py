@@ -178,6 +178,25 @@ def test_pool_checks_accept_valid_and_flag_mutations(policy):
             "slot order swap"} <= seen_c
 
 
+def test_compact_checks_follow_the_receiver_rotation():
+    rng = np.random.default_rng(71)
+    n_dest, L, cap, lcap = 5, 2, 6, 4
+    pools = np.zeros((n_dest, cap + 1, 8), np.uint16)
+    pools[:, 0, :] = oracle.EMPTY_HEADER
+    for D in range(n_dest):
+        f = int(rng.integers(2, cap + 1))
+        pools[D, 0, :f] = rng.integers(0, L, f)
+    hdr = pools[:, 0, :]
+    for first in range(n_dest):
+        cp = oracle.pool_compact(pools, cap, L, lcap, first)
+        assert oracle.compact_violations(hdr, cap, L, lcap, cp["local_counts"],
+                                         cp["poolrow_to_row"], first) == []
+        if first:
+            # the same maps read with the fixed source order break the order checks
+            assert oracle.compact_violations(hdr, cap, L, lcap, cp["local_counts"],
+                                             cp["poolrow_to_row"], 0) != []
+
+
 def test_pool_checks_accept_the_oracle_layout():
     rng = np.random.default_rng(61)
     n_dest, L, n_waves, cap, lcap, T, k, d = 4, 3, 3, 5, 6, 40, 3, 8

@@ -512,6 +512,52 @@ def test_pool_pack_compact_brute_force(policy):
         assert total_s + total_r + total_acc == T * k
 
 
+def _py_compact_rotated(hdr, cap, n_local, local_cap, first):
+    """Brute force of the rotated visit: sources first, first+1, ..., wrapping."""
+    n_src = len(hdr)
+    cnt = [0] * n_local
+    out = [-1] * (n_src * cap)
+    drops = 0
+    for j in range(n_src):
+        s_ = (first + j) % n_src
+        for r in range(cap):
+            l = hdr[s_][r]
+            if l >= n_local:
+                continue
+            if cnt[l] < local_cap:
+                out[s_ * cap + r] = l * local_cap + cnt[l]
+            else:
+                drops += 1
+            cnt[l] += 1
+    return out, [min(c, local_cap) for c in cnt], drops
+
+
+def test_pool_compact_rotation_brute_force():
+    """[POOL] 07's proposed per-receiver rotation: the overflow falls on the sources
+    visited last, whichever they are."""
+    rng = np.random.default_rng(12)
+    for _ in range(40):
+        n_src, cap, n_local = int(rng.integers(1, 6)), int(rng.integers(1, 5)), int(rng.integers(1, 4))
+        lcap = int(rng.integers(1, 5))
+        pools = np.zeros((n_src, cap + 1, 4), np.uint16)
+        pools[:, 0, :] = 0xFFFF
+        for s_ in range(n_src):
+            fill = int(rng.integers(0, cap + 1))
+            pools[s_, 0, :fill] = rng.integers(0, n_local, fill)
+        hdr = pools[:, 0, :cap].tolist()
+        for first in range(n_src):
+            cp = oracle.pool_compact(pools, cap, n_local, lcap, first)
+            p2r, counts, drops = _py_compact_rotated(hdr, cap, n_local, lcap, first)
+            assert cp["poolrow_to_row"].tolist() == p2r
+            assert cp["local_counts"].tolist() == counts
+            assert cp["receiver_drops"] == drops
+        # no rotation is the fixed source order
+        base = oracle.pool_compact(pools, cap, n_local, lcap)
+        assert base["poolrow_to_row"].tolist() == _py_compact(hdr, cap, n_local, lcap)[0]
+    with pytest.raises(ValueError):
+        oracle.pool_compact(np.zeros((2, 3, 4), np.uint16), 2, 1, 1, 2)
+
+
 def test_pool_compact_skips_invalid_header_ids():
     pools = np.zeros((2, 4, 3), np.uint16)
     pools[:, 0, :] = 0xFFFF
