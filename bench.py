@@ -450,6 +450,7 @@ def run_ours(args, dist, w):
     if flush_l2:  # the steps' own spans, without the flushes between them
         elapsed_ms = sum(a.elapsed_time(b) for a, b in spans)
     max_ms = dist.max(elapsed_ms)
+    quantiles = step_quantiles(spans if flush_l2 else None, stages, stream, steps, use_graph)
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after timed steps")
 
@@ -537,6 +538,7 @@ def run_ours(args, dist, w):
                    if flush_l2 else
                    "eager launches with CUDA events between the stages of every timed step"),
         "clocks": sampler.summary(),
+        "step_ms_quantiles": quantiles,
         "gpu_launches": int(launches),
     }
     if not args.no_e2e:
@@ -546,6 +548,41 @@ def run_ours(args, dist, w):
         result["extras"] = run_extras(args, w, layer, stream, steps, x)
     result["routing"] = routing_report(w, layer, stream)
     return result, layer, logits, sel_bias, x
+
+
+def nearest_rank(xs, q):
+    """The nearest-rank q-quantile: the ceil(q n)-th smallest of n values."""
+    xs = sorted(xs)
+    return xs[max(0, min(len(xs) - 1, int(np.ceil(q * len(xs))) - 1))]
+
+
+def step_quantiles(spans, stages, stream, steps, use_graph):
+    """Nearest-rank p50 / p90 of single steps, beside the K-step mean `value`: the spans
+    of the timed steps when they were timed one by one (L2 flushed), else K more steps
+    replayed one at a time from a one-step graph (or launched eagerly) with events at
+    each step's start and end only."""
+    if spans is None:
+        spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)]
+        g1 = None
+        if use_graph:
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream):
+                for _, fn, _ in stages:
+                    fn(None)
+        with torch.cuda.stream(stream):
+            for a, b in spans:
+                a.record(stream)
+                if g1 is not None:
+                    g1.replay()
+                else:
+                    for _, fn, _ in stages:
+                        fn(stream)
+                b.record(stream)
+        stream.synchronize()
+    ms = [a.elapsed_time(b) for a, b in spans]
+    return {"p50": round(nearest_rank(ms, 0.5), 5), "p90": round(nearest_rank(ms, 0.9), 5),
+            "n": len(ms), "note": "single-step spans; nearest-rank quantiles"}
 
 
 def routing_report(w, layer, stream):

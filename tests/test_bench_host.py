@@ -64,3 +64,11 @@ def test_committed_traffic_lines_are_read_only_for_the_current_source():
     line = bench.lookup_traffic("gate_up", "decode_T128")
     # the profiles committed with this source carry the gate/up pass's DRAM bytes
     assert line is None or 7e8 < line < 9e8
+
+
+def test_nearest_rank_quantiles():
+    """Q_q = x_(ceil(q n)): the smallest value with at least q n values at or below it."""
+    assert bench.nearest_rank([5, 1, 3, 2, 4], 0.5) == 3
+    assert bench.nearest_rank([1, 2, 3, 4], 0.5) == 2
+    assert bench.nearest_rank(list(range(1, 11)), 0.9) == 9
+    assert bench.nearest_rank([7.0], 0.9) == 7.0
