@@ -59,6 +59,9 @@ def parse_args():
                     help="time eager launches instead of CUDA-graph replays of the step")
     ap.add_argument("--payload", default="bf16", choices=["bf16", "fp8_row", "fp8_block128"],
                     help="dispatch payload of the expert input rows (not for --config pooled)")
+    ap.add_argument("--fp8-loader", default="auto", choices=["auto", "fused", "dequantize"],
+                    help="FP8 payload: dequantize in the gate/up loader ('fused'), once into bf16 "
+                         "rows before the bf16 pass ('dequantize'), or by rows per expert ('auto')")
     ap.add_argument("--gather", action="store_true",
                     help="bf16 payload: permute the maps only and gather the expert rows in the "
                          "gate/up loader instead of copying them in the permute")
@@ -277,7 +280,7 @@ def lookup_traffic(stage, workload_name):
 # our arm
 # ----------------------------------------------------------------------------
 
-def build_layer(w, device, payload="bf16", gather=False):
+def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto"):
     import grouped_expert_gemm_gb300 as g
     if w.pooled and payload != "bf16":
         raise SystemExit("--payload applies to the routed (non-pooled) workloads")
@@ -295,7 +298,8 @@ def build_layer(w, device, payload="bf16", gather=False):
         layer = g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                            n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                            sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
-                           payload=payload, gather=gather, device=device)
+                           payload=payload, gather=gather, fp8_loader=fp8_loader,
+                           device=device)
     return layer, logits, sel_bias, x
 
 
@@ -321,7 +325,8 @@ def run_ours(args, dist, w):
     device = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
-    layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather)
+    layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather,
+                                             args.fp8_loader)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _, _ in stages]

@@ -48,7 +48,7 @@ class MoELayer:
                  capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
                  topk_group: int = 1, route_scale: float = 1.0, sel_bias=None,
                  shared_weights=None, payload: str = "bf16", gather: bool = False,
-                 device="cuda"):
+                 fp8_loader: str = "auto", device="cuda"):
         self.T, self.d, self.E, self.k, self.I = T, d, E, k, I
         if payload not in PAYLOADS:
             raise ValueError(f"payload must be one of {sorted(PAYLOADS)}")
@@ -63,12 +63,15 @@ class MoELayer:
         i32 = dict(dtype=torch.int32, device=dev)
         self.topk_ids = torch.empty((T, k), **i32)
         self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
-        # FP8 payload: where experts hold many rows each (>= 128 on average, the
-        # tensor-bound shapes) the permuted rows are dequantized once into bf16 and
-        # the bf16 pass runs -- the fused loader would convert every row block once
-        # per output-column block (measured 1.5x slower on prefill); with few rows per
-        # expert the gate/up pass dequantizes in its loader.  Both give the same bits.
-        self.fused_fp8 = payload != "bf16" and R < 128 * E
+        # FP8 payload: by default ("auto") the permuted E4M3 rows are dequantized once
+        # into bf16 and the bf16 pass runs.  The gate/up pass can instead dequantize in
+        # its loader ("fused"): the bf16 rows then never exist in HBM, but it converts
+        # every row block once per output-column block (1.5x slower on prefill) and its
+        # tensor-memory A slots leave room for one accumulator buffer only (2-6 %
+        # slower on decode, T = 8..128).  Both give the same bits.
+        if fp8_loader not in ("auto", "fused", "dequantize"):
+            raise ValueError("fp8_loader must be 'auto', 'fused' or 'dequantize'")
+        self.fused_fp8 = payload != "bf16" and fp8_loader == "fused"
         # bf16 payload, gather=True: the permute writes the maps only and the gate/up
         # pass gathers each expert row from token order (moe_grouped_gate_up_gather).
         # Off by default: one TMA gather moves four 128-byte rows, and at that

@@ -25,26 +25,27 @@ def built():
     build.build()
 
 
-def make_layer(w, wg, wu, wd, sel_bias=None, shared=None, payload="bf16", gather=False):
+def make_layer(w, wg, wu, wd, sel_bias=None, shared=None, payload="bf16", gather=False,
+               fp8_loader="auto"):
     import grouped_expert_gemm_gb300 as g
     cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
     score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
     return g.MoELayer(w.T, w.d, w.E, w.k, w.I, wg, wu, wd, capacity=cap, score_fn=score,
                       n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                       sel_bias=sel_bias, shared_weights=shared, payload=payload, gather=gather,
-                      device=DEV)
+                      fp8_loader=fp8_loader, device=DEV)
 
 
 SCALE_GROUP = {"fp8_row": 0, "fp8_block128": 128}
 
 
 def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, payload="bf16",
-                  gather=False):
+                  gather=False, fp8_loader="auto"):
     logits, sel_bias = workloads.make_router_inputs(w, DEV)
     x = workloads.make_activations(w, DEV)
     wg, wu, wd = weights if weights is not None else workloads.make_expert_weights(w, DEV)
     shared = workloads.make_shared_weights(w, DEV)
-    layer = make_layer(w, wg, wu, wd, sel_bias, shared, payload, gather)
+    layer = make_layer(w, wg, wu, wd, sel_bias, shared, payload, gather, fp8_loader)
     out = layer.forward(logits, x)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
@@ -165,6 +166,20 @@ def test_tiny_full_fp8(payload):
 @pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
 def test_decode_T128_full_fp8(payload, decode_weights):
     run_and_check(workloads.decode(128), weights=decode_weights, sample_rows=4096, payload=payload)
+
+
+@pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
+def test_decode_T128_full_fp8_fused_loader(payload, decode_weights):
+    """The gate/up pass dequantizing E4M3 tiles in its loader, in the layer."""
+    layer, _ = run_and_check(workloads.decode(128), weights=decode_weights, sample_rows=4096,
+                             payload=payload, fp8_loader="fused")
+    assert layer.fused_fp8
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_fp8_fused_loader_small(T, decode_weights):
+    run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096,
+                  payload="fp8_block128", fp8_loader="fused")
 
 
 @pytest.mark.parametrize("payload", ["fp8_row", "fp8_block128"])
