@@ -25,8 +25,8 @@ __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(int T, int k, int chunks, int parts, const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ route_to_row, const float* __restrict__ gates,
                const uint4* __restrict__ shared_y, int accumulate, float4* __restrict__ out,
-               uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid) {
-  pdl_wait();
+               uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid, bool early) {
+  pdl_wait_then_trigger(early);
   constexpr int UNROLL = KMAX >= 8 ? 1 : (KMAX >= 4 ? 2 : 4);
   __shared__ int32_t s_row[KMAX];
   __shared__ float s_gate[KMAX];
@@ -108,7 +108,7 @@ combine_kernel(int T, int k, int chunks, int parts, const uint4* __restrict__ y,
     }
     __syncthreads();
   }
-  pdl_trigger();
+  if (!early) pdl_trigger();
 }
 
 }  // namespace
@@ -175,7 +175,7 @@ static moe_status combine_impl(int32_t T, int32_t k, int32_t d, const moe_bf16* 
   launch(combine_kernel<K>, dim3(grid), dim3(kCombThreads), 0, s, T, k, chunks, parts,        \
          reinterpret_cast<const uint4*>(y), y_rows, route_to_row, gates,                      \
          reinterpret_cast<const uint4*>(shared_y), static_cast<int>(accumulate),              \
-         reinterpret_cast<float4*>(out), dev_status, valid)
+         reinterpret_cast<float4*>(out), dev_status, valid, one_wave(grid))
   if (k <= 1) MOE_COMBINE_CASE(1);
   else if (k <= 2) MOE_COMBINE_CASE(2);
   else if (k <= 4) MOE_COMBINE_CASE(4);

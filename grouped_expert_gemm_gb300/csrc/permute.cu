@@ -58,10 +58,10 @@ PermTiling permute_tiling(int64_t R) {
 __global__ void __launch_bounds__(kHistThreads)
 permute_hist(int R, int E, int k, int routes_per_tile, const int32_t* __restrict__ ids,
              int32_t* __restrict__ hist, uint32_t* __restrict__ dev_status,
-             const int32_t* __restrict__ valid) {
+             const int32_t* __restrict__ valid, bool early) {
   extern __shared__ int32_t sh[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
-  pdl_wait();
+  pdl_wait_then_trigger(early);
   __syncthreads();
   const int R_live = valid_routes(R, k, valid);
   const int r0 = blockIdx.x * routes_per_tile;
@@ -75,7 +75,7 @@ permute_hist(int R, int E, int k, int routes_per_tile, const int32_t* __restrict
   __syncthreads();
   int32_t* out = hist + static_cast<int64_t>(blockIdx.x) * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = sh[e];
-  pdl_trigger();
+  if (!early) pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kRankThreads)
@@ -84,7 +84,7 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ n_dropped, int32_t* __restrict__ row_to_route,
              int32_t* __restrict__ route_to_row, uint32_t* __restrict__ dev_status,
-             const int32_t* __restrict__ valid) {
+             const int32_t* __restrict__ valid, bool early) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kRankWarps][E]
   int32_t* off = cnt + kRankWarps * E;  // [E]
@@ -93,7 +93,7 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
   const int tile = blockIdx.x;
 
   for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
-  pdl_wait();
+  pdl_wait_then_trigger(early);
   __syncthreads();
   // Routes at or past R_live belong to masked padding tokens of a fixed bucket:
   // they are neither counted, admitted nor dropped, and map to row -1.
@@ -195,7 +195,7 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
       route_to_row[r] = row;
     }
   }
-  pdl_trigger();
+  if (!early) pdl_trigger();
 }
 
 // One warp per (token, column part): read the part of the row once, store it to
@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 permute_copy(int T, int k, int chunks, int parts, const int32_t* __restrict__ route_to_row,
              const uint4* __restrict__ x, uint4* __restrict__ x_perm,
              const int32_t* __restrict__ valid, int G, const float* __restrict__ scales,
-             float* __restrict__ scales_perm) {
-  pdl_wait();
+             float* __restrict__ scales_perm, bool early) {
+  pdl_wait_then_trigger(early);
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int T_live = valid_routes(T, 1, valid);
@@ -248,7 +248,7 @@ permute_copy(int T, int k, int chunks, int parts, const int32_t* __restrict__ ro
       }
     }
   }
-  pdl_trigger();
+  if (!early) pdl_trigger();
 }
 
 }  // namespace
@@ -295,16 +295,16 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
     // No routes: one rank block with no tiles writes empty counts and offsets.
     launch(permute_rank, dim3(1), dim3(kRankThreads), rank_smem, s, 0, E, k, 1, 0, capacity,
            topk_ids, static_cast<const int32_t*>(nullptr), counts, offsets, n_dropped,
-           row_to_route, route_to_row, dev_status, static_cast<const int32_t*>(nullptr));
+           row_to_route, route_to_row, dev_status, static_cast<const int32_t*>(nullptr), true);
     return launch_status();
   }
   if (tl.n_tiles > 1)
     launch(permute_hist, dim3(tl.n_tiles), dim3(kHistThreads), E * sizeof(int32_t), s, R, E, k,
-           tl.routes_per_tile, topk_ids, hist, dev_status, valid);
+           tl.routes_per_tile, topk_ids, hist, dev_status, valid, one_wave(tl.n_tiles));
   launch(permute_rank, dim3(tl.n_tiles), dim3(kRankThreads), rank_smem, s, R, E, k,
          tl.routes_per_tile, tl.n_tiles, capacity, topk_ids,
          static_cast<const int32_t*>(tl.n_tiles > 1 ? hist : nullptr), counts, offsets, n_dropped,
-         row_to_route, route_to_row, dev_status, valid);
+         row_to_route, route_to_row, dev_status, valid, one_wave(tl.n_tiles));
   if (maps_only) return launch_status();
   const int warps = kCopyThreads / 32;
   const int chunks = static_cast<int>(row_bytes / 16);
@@ -319,11 +319,11 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
     launch(permute_copy<false>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T,
            k, chunks, parts, static_cast<const int32_t*>(route_to_row),
            static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), valid, 0, scales,
-           scales_perm);
+           scales_perm, one_wave(blocks));
   else
     launch(permute_copy<true>, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s, T, k,
            chunks, parts, static_cast<const int32_t*>(route_to_row), static_cast<const uint4*>(x),
-           static_cast<uint4*>(x_perm), valid, G, scales, scales_perm);
+           static_cast<uint4*>(x_perm), valid, G, scales, scales_perm, one_wave(blocks));
   return launch_status();
 }
 

@@ -82,8 +82,8 @@ __global__ void __launch_bounds__(kTokensPerBlock * 32)
 route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale,
              const float* __restrict__ logits, const float* __restrict__ sel_bias,
              int32_t* __restrict__ topk_ids, float* __restrict__ gates,
-             uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid) {
-  pdl_wait();
+             uint32_t* __restrict__ dev_status, const int32_t* __restrict__ valid, bool early) {
+  pdl_wait_then_trigger(early);
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTokensPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -220,7 +220,7 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
     topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
     gates[static_cast<int64_t>(t) * k + lane] = g;
   }
-  pdl_trigger();
+  if (!early) pdl_trigger();
 }
 
 template <bool GROUPED>
@@ -230,9 +230,10 @@ moe_status launch_route(const moe_route_params* p, const float* logits, const fl
   const int vpl = static_cast<int>(ceil_div(p->E, 32));
   const dim3 grid(static_cast<unsigned>(ceil_div(p->T, kTokensPerBlock)));
   const dim3 block(kTokensPerBlock * 32);
+  const bool early = one_wave(grid.x);
 #define MOE_ROUTE_CASE(V)                                                                \
   launch(route_kernel<V, GROUPED>, grid, block, 0, s, p->T, p->E, p->k, p->n_group,        \
-         p->topk_group, p->route_scale, logits, sel_bias, ids, gates, st, valid)
+         p->topk_group, p->route_scale, logits, sel_bias, ids, gates, st, valid, early)
   if (vpl <= 1) MOE_ROUTE_CASE(1);
   else if (vpl <= 2) MOE_ROUTE_CASE(2);
   else if (vpl <= 4) MOE_ROUTE_CASE(4);
