@@ -252,8 +252,12 @@ def kernel_source_sha(name):
            "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
            "quantize": "fp8.cu", "dequantize": "fp8.cu",
            "combine": "combine.cu", "pool_pack": "pool.cu", "pool_compact": "pool.cu"}[name]
-    with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", src), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    # the kernel's own file and the header of helpers every kernel includes
+    for fn in (src, "common.cuh"):
+        with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def lookup_traffic(stage, workload_name):
