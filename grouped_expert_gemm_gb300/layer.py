@@ -3,9 +3,10 @@
 ``MoELayer``       route -> permute (capacity or dropless) -> grouped SwiGLU over
                    the expert segments (+ an optional always-on shared expert)
                    -> gate-weighted fp32 combine.  With an FP8 payload the token
-                   rows are quantized to E4M3 + fp32 scales first, the pair is
-                   permuted together and the gate/up GEMM dequantizes in its
-                   loader.
+                   rows are quantized to E4M3 + fp32 scales first and the pair is
+                   permuted together; the permuted rows are then dequantized once
+                   before the bf16 gate/up pass (or, with fp8_loader="fused", in
+                   the gate/up GEMM's own loader).
 ``DecodeBucket``   a fixed token bucket for decode steps: stable buffers, one
                    captured CUDA graph of the bucketed layer, a device-side
                    valid-token count, exact admission and an eager fallback.
