@@ -771,7 +771,10 @@ def working_set_bytes(w, layer):
     """Bytes one step touches: the experts that received rows (all of them for the
     pooled layout), the shared expert, and the step's activations and buffers."""
     if w.pooled:
-        return sum(t.numel() * 2 for t in (layer.w_gate, layer.w_up, layer.w_down))
+        b = sum(t.numel() * 2 for t in (layer.w_gate, layer.w_up, layer.w_down))
+        b += w.T * w.E * 4 + w.T * w.d * 2                      # logits, token rows
+        b += (layer.pools.numel() + layer.compact.numel() + layer.y.numel()) * 2
+        return b + layer.rows * w.I * 2 + w.T * w.d * 4         # H, fp32 output
     touched = int((layer.counts > 0).sum().item())
     R = w.T * w.k
     b = touched * 3 * w.d * w.I * 2 + (3 * w.d * w.shared_I * 2 if w.shared_I else 0)

@@ -34,6 +34,18 @@ def test_l2_rule_flushes_exactly_the_small_working_sets():
     assert bench.working_set_bytes(d128, _layer(d128, 123)) > 2 * bench.L2_BYTES
     tiny = workloads.tiny()
     assert bench.working_set_bytes(tiny, _layer(tiny, 8)) < 2 * bench.L2_BYTES
+    # the pooled step streams its pools, compact arrays and outputs (GBs), not only the
+    # six local experts' weights (170 MB)
+    p = workloads.pooled()
+    m = dict(dtype=torch.bfloat16, device="meta")
+    rows = p.local_per_dest * 33497
+    pl = types.SimpleNamespace(w_gate=torch.empty((6, p.d, p.I), **m),
+                               w_up=torch.empty((6, p.d, p.I), **m),
+                               w_down=torch.empty((6, p.I, p.d), **m),
+                               pools=torch.empty((p.n_dest, 3005, p.d), **m),
+                               compact=torch.empty((rows, p.d), **m),
+                               y=torch.empty((rows, p.d), **m), rows=rows)
+    assert bench.working_set_bytes(p, pl) > 5e9
 
 
 def test_stage_work_follows_the_method_and_the_gather_option():
