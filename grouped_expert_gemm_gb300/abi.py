@@ -48,7 +48,8 @@ EXPORTED = [
     "moe_version", "moe_status_string", "moe_capacity", "moe_route", "moe_sigmoid_det",
     "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
     "moe_grouped_swiglu_workspace_size",
-    "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
+    "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_grouped_down_chained",
+    "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_pool_compact_rotated",
     "moe_compose_map",
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
@@ -99,6 +100,7 @@ _SIGS = {
                                   _P, _P]),
     "moe_grouped_gate_up": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_down": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_grouped_down_chained": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_combine": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_pool_pack_workspace_size": (_SZ, [ctypes.POINTER(PoolParams), _I32, _I32]),
     "moe_pool_pack": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _I32, _P, _P, _P, _P,
@@ -322,6 +324,16 @@ def moe_grouped_gate_up_fp8(n_seg, d, I, max_rows, group, xq, scales, seg_begin,
 def moe_grouped_down(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status=None,
                      stream=None):
     _check("moe_grouped_down", lib().moe_grouped_down(
+        n_seg, I, d, max_rows, _ptr(h), _ptr(seg_begin), _ptr(seg_count), _ptr(w_down), _ptr(y),
+        _ptr(dev_status), _stream(stream)))
+    _count(1 if max_rows > 0 else 0)
+
+
+def moe_grouped_down_chained(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y,
+                             dev_status=None, stream=None):
+    """moe_grouped_down right after this library's gate/up pass on the same stream and
+    segment table (see include/moe.h for the precondition)."""
+    _check("moe_grouped_down_chained", lib().moe_grouped_down_chained(
         n_seg, I, d, max_rows, _ptr(h), _ptr(seg_begin), _ptr(seg_count), _ptr(w_down), _ptr(y),
         _ptr(dev_status), _stream(stream)))
     _count(1 if max_rows > 0 else 0)

@@ -169,6 +169,11 @@ struct GemmArgs {
   const int32_t* gather;
   int gather_k;
   int gather_T;
+  // bf16 down pass (single-CTA kernel) issued right after this library's gate/up
+  // pass on the same stream and segment table: the segment table and the first
+  // tile's weight atoms are read before waiting for the gate/up pass (see
+  // moe_grouped_down_chained).
+  int chained;
 };
 
 // ------------------------------ PTX wrappers -------------------------------
@@ -817,7 +822,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b1)) : "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
-  pdl_wait();  // everything above is local; global data only from here on
+  // Everything above is local; global data only after the wait.  A chained down
+  // pass reads only data written before the gate/up pass began (the segment table,
+  // the weights) until its producer waits, just before its first A load; its other
+  // warps touch no global data the gate/up pass writes.  The gate/up pass lets its
+  // dependents launch right after its own wait: its grid is one CTA per SM, all
+  // resident by then, and a chained down pass then stages weights on the SMs the
+  // gate/up tiles leave idle or free first.
+  const bool chained = !SWIGLU && !FP8A && args.chained != 0;
+  if (!chained) pdl_wait();
+  if (SWIGLU) pdl_trigger();
   if (threadIdx.x >= 64 && threadIdx.x < 192)
     build_segment_table(args, args.bm, n_blocks, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
   tc_fence_before();
@@ -878,16 +892,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
+      int staged = 0;  // k-steps of the first tile whose weight atoms precede the wait
+      if (chained) {
+        if (static_cast<int>(blockIdx.x) < total_tiles) {
+          const Tile tl = tile_of(blockIdx.x, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg,
+                                  args.bm, kBnOut, n_blocks, args.m_outer);
+          const int b_row0 = tl.seg * args.K;
+          staged = min(kStages, k_steps);
+          for (int ks = 0; ks < staged; ++ks) {  // the ring's first round: all slots free
+            const uint32_t st = smem_u32(stage_base + ks * G::kStageBytes);
+            mbar_arrive_expect_tx(full_bar(ks), args.a_box_bytes + N_ATOMS * kAtomBytes);
+#pragma unroll
+            for (int a = 0; a < N_ATOMS; ++a)
+              tma_load_2d(st + G::kBOff + a * kAtomBytes, &tmap_b0, full_bar(ks), tl.n0 + a * 64,
+                          b_row0 + ks * kBK);
+          }
+        }
+        pdl_wait();  // the A rows (H) are the gate/up pass's output
+      }
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const Tile tl = tile_of(t, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, args.bm, kBnOut,
                                 n_blocks, args.m_outer);
         const int b_row0 = tl.seg * args.K;
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+          const bool pre = t == static_cast<int>(blockIdx.x) && ks < staged;
           const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
-          mbar_arrive_expect_tx(full_bar(s), args.a_box_bytes + N_ATOMS * kAtomBytes);
+          if (!pre) {
+            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+            mbar_arrive_expect_tx(full_bar(s), args.a_box_bytes + N_ATOMS * kAtomBytes);
+          }
           // A: the bf16 tile, or the E4M3 tile for the converter warps
           tma_load_2d(FP8A ? st + G::kRawOff : st, &tmap_a, full_bar(s), ks * kBK, tl.row0);
+          if (pre) {  // its weight atoms are already on their way
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+            continue;
+          }
 #pragma unroll
           for (int a = 0; a < N_ATOMS; ++a) {
             const uint32_t dst = st + G::kBOff + a * kAtomBytes;
@@ -1640,10 +1679,10 @@ MOE_API moe_status moe_grouped_gate_up_fp8(int32_t n_seg, int32_t d, int32_t I, 
   return launch_gemm<2, true, true>(m_x, m_wg, m_wu, a, s);
 }
 
-MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
-                                    const moe_bf16* h, const int32_t* seg_begin,
-                                    const int32_t* seg_count, const moe_bf16* w_down, moe_bf16* y,
-                                    uint32_t* dev_status, moe_stream_t stream) {
+static moe_status down_impl(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                            const moe_bf16* h, const int32_t* seg_begin, const int32_t* seg_count,
+                            const moe_bf16* w_down, moe_bf16* y, uint32_t* dev_status,
+                            moe_stream_t stream, int chained) {
   moe_status st = check_common(n_seg, I, d, max_rows);
   if (st != MOE_OK || max_rows == 0) return st;
   if (h == nullptr || seg_begin == nullptr || seg_count == nullptr || w_down == nullptr ||
@@ -1656,7 +1695,8 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   if (!make_map(&m_h, h, max_rows, I, bm) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
-             dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0, bm, bm * kBK * 2};
+             dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0, bm, bm * kBK * 2,
+             nullptr, 0, 0, chained};
   cudaStream_t s = as_cuda(stream);
   // The widest output tile the width allows (narrower 128-row tiles for one-token
   // decode were measured slower: the few tiles there are bound by pipeline latency).
@@ -1664,6 +1704,23 @@ MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t
   if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
   if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
   return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
+}
+
+MOE_API moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                                    const moe_bf16* h, const int32_t* seg_begin,
+                                    const int32_t* seg_count, const moe_bf16* w_down, moe_bf16* y,
+                                    uint32_t* dev_status, moe_stream_t stream) {
+  return down_impl(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status, stream,
+                   0);
+}
+
+MOE_API moe_status moe_grouped_down_chained(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                                            const moe_bf16* h, const int32_t* seg_begin,
+                                            const int32_t* seg_count, const moe_bf16* w_down,
+                                            moe_bf16* y, uint32_t* dev_status,
+                                            moe_stream_t stream) {
+  return down_impl(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status, stream,
+                   1);
 }
 
 MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
@@ -1685,8 +1742,8 @@ MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32
   st = moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, h,
                            dev_status, stream);
   if (st != MOE_OK) return st;
-  return moe_grouped_down(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y, dev_status,
-                          stream);
+  return moe_grouped_down_chained(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y,
+                                  dev_status, stream);
 }
 
 MOE_API moe_status moe_debug_wait_timeout(int64_t limit_ns, uint32_t* dev_status,

@@ -183,9 +183,11 @@ class MoELayer:
                                 self.w_gate, self.w_up, self.H, self.dev_status, stream)
 
     def experts_down(self, stream=None):
+        """The down pass; it follows experts_gate_up on the same stream (as in `stages`),
+        so it stages its first weight tiles while the gate/up pass finishes."""
         R = max(self.T * self.k, 1)
-        abi.moe_grouped_down(self.E, self.I, self.d, R, self.H, self.offsets, self.counts,
-                             self.w_down, self.y, self.dev_status, stream)
+        abi.moe_grouped_down_chained(self.E, self.I, self.d, R, self.H, self.offsets,
+                                     self.counts, self.w_down, self.y, self.dev_status, stream)
 
     def experts(self, stream=None, x=None):
         self.experts_gate_up(stream, x)
@@ -341,8 +343,10 @@ class PooledMoELayer:
                                 self.dev_status, stream)
 
     def experts_down(self, stream=None):
-        abi.moe_grouped_down(self.L, self.I, self.d, self.rows, self.H, self.local_begin,
-                             self.local_counts, self.w_down, self.y, self.dev_status, stream)
+        """The down pass; it follows experts_gate_up on the same stream (as in `stages`)."""
+        abi.moe_grouped_down_chained(self.L, self.I, self.d, self.rows, self.H, self.local_begin,
+                                     self.local_counts, self.w_down, self.y, self.dev_status,
+                                     stream)
 
     @property
     def H(self) -> torch.Tensor:

@@ -235,6 +235,21 @@ moe_status moe_grouped_down(int32_t n_seg, int32_t I, int32_t d, int32_t max_row
                             const moe_bf16* h, const int32_t* seg_begin, const int32_t* seg_count,
                             const moe_bf16* w_down, moe_bf16* y, uint32_t* dev_status,
                             moe_stream_t stream);
+/* moe_grouped_down for a call that directly follows this library's
+ * moe_grouped_gate_up (or _gate_up_fp8 / _gate_up_gather) on the same stream,
+ * with the same seg_begin / seg_count, and with h that pass's output.  It
+ * computes the same y, bit for bit.  The gate/up pass lets the next kernel
+ * launch early.  This call then reads the segment table and stages its first
+ * tile's W_down atoms before that pass has finished.  It waits for the pass only
+ * before its first read of h.  Precondition: nothing the gate/up pass or a kernel
+ * enqueued after it writes seg_begin, seg_count or W_down.  If the precondition
+ * is broken, the result is undefined.  The kernel still reads and writes only
+ * inside the bounds the segment checks allow.  moe_grouped_swiglu issues its
+ * down pass this way.  Arguments, limits and errors as moe_grouped_down.      */
+moe_status moe_grouped_down_chained(int32_t n_seg, int32_t I, int32_t d, int32_t max_rows,
+                                    const moe_bf16* h, const int32_t* seg_begin,
+                                    const int32_t* seg_count, const moe_bf16* w_down,
+                                    moe_bf16* y, uint32_t* dev_status, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Combine                                                                  */

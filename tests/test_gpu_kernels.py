@@ -333,6 +333,46 @@ def test_grouped_swiglu_max_segments():
     _gemm_case(1024, 64, 128, rng.integers(0, 4, size=1024), sample=256)
 
 
+@pytest.mark.parametrize("n_seg,d,I,counts", [
+    (128, 2048, 768, [1 if e % 16 == 3 else 0 for e in range(128)]),  # one-token decode, 4 atoms
+    (8, 192, 128, [3, 0, 5, 1, 0, 2, 7, 4]),       # one 64-column atom, 2 k-steps < ring depth
+    (4, 128, 256, [40, 0, 17, 90]),                 # two atoms, 64-row boxes
+    (64, 512, 1024, [30 + (e * 7) % 11 for e in range(64)]),  # several tiles per CTA
+    (2, 256, 128, [300, 260]),                      # CTA-pair kernel (chaining not used)
+])
+def test_down_chained_equals_plain_down(n_seg, d, I, counts):
+    """The chained down pass (weights staged before the gate/up pass ends) writes the
+    same y bits as the plain call, on every kernel shape; sampled rows match the oracle."""
+    g = G()
+    counts = np.asarray(counts, np.int32)
+    begins = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int32)
+    max_rows = max(int(counts.sum()), 1)
+    w = workloads.scaled(workloads.tiny(), d=d, I=I, E=n_seg, seed=5)
+    gen = torch.Generator(device=DEV).manual_seed(12)
+    x = torch.randn((max_rows, d), generator=gen, device=DEV).to(torch.bfloat16)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV, n_experts=n_seg)
+    b_t, c_t = torch.from_numpy(begins).to(DEV), torch.from_numpy(counts).to(DEV)
+    h = torch.empty((max_rows, I), dtype=torch.bfloat16, device=DEV)
+    ys = []
+    st = status0()
+    for chained in (False, True):
+        y = torch.full((max_rows, d), 7.0, dtype=torch.bfloat16, device=DEV)
+        g.moe_grouped_gate_up(n_seg, d, I, max_rows, x, b_t, c_t, wg, wu, h, st)
+        down = g.moe_grouped_down_chained if chained else g.moe_grouped_down
+        down(n_seg, I, d, max_rows, h, b_t, c_t, wd, y, st)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    assert np.array_equal(bits(ys[0]), bits(ys[1]))
+    pick = np.sort(np.random.default_rng(3).choice(int(counts.sum()), min(8, int(counts.sum())),
+                                                   replace=False))
+    yr, _ = oracle.grouped_swiglu_rows(bits(x), begins, counts, bits(wg), bits(wu), bits(wd),
+                                       rows=pick)
+    r = sorted(yr)
+    assert_float_parity(oracle.bf16_to_f64(bits(ys[1])[r]),
+                        oracle.bf16_to_f64(np.stack([yr[i] for i in r])), "y")
+
+
 def test_grouped_swiglu_bad_segment_is_reported():
     g = G()
     d, I = 64, 128
