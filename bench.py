@@ -1002,10 +1002,19 @@ def run_cpu_baseline(args, w, layer, logits, sel_bias, x):
     hi = host_inputs_of(w, logits, sel_bias, x, layer)
     rng = np.random.default_rng(0)
     toks, dt = cpu_sample_tokens(w, args.cpu_budget, hi, rng)
-    return {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": cores(),
+    # when the whole workload takes well under the budget, repeat it until the oracle has
+    # worked about that long, so the rate is not one short pass
+    passes, total = 1, dt
+    while total < args.cpu_budget * 0.75 and passes < 64:
+        t0 = time.perf_counter()
+        oracle_step(w, hi, toks)
+        total += time.perf_counter() - t0
+        passes += 1
+    return {"value": round(len(toks) * passes / total, 4), "unit": "tokens/s", "cores": cores(),
             "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{len(toks)} of {w.T} tokens of {w.name} (routing/admission over all "
-                      f"tokens, expert math + combine for the sample), one pass, {dt:.1f} s"}
+                      f"tokens, expert math + combine for the sample), {passes} pass"
+                      f"{'es' if passes > 1 else ''}, {total:.1f} s"}
 
 
 def run_reference(args, dist, w):
