@@ -120,6 +120,31 @@ def test_decode_sweep_full(T, decode_weights):
     run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096)
 
 
+@pytest.mark.parametrize("case", ["decode_hot8", "tiny_hot2_capacity", "prefill_hot2",
+                                  "v3_hot_group"])
+def test_degenerate_routing_skew(case, decode_weights):
+    """Every token prefers the same few experts: segments of many rows beside empty
+    ones (decode: 8 experts x 128 rows; prefill-like: 2 experts x T rows in the CTA-pair
+    kernel), and with a capacity most routes are dropped."""
+    if case == "decode_hot8":
+        w = workloads.scaled(workloads.decode(128), logit_bias="hot8")
+        layer, perm = run_and_check(w, weights=decode_weights, sample_rows=256, sample_tokens=32)
+        assert sorted(np.nonzero(perm["counts"])[0].tolist()) == list(range(8))
+    elif case == "tiny_hot2_capacity":
+        w = workloads.scaled(workloads.tiny(), logit_bias="hot2")
+        layer, perm = run_and_check(w)
+        assert perm["counts"].tolist()[:2] == [80, 80] and perm["n_dropped"] == 2 * 256 - 160
+    elif case == "prefill_hot2":
+        w = workloads.scaled(workloads.prefill(), T=1024, d=512, I=1024, logit_bias="hot2")
+        layer, perm = run_and_check(w, sample_rows=128, sample_tokens=48)
+        assert perm["counts"].tolist() == [1024, 1024, 0, 0, 0, 0, 0, 0]
+    else:
+        w = workloads.scaled(workloads.v3(), T=384, d=256, I=128, shared_I=128,
+                             logit_bias="hot8")
+        layer, perm = run_and_check(w, sample_rows=128, sample_tokens=48)
+        assert perm["n_dropped"] > 0
+
+
 def test_tiny_full_gathered_rows():
     """The maps-only permute with the gathering gate/up loader gives the same checks."""
     run_and_check(workloads.tiny(), gather=True)

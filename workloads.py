@@ -54,7 +54,7 @@ class Workload:
     topk_group: int = 1
     route_scale: float = 1.0
     shared_I: int = 0  # intermediate width of the always-on shared expert (0 = none)
-    logit_bias: str = "none"  # "none" | "normal0.5" | "zipf1.0"
+    logit_bias: str = "none"  # "none" | "normal0.5" | "zipf1.0" | "hot<n>" (edge-case tests)
     selection_bias: str = "none"  # "none" | "zipf1.1x0.2" (sigmoid_group only)
     # pooled-wave layout (0 = not pooled)
     n_dest: int = 0
@@ -144,6 +144,10 @@ def make_router_inputs(w: Workload, device="cpu"):
         logits = logits + b
     elif w.logit_bias == "zipf1.0":
         logits = logits + _zipf_ranked(w.E, 1.0, 1.0, gb, device)
+    elif w.logit_bias.startswith("hot"):
+        # degenerate skew for edge-case tests: every token prefers the first n experts
+        n = int(w.logit_bias[3:])
+        logits[:, :n] += 20.0
     sel_bias = None
     if w.selection_bias == "zipf1.1x0.2":
         sel_bias = _zipf_ranked(w.E, 1.1, 0.2, gb, device)
