@@ -65,6 +65,11 @@ def parse_args():
     ap.add_argument("--gather", action="store_true",
                     help="bf16 payload: permute the maps only and gather the expert rows in the "
                          "gate/up loader instead of copying them in the permute")
+    ap.add_argument("--jsonl", default=None,
+                    help="also append the JSON line to this file (a results log for sweeps)")
+    ap.add_argument("--resume", action="store_true",
+                    help="with --jsonl: if the file already holds a line for the same run "
+                         "arguments, print that line and run nothing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -1051,26 +1056,67 @@ def run_reference(args, dist, w):
                     "d2h_bytes_per_step": 0}}
 
 
+RUN_KEYS = ("impl", "gpus", "steps", "warmup", "config", "tokens", "bucket", "payload",
+            "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras")
+
+
+def run_key(args) -> dict:
+    """The arguments that decide what a run measures (the identity of a results-log line)."""
+    return {k: getattr(args, k) for k in RUN_KEYS}
+
+
+def logged_line(path, key):
+    """The last line of the results log `path` recorded for run arguments `key`, or None."""
+    if not path or not os.path.exists(path):
+        return None
+    found = None
+    with open(path) as f:
+        for line in f:
+            try:
+                rec = json.loads(line)
+            except ValueError:
+                continue  # a torn last line of an interrupted append
+            if isinstance(rec, dict) and rec.get("run") == key:
+                found = rec
+    return found
+
+
+def emit(res, args):
+    """Print the run's JSON line and, with --jsonl, append it to the results log."""
+    if args.jsonl:
+        res = dict(res, run=run_key(args))
+    line = json.dumps(res)
+    print(line, flush=True)
+    if args.jsonl:
+        with open(args.jsonl, "a") as f:
+            f.write(line + "\n")
+
+
 def main():
     args = parse_args()
+    if args.resume and args.jsonl and int(os.environ.get("RANK", "0")) == 0:
+        prev = logged_line(args.jsonl, run_key(args))
+        if prev is not None and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+            print(json.dumps(prev), flush=True)
+            return
     dist = Dist()
     w = workload_for(args)
     try:
         if args.impl == "reference":
             res = run_reference(args, dist, w)
             if res is not None:
-                print(json.dumps(res), flush=True)
+                emit(res, args)
             return
         if args.bucket:
             res = run_bucket(args, dist, w)
             if dist.rank == 0:
-                print(json.dumps(res), flush=True)
+                emit(res, args)
             return
         res, layer, logits, sel_bias, x = run_ours(args, dist, w)
         if dist.rank == 0 and not args.no_cpu_baseline:
             res["cpu_baseline"] = run_cpu_baseline(args, w, layer, logits, sel_bias, x)
         if dist.rank == 0:
-            print(json.dumps(res), flush=True)
+            emit(res, args)
     finally:
         dist.close()
 

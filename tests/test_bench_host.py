@@ -1,6 +1,7 @@
 """Host-side rules of the benchmark, on CPU: which workloads flush L2 between timed
 steps, the algorithmic bytes and FLOPs charged to each stage, and the keys under
 which committed profiles record a stage's DRAM traffic."""
+import json
 import os
 import sys
 import types
@@ -84,3 +85,26 @@ def test_nearest_rank_quantiles():
     assert bench.nearest_rank([1, 2, 3, 4], 0.5) == 2
     assert bench.nearest_rank(list(range(1, 11)), 0.9) == 9
     assert bench.nearest_rank([7.0], 0.9) == 7.0
+
+
+def test_results_log_appends_and_resumes(tmp_path, capsys):
+    """--jsonl appends each run's line with its run arguments; --resume finds the last
+    line recorded for the same arguments (a torn last line is skipped)."""
+    log = str(tmp_path / "runs.jsonl")
+    args = types.SimpleNamespace(**{k: None for k in bench.RUN_KEYS})
+    args.jsonl, args.config, args.tokens = log, "decode", 8
+    bench.emit({"value": 1.0}, args)
+    args.tokens = 32
+    bench.emit({"value": 2.0}, args)
+    args.tokens = 8
+    bench.emit({"value": 3.0}, args)
+    with open(log, "a") as f:
+        f.write('{"value": 4.0, "run": ')  # an interrupted append
+    assert bench.logged_line(log, bench.run_key(args))["value"] == 3.0
+    args.tokens = 32
+    assert bench.logged_line(log, bench.run_key(args))["value"] == 2.0
+    args.tokens = 1
+    assert bench.logged_line(log, bench.run_key(args)) is None
+    assert bench.logged_line(str(tmp_path / "missing.jsonl"), bench.run_key(args)) is None
+    out = capsys.readouterr().out.strip().splitlines()
+    assert [json.loads(l)["value"] for l in out] == [1.0, 2.0, 3.0]
