@@ -221,12 +221,13 @@ def moe_sigmoid_det(n: int, z, s, stream=None):
 
 def _permute_launches(T: int, k: int, copy: bool = True) -> int:
     """Kernels one permute call launches: the tile histogram runs only with several tiles,
-    the row copy only when rows are copied (not for the maps-only form)."""
+    the row copy only when rows are copied (not for the maps-only form) and as a launch
+    of its own only above 16 routes (below, the rank block copies them)."""
     R = T * k
     if R <= 0:
         return 1
     per_tile = max(2048, -(-R // 128))
-    return (3 if -(-R // per_tile) > 1 else 2) - (0 if copy else 1)
+    return (3 if -(-R // per_tile) > 1 else 2) - (0 if copy and R > 16 else 1)
 
 
 def moe_permute_workspace_size(T: int, k: int, E: int) -> int:

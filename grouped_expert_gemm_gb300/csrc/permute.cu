@@ -21,7 +21,11 @@
 //   3. permute_copy  token-major row copy over many blocks: every token row is
 //                    read once and written to its admitted rows with 16-byte
 //                    accesses.  Skipped when the caller wants the maps only (the
-//                    gate/up pass can gather the rows itself).
+//                    gate/up pass can gather the rows itself).  With at most 16
+//                    routes (one or two tokens at top-8) the rank block copies
+//                    the rows itself after ranking, and this launch is left out
+//                    (one-token decode 36.9 -> 35.7 us per step; at 32 or 64
+//                    routes one block copying was slower than the copy kernel).
 #include "common.cuh"
 
 namespace moe {
@@ -45,6 +49,10 @@ struct PermTiling {
   int routes_per_tile;
   int n_tiles;
 };
+
+// Routes up to which the rank block also copies the rows (a single tile).
+constexpr int kFusedCopyRoutes = 16;
+inline bool fuse_row_copy(int64_t R) { return R <= kFusedCopyRoutes; }
 
 PermTiling permute_tiling(int64_t R) {
   PermTiling p;
@@ -84,7 +92,9 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
              int32_t* __restrict__ n_dropped, int32_t* __restrict__ row_to_route,
              int32_t* __restrict__ route_to_row, uint32_t* __restrict__ dev_status,
-             const int32_t* __restrict__ valid, bool early) {
+             const int32_t* __restrict__ valid, bool early, const uint4* __restrict__ x,
+             uint4* __restrict__ x_perm, int chunks, int G, const float* __restrict__ scales,
+             float* __restrict__ scales_perm) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;                    // [kRankWarps][E]
   int32_t* off = cnt + kRankWarps * E;  // [E]
@@ -195,6 +205,22 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
       route_to_row[r] = row;
     }
   }
+  if (x_perm != nullptr) {
+    // 5. the row copy, in this block when every route is in this one tile and there
+    //    are few (a handful of tokens): one warp per admitted row, whose route this
+    //    block has just written (visible to the block after the barrier)
+    __syncthreads();
+    int32_t n_rows = 0;
+    for (int i = 0; i < kRankWarps; ++i) n_rows += warp_tot[i];
+    for (int row = w; row < n_rows; row += kRankWarps) {
+      const int t = row_to_route[row] / k;
+      const uint4* src = x + static_cast<int64_t>(t) * chunks;
+      uint4* dst = x_perm + static_cast<int64_t>(row) * chunks;
+      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+      for (int g = lane; g < G; g += 32)
+        scales_perm[static_cast<int64_t>(row) * G + g] = __ldg(scales + static_cast<int64_t>(t) * G + g);
+    }
+  }
   if (!early) pdl_trigger();
 }
 
@@ -295,19 +321,26 @@ static moe_status permute_impl(int32_t T, int64_t row_bytes, int32_t E, int32_t 
     // No routes: one rank block with no tiles writes empty counts and offsets.
     launch(permute_rank, dim3(1), dim3(kRankThreads), rank_smem, s, 0, E, k, 1, 0, capacity,
            topk_ids, static_cast<const int32_t*>(nullptr), counts, offsets, n_dropped,
-           row_to_route, route_to_row, dev_status, static_cast<const int32_t*>(nullptr), true);
+           row_to_route, route_to_row, dev_status, static_cast<const int32_t*>(nullptr), true,
+           static_cast<const uint4*>(nullptr), static_cast<uint4*>(nullptr), 0, 0,
+           static_cast<const float*>(nullptr), static_cast<float*>(nullptr));
     return launch_status();
   }
   if (tl.n_tiles > 1)
     launch(permute_hist, dim3(tl.n_tiles), dim3(kHistThreads), E * sizeof(int32_t), s, R, E, k,
            tl.routes_per_tile, topk_ids, hist, dev_status, valid, one_wave(tl.n_tiles));
+  const int chunks = static_cast<int>(row_bytes / 16);
+  // A handful of tokens: the rank block copies the rows itself (one launch less).
+  const bool fused_copy = !maps_only && fuse_row_copy(R);
   launch(permute_rank, dim3(tl.n_tiles), dim3(kRankThreads), rank_smem, s, R, E, k,
          tl.routes_per_tile, tl.n_tiles, capacity, topk_ids,
          static_cast<const int32_t*>(tl.n_tiles > 1 ? hist : nullptr), counts, offsets, n_dropped,
-         row_to_route, route_to_row, dev_status, valid, one_wave(tl.n_tiles));
-  if (maps_only) return launch_status();
+         row_to_route, route_to_row, dev_status, valid, one_wave(tl.n_tiles),
+         static_cast<const uint4*>(fused_copy ? x : nullptr),
+         static_cast<uint4*>(fused_copy ? x_perm : nullptr), chunks, fused_copy ? G : 0, scales,
+         scales_perm);
+  if (maps_only || fused_copy) return launch_status();
   const int warps = kCopyThreads / 32;
-  const int chunks = static_cast<int>(row_bytes / 16);
   // Column parts: enough warps for every SM when tokens are few, at least 64
   // chunks (1 KB) per part.
   int parts = 1;

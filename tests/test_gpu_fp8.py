@@ -83,7 +83,8 @@ def test_quantize_reports_nonfinite_input():
 
 @pytest.mark.parametrize("group", [0, 128])
 @pytest.mark.parametrize("T,d,E,k,cap", [(256, 64, 8, 2, 80), (300, 2048, 128, 8, -1),
-                                         (5000, 192, 32, 4, 600), (1, 16, 4, 4, -1)])
+                                         (5000, 192, 32, 4, 600), (1, 16, 4, 4, -1),
+                                         (2, 2048, 128, 8, 1)])  # 16 routes: copied by the rank block
 def test_permute_fp8_moves_rows_and_scales_together(group, T, d, E, k, cap):
     g = G()
     rng = np.random.default_rng(T + d)

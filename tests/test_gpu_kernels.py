@@ -170,7 +170,7 @@ def _check_permute(T, d, E, k, cap, ids_np, seed=0):
                                          (1000, 128, 128, 8, -1), (997, 64, 256, 8, 31),
                                          (4099, 64, 8, 2, 0), (500, 64, 16, 4, 1),
                                          (129, 192, 384, 8, -1), (2000, 64, 512, 16, 40),
-                                         (64, 64, 1, 1, -1)])
+                                         (64, 64, 1, 1, -1), (2, 4096, 16, 8, 1)])
 def test_permute_parity(T, d, E, k, cap):
     rng = np.random.default_rng(T + E)
     # skewed expert choice so that some experts are empty and some overflow
@@ -444,7 +444,8 @@ def test_gate_up_gather_equals_copy_path(T, d, E, k, I, cap):
 
 @pytest.mark.parametrize("T,E,k,cap", [(300, 32, 4, 40), (5000, 128, 8, -1), (1, 8, 2, -1)])
 def test_permute_maps_only_equals_the_copying_call(T, E, k, cap):
-    """x = x_perm = NULL: the same maps, counts, offsets and drops, one launch fewer."""
+    """x = x_perm = NULL: the same maps, counts, offsets and drops, and one launch fewer
+    where the rows have a copy launch of their own (above 16 routes)."""
     g = G()
     rng = np.random.default_rng(T)
     ids_np = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
@@ -460,7 +461,9 @@ def test_permute_maps_only_equals_the_copying_call(T, E, k, cap):
     st = status0()
     n0 = g.launch_count()
     g.moe_permute(T, 64, E, k, cap, ids, None, None, counts, offsets, r2r, inv, nd, ws, wsb, st)
-    assert g.launch_count() - n0 == g.abi._permute_launches(T, k) - 1
+    assert g.launch_count() - n0 == g.abi._permute_launches(T, k, copy=False)
+    assert g.abi._permute_launches(T, k, copy=False) == \
+        g.abi._permute_launches(T, k) - (1 if T * k > 16 else 0)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     acc = int(full["offsets"][-1])
