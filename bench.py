@@ -772,15 +772,17 @@ def traffic_key(w, layer):
 L2_BYTES = 129 * 1024 * 1024
 
 
-def working_set_bytes(w, layer):
+def working_set_bytes(w, layer, touched=None):
     """Bytes one step touches: the experts that received rows (all of them for the
-    pooled layout), the shared expert, and the step's activations and buffers."""
+    pooled layout; `touched` overrides the count read from the layer's last step),
+    the shared expert, and the step's activations and buffers."""
     if w.pooled:
         b = sum(t.numel() * 2 for t in (layer.w_gate, layer.w_up, layer.w_down))
         b += w.T * w.E * 4 + w.T * w.d * 2                      # logits, token rows
         b += (layer.pools.numel() + layer.compact.numel() + layer.y.numel()) * 2
         return b + layer.rows * w.I * 2 + w.T * w.d * 4         # H, fp32 output
-    touched = int((layer.counts > 0).sum().item())
+    if touched is None:
+        touched = int((layer.counts > 0).sum().item())
     R = w.T * w.k
     b = touched * 3 * w.d * w.I * 2 + (3 * w.d * w.shared_I * 2 if w.shared_I else 0)
     b += w.T * w.E * 4 + w.T * w.d * 2 + 2 * R * w.d * 2 + R * w.I * 2 + w.T * w.d * 4
@@ -1034,6 +1036,19 @@ def run_reference(args, dist, w):
     else:
         raise RuntimeError("the reference arm generates the same seeded inputs on the GPU")
     hi = host_inputs_of(w, logits, sel_bias, x, layer)
+    # the same config object as our arm's line, its working set from the oracle's routing
+    touched = None
+    if not w.pooled:
+        import oracle
+        if w.score_fn == "softmax":
+            ids, _ = oracle.route_softmax(hi[0], w.k)
+        else:
+            ids, _ = oracle.route_sigmoid_group(hi[0], hi[1], w.k, w.n_group, w.topk_group,
+                                                w.route_scale)
+        cap = -1 if w.capacity_factor is None else layer.capacity
+        touched = int((oracle.permute(ids, w.E, cap)["counts"] > 0).sum())
+    ws_bytes = working_set_bytes(w, layer, touched)
+    config = config_dict(w, layer, ws_bytes, ws_bytes < 2 * L2_BYTES)
     rng = np.random.default_rng(0)
     # size the per-step sample so that one step takes ~2 s of oracle work
     toks, _ = cpu_sample_tokens(w, 4.0, hi, rng)
@@ -1049,7 +1064,7 @@ def run_reference(args, dist, w):
             "n_gpus": 1, "steps": steps, "warmup": args.warmup,
             "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I},
+            "config": config,
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores(),
                              "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
