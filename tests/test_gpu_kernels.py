@@ -557,6 +557,7 @@ def _pool_case(T, d, k, n_dest, L, n_waves, pool_cap, local_cap, policy, seed=0)
     (1000, 128, 8, 16, 6, 3, 64, 150),
     (77, 64, 2, 2, 2, 1, 64, 1000),     # nothing dropped
     (500, 64, 8, 8, 4, 2, 5, 7),        # heavy drops on both sides
+    (3, 64, 2, 16, 2, 2, 8, 4),         # most pools (and local experts) empty
 ])
 def test_pool_pack_compact_parity(policy, T, d, k, n_dest, L, n_waves, pool_cap, local_cap):
     _pool_case(T, d, k, n_dest, L, n_waves, pool_cap, local_cap, policy)
