@@ -697,8 +697,9 @@ def run_bucket(args, dist, w):
                        "l2": ("flushed before every step (working set fits L2); value from "
                               "the steps' own spans" if flush_l2 else
                               "the step's working set is over twice L2")},
-            "timing": "each step: input copies into the stable buffers, valid-count write, "
-                      "graph replay", "clocks": sampler.summary()}
+            "timing": "each step: one staging kernel (input copies into the stable buffers and "
+                      "the valid count), graph replay", "clocks": sampler.summary(),
+            "gpu_launches": steps * (1 + bucket.graph_launches)}
 
 
 def run_extras(args, w, layer, stream, steps, layer_x=None):

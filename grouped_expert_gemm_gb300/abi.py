@@ -53,7 +53,7 @@ EXPORTED = [
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_pool_compact_rotated",
     "moe_compose_map",
     "moe_combine_backward", "moe_unpermute_grad", "moe_load_stats", "moe_bias_update",
-    "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
+    "moe_bucket_stage", "moe_route_bucket", "moe_permute_bucket", "moe_combine_bucket",
     "moe_payload_bytes", "moe_quantize_fp8", "moe_dequantize_fp8", "moe_permute_fp8",
     "moe_grouped_gate_up_fp8", "moe_grouped_gate_up_gather", "moe_expert_demand", "moe_validate_permutation",
     "moe_validate_pools_workspace_size", "moe_validate_pools",
@@ -114,6 +114,7 @@ _SIGS = {
     "moe_combine_backward": (_I32, [_I32, _I32, _I32, _P, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_grad": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
     "moe_load_stats": (_I32, [_I32, _P, _P, _P]),
+    "moe_bucket_stage": (_I32, [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "moe_route_bucket": (_I32, [ctypes.POINTER(RouteParams), _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute_bucket": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _SZ, _P, _P]),
@@ -414,6 +415,13 @@ def moe_load_stats(U, counts, stats, stream=None):
 def moe_bias_update(E, counts, bias, u, rule=MOE_BIAS_SIGN, stream=None):
     _check("moe_bias_update", lib().moe_bias_update(E, _ptr(counts), _ptr(bias), float(u), rule,
                                                     _stream(stream)))
+    _count(1)
+
+
+def moe_bucket_stage(T, E, d, logits, x, logits_dst, x_dst, valid_tokens, stream=None):
+    _check("moe_bucket_stage", lib().moe_bucket_stage(
+        T, E, d, _ptr(logits), _ptr(x), _ptr(logits_dst), _ptr(x_dst), _ptr(valid_tokens),
+        _stream(stream)))
     _count(1)
 
 

@@ -252,10 +252,50 @@ __global__ void sigmoid_det_kernel(int64_t n, const float* __restrict__ z, float
   pdl_trigger();
 }
 
+// Decode bucket staging: the step's logits and token rows into rows [0, T) of
+// the bucket's stable buffers, and the real token count into its device int32.
+// One grid-stride pass over both copies (16-byte units where both sides allow).
+__global__ void bucket_stage_kernel(int T, int64_t n_logit_vec, int64_t n_logit,
+                                    int64_t n_x_vec, const float4* __restrict__ logits_v,
+                                    const float* __restrict__ logits, float4* __restrict__ dst_v,
+                                    float* __restrict__ dst, const uint4* __restrict__ x,
+                                    uint4* __restrict__ x_dst, int32_t* __restrict__ valid) {
+  pdl_wait();  // the previous step's kernels may still read the stable buffers
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  for (int64_t i = i0; i < n_logit_vec; i += stride) dst_v[i] = __ldg(logits_v + i);
+  for (int64_t i = n_logit_vec * 4 + i0; i < n_logit; i += stride) dst[i] = __ldg(logits + i);
+  for (int64_t i = i0; i < n_x_vec; i += stride) x_dst[i] = __ldg(x + i);
+  if (i0 == 0) *valid = T;
+  pdl_trigger();
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+MOE_API moe_status moe_bucket_stage(int32_t T, int32_t E, int32_t d, const float* logits,
+                                    const moe_bf16* x, float* logits_dst, moe_bf16* x_dst,
+                                    int32_t* valid_tokens, moe_stream_t stream) {
+  if (T < 0 || E <= 0 || d <= 0 || valid_tokens == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (logits == nullptr || x == nullptr || logits_dst == nullptr || x_dst == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (d % 8 != 0 || (T > 0 && (!aligned16(x) || !aligned16(x_dst)))) return MOE_ERR_UNSUPPORTED;
+  const int64_t n_logit = static_cast<int64_t>(T) * E;
+  const bool vec = aligned16(logits) && aligned16(logits_dst);
+  const int64_t n_logit_vec = vec ? n_logit / 4 : 0;
+  const int64_t n_x_vec = static_cast<int64_t>(T) * d / 8;
+  const int64_t work = n_logit_vec + (n_logit - 4 * n_logit_vec) + n_x_vec;
+  int64_t blocks = ceil_div(work > 0 ? work : 1, 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  launch(bucket_stage_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+         as_cuda(stream), T, n_logit_vec, n_logit, n_x_vec,
+         reinterpret_cast<const float4*>(logits), logits, reinterpret_cast<float4*>(logits_dst),
+         logits_dst, reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_dst),
+         valid_tokens);
+  return launch_status();
+}
 
 static moe_status route_impl(const moe_route_params* p, const int32_t* valid, const float* logits,
                              const float* sel_bias, int32_t* topk_ids, float* gates,

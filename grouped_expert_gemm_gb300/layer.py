@@ -504,8 +504,10 @@ class DecodeBucket:
             self.step(s)
         s.synchronize()
         self.graph = torch.cuda.CUDAGraph()
+        n0 = abi.launch_count()
         with torch.cuda.graph(self.graph, stream=s):
             self.step(None)
+        self.graph_launches = abi.launch_count() - n0  # kernels one replay runs
         return self.graph
 
     def admit(self, T: int, phase: str = "decode", key=None):
@@ -527,9 +529,10 @@ class DecodeBucket:
         s = torch.cuda.current_stream() if stream is None else stream
         if ok:
             with torch.cuda.stream(s):
-                self.logits[:T].copy_(logits, non_blocking=True)
-                self.x[:T].copy_(x, non_blocking=True)
-                self.valid.fill_(T)
+                # the inputs into the stable buffers and the count, one kernel
+                lg = logits.to(torch.float32).contiguous()
+                xs = x.to(torch.bfloat16).contiguous()
+                abi.moe_bucket_stage(T, self.E, self.d, lg, xs, self.logits, self.x, self.valid, s)
                 self.graph.replay()
             return self.layer.out[:T], "replay"
         if T not in self._eager:

@@ -357,6 +357,18 @@ moe_status moe_compose_map(int64_t n, const int32_t* a, const int32_t* b, int64_
  *                       are when accumulating).
  * The capacity argument of moe_permute_bucket is fixed at capture (it is part
  * of the graph's key).  Everything else as the unbucketed calls.            */
+/* moe_bucket_stage: one step's inputs into a bucket's stable buffers, in one
+ * launch.  Copies logits [T, E] fp32 and x [T, d] bf16 (token-major, contiguous)
+ * into rows [0, T) of logits_dst [B, E] and x_dst [B, d], and writes T to the
+ * DEVICE int32 *valid_tokens.  It waits for the previous kernel on the stream, so a
+ * replay of the bucket's graph that still reads the buffers has finished.  The
+ * caller keeps T <= B (the bucket's slot count; the buffers are not bounds
+ * checked against B).  Rows [T, B) are left as they are: the bucketed calls mask
+ * them.  T = 0 only writes the count.  Limits: d % 8 == 0, x and x_dst 16-byte
+ * aligned (logits use 16-byte copies when both sides are aligned).             */
+moe_status moe_bucket_stage(int32_t T, int32_t E, int32_t d, const float* logits,
+                            const moe_bf16* x, float* logits_dst, moe_bf16* x_dst,
+                            int32_t* valid_tokens, moe_stream_t stream);
 moe_status moe_route_bucket(const moe_route_params* p, const int32_t* valid_tokens,
                             const float* logits, const float* sel_bias, int32_t* topk_ids,
                             float* gates, uint32_t* dev_status, moe_stream_t stream);

@@ -61,6 +61,12 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.moe_route(P(4, 10, 2, 1, 4, 2, 2.5), 16, None, 16, 16, None, None) == abi.MOE_ERR_INVALID_ARG
     assert lib.moe_route(P(4, 16, 8, 1, 4, 1, 2.5), 16, None, 16, 16, None, None) == abi.MOE_ERR_UNSUPPORTED
     assert lib.moe_route(P(0, 8, 2, 0, 1, 1, 1.0), None, None, None, None, None, None) == abi.MOE_OK
+    # bucket staging: negative T, no count pointer, d not a multiple of 8, misaligned rows
+    assert lib.moe_bucket_stage(-1, 8, 64, 16, 16, 16, 16, 16, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_bucket_stage(2, 8, 64, 16, 16, 16, 16, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_bucket_stage(2, 8, 64, None, 16, 16, 16, 16, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_bucket_stage(2, 8, 60, 16, 16, 16, 16, 16, None) == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_bucket_stage(2, 8, 64, 16, 24, 16, 16, 16, None) == abi.MOE_ERR_UNSUPPORTED
     # permute: d not a multiple of 8, workspace too small, misaligned x
     assert lib.moe_permute(4, 12, 8, 2, -1, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 20, None,
                            None) == abi.MOE_ERR_UNSUPPORTED

@@ -111,3 +111,23 @@ def test_permute_bucket_parity(cap):
     assert int(outs["nd"].item()) == ref["n_dropped"]
     assert np.array_equal(bits(outs["x_perm"])[:acc],
                           oracle.gather_rows(bits(x), ref["row_to_route"], k))
+
+
+@pytest.mark.parametrize("T,E,d", [(1, 128, 2048), (37, 128, 2048), (5, 7, 64), (0, 8, 64)])
+def test_bucket_stage_copies_the_inputs_and_the_count(T, E, d):
+    """One launch copies logits [T, E] and x [T, d] into the first T rows of the stable
+    buffers, bit for bit, writes the count, and leaves the other rows alone."""
+    import grouped_expert_gemm_gb300 as g
+    B = 40 if T <= 40 else T
+    gen = torch.Generator(device=DEV).manual_seed(T + E)
+    logits = torch.randn((T, E), generator=gen, device=DEV)
+    x = torch.randn((T, d), generator=gen, device=DEV).to(torch.bfloat16)
+    ldst = torch.full((B, E), -3.0, device=DEV)
+    xdst = torch.full((B, d), 5.0, dtype=torch.bfloat16, device=DEV)
+    valid = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    g.moe_bucket_stage(T, E, d, logits, x, ldst, xdst, valid)
+    torch.cuda.synchronize()
+    assert int(valid.item()) == T
+    assert torch.equal(ldst[:T], logits) and bool((ldst[T:] == -3.0).all())
+    assert torch.equal(xdst[:T].view(torch.int16), x.view(torch.int16))
+    assert bool((xdst[T:] == 5.0).all())
