@@ -49,9 +49,11 @@ def parse_args():
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
                          "a smaller T for short profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--bucket", type=int, default=0,
+    ap.add_argument("--bucket", default="",
                     help="decode: replay one captured graph over a fixed bucket of this many "
-                         "token slots, serving --tokens real tokens per step")
+                         "token slots, serving --tokens real tokens per step; a comma list "
+                         "(e.g. 1,2,4,8,16,32,64,128) is a ladder of buckets, each step "
+                         "replaying the smallest that holds its tokens")
     ap.add_argument("--extras", action="store_true",
                     help="also time the backward of the transpose and the telemetry/bias calls "
                          "on this workload's buffers")
@@ -642,23 +644,30 @@ def run_bucket(args, dist, w):
     device = torch.device(f"cuda:{dist.local}")
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
-    B = args.bucket
+    sizes = sorted({int(v) for v in str(args.bucket).split(",")})
+    B = sizes[-1]
     wb = workloads.scaled(w, T=B)
     wg, wu, wd = workloads.make_expert_weights(wb, device)
-    bucket = g.DecodeBucket(B, w.d, w.E, w.k, w.I, wg, wu, wd, device=device)
+    if len(sizes) == 1:
+        bucket = g.DecodeBucket(B, w.d, w.E, w.k, w.I, wg, wu, wd, device=device)
+    else:
+        bucket = g.DecodeBucketLadder(sizes, w.d, w.E, w.k, w.I, wg, wu, wd, device=device)
     stream = torch.cuda.Stream(device)
     bucket.capture(stream)
+    served = bucket if len(sizes) == 1 else bucket.pick(w.T)
+    if served is None:
+        raise SystemExit(f"--tokens {w.T} exceeds every bucket ({args.bucket})")
     logits, _ = workloads.make_router_inputs(w, device)
     x = workloads.make_activations(w, device)
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             out, path = bucket.forward(logits, x, stream=stream)
     stream.synchronize()
-    assert path == "replay", path
+    assert path.startswith("replay"), path
     # the same L2 rule as the exact-shape steps: a working set that fits L2 is
     # flushed before every step and the steps' own spans are summed
-    touched = int((bucket.layer.counts > 0).sum().item())
-    ws_bytes = touched * 3 * w.d * w.I * 2 + B * (w.E * 4 + w.d * 2 + w.d * 4)
+    touched = int((served.layer.counts > 0).sum().item())
+    ws_bytes = touched * 3 * w.d * w.I * 2 + served.B * (w.E * 4 + w.d * 2 + w.d * 4)
     flush_l2 = ws_bytes < 2 * L2_BYTES
     flush_buf = torch.empty(L2_BYTES, dtype=torch.int32, device=device) if flush_l2 else None
     spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -684,14 +693,14 @@ def run_bucket(args, dist, w):
     if flush_l2:
         ms = sum(e0.elapsed_time(e1) for e0, e1 in spans)
     ms = dist.max(ms)
-    if int(bucket.layer.dev_status.item()) != 0:
+    if int(served.layer.dev_status.item()) != 0:
         raise RuntimeError("device status after bucket steps")
     return {"metric": METRIC, "value": round(dist.world * w.T * steps / (ms / 1e3), 2),
             "unit": "tokens/s", "n_gpus": dist.world, "steps": steps, "warmup": args.warmup,
             "ms_per_step": round(ms / steps, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "T": w.T, "bucket": B, "d": w.d, "E": w.E,
-                       "top_k": w.k, "I": w.I,
+            "config": {"workload": w.name, "T": w.T, "bucket": served.B,
+                       "buckets": sizes, "d": w.d, "E": w.E, "top_k": w.k, "I": w.I,
                        "path": "graph replay over the bucket, device-side valid count",
                        "step_working_set_bytes": int(ws_bytes),
                        "l2": ("flushed before every step (working set fits L2); value from "
@@ -699,7 +708,7 @@ def run_bucket(args, dist, w):
                               "the step's working set is over twice L2")},
             "timing": "each step: one staging kernel (input copies into the stable buffers and "
                       "the valid count), graph replay", "clocks": sampler.summary(),
-            "gpu_launches": steps * (1 + bucket.graph_launches)}
+            "gpu_launches": steps * (1 + served.graph_launches)}
 
 
 def run_extras(args, w, layer, stream, steps, layer_x=None):

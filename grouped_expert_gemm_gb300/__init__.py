@@ -5,6 +5,8 @@ composes the calls into one layer forward.
 """
 from . import abi  # noqa: F401
 from .abi import *  # noqa: F401,F403
-from .layer import DecodeBucket, HostPipeline, MoELayer, PooledMoELayer, capacity_from_factor  # noqa: F401
+from .layer import (DecodeBucket, DecodeBucketLadder, HostPipeline, MoELayer,  # noqa: F401
+                    PooledMoELayer, capacity_from_factor)
 
-__all__ = ["abi", "MoELayer", "PooledMoELayer", "DecodeBucket", "HostPipeline", "capacity_from_factor"] + abi.EXPORTED
+__all__ = ["abi", "MoELayer", "PooledMoELayer", "DecodeBucket", "DecodeBucketLadder", "HostPipeline",
+           "capacity_from_factor"] + abi.EXPORTED

@@ -371,6 +371,39 @@ class PooledMoELayer:
     forward_host = MoELayer.forward_host
 
 
+class DecodeBucketLadder:
+    """Decode steps over a ladder of fixed token buckets (for example 1, 2, 4, ..., 128
+    slots), each a DecodeBucket with its own stable buffers and captured graph over the
+    same weights.  A step replays the smallest bucket that holds its tokens, so a small
+    step runs the tile shapes of its own size instead of the largest bucket's; a step
+    larger than every bucket runs the eager layer (the largest bucket's fallback)."""
+
+    def __init__(self, sizes, d: int, E: int, k: int, I: int, w_gate, w_up, w_down, **kw):
+        sizes = sorted({int(b) for b in sizes})
+        if not sizes or sizes[0] < 1:
+            raise ValueError("bucket sizes must be positive")
+        self.sizes = sizes
+        self.buckets = [DecodeBucket(B, d, E, k, I, w_gate, w_up, w_down, **kw) for B in sizes]
+
+    def capture(self, stream=None):
+        for b in self.buckets:
+            b.capture(stream)
+
+    def pick(self, T: int) -> Optional["DecodeBucket"]:
+        """The smallest bucket with at least T slots, or None."""
+        for b in self.buckets:
+            if T <= b.B:
+                return b
+        return None
+
+    def forward(self, logits, x, phase: str = "decode", key=None, stream=None):
+        """One step; returns (out [T, d] fp32, path): "replay:B" for a replay of the
+        B-slot bucket, else the fallback reason."""
+        b = self.pick(int(logits.shape[0]))
+        out, path = (b or self.buckets[-1]).forward(logits, x, phase, key, stream)
+        return out, (f"replay:{b.B}" if path == "replay" else path)
+
+
 class HostPipeline:
     """Layer steps served from host-resident (pinned) inputs with the copies overlapped.
 

@@ -131,3 +131,22 @@ def test_bucket_stage_copies_the_inputs_and_the_count(T, E, d):
     assert torch.equal(ldst[:T], logits) and bool((ldst[T:] == -3.0).all())
     assert torch.equal(xdst[:T].view(torch.int16), x.view(torch.int16))
     assert bool((xdst[T:] == 5.0).all())
+
+
+def test_ladder_replays_the_smallest_bucket_bit_identical_to_eager():
+    """A ladder of buckets: each step replays the smallest bucket holding its tokens,
+    with the eager layer's bits; above the largest bucket it falls back."""
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.decode(128)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    ladder = g.DecodeBucketLadder([1, 4, 16], w.d, w.E, w.k, w.I, wg, wu, wd, device=DEV)
+    ladder.capture()
+    for T, want in [(1, "replay:1"), (3, "replay:4"), (4, "replay:4"), (11, "replay:16"),
+                    (17, "token_capacity_exceeded")]:
+        logits, x = _inputs(T, seed=100 + T)
+        out, path = ladder.forward(logits, x)
+        ref = g.MoELayer(T, **ladder.buckets[0].cfg).forward(logits, x)
+        torch.cuda.synchronize()
+        assert path == want, (T, path)
+        assert torch.equal(out, ref), T
+    assert ladder.pick(16).B == 16 and ladder.pick(17) is None
