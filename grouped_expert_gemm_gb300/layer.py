@@ -559,15 +559,26 @@ class DecodeBucket:
         """One step on T = logits.shape[0] tokens; returns (out [T, d] fp32, path)."""
         T = int(logits.shape[0])
         ok, why = self.admit(T, phase, key)
-        s = torch.cuda.current_stream() if stream is None else stream
+        cur = torch.cuda.current_stream()
+        s = cur if stream is None else stream
         if ok:
-            with torch.cuda.stream(s):
-                # the inputs into the stable buffers and the count, one kernel
-                lg = logits.to(torch.float32).contiguous()
-                xs = x.to(torch.bfloat16).contiguous()
-                abi.moe_bucket_stage(T, self.E, self.d, lg, xs, self.logits, self.x, self.valid, s)
-                self.graph.replay()
+            # a decode step's host cost adds to its latency: no stream switch when the step
+            # runs on the current stream, no conversion of inputs already in the right form
+            lg = logits if logits.dtype == torch.float32 and logits.is_contiguous() else \
+                logits.to(torch.float32).contiguous()
+            xs = x if x.dtype == torch.bfloat16 and x.is_contiguous() else \
+                x.to(torch.bfloat16).contiguous()
+            if s.cuda_stream == cur.cuda_stream:
+                self._replay(T, lg, xs, s)
+            else:
+                with torch.cuda.stream(s):
+                    self._replay(T, lg, xs, s)
             return self.layer.out[:T], "replay"
         if T not in self._eager:
             self._eager[T] = MoELayer(T, **self.cfg)
         return self._eager[T].forward(logits, x, s), why
+
+    def _replay(self, T, logits, x, s):
+        # the inputs into the stable buffers and the count (one kernel), then the graph
+        abi.moe_bucket_stage(T, self.E, self.d, logits, x, self.logits, self.x, self.valid, s)
+        self.graph.replay()
