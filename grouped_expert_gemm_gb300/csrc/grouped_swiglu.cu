@@ -1533,16 +1533,22 @@ int choose_bm(int32_t n_seg, int32_t max_rows) {
   return four_avg <= 16 ? 16 : four_avg <= 32 ? 32 : four_avg <= 64 ? 64 : kBM;
 }
 
-// Single-CTA gate/up tiles of 2 x 128 columns unless even one tile per touched
-// expert and n-block (at most min(n_seg, max_rows) experts hold rows) leaves SMs
-// without work -- one-token decode -- then 2 x 64 (with small-M boxes measured
-// 20.5 -> 18.4 us for the gate/up pass at T = 1; the down pass is better off wide).
+// Single-CTA gate/up tile width: 2 x 128 or 2 x 64 columns, whichever leaves the
+// busiest CTA less to do.  With at most min(n_seg, max_rows) experts holding rows,
+// the wide tiles take ceil(n / SMs) rounds per CTA and the narrow ones
+// ceil(2n / SMs) rounds of about 0.6 of a wide tile's time (narrow tiles stream
+// half the columns with the same per-tile start-up).  Measured on decode
+// (E = 128, top-8, I = 768), narrow against wide, µs per step: T = 1 narrow
+// (gate/up 18.4 against 20.5), T = 2 wide (43.7 against 47.7), T = 4 narrow
+// (64.2 against 66.2), T >= 8 wide (T = 128: 182.7 against 187.5).
 bool wide_gate_up(int32_t n_seg, int32_t max_rows, int32_t I) {
   if (I % 128 != 0) return false;
   static int sms = 0;
   if (sms == 0) sms = num_sms();
   const int64_t touched = n_seg < max_rows ? n_seg : max_rows;
-  return touched * (I / 128) >= sms;
+  const int64_t n_wide = touched * (I / 128);
+  const int64_t rounds_wide = ceil_div(n_wide, sms), rounds_narrow = ceil_div(2 * n_wide, sms);
+  return 10 * rounds_wide <= 6 * rounds_narrow;
 }
 
 bool pair_shape(int32_t n_seg, int32_t max_rows) {
