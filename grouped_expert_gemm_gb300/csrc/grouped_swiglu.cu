@@ -1533,22 +1533,27 @@ int choose_bm(int32_t n_seg, int32_t max_rows) {
   return four_avg <= 16 ? 16 : four_avg <= 32 ? 32 : four_avg <= 64 ? 64 : kBM;
 }
 
-// Single-CTA gate/up tile width: 2 x 128 or 2 x 64 columns, whichever leaves the
-// busiest CTA less to do.  With at most min(n_seg, max_rows) experts holding rows,
-// the wide tiles take ceil(n / SMs) rounds per CTA and the narrow ones
-// ceil(2n / SMs) rounds of about 0.6 of a wide tile's time (narrow tiles stream
-// half the columns with the same per-tile start-up).  Measured on decode
-// (E = 128, top-8, I = 768), narrow against wide, µs per step: T = 1 narrow
-// (gate/up 18.4 against 20.5), T = 2 wide (43.7 against 47.7), T = 4 narrow
-// (64.2 against 66.2), T >= 8 wide (T = 128: 182.7 against 187.5).
-bool wide_gate_up(int32_t n_seg, int32_t max_rows, int32_t I) {
-  if (I % 128 != 0) return false;
+// Single-CTA tile width: the wide tiles (gate/up 2 x 128 columns, down 256) or
+// the narrow ones (half as wide), whichever leaves the busiest CTA less to do.
+// With at most min(n_seg, max_rows) experts holding rows and wide_blocks wide
+// tiles per expert, the wide tiles take ceil(n / SMs) rounds per CTA and the
+// narrow ones ceil(2n / SMs) rounds of about 0.6 of a wide tile's time (half the
+// columns with the same per-tile start-up).  Measured on decode (E = 128, top-8,
+// d = 2048, I = 768), narrow against wide, µs per step: gate/up T = 1 narrow
+// (the pass 18.4 against 20.5), T = 2 wide (43.7 against 47.7), T = 4 narrow
+// (64.2 against 66.2), T >= 8 wide (T = 128: 182.7 against 187.5); down T = 1
+// narrow (37.5 against 38.6), T = 2 wide (51.8 against 53.3).
+bool wide_tiles(int32_t n_seg, int32_t max_rows, int64_t wide_blocks) {
   static int sms = 0;
   if (sms == 0) sms = num_sms();
   const int64_t touched = n_seg < max_rows ? n_seg : max_rows;
-  const int64_t n_wide = touched * (I / 128);
+  const int64_t n_wide = touched * wide_blocks;
   const int64_t rounds_wide = ceil_div(n_wide, sms), rounds_narrow = ceil_div(2 * n_wide, sms);
   return 10 * rounds_wide <= 6 * rounds_narrow;
+}
+
+bool wide_gate_up(int32_t n_seg, int32_t max_rows, int32_t I) {
+  return I % 128 == 0 && wide_tiles(n_seg, max_rows, I / 128);
 }
 
 bool pair_shape(int32_t n_seg, int32_t max_rows) {
@@ -1704,10 +1709,9 @@ static moe_status down_impl(int32_t n_seg, int32_t I, int32_t d, int32_t max_row
              dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0, bm, bm * kBK * 2,
              nullptr, 0, 0, chained};
   cudaStream_t s = as_cuda(stream);
-  // The widest output tile the width allows (narrower 128-row tiles for one-token
-  // decode were measured slower: the few tiles there are bound by pipeline latency).
   if (pair) return launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s);
-  if (d % 256 == 0) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
+  if (d % 256 == 0 && wide_tiles(n_seg, max_rows, d / 256))
+    return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
   if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
   return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
 }
