@@ -115,7 +115,7 @@ def decode_weights():
     return workloads.make_expert_weights(workloads.decode(128), DEV)
 
 
-@pytest.mark.parametrize("T", [1, 8, 32, 128])
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 32, 128])  # 1, 4: narrow gate/up tiles; 1: narrow down
 def test_decode_sweep_full(T, decode_weights):
     run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096)
 
