@@ -7,6 +7,7 @@ are rebuilt only when a source or header is newer than the library.
 from __future__ import annotations
 
 import concurrent.futures
+import fcntl
 import glob
 import os
 import shutil
@@ -49,9 +50,23 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library; returns its path."""
+    """Compile and link the library; returns its path.  Processes that build at the same
+    time (one per GPU under torchrun) take turns on a file lock: the first compiles, the
+    others then find the library up to date."""
     if not force and up_to_date():
         return LIBPATH
+    os.makedirs(LIBDIR, exist_ok=True)
+    with open(os.path.join(LIBDIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIBPATH
+            return _build_locked(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool) -> str:
     nvcc = _nvcc()
     objdir = os.path.join(LIBDIR, "obj")
     os.makedirs(objdir, exist_ok=True)
