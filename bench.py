@@ -7,6 +7,10 @@ clocks seen during the timed region, and the CPU oracle timed on a bounded sampl
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|tiny|prefill|v3|pooled]
                   [--tokens T] [--impl ours|reference]
 
+The default workload is the pooled 8-of-384 layer (T = 65,536 tokens, d = 3072,
+64 destinations x 6 local experts, top-8, 3 waves, I = 1536), the largest one that
+fits one GPU; the others are selected with --config.
+
 One JSON line on stdout (rank 0).  ``--impl reference`` times the CPU oracle on
 the same workload and prints the same line with "impl": "reference".
 """
@@ -23,6 +27,7 @@ import statistics
 import sys
 import threading
 import time
+import types
 
 import numpy as np
 import torch
@@ -43,7 +48,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode",
+    ap.add_argument("--config", default="pooled",
                     choices=["decode", "tiny", "prefill", "v3", "pooled"])
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
@@ -88,7 +93,8 @@ def workload_for(args) -> workloads.Workload:
     return w
 
 
-DEFAULT_STEPS = {"decode": 200, "tiny": 200, "prefill": 20, "v3": 10, "pooled": 5}
+# default timed steps: a timed region of at least about one second on every workload
+DEFAULT_STEPS = {"decode": 5000, "tiny": 2000, "prefill": 600, "v3": 240, "pooled": 120}
 
 
 # ----------------------------------------------------------------------------
@@ -499,7 +505,9 @@ def run_ours(args, dist, w):
         counts = layer.counts.cpu().numpy()
     I, d = w.I, w.d
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
-    long_region = max_ms > 2000.0
+    # a timed region of a second or more runs under the steady power cap: tensor-bound
+    # kernels are measured against the sustained bf16 peak there, the burst one otherwise
+    long_region = max_ms > 1000.0
     tf_peak = tf_sust if long_region else tf_burst
     per_stage = {}
     for n in stage_ms:
@@ -809,7 +817,11 @@ def config_dict(w, layer, ws_bytes=None, flush_l2=False):
                                 if layer.gather else "permuted copy written by the permute")
         if layer.payload != "bf16":
             c["payload_bytes_per_row"] = w.d + layer.xs.shape[1] * 4
-    if w.capacity_factor is not None:
+    if w.pooled:
+        c["capacity"] = ("fixed pools: sender factor {} (pool_cap rows per destination per "
+                         "wave), receiver factor {} (local_cap rows per local expert per wave)"
+                         .format(w.sender_cf, w.receiver_cf))
+    elif w.capacity_factor is not None:
         c["capacity_factor"] = w.capacity_factor
         c["capacity"] = layer.capacity
     else:
@@ -907,42 +919,43 @@ def run_e2e(args, dist, w, layer, logits, x, stream, steps, use_graph, flush_buf
 # the CPU oracle on a bounded sample (baseline leg and --impl reference)
 # ----------------------------------------------------------------------------
 
-def oracle_step(w, host_inputs, tokens):
-    """One oracle pass over the workload for the sampled `tokens` (routing, admission and
-    permutation over all tokens, expert math and combine for the sample)."""
+def oracle_batch(w, inputs):
+    """One pass of the oracle over a whole batch of tokens: routing, admission and
+    permutation (or, pooled, pack and compact in every wave), the SwiGLU of every
+    accepted route, and the fp32 combine.  `inputs` holds host copies of the batch's
+    logits and token rows (the batch's size is its number of rows), the selection
+    bias, a per-expert weight fetcher, the shared expert and the FP8 scale group.
+    Capacities follow the workload's capacity factors for this batch size."""
     import oracle
-    logits, sel_bias, xb, weights_of, shared, scale_group = host_inputs
+    logits, sel_bias, xb, weights_of, shared, scale_group = inputs
+    T, k = xb.shape[0], w.k
     if w.score_fn == "softmax":
-        ids, gates = oracle.route_softmax(logits, w.k)
+        ids, gates = oracle.route_softmax(logits, k)
     else:
-        ids, gates = oracle.route_sigmoid_group(logits, sel_bias, w.k, w.n_group, w.topk_group,
+        ids, gates = oracle.route_sigmoid_group(logits, sel_bias, k, w.n_group, w.topk_group,
                                                 w.route_scale)
     if w.pooled:
-        # the pooled layout's per-route fate over all waves; expert = local id
-        pc = oracle.pool_capacity(w.sender_cf, w.T, w.k, w.n_dest, w.n_waves)
-        lc = oracle.local_capacity(w.receiver_cf, w.T, w.k, w.local_per_dest, w.n_waves)
-        row_of = np.full(w.R, -1)
-        expert_of_row = {}
+        # each route's fate over all waves; its expert is the local id at its destination
+        pc = oracle.pool_capacity(w.sender_cf, T, k, w.n_dest, w.n_waves)
+        lc = oracle.local_capacity(w.receiver_cf, T, k, w.local_per_dest, w.n_waves)
+        row_of = np.full(T * k, -1)
         for wave in range(w.n_waves):
             rp = oracle.pool_pack(ids, xb, w.n_dest, w.local_per_dest, w.n_waves, pc, wave)
             rc = oracle.pool_compact(rp["pools"], pc, w.local_per_dest, lc)
             comp = oracle.compose_map(rp["route_to_poolrow"], rc["poolrow_to_row"])
             ok = comp >= 0
             row_of[ok] = comp[ok] + wave * w.local_per_dest * lc
-        perm = {"route_to_row": row_of}
+        route_to_row = row_of
         eids = ids % w.local_per_dest
     else:
-        cap = -1 if w.capacity_factor is None else oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
-        perm = oracle.permute(ids, w.E, cap)
+        cap = -1 if w.capacity_factor is None else oracle.capacity(w.capacity_factor, T, k, w.E)
+        route_to_row = oracle.permute(ids, w.E, cap)["route_to_row"]
         eids = ids
-    k = w.k
-    need = {}
-    for t in tokens:
-        for j in range(k):
-            if perm["route_to_row"][t * k + j] >= 0:
-                need.setdefault(int(eids[t, j]), []).append(t * k + j)
+    by_expert = {}
+    for r in np.nonzero(route_to_row >= 0)[0]:
+        by_expert.setdefault(int(eids.reshape(-1)[r]), []).append(int(r))
     y = {}
-    for e, routes in need.items():
+    for e, routes in by_expert.items():
         wg, wu, wd = weights_of(e)
         xr = xb[np.array(routes) // k]
         if scale_group is not None:  # FP8 payload: the experts see the dequantized rows
@@ -950,43 +963,56 @@ def oracle_step(w, host_inputs, tokens):
         _, ye = oracle.swiglu(oracle.bf16_to_f64(xr), oracle.bf16_to_f64(wg),
                               oracle.bf16_to_f64(wu), oracle.bf16_to_f64(wd))
         for i, r in enumerate(routes):
-            y[int(perm["route_to_row"][r])] = ye[i]
+            y[int(route_to_row[r])] = ye[i]
     sh = None
     if shared is not None:
         sg, su, sd = shared
-        _, sh = oracle.swiglu(oracle.bf16_to_f64(xb[np.array(tokens)]), oracle.bf16_to_f64(sg[0]),
+        _, sh = oracle.swiglu(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(sg[0]),
                               oracle.bf16_to_f64(su[0]), oracle.bf16_to_f64(sd[0]))
-    out = [oracle.combine_token(lambda r: y[r], perm["route_to_row"][t * k:(t + 1) * k], gates[t],
-                                None if sh is None else sh[i]) for i, t in enumerate(tokens)]
-    return out
+    return [oracle.combine_token(lambda r: y[r], route_to_row[t * k:(t + 1) * k], gates[t],
+                                 None if sh is None else sh[t]) for t in range(T)]
 
 
-def host_inputs_of(w, logits, sel_bias, x, layer):
-    """Host copies of the inputs (weights fetched per expert on demand)."""
+def host_inputs(logits, sel_bias, x, w_gate, w_up, w_down, shared=None, scale_group=None):
+    """Host copies of the inputs (expert weights fetched per expert on demand)."""
     cache = {}
 
     def weights_of(e):
         if e not in cache:
-            cache[e] = tuple(workloads.bf16_bits(t[e]) for t in (layer.w_gate, layer.w_up, layer.w_down))
+            cache[e] = tuple(workloads.bf16_bits(t[e]) for t in (w_gate, w_up, w_down))
         return cache[e]
-    shared = None
-    if getattr(layer, "shared", None) is not None:
-        shared = tuple(workloads.bf16_bits(t) for t in layer.shared)
+    sh = None if shared is None else tuple(workloads.bf16_bits(t) for t in shared)
     return (logits.cpu().numpy(), None if sel_bias is None else sel_bias.cpu().numpy(),
-            workloads.bf16_bits(x), weights_of, shared, getattr(layer, "scale_group", None))
+            workloads.bf16_bits(x), weights_of, sh, scale_group)
 
 
-def cpu_sample_tokens(w, budget_s, host_inputs, rng):
-    """Grow the token sample until one oracle pass takes about `budget_s` seconds."""
-    n = 1
+def first_tokens(inputs, n):
+    """The batch of the first n tokens of `inputs`."""
+    logits, sel_bias, xb, weights_of, shared, scale_group = inputs
+    return (logits[:n], sel_bias, xb[:n], weights_of, shared, scale_group)
+
+
+def oracle_sample(w, inputs, budget_s):
+    """A batch of the workload's first tokens (16, 32, 64, ... or all T) whose oracle
+    pass takes about `budget_s` seconds: doubled while a pass takes under half the
+    budget.  Returns (n, seconds of its last pass)."""
+    n = min(16, w.T)
     while True:
-        toks = np.sort(rng.choice(w.T, min(n, w.T), replace=False))
         t0 = time.perf_counter()
-        oracle_step(w, host_inputs, toks)
+        oracle_batch(w, first_tokens(inputs, n))
         dt = time.perf_counter() - t0
-        if dt >= budget_s * 0.5 or n >= w.T:
-            return toks, dt
-        n = min(w.T, n * 4 if dt < budget_s / 16 else n * 2)
+        if n >= w.T or dt * 2 > budget_s:
+            return n, dt
+        n = min(w.T, n * 2)
+
+
+def sample_text(w, n):
+    caps = "the capacities recomputed from the same factors for that batch size" \
+        if (w.pooled or w.capacity_factor is not None) else "dropless"
+    return (f"the first {n} of {w.T} tokens of {w.name} as a batch of their own ({caps}); "
+            f"each pass runs the whole oracle path on it: routing, "
+            f"{'pool pack and compact in every wave' if w.pooled else 'admission and permutation'}"
+            f", the fp64 SwiGLU of every accepted route, the combine")
 
 
 def cores():
@@ -1015,68 +1041,96 @@ def cpu_model():
     return None
 
 
+CORES_NOTE = ("threads available to the process; numpy runs its matrix products on the BLAS "
+              "thread pool over these cores and the rest of the oracle on one thread")
+
+
 def run_cpu_baseline(args, w, layer, logits, sel_bias, x):
-    hi = host_inputs_of(w, logits, sel_bias, x, layer)
-    rng = np.random.default_rng(0)
-    toks, dt = cpu_sample_tokens(w, args.cpu_budget, hi, rng)
-    # when the whole workload takes well under the budget, repeat it until the oracle has
-    # worked about that long, so the rate is not one short pass
+    inp = host_inputs(logits, sel_bias, x, layer.w_gate, layer.w_up, layer.w_down,
+                      getattr(layer, "shared", None), getattr(layer, "scale_group", None))
+    n, dt = oracle_sample(w, inp, args.cpu_budget)
+    # repeat the pass until the oracle has worked about the budget, so the rate is not
+    # one short pass
     passes, total = 1, dt
     while total < args.cpu_budget * 0.75 and passes < 64:
         t0 = time.perf_counter()
-        oracle_step(w, hi, toks)
+        oracle_batch(w, first_tokens(inp, n))
         total += time.perf_counter() - t0
         passes += 1
-    return {"value": round(len(toks) * passes / total, 4), "unit": "tokens/s", "cores": cores(),
-            "cpu_model": cpu_model(), "kind": "oracle",
-            "sample": f"{len(toks)} of {w.T} tokens of {w.name} (routing/admission over all "
-                      f"tokens, expert math + combine for the sample), {passes} pass"
-                      f"{'es' if passes > 1 else ''}, {total:.1f} s"}
+    return {"value": round(n * passes / total, 4), "unit": "tokens/s", "cores": cores(),
+            "cores_note": CORES_NOTE, "cpu_model": cpu_model(), "kind": "oracle",
+            "sample": f"{sample_text(w, n)}; {passes} pass{'es' if passes > 1 else ''}, "
+                      f"{total:.1f} s"}
+
+
+def oracle_layer_shape(w, wg, wu, wd):
+    """What the config line and the working-set count read from a layer, taken from the
+    workload and the oracle's capacities (the reference arm builds no layer)."""
+    import oracle
+    ns = types.SimpleNamespace(payload="bf16", gather=False, w_gate=wg, w_up=wu, w_down=wd)
+    if w.pooled:
+        ns.pool_cap = oracle.pool_capacity(w.sender_cf, w.T, w.k, w.n_dest, w.n_waves)
+        ns.local_cap = oracle.local_capacity(w.receiver_cf, w.T, w.k, w.local_per_dest,
+                                             w.n_waves)
+        ns.rows = w.local_per_dest * ns.local_cap
+        m = dict(dtype=torch.bfloat16, device="meta")
+        ns.pools = torch.empty((w.n_dest, ns.pool_cap + 1, w.d), **m)
+        ns.compact = torch.empty((ns.rows, w.d), **m)
+        ns.y = torch.empty((ns.rows, w.d), **m)
+    else:
+        ns.capacity = -1 if w.capacity_factor is None else \
+            oracle.capacity(w.capacity_factor, w.T, w.k, w.E)
+    return ns
 
 
 def run_reference(args, dist, w):
+    """The oracle, as it stands, on this workload's seeded inputs (drawn with the same
+    generators and device as our arm's, so the tensors are the same), timed on the host
+    cores.  Nothing of the CUDA library is built, loaded or called."""
     if dist.rank != 0:
         return None
+    import oracle
     steps = args.steps if args.steps is not None else 5
-    device = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    if device.type == "cuda":
-        from grouped_expert_gemm_gb300 import build
-        build.build()
-        layer, logits, sel_bias, x = build_layer(w, device)
-    else:
-        raise RuntimeError("the reference arm generates the same seeded inputs on the GPU")
-    hi = host_inputs_of(w, logits, sel_bias, x, layer)
-    # the same config object as our arm's line, its working set from the oracle's routing
+    if not torch.cuda.is_available():
+        raise RuntimeError("the reference arm draws the same seeded inputs on the GPU")
+    device = torch.device("cuda:0")
+    logits, sel_bias = workloads.make_router_inputs(w, device)
+    x = workloads.make_activations(w, device)
+    wg, wu, wd = workloads.make_expert_weights(w, device)
+    shared = workloads.make_shared_weights(w, device)
+    inp = host_inputs(logits, sel_bias, x, wg, wu, wd, shared)
+    shape = oracle_layer_shape(w, wg, wu, wd)
     touched = None
     if not w.pooled:
-        import oracle
         if w.score_fn == "softmax":
-            ids, _ = oracle.route_softmax(hi[0], w.k)
+            ids, _ = oracle.route_softmax(inp[0], w.k)
         else:
-            ids, _ = oracle.route_sigmoid_group(hi[0], hi[1], w.k, w.n_group, w.topk_group,
+            ids, _ = oracle.route_sigmoid_group(inp[0], inp[1], w.k, w.n_group, w.topk_group,
                                                 w.route_scale)
-        cap = -1 if w.capacity_factor is None else layer.capacity
-        touched = int((oracle.permute(ids, w.E, cap)["counts"] > 0).sum())
-    ws_bytes = working_set_bytes(w, layer, touched)
-    config = config_dict(w, layer, ws_bytes, ws_bytes < 2 * L2_BYTES)
-    rng = np.random.default_rng(0)
-    # size the per-step sample so that one step takes ~2 s of oracle work
-    toks, _ = cpu_sample_tokens(w, 4.0, hi, rng)
+        touched = int((oracle.permute(ids, w.E, shape.capacity)["counts"] > 0).sum())
+    ws_bytes = working_set_bytes(w, shape, touched)
+    config = config_dict(w, shape, ws_bytes, ws_bytes < 2 * L2_BYTES)
+    # per step a sample sized so that the whole --steps K --warmup W run takes a few
+    # minutes at most
+    budget = min(4.0, max(0.25, 150.0 / (steps + args.warmup + 2)))
+    n, _ = oracle_sample(w, inp, budget)
+    batch = first_tokens(inp, n)
     for _ in range(args.warmup):
-        oracle_step(w, hi, toks)
+        oracle_batch(w, batch)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle_step(w, hi, toks)
+        oracle_batch(w, batch)
     dt = time.perf_counter() - t0
-    value = len(toks) * steps / dt
-    sample = f"{len(toks)} of {w.T} tokens of {w.name} per step (routing/admission over all tokens)"
+    value = n * steps / dt
+    sample = f"{sample_text(w, n)}; one pass per step"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
             "n_gpus": 1, "steps": steps, "warmup": args.warmup,
             "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": config,
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores(),
-                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
+                             "cores_note": CORES_NOTE, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -49,6 +49,7 @@
 // MMAs in flight, frees its tensor memory and returns.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1426,11 +1427,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return true;
 }
 
+// SM count of the current device, read once per device (each entry is written
+// with the same value by whichever host thread gets there first).
 int num_sms() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev] = {};
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDev) {
+    n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < kMaxDev) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 template <int N_ATOMS, bool SWIGLU, bool FP8A = false, bool SMALLA = false>
@@ -1544,8 +1555,7 @@ int choose_bm(int32_t n_seg, int32_t max_rows) {
 // (64.2 against 66.2), T >= 8 wide (T = 128: 182.7 against 187.5); down T = 1
 // narrow (37.5 against 38.6), T = 2 wide (51.8 against 53.3).
 bool wide_tiles(int32_t n_seg, int32_t max_rows, int64_t wide_blocks) {
-  static int sms = 0;
-  if (sms == 0) sms = num_sms();
+  const int sms = num_sms();
   const int64_t touched = n_seg < max_rows ? n_seg : max_rows;
   const int64_t n_wide = touched * wide_blocks;
   const int64_t rounds_wide = ceil_div(n_wide, sms), rounds_narrow = ceil_div(2 * n_wide, sms);

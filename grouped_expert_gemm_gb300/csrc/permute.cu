@@ -426,7 +426,10 @@ std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_permute_scratch on the current device, looked up once per
-// device (in host code the array's name is only a host-side stand-in).
+// device (in host code the array's name is only a host-side stand-in).  The
+// cached address lives as long as the process; cudaDeviceReset unloads the module
+// on that device, after which the array may be placed elsewhere, so this entry
+// point is not for use after a device reset.
 moe_status static_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;

@@ -558,20 +558,28 @@ class DecodeBucket:
     def forward(self, logits, x, phase: str = "decode", key=None, stream=None):
         """One step on T = logits.shape[0] tokens; returns (out [T, d] fp32, path)."""
         T = int(logits.shape[0])
+        if tuple(logits.shape) != (T, self.E) or tuple(x.shape) != (T, self.d):
+            raise ValueError(f"expected logits [T, {self.E}] and x [T, {self.d}], got "
+                             f"{tuple(logits.shape)} and {tuple(x.shape)}")
         ok, why = self.admit(T, phase, key)
         cur = torch.cuda.current_stream()
         s = cur if stream is None else stream
         if ok:
             # a decode step's host cost adds to its latency: no stream switch when the step
             # runs on the current stream, no conversion of inputs already in the right form
-            lg = logits if logits.dtype == torch.float32 and logits.is_contiguous() else \
-                logits.to(torch.float32).contiguous()
-            xs = x if x.dtype == torch.bfloat16 and x.is_contiguous() else \
-                x.to(torch.bfloat16).contiguous()
-            if s.cuda_stream == cur.cuda_stream:
-                self._replay(T, lg, xs, s)
+            same = s.cuda_stream == cur.cuda_stream
+            convert = not (logits.dtype == torch.float32 and logits.is_contiguous()
+                           and x.dtype == torch.bfloat16 and x.is_contiguous())
+            if same and not convert:
+                self._replay(T, logits, x, s)
             else:
+                # conversions run on `s` after the caller's pending work, so the staging
+                # kernel reads finished inputs and the temporaries are freed to `s`
+                if not same:
+                    s.wait_stream(cur)
                 with torch.cuda.stream(s):
+                    lg = logits.to(torch.float32).contiguous()
+                    xs = x.to(torch.bfloat16).contiguous()
                     self._replay(T, lg, xs, s)
             return self.layer.out[:T], "replay"
         if T not in self._eager:

@@ -164,7 +164,9 @@ moe_status moe_permute(int32_t T, int32_t d, int32_t E, int32_t k, int32_t capac
  * up to E = 127 every size fits.  Nothing is allocated or freed.
  * The first call on a device looks up the array's device address for that
  * device (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture.  Every call on a device shares the one array and
+ * before any stream capture.  The address is kept for the life of the process:
+ * after cudaDeviceReset (which unloads the library's module on that device) this
+ * call must not be used again in the same process.  Every call on a device shares the one array and
  * it keeps the last call's contents (each call overwrites every entry it reads
  * before reading it, so nothing needs clearing).  Calls whose work overlaps on
  * the GPU -- other streams, other host threads -- race on the array: serialise

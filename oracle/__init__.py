@@ -9,8 +9,9 @@ is listed in tests/test_oracle_pins.py):
   route_softmax, route_sigmoid_group, sigmoid_det_f32, permute, combine,
   pool_pack, pool_compact, compose_map, capacity helpers: pinned.
   swiglu / grouped_swiglu_rows: pinned by special cases only (dense reduction
-  against an independent matmul, fused-equals-sum, closed form at d=I=1); the
-  pages print no SwiGLU output values.
+  against an independent matmul, fused-equals-sum, closed form at d=I=1, and
+  several segments with distinct scalar experts, each row against its own
+  expert's closed form); the pages print no SwiGLU output values.
 """
 from .moe_oracle import *  # noqa: F401,F403
 from .moe_oracle import EMPTY_HEADER  # noqa: F401

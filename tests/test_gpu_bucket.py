@@ -1,14 +1,16 @@
 """Decode graphs over a fixed token bucket ([M6.6] 0x05C-0x05F): padding slots are
-masked before they get expert identities, a replay gives the real tokens exactly
-the eager layer's result, and the exact admission predicate falls back to the
-eager layer without changing the result."""
+masked before they get expert identities, a replay gives the real tokens the
+oracle's routes, maps and outputs (and exactly the eager layer's bits), and the
+exact admission predicate falls back to the eager layer without changing the
+result."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
-from moe_check import bits, host
+from moe_check import (assert_float_parity, assert_gates, bits, host, oracle_token_outputs,
+                       weights_fetcher)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -21,13 +23,73 @@ def built():
 
 
 @pytest.fixture(scope="module")
-def bucket():
+def weights():
+    return workloads.make_expert_weights(workloads.decode(128), DEV)
+
+
+@pytest.fixture(scope="module")
+def bucket(weights):
     import grouped_expert_gemm_gb300 as g
     w = workloads.decode(128)
-    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    wg, wu, wd = weights
     b = g.DecodeBucket(128, w.d, w.E, w.k, w.I, wg, wu, wd, device=DEV)
     b.capture()
     return b
+
+
+@pytest.fixture(scope="module")
+def ladder(weights):
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.decode(128)
+    wg, wu, wd = weights
+    lad = g.DecodeBucketLadder([1, 2, 4, 8, 16, 32, 64, 128], w.d, w.E, w.k, w.I, wg, wu, wd,
+                               device=DEV)
+    lad.capture()
+    return lad
+
+
+@pytest.mark.parametrize("form", ["bucket", "ladder"])
+@pytest.mark.parametrize("T", [1, 3, 5, 37, 128])
+def test_replay_matches_the_oracle(request, weights, form, T):
+    """A replay against the oracle on the decode workload's own inputs: the real
+    tokens' ids, gates, counts, offsets and both maps (bit-exact or to the gate
+    tolerance), every expert row y and the real tokens' output; padding slots keep
+    masked ids, zero gates, -1 maps and zero output."""
+    import grouped_expert_gemm_gb300 as g
+    runner = request.getfixturevalue(form)
+    w = workloads.decode(T)
+    logits, _ = workloads.make_router_inputs(w, DEV)
+    x = workloads.make_activations(w, DEV)
+    out, path = runner.forward(logits, x)
+    torch.cuda.synchronize()
+    served = runner if form == "bucket" else runner.pick(T)
+    assert path == ("replay" if form == "bucket" else f"replay:{served.B}")
+    L, B, k = served.layer, served.B, w.k
+    assert int(L.dev_status.item()) == 0
+    ids, gates = oracle.route_softmax(host(logits), k)
+    perm = oracle.permute(ids, w.E, -1)
+    acc = int(perm["offsets"][-1])
+    assert np.array_equal(host(L.topk_ids)[:T], ids)
+    assert_gates(host(L.gates)[:T], gates)
+    assert np.array_equal(host(L.counts), perm["counts"])
+    assert np.array_equal(host(L.offsets), perm["offsets"])
+    assert np.array_equal(host(L.row_to_route)[:acc], perm["row_to_route"])
+    assert np.array_equal(host(L.route_to_row)[: T * k], perm["route_to_row"])
+    assert int(L.n_dropped.item()) == 0
+    # padding slots
+    assert np.all(host(L.topk_ids)[T:] == g.MOE_ROUTE_MASKED)
+    assert np.all(host(L.gates)[T:] == 0)
+    assert np.all(host(L.route_to_row)[T * k: B * k] == -1)
+    assert np.all(host(L.out)[T:] == 0)
+    # expert rows and the real tokens' output
+    xb = bits(x)
+    ref_out, y_of_row = oracle_token_outputs(w, np.arange(T), xb, ids, gates, perm,
+                                             weights_fetcher(*weights))
+    yrows = np.array(sorted(y_of_row))
+    assert yrows.size == acc
+    got_y = oracle.bf16_to_f64(bits(L.y[torch.from_numpy(yrows).to(DEV)]))
+    assert_float_parity(got_y, np.stack([y_of_row[r] for r in yrows]), "bucket replay y")
+    assert_float_parity(host(out), ref_out, "bucket replay output")
 
 
 def _inputs(T, seed, E=128, d=2048):
@@ -59,6 +121,38 @@ def test_replay_equals_eager_on_the_real_tokens(bucket, T):
     assert int(L.n_dropped.item()) == 0
     assert torch.all(L.out[T:] == 0)
     assert torch.equal(L.route_to_row[: T * k], eager.route_to_row[: T * k])
+
+
+def test_replay_on_a_side_stream_with_inputs_to_convert(bucket):
+    """Inputs that need conversion (fp16 logits, non-contiguous bf16 rows) written on
+    the current stream, the step on another stream: the conversions wait for the
+    writes and the replay gives the eager layer's bits."""
+    import grouped_expert_gemm_gb300 as g
+    T = 37
+    logits, x = _inputs(T, seed=77)
+    side = torch.cuda.Stream(DEV)
+    for _ in range(3):  # each time on freshly written inputs
+        lg16 = torch.empty((T, bucket.E), dtype=torch.float16, device=DEV)
+        xt = torch.empty((bucket.d, T), dtype=torch.bfloat16, device=DEV)
+        torch.cuda._sleep(2_000_000)  # the writes land well after the step is enqueued
+        lg16.copy_(logits)
+        xt.copy_(x.t())
+        out, path = bucket.forward(lg16, xt.t(), stream=side)
+        assert path == "replay"
+        torch.cuda.current_stream().wait_stream(side)
+        got = out.clone()
+        torch.cuda.synchronize()
+        ref = g.MoELayer(T, **bucket.cfg).forward(lg16.float(), xt.t().contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+
+
+def test_bucket_rejects_misshapen_inputs(bucket):
+    logits, x = _inputs(4, seed=3)
+    with pytest.raises(ValueError):
+        bucket.forward(logits[:, :64], x)
+    with pytest.raises(ValueError):
+        bucket.forward(logits, x[:3])
 
 
 def test_exact_admission_and_fallback(bucket):

@@ -55,6 +55,46 @@ def test_sigmoid_det_is_bitwise_identical_to_the_oracle():
     assert bad.size == 0, f"{bad.size} mismatches, first z={z[bad[:5]]}"
 
 
+@pytest.mark.slow
+def test_sigmoid_det_is_bitwise_identical_over_every_finite_fp32():
+    """Every finite fp32 input (both signs, zeros, subnormals, |z| >= 128): the GPU's
+    sigma_det and the oracle's give the same bits.  The oracle runs in chunks on a
+    pool of spawned processes while the GPU works through the same chunks; each side
+    reduces a chunk to a SHA-256 of its output bits, and a chunk whose digests differ
+    is recomputed here to name its first differing inputs."""
+    import hashlib
+    import multiprocessing as mp
+    import os
+
+    import sigmoid_chunks as sc
+    g = G()
+    chunks = sc.finite_chunks()
+    assert sum(n for _, n in chunks) == 2 * 0x7F800000
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(max(1, min(16, os.cpu_count() or 1))) as pool:
+        pending = pool.starmap_async(sc.oracle_chunk_digest, chunks)
+        gpu = []
+        zd = torch.empty(sc.CHUNK, dtype=torch.int32, device=DEV)
+        sd = torch.empty(sc.CHUNK, dtype=torch.float32, device=DEV)
+        for start, n in chunks:
+            signed = start - (1 << 32) if start >= (1 << 31) else start
+            torch.arange(signed, signed + n, dtype=torch.int32, device=DEV, out=zd[:n])
+            g.moe_sigmoid_det(n, zd[:n].view(torch.float32), sd[:n])
+            gpu.append(hashlib.sha256(host(sd[:n]).view(np.uint8)).hexdigest())
+        ref = pending.get(timeout=1800)
+    bad = [i for i, (a, b) in enumerate(zip(gpu, ref)) if a != b]
+    if bad:
+        start, n = chunks[bad[0]]
+        signed = start - (1 << 32) if start >= (1 << 31) else start
+        torch.arange(signed, signed + n, dtype=torch.int32, device=DEV, out=zd[:n])
+        g.moe_sigmoid_det(n, zd[:n].view(torch.float32), sd[:n])
+        got = host(sd[:n]).view(np.uint32)
+        want = sc.oracle_chunk(start, n).view(np.uint32)
+        where = np.nonzero(got != want)[0][:5]
+        raise AssertionError(f"{len(bad)} chunks differ; first inputs (bits) "
+                             f"{[hex(start + int(i)) for i in where]}")
+
+
 def _route(w, logits, sel_bias):
     g = G()
     score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP

@@ -12,8 +12,9 @@ import torch
 
 import oracle
 import workloads
-from moe_check import (assert_float_parity, assert_gates, bits, host, oracle_capacity,
-                       oracle_route, oracle_token_outputs, weights_fetcher)
+from moe_check import (assert_every_tile_reached, assert_float_parity, assert_gates, bits, host,
+                       oracle_capacity, oracle_expert_rows, oracle_route, oracle_token_outputs,
+                       stratified_rows, weights_fetcher, weights_fetcher_uncached)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -40,7 +41,9 @@ SCALE_GROUP = {"fp8_row": 0, "fp8_block128": 128}
 
 
 def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, payload="bf16",
-                  gather=False, fp8_loader="auto"):
+                  gather=False, fp8_loader="auto", every_tile=False):
+    """The layer on workload `w` against the oracle.  With every_tile, H and y are also
+    checked on rows that reach every 128-row m-tile of every expert segment."""
     logits, sel_bias = workloads.make_router_inputs(w, DEV)
     x = workloads.make_activations(w, DEV)
     wg, wu, wd = weights if weights is not None else workloads.make_expert_weights(w, DEV)
@@ -101,12 +104,22 @@ def run_and_check(w, sample_tokens=None, sample_rows=64, seed=0, weights=None, p
         assert_float_parity(got_y, np.stack([y_of_row[r] for r in yrows]), "expert rows y")
     got = host(out)[tokens]
     assert_float_parity(got, ref_out, "combined output")
+    if every_tile:
+        trows = stratified_rows(perm["offsets"][:-1], perm["counts"], rng)
+        assert_every_tile_reached(trows, perm["offsets"][:-1], perm["counts"])
+        seg = np.searchsorted(perm["offsets"], trows, side="right") - 1
+        tok = perm["row_to_route"][trows] // w.k
+        h_ref, y_ref = oracle_expert_rows(trows, seg, x_expert[tok],
+                                          weights_fetcher_uncached(wg, wu, wd))
+        idx = torch.from_numpy(trows).to(DEV)
+        assert_float_parity(oracle.bf16_to_f64(bits(layer.H[idx])), h_ref, "H on every m-tile")
+        assert_float_parity(oracle.bf16_to_f64(bits(layer.y[idx])), y_ref, "y on every m-tile")
     return layer, perm
 
 
 def test_tiny_full():
     w = workloads.tiny()
-    layer, perm = run_and_check(w)
+    layer, perm = run_and_check(w, every_tile=True)
     assert oracle.capacity(1.25, 256, 2, 8) == layer.capacity == 80
 
 
@@ -117,7 +130,7 @@ def decode_weights():
 
 @pytest.mark.parametrize("T", [1, 2, 4, 8, 32, 128])  # 1, 4: narrow gate/up tiles; 1: narrow down
 def test_decode_sweep_full(T, decode_weights):
-    run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096)
+    run_and_check(workloads.decode(T), weights=decode_weights, sample_rows=4096, every_tile=True)
 
 
 @pytest.mark.parametrize("case", ["decode_hot8", "tiny_hot2_capacity", "prefill_hot2",
@@ -162,12 +175,13 @@ def test_v3_small_full_gathered_rows():
 
 @pytest.mark.slow
 def test_prefill_full_size_sampled():
-    run_and_check(workloads.prefill(), sample_tokens=12, sample_rows=256, seed=2)
+    run_and_check(workloads.prefill(), sample_tokens=12, sample_rows=256, seed=2, every_tile=True)
 
 
 @pytest.mark.slow
 def test_v3_full_size_sampled():
-    layer, perm = run_and_check(workloads.v3(), sample_tokens=6, sample_rows=256, seed=3)
+    layer, perm = run_and_check(workloads.v3(), sample_tokens=6, sample_rows=256, seed=3,
+                                every_tile=True)
     assert layer.capacity == 256
     # capacity 1.0 with a skewed selection bias must actually drop routes
     assert perm["n_dropped"] > 0
@@ -281,6 +295,20 @@ def pooled_check(w, policy, sample_tokens, sample_rows, seed):
             keep = cr >= 0
             got_c = bits(layer.compact[torch.from_numpy(cr[keep]).to(DEV)])
             assert np.array_equal(got_c, xb[pick[keep] // w.k])
+        # H and y on rows reaching every 128-row m-tile of each local expert's array
+        begins = np.arange(w.local_per_dest) * local_cap
+        trows = stratified_rows(begins, rc["local_counts"], rng)
+        assert_every_tile_reached(trows, begins, rc["local_counts"])
+        route_of_row = np.full(w.local_per_dest * local_cap, -1)
+        route_of_row[comp[comp >= 0]] = np.nonzero(comp >= 0)[0]
+        assert np.all(route_of_row[trows] >= 0)
+        h_ref, y_ref = oracle_expert_rows(trows, trows // local_cap,
+                                          xb[route_of_row[trows] // w.k], fetch)
+        idx = torch.from_numpy(trows).to(DEV)
+        assert_float_parity(oracle.bf16_to_f64(bits(layer.H[idx])), h_ref,
+                            f"pooled H on every m-tile, wave {wave}")
+        assert_float_parity(oracle.bf16_to_f64(bits(layer.y[idx])), y_ref,
+                            f"pooled y on every m-tile, wave {wave}")
         # sampled expert rows and this wave's contribution to the sampled tokens
         for i, t in enumerate(tokens):
             for j in range(w.k):

@@ -369,6 +369,34 @@ def test_swiglu_closed_form_scalar():
     assert abs(y[0, 0] - expect_h * wd) < 1e-14
 
 
+def test_grouped_rows_use_each_segments_own_expert():
+    """Several segments with distinct scalar experts (d = I = 1): every row's h and y
+    equal the closed form of its own segment's expert, each rounded to bf16 by torch,
+    so a segment/expert mix-up, a shifted segment start or a dropped row fails."""
+    # expert q: (wg, wu, wd); values exact in bf16 and distinct per expert
+    experts = [(0.5, 3.0, 0.25), (-1.0, 2.0, 0.5), (2.0, -0.5, -1.5), (0.75, 1.25, 4.0)]
+    begins, counts = [0, 3, 3, 7], [3, 0, 4, 2]    # segment 1 is empty, 2 starts at row 3
+    xs = [1.0, -2.0, 0.5, 3.0, -0.25, 1.5, 2.5, -1.0, 0.125]
+    to_bits = lambda v: torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+    x = to_bits([[v] for v in xs])
+    wg = to_bits([[[e[0]]] for e in experts])
+    wu = to_bits([[[e[1]]] for e in experts])
+    wd = to_bits([[[e[2]]] for e in experts])
+    y, h = oracle.grouped_swiglu_rows(x, begins, counts, wg, wu, wd)
+    rows = [r for b, c in zip(begins, counts) for r in range(b, b + c)]
+    assert sorted(y) == rows and sorted(h) == rows
+    for q, (b, c) in enumerate(zip(begins, counts)):
+        g_w, u_w, d_w = experts[q]
+        for r in range(b, b + c):
+            g, u = xs[r] * g_w, xs[r] * u_w
+            h_ref = to_bits(g / (1.0 + math.exp(-g)) * u)
+            y_ref = to_bits(float(torch.from_numpy(h_ref.view(np.int16)).view(torch.bfloat16)
+                                  .to(torch.float64)) * d_w)
+            assert h[r].tolist() == [int(h_ref)], (q, r)
+            assert y[r].tolist() == [int(y_ref)], (q, r)
+
+
 def test_dense_reduction_matches_independent_library():
     """E = k = 1 dropless: the layer is one dense SwiGLU FFN (checked with torch CPU fp64)."""
     rng = np.random.default_rng(7)

@@ -1,4 +1,5 @@
-"""The allocation-free permute entry point (moe_permute_noalloc) against moe_permute.
+"""The allocation-free permute entry point (moe_permute_noalloc) against moe_permute
+and the oracle.
 
 moe_permute_noalloc serves callers that cannot call cudaMalloc and have no
 workspace to lend (an inference runtime's plugin hook that may only enqueue on
@@ -6,14 +7,17 @@ the stream it is given, a latency-critical loop where an allocation could
 synchronise the device).  It keeps its scratch in a fixed device array of the
 library, shared by every call, so the test makes two calls in a row on
 different inputs and checks that each matches moe_permute on the same input
-bit for bit (the bar for integer and byte outputs).  The file is collected last
-so that a run stopping at the first failure has run every other test already.
+bit for bit (the bar for integer and byte outputs), and that each matches the
+oracle's permutation.  The file is collected last so that a run stopping at
+the first failure has run every other test already.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -72,6 +76,16 @@ def test_noalloc_matches_permute_on_two_calls_in_a_row(lib, T, d, E, k, cap):
         assert torch.equal(got["route_to_row"][: T * k], ref["route_to_row"][: T * k])
         assert torch.equal(got["row_to_route"][:acc], ref["row_to_route"][:acc])
         assert torch.equal(got["x_perm"][:acc], ref["x_perm"][:acc])
+        # and the oracle's permutation of the same routes
+        orc = oracle.permute(ids_np.astype(np.int32), E, cap)
+        assert got["counts"].cpu().numpy().tolist() == orc["counts"].tolist()
+        assert got["offsets"].cpu().numpy().tolist() == orc["offsets"].tolist()
+        assert int(got["n_dropped"].item()) == orc["n_dropped"]
+        assert np.array_equal(got["route_to_row"][: T * k].cpu().numpy(), orc["route_to_row"])
+        assert np.array_equal(got["row_to_route"][:acc].cpu().numpy(), orc["row_to_route"])
+        xb = x.cpu().numpy().view(np.uint16)
+        assert np.array_equal(got["x_perm"][:acc].cpu().numpy().view(np.uint16),
+                              oracle.gather_rows(xb, orc["row_to_route"], k))
         outs.append(got)
     # the second call really saw different routing (the shared scratch was reused)
     assert not torch.equal(outs[0]["counts"], outs[1]["counts"])
