@@ -11,6 +11,8 @@
 // -inf, which ranks below every number.
 #include "common.cuh"
 
+#include <atomic>
+
 namespace moe {
 namespace {
 
@@ -223,11 +225,288 @@ route_kernel(int T, int E, int k, int n_group, int topk_group, float route_scale
   if (!early) pdl_trigger();
 }
 
+// ---- threshold-and-rank router ---------------------------------------------
+//
+// One warp per token at a time, in a grid-stride loop that loads the next
+// token's row while it selects the current one.  Lane l holds the VPL
+// consecutive experts l*VPL .. l*VPL + VPL - 1 (16-byte loads when the row
+// allows), so a contiguous group of experts spans whole lanes.
+//
+// Selection without k serial arg-max rounds: theta = the k-th largest of the 32
+// lane maxima (counted with multiplicity) is a lower bound of the k-th largest
+// score, since the k lanes holding those maxima hold k scores >= theta.  Every
+// score >= theta is a candidate; usually a dozen or two remain.  With at most 32
+// candidates each lane takes one (64-bit key: orderable score bits, then the
+// complement of the expert index) and its slot is the number of larger keys,
+// which orders by score descending with ties to the lower expert.  More than 32
+// candidates (heavy ties) fall back to k arg-max rounds.
+constexpr int kRouteWarps = 8;
+
+struct RouteArgs {
+  int T, E, k, n_group, topk_group;
+  float route_scale;
+  const float* logits;
+  const float* sel_bias;
+  int32_t* topk_ids;
+  float* gates;
+  uint32_t* dev_status;
+  const int32_t* valid;
+};
+
+template <int VPL, bool VEC>
+__device__ __forceinline__ void load_row(const float* __restrict__ row, int E, int lane,
+                                         float (&v)[VPL]) {
+  const int e0 = lane * VPL;
+  if (VEC) {
+#pragma unroll
+    for (int q = 0; q < VPL / 4; ++q) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + 4 * q < E) f = __ldg(reinterpret_cast<const float4*>(row + e0) + q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) v[c] = e0 + c < E ? __ldg(row + e0 + c) : 0.f;
+  }
+}
+
+template <int VPL, bool GROUPED, bool VEC>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_rank_kernel(RouteArgs a, bool early) {
+  __shared__ uint64_t s_key[kRouteWarps][32];
+  __shared__ float s_aff[kRouteWarps][32];
+  pdl_wait_then_trigger(early);
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int nwarps = gridDim.x * kRouteWarps;
+  const int E = a.E, k = a.k;
+  const int valid = a.valid != nullptr ? min(max(__ldg(a.valid), 0), a.T) : a.T;
+  float bias[VPL];
+#pragma unroll
+  for (int c = 0; c < VPL; ++c) {
+    const int e = lane * VPL + c;
+    bias[c] = (GROUPED && a.sel_bias != nullptr && e < E) ? __ldg(a.sel_bias + e) : 0.f;
+  }
+  int t = blockIdx.x * kRouteWarps + wib;
+  float cur[VPL];
+  if (t < valid) load_row<VPL, VEC>(a.logits + static_cast<int64_t>(t) * E, E, lane, cur);
+  bool saw_nan = false;
+  for (; t < a.T; t += nwarps) {
+    const int tn = t + nwarps;
+    float nxt[VPL];
+    if (tn < valid) load_row<VPL, VEC>(a.logits + static_cast<int64_t>(tn) * E, E, lane, nxt);
+    int32_t* ids_t = a.topk_ids + static_cast<int64_t>(t) * k;
+    float* gates_t = a.gates + static_cast<int64_t>(t) * k;
+    if (t >= valid) {
+      // padding slot of a fixed token bucket: no expert identity, zero gate
+      if (lane < k) { ids_t[lane] = MOE_ROUTE_MASKED; gates_t[lane] = 0.0f; }
+      continue;
+    }
+    // selection keys: 0 marks "not selectable" (the orderable bits of a number or
+    // -inf are never 0)
+    uint32_t u[VPL];
+    float aff[VPL];
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) {
+      const int e = lane * VPL + c;
+      float z = cur[c];
+      if (z != z) { saw_nan = true; z = -INFINITY; }
+      float sel = z;
+      aff[c] = 0.f;
+      if (GROUPED) {
+        aff[c] = sigmoid_det(z);
+        sel = __fadd_rn(aff[c], bias[c]);
+      }
+      cur[c] = sel;
+      u[c] = e < E ? ord_bits(sel) : 0u;
+    }
+    if (GROUPED) {
+      // group score: the sum of the two largest corrected scores of the group's
+      // gs / VPL lanes (a power of two), then the topk_group best groups
+      // (ties to the lower group), each lane ranking its own group by counting
+      const int gs = E / a.n_group, lpg = gs / VPL;
+      float b1 = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) {
+        if (lane * VPL + c < E) {
+          const float v = cur[c];
+          if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+        }
+      }
+      for (int o = 1; o < lpg; o <<= 1) {
+        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o);
+        const float o2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
+        const float n1 = fmaxf(b1, o1);
+        const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
+        b1 = n1; b2 = n2;
+      }
+      const float gsc = __fadd_rn(b1, b2);
+      const int g = lane / lpg;
+      int grank = 0;
+      for (int h = 0; h < a.n_group; ++h) {
+        const float sh = __shfl_sync(0xFFFFFFFFu, gsc, h * lpg);
+        grank += (sh > gsc) || (sh == gsc && h < g);
+      }
+      if (lane * VPL >= E || grank >= a.topk_group) {
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) u[c] = 0u;
+      }
+    }
+    // theta: the k-th largest lane maximum, with multiplicity; when fewer than k
+    // lanes hold a selectable score, every selectable score is a candidate
+    uint32_t m = u[0];
+#pragma unroll
+    for (int c = 1; c < VPL; ++c) m = max(m, u[c]);
+    uint32_t theta = 1u, top = 0u;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t M = __reduce_max_sync(0xFFFFFFFFu, m);
+      if (r == 0) top = M;
+      if (M == 0u) { theta = 1u; break; }
+      theta = M;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, m == M);
+      if (lane == __ffs(bal) - 1) m = 0u;
+    }
+    uint32_t cmask = 0;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) cmask |= (u[c] >= theta ? 1u : 0u) << c;
+    const int n = __popc(cmask);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int C = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    // what this lane ends with: slot `my_slot` (or -1) holding expert my_id
+    int my_slot = -1, my_id = 0;
+    float my_val = 0.f, my_aff = 0.f;
+    if (C <= 32) {
+      int p = incl - n;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) {
+        if ((cmask >> c) & 1u) {
+          const int e = lane * VPL + c;
+          s_key[wib][p] = (static_cast<uint64_t>(u[c]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+          s_aff[wib][p] = aff[c];
+          ++p;
+        }
+      }
+      __syncwarp();
+      const uint64_t mine = lane < C ? s_key[wib][lane] : 0ull;
+      int rank = 0;
+      for (int i = 0; i < C; ++i) rank += s_key[wib][i] > mine;
+      if (lane < C && rank < k) {
+        my_slot = rank;
+        my_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
+        my_val = ord_to_float(static_cast<uint32_t>(mine >> 32));
+        my_aff = s_aff[wib][lane];
+      }
+      __syncwarp();
+    } else {
+      // heavy ties: k rounds of warp arg-max (lowest expert among equal scores)
+      for (int j = 0; j < k; ++j) {
+        uint32_t lm = u[0];
+#pragma unroll
+        for (int c = 1; c < VPL; ++c) lm = max(lm, u[c]);
+        const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, lm);
+        uint32_t cand = 0xFFFFFFFFu;
+#pragma unroll
+        for (int c = VPL - 1; c >= 0; --c)
+          if (u[c] == gm) cand = static_cast<uint32_t>(lane * VPL + c);
+        const int e = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+        const int owner = e / VPL, slot = e - owner * VPL;
+        float av = 0.f;
+        if (lane == owner) {
+#pragma unroll
+          for (int c = 0; c < VPL; ++c)
+            if (c == slot) { u[c] = 0u; av = aff[c]; }
+        }
+        av = __shfl_sync(0xFFFFFFFFu, av, owner);
+        if (lane == j) { my_slot = j; my_id = e; my_val = ord_to_float(gm); my_aff = av; }
+      }
+    }
+    float g;
+    if (GROUPED) {
+      const float s = warp_sum(my_slot >= 0 ? my_aff : 0.0f);
+      g = a.route_scale * my_aff / s;
+    } else {
+      const float ex = my_slot >= 0 ? expf(my_val - ord_to_float(top)) : 0.0f;
+      const float s = warp_sum(ex);
+      g = ex / s;
+    }
+    if (my_slot >= 0) {
+      ids_t[my_slot] = my_id;
+      gates_t[my_slot] = g;
+    }
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) cur[c] = nxt[c];
+  }
+  if (__any_sync(0xFFFFFFFFu, saw_nan) && lane == 0) report(a.dev_status, MOE_DEV_NONFINITE_LOGIT);
+  if (!early) pdl_trigger();
+}
+
+// Resident blocks per SM of a route_rank_kernel instance, read once per device.
+template <int VPL, bool GROUPED, bool VEC>
+int route_rank_grid(int T) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> occ[kMaxDev] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int per_sm = (dev >= 0 && dev < kMaxDev) ? occ[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, route_rank_kernel<VPL, GROUPED, VEC>, kRouteWarps * 32, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    if (dev >= 0 && dev < kMaxDev) occ[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t need = ceil_div(T, kRouteWarps);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  return static_cast<int>(need < cap ? need : cap);
+}
+
+template <int VPL, bool GROUPED, bool VEC>
+void launch_rank(const RouteArgs& a, cudaStream_t s) {
+  const int grid = route_rank_grid<VPL, GROUPED, VEC>(a.T);
+  launch(route_rank_kernel<VPL, GROUPED, VEC>, dim3(grid), dim3(kRouteWarps * 32), 0, s, a,
+         one_wave(grid));
+}
+
+// Lanes per expert group of the rank kernel's layout when groups span whole
+// lanes in a power of two, else 0 (the grouped router then takes the one-slot-
+// per-lane kernel above).
+inline int lanes_per_group(int E, int n_group, int vpl) {
+  const int gs = E / n_group;
+  if (gs % vpl != 0) return 0;
+  const int lpg = gs / vpl;
+  return (lpg > 0 && lpg <= 32 && (lpg & (lpg - 1)) == 0) ? lpg : 0;
+}
+
 template <bool GROUPED>
 moe_status launch_route(const moe_route_params* p, const float* logits, const float* sel_bias,
                         int32_t* ids, float* gates, uint32_t* st, cudaStream_t s,
                         const int32_t* valid) {
-  const int vpl = static_cast<int>(ceil_div(p->E, 32));
+  int vpl = static_cast<int>(ceil_div(p->E, 32));
+  vpl = vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 12 ? 12 : 16;
+  if (!GROUPED || lanes_per_group(p->E, p->n_group, vpl) > 0) {
+    const RouteArgs a{p->T, p->E, p->k, p->n_group, p->topk_group, p->route_scale, logits,
+                      sel_bias, ids, gates, st, valid};
+    const bool vec = vpl % 4 == 0 && p->E % 4 == 0 && aligned16(logits);
+#define MOE_RANK_CASE(V)                                                   \
+  do {                                                                     \
+    if (vec) launch_rank<V, GROUPED, true>(a, s);                          \
+    else launch_rank<V, GROUPED, false>(a, s);                             \
+  } while (0)
+    switch (vpl) {
+      case 1: launch_rank<1, GROUPED, false>(a, s); break;
+      case 2: launch_rank<2, GROUPED, false>(a, s); break;
+      case 4: MOE_RANK_CASE(4); break;
+      case 8: MOE_RANK_CASE(8); break;
+      case 12: MOE_RANK_CASE(12); break;
+      default: MOE_RANK_CASE(16); break;
+    }
+#undef MOE_RANK_CASE
+    return launch_status();
+  }
   const dim3 grid(static_cast<unsigned>(ceil_div(p->T, kTokensPerBlock)));
   const dim3 block(kTokensPerBlock * 32);
   const bool early = one_wave(grid.x);
