@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--fp8-loader", default="auto", choices=["auto", "fused", "dequantize"],
                     help="FP8 payload: dequantize in the gate/up loader ('fused'), once into bf16 "
                          "rows before the bf16 pass ('dequantize'), or by rows per expert ('auto')")
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "fused", "separate"],
+                    help="decode-sized batches: the one-launch layer (fused), the per-stage "
+                         "calls (separate), or whichever the layer picks for the size (auto)")
     ap.add_argument("--gather", action="store_true",
                     help="bf16 payload: permute the maps only and gather the expert rows in the "
                          "gate/up loader instead of copying them in the permute")
@@ -77,6 +80,9 @@ def parse_args():
     ap.add_argument("--resume", action="store_true",
                     help="with --jsonl: if the file already holds a line for the same run "
                          "arguments, print that line and run nothing")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time the router alone on this workload's logits (a few MB on the "
+                         "device; for kernel profiling), one JSON line with its duration")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
@@ -215,6 +221,13 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
         row_b = d + layer.xs.shape[1] * 4
     if name == "route":
         return T * E * 4 + T * k * 8, 0
+    if name == "decode_layer":
+        # the whole layer in one launch: logits in, routes out, token rows in, the
+        # permuted copy, the touched experts' weights, H and y written, the fp32 output
+        # and the maps
+        b = (T * E * 4 + T * k * 8 + T * d * 2 + acc_rows * d * 2 + touched * 3 * d * I * 2
+             + acc_rows * I * 2 + acc_rows * d * 2 + T * d * 4 + 3 * T * k * 4 + (2 * E + 1) * 4)
+        return b, 6 * acc_rows * d * I
     if name == "quantize":
         return T * d * 2 + T * row_b, 0
     gather = getattr(layer, "gather", False)
@@ -262,12 +275,15 @@ def load_peaks():
 
 def kernel_source_sha(name):
     src = {"gate_up": "grouped_swiglu.cu", "down": "grouped_swiglu.cu",
+           "decode_layer": "decode.cu",
            "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
            "quantize": "fp8.cu", "dequantize": "fp8.cu",
            "combine": "combine.cu", "pool_pack": "pool.cu", "pool_compact": "pool.cu"}[name]
     h = hashlib.sha256()
-    # the kernel's own file and the header of helpers every kernel includes
-    for fn in (src, "common.cuh"):
+    # the kernel's own file, the router's device header where it is used, and the
+    # header of helpers every kernel includes
+    extra = ("route_dev.cuh",) if name in ("route", "decode_layer") else ()
+    for fn in (src,) + extra + ("common.cuh",):
         with open(os.path.join(ROOT, "grouped_expert_gemm_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -297,7 +313,7 @@ def lookup_traffic(stage, workload_name):
 # our arm
 # ----------------------------------------------------------------------------
 
-def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto"):
+def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", decode_path="auto"):
     import grouped_expert_gemm_gb300 as g
     if w.pooled and payload != "bf16":
         raise SystemExit("--payload applies to the routed (non-pooled) workloads")
@@ -316,7 +332,7 @@ def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto"):
                            n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                            sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
                            payload=payload, gather=gather, fp8_loader=fp8_loader,
-                           device=device)
+                           decode_path=decode_path, device=device)
     return layer, logits, sel_bias, x
 
 
@@ -343,7 +359,7 @@ def run_ours(args, dist, w):
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
     layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather,
-                                             args.fp8_loader)
+                                             args.fp8_loader, args.decode_path)
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _, _ in stages]
@@ -717,6 +733,51 @@ def run_bucket(args, dist, w):
             "timing": "each step: one staging kernel (input copies into the stable buffers and "
                       "the valid count), graph replay", "clocks": sampler.summary(),
             "gpu_launches": steps * (1 + served.graph_launches)}
+
+
+def run_route_only(args, dist, w):
+    """The router alone on the workload's seeded logits: `steps` launches timed with
+    CUDA events on the launching stream after `warmup` untimed ones, with the logits
+    (and outputs) rotated over enough copies that together they exceed twice the L2,
+    so every launch reads its logits from HBM."""
+    import grouped_expert_gemm_gb300 as g
+    from grouped_expert_gemm_gb300 import abi, build
+    build.build()
+    device = torch.device(f"cuda:{dist.local}")
+    torch.cuda.set_device(device)
+    logits, sel_bias = workloads.make_router_inputs(w, device)
+    nbytes = w.T * w.E * 4 + w.T * w.k * 8
+    copies = max(1, int(np.ceil(2 * L2_BYTES / max(nbytes, 1))) + 1)
+    banks = [logits] + [logits.clone() for _ in range(copies - 1)]
+    ids = [torch.empty((w.T, w.k), dtype=torch.int32, device=device) for _ in banks]
+    gates = [torch.empty((w.T, w.k), dtype=torch.float32, device=device) for _ in banks]
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    score = abi.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else abi.MOE_SCORE_SIGMOID_GROUP
+    p = abi.RouteParams(w.T, w.E, w.k, score, w.n_group, w.topk_group, w.route_scale)
+    stream = torch.cuda.Stream(device)
+    steps = args.steps if args.steps is not None else 200
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            b = i % copies
+            abi.moe_route(p, banks[b], sel_bias, ids[b], gates[b], st, stream)
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            b = i % copies
+            abi.moe_route(p, banks[b], sel_bias, ids[b], gates[b], st, stream)
+        e.record(stream)
+        stream.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    us = a.elapsed_time(e) / steps * 1e3
+    hbm, _, _, src = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"kernel": "route", "workload": w.name, "T": w.T, "E": w.E, "top_k": w.k,
+            "router": w.score_fn, "us_per_launch": round(us, 3), "alg_bytes": nbytes,
+            "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+            "peak_source": src, "launches": steps, "banks": copies}
 
 
 def run_extras(args, w, layer, stream, steps, layer_x=None):
@@ -1136,7 +1197,8 @@ def run_reference(args, dist, w):
 
 
 RUN_KEYS = ("impl", "gpus", "steps", "warmup", "config", "tokens", "bucket", "payload",
-            "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras")
+            "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras",
+            "route_only", "decode_path")
 
 
 def run_key(args) -> dict:
@@ -1185,6 +1247,11 @@ def main():
             res = run_reference(args, dist, w)
             if res is not None:
                 emit(res, args)
+            return
+        if args.route_only:
+            res = run_route_only(args, dist, w)
+            if dist.rank == 0:
+                print(json.dumps(res), flush=True)
             return
         if args.bucket:
             res = run_bucket(args, dist, w)

@@ -58,6 +58,7 @@ EXPORTED = [
     "moe_grouped_gate_up_fp8", "moe_grouped_gate_up_gather", "moe_expert_demand", "moe_validate_permutation",
     "moe_validate_pools_workspace_size", "moe_validate_pools",
     "moe_validate_compact_workspace_size", "moe_validate_compact", "moe_debug_wait_timeout",
+    "moe_decode_workspace_size", "moe_decode_layer",
 ]
 
 
@@ -89,6 +90,10 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_capacity": (_I64, [_I64, _I64, _I64, _I64]),
     "moe_route": (_I32, [ctypes.POINTER(RouteParams), _P, _P, _P, _P, _P, _P]),
+    "moe_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "moe_decode_layer": (_I32, [ctypes.POINTER(RouteParams), _I32, _I32, _I32, _P, _P, _P, _P, _P,
+                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P,
+                                _P]),
     "moe_sigmoid_det": (_I32, [_I64, _P, _P, _P]),
     "moe_permute_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "moe_permute": (_I32, [_I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -449,6 +454,22 @@ def moe_combine_bucket(T, k, d, valid_tokens, y, y_rows, route_to_row, gates, sh
         T, k, d, _ptr(valid_tokens), _ptr(y), y_rows, _ptr(route_to_row), _ptr(gates),
         _ptr(shared_y), int(accumulate), _ptr(out), _ptr(dev_status), _stream(stream)))
     _count(1 if T > 0 else 0)
+
+
+def moe_decode_workspace_size(T, d, E, k, I) -> int:
+    return lib().moe_decode_workspace_size(T, d, E, k, I)
+
+
+def moe_decode_layer(p: RouteParams, d, I, capacity, valid_tokens, logits, sel_bias, x, w_gate,
+                     w_up, w_down, topk_ids, gates, counts, offsets, row_to_route, route_to_row,
+                     n_dropped, x_perm, h, y, out, ws, ws_bytes, dev_status=None, stream=None):
+    _check("moe_decode_layer", lib().moe_decode_layer(
+        ctypes.byref(p), d, I, capacity, _ptr(valid_tokens), _ptr(logits), _ptr(sel_bias),
+        _ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(topk_ids), _ptr(gates),
+        _ptr(counts), _ptr(offsets), _ptr(row_to_route), _ptr(route_to_row), _ptr(n_dropped),
+        _ptr(x_perm), _ptr(h), _ptr(y), _ptr(out), _ptr(ws), ws_bytes, _ptr(dev_status),
+        _stream(stream)))
+    _count(1)
 
 
 def moe_expert_demand(T, k, E, valid_tokens, topk_ids, demand, dev_status=None, stream=None):

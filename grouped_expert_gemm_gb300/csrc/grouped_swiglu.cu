@@ -53,6 +53,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace moe {
 namespace {
@@ -61,7 +62,6 @@ constexpr int kBM = 128;          // rows per tile (MMA M)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int kMaxSeg = 1024;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s without progress = broken pipeline
 
 constexpr int kABytes = kBM * kBK * 2;        // 16 KB
 constexpr int kAtomBytes = kBK * 64 * 2;      // 8 KB: [64 K rows][64 N cols]
@@ -178,90 +178,6 @@ struct GemmArgs {
 };
 
 // ------------------------------ PTX wrappers -------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// CLUSTER: acquire at cluster scope (the phase was completed by a release of
-// another CTA of the cluster whose prior writes this thread relies on).
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  if constexpr (CLUSTER) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  }
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity` to complete.  Returns false when the
-// CTA is aborting (another role gave up) or when this wait itself times out.
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint32_t* dev_status,
-                                             uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      report(dev_status, MOE_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Short bounded wait used only while tearing down after an abort.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > 100000000ull) return;  // 100 ms
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c_inner, int32_t c_outer) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(c_outer)
-      : "memory");
-}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
@@ -1358,26 +1274,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }
 
 // ------------------------------ host side ----------------------------------
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
 
 // 2-D tensor [rows, cols] (cols contiguous) with a box of [box_rows, 64]
 // elements: bf16 with 128-byte swizzle, or (fp8) bytes with 64-byte swizzle.

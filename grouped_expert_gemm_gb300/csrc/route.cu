@@ -3,79 +3,19 @@
 //
 // [M6.2] 0x06L1 (family table), 0x06A-0x06D and 0x06I (V3 group rule and gate).
 //
-// One warp owns one token.  Lane l holds experts e = 32*i + l (coalesced 128-byte
-// row segments per load).  Each selection round is a warp all-reduce of 64-bit
-// keys (orderable score bits << 32 | ~expert), so the maximum key is the highest
-// score and, among equal scores, the lowest expert index; +0.0 and -0.0 are
-// folded together first so they tie.  NaN logits are reported and replaced by
-// -inf, which ranks below every number.
-#include "common.cuh"
+// Two kernels.  route_rank_kernel (every softmax router, and grouped routers
+// whose expert groups span whole lanes) selects by threshold and rank, see
+// route_token in route_dev.cuh.  route_kernel (the remaining grouped shapes)
+// gives lane l the experts 32*i + l and runs k rounds of a warp all-reduce of
+// 64-bit keys (orderable score bits << 32 | ~expert), so the maximum key is the
+// highest score and, among equal scores, the lowest expert index.  In both,
+// +0.0 and -0.0 tie, and NaN logits are reported and rank below every number.
+#include "route_dev.cuh"
 
 #include <atomic>
 
 namespace moe {
 namespace {
-
-// ---- deterministic fp32 sigmoid -------------------------------------------
-// e^x: Cody-Waite reduction with ln2 split at 16 significant bits, degree-7
-// Taylor polynomial of e^r in Horner form, scale by 2^n from exponent bits.
-// Every step is an explicitly rounded single fp32 operation (no contraction),
-// so a host implementation of the same steps gets identical bits.
-__device__ __forceinline__ float exp_det(float x) {
-  x = fminf(fmaxf(x, -87.0f), 87.0f);
-  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));                 // x * log2(e)
-  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0x1.62e4p-1f)),  // - n * ln2_hi
-                            __fmul_rn(n, 0x1.7f7d1cp-20f));            // - n * ln2_lo
-  float p = 0x1.a01a02p-13f;                                           // 1/7!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);                     // 1/6!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);                      // 1/5!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);                      // 1/4!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);                      // 1/3!
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);                                // 1/2!
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                                // 1/1!
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                                // 1/0!
-  const float two_n = __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23);
-  return __fmul_rn(p, two_n);
-}
-
-__device__ __forceinline__ float sigmoid_det(float z) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_det(-z)));
-}
-
-// Orderable bits of a float: unsigned comparison of the result follows float order.
-__device__ __forceinline__ uint32_t ord_bits(float v) {
-  if (v == 0.0f) v = 0.0f;  // fold -0.0 into +0.0
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float ord_to_float(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-
-__device__ __forceinline__ uint64_t make_key(float v, int e) {
-  return (static_cast<uint64_t>(ord_bits(v)) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
-}
-
-__device__ __forceinline__ int key_expert(uint64_t key) {
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-}
-
-// Warp maximum of 64-bit keys with two 32-bit reductions: the high words first,
-// then the low words of the lanes that hold the maximal high word.
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-  const uint32_t hi = static_cast<uint32_t>(v >> 32);
-  const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
-  const uint32_t lo = hi == mhi ? static_cast<uint32_t>(v) : 0u;
-  const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lo);
-  return (static_cast<uint64_t>(mhi) << 32) | mlo;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
 
 constexpr int kTokensPerBlock = 8;
 
@@ -253,28 +193,10 @@ struct RouteArgs {
   const int32_t* valid;
 };
 
-template <int VPL, bool VEC>
-__device__ __forceinline__ void load_row(const float* __restrict__ row, int E, int lane,
-                                         float (&v)[VPL]) {
-  const int e0 = lane * VPL;
-  if (VEC) {
-#pragma unroll
-    for (int q = 0; q < VPL / 4; ++q) {
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + 4 * q < E) f = __ldg(reinterpret_cast<const float4*>(row + e0) + q);
-      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) v[c] = e0 + c < E ? __ldg(row + e0 + c) : 0.f;
-  }
-}
-
 template <int VPL, bool GROUPED, bool VEC>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_rank_kernel(RouteArgs a, bool early) {
-  __shared__ uint64_t s_key[kRouteWarps][32];
-  __shared__ float s_aff[kRouteWarps][32];
+  __shared__ RouteSmem<VPL, GROUPED> s_route[kRouteWarps];
   pdl_wait_then_trigger(early);
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int nwarps = gridDim.x * kRouteWarps;
@@ -301,141 +223,12 @@ route_rank_kernel(RouteArgs a, bool early) {
       if (lane < k) { ids_t[lane] = MOE_ROUTE_MASKED; gates_t[lane] = 0.0f; }
       continue;
     }
-    // selection keys: 0 marks "not selectable" (the orderable bits of a number or
-    // -inf are never 0)
-    uint32_t u[VPL];
-    float aff[VPL];
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) {
-      const int e = lane * VPL + c;
-      float z = cur[c];
-      if (z != z) { saw_nan = true; z = -INFINITY; }
-      float sel = z;
-      aff[c] = 0.f;
-      if (GROUPED) {
-        aff[c] = sigmoid_det(z);
-        sel = __fadd_rn(aff[c], bias[c]);
-      }
-      cur[c] = sel;
-      u[c] = e < E ? ord_bits(sel) : 0u;
-    }
-    if (GROUPED) {
-      // group score: the sum of the two largest corrected scores of the group's
-      // gs / VPL lanes (a power of two), then the topk_group best groups
-      // (ties to the lower group), each lane ranking its own group by counting
-      const int gs = E / a.n_group, lpg = gs / VPL;
-      float b1 = -INFINITY, b2 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < VPL; ++c) {
-        if (lane * VPL + c < E) {
-          const float v = cur[c];
-          if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-        }
-      }
-      for (int o = 1; o < lpg; o <<= 1) {
-        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o);
-        const float o2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
-        const float n1 = fmaxf(b1, o1);
-        const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
-        b1 = n1; b2 = n2;
-      }
-      const float gsc = __fadd_rn(b1, b2);
-      const int g = lane / lpg;
-      int grank = 0;
-      for (int h = 0; h < a.n_group; ++h) {
-        const float sh = __shfl_sync(0xFFFFFFFFu, gsc, h * lpg);
-        grank += (sh > gsc) || (sh == gsc && h < g);
-      }
-      if (lane * VPL >= E || grank >= a.topk_group) {
-#pragma unroll
-        for (int c = 0; c < VPL; ++c) u[c] = 0u;
-      }
-    }
-    // theta: the k-th largest lane maximum, with multiplicity; when fewer than k
-    // lanes hold a selectable score, every selectable score is a candidate
-    uint32_t m = u[0];
-#pragma unroll
-    for (int c = 1; c < VPL; ++c) m = max(m, u[c]);
-    uint32_t theta = 1u, top = 0u;
-    for (int r = 0; r < k; ++r) {
-      const uint32_t M = __reduce_max_sync(0xFFFFFFFFu, m);
-      if (r == 0) top = M;
-      if (M == 0u) { theta = 1u; break; }
-      theta = M;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, m == M);
-      if (lane == __ffs(bal) - 1) m = 0u;
-    }
-    uint32_t cmask = 0;
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) cmask |= (u[c] >= theta ? 1u : 0u) << c;
-    const int n = __popc(cmask);
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int C = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    // what this lane ends with: slot `my_slot` (or -1) holding expert my_id
-    int my_slot = -1, my_id = 0;
-    float my_val = 0.f, my_aff = 0.f;
-    if (C <= 32) {
-      int p = incl - n;
-#pragma unroll
-      for (int c = 0; c < VPL; ++c) {
-        if ((cmask >> c) & 1u) {
-          const int e = lane * VPL + c;
-          s_key[wib][p] = (static_cast<uint64_t>(u[c]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
-          s_aff[wib][p] = aff[c];
-          ++p;
-        }
-      }
-      __syncwarp();
-      const uint64_t mine = lane < C ? s_key[wib][lane] : 0ull;
-      int rank = 0;
-      for (int i = 0; i < C; ++i) rank += s_key[wib][i] > mine;
-      if (lane < C && rank < k) {
-        my_slot = rank;
-        my_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
-        my_val = ord_to_float(static_cast<uint32_t>(mine >> 32));
-        my_aff = s_aff[wib][lane];
-      }
-      __syncwarp();
-    } else {
-      // heavy ties: k rounds of warp arg-max (lowest expert among equal scores)
-      for (int j = 0; j < k; ++j) {
-        uint32_t lm = u[0];
-#pragma unroll
-        for (int c = 1; c < VPL; ++c) lm = max(lm, u[c]);
-        const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, lm);
-        uint32_t cand = 0xFFFFFFFFu;
-#pragma unroll
-        for (int c = VPL - 1; c >= 0; --c)
-          if (u[c] == gm) cand = static_cast<uint32_t>(lane * VPL + c);
-        const int e = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
-        const int owner = e / VPL, slot = e - owner * VPL;
-        float av = 0.f;
-        if (lane == owner) {
-#pragma unroll
-          for (int c = 0; c < VPL; ++c)
-            if (c == slot) { u[c] = 0u; av = aff[c]; }
-        }
-        av = __shfl_sync(0xFFFFFFFFu, av, owner);
-        if (lane == j) { my_slot = j; my_id = e; my_val = ord_to_float(gm); my_aff = av; }
-      }
-    }
-    float g;
-    if (GROUPED) {
-      const float s = warp_sum(my_slot >= 0 ? my_aff : 0.0f);
-      g = a.route_scale * my_aff / s;
-    } else {
-      const float ex = my_slot >= 0 ? expf(my_val - ord_to_float(top)) : 0.0f;
-      const float s = warp_sum(ex);
-      g = ex / s;
-    }
-    if (my_slot >= 0) {
-      ids_t[my_slot] = my_id;
-      gates_t[my_slot] = g;
+    const RouteLane r = route_token<VPL, GROUPED>(cur, bias, lane, E, k, a.n_group,
+                                                  a.topk_group, a.route_scale, s_route[wib],
+                                                  saw_nan);
+    if (r.slot >= 0) {
+      ids_t[r.slot] = r.id;
+      gates_t[r.slot] = r.gate;
     }
 #pragma unroll
     for (int c = 0; c < VPL; ++c) cur[c] = nxt[c];

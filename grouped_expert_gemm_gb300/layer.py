@@ -49,7 +49,7 @@ class MoELayer:
                  capacity: int = -1, score_fn: int = abi.MOE_SCORE_SOFTMAX, n_group: int = 1,
                  topk_group: int = 1, route_scale: float = 1.0, sel_bias=None,
                  shared_weights=None, payload: str = "bf16", gather: bool = False,
-                 fp8_loader: str = "auto", device="cuda"):
+                 fp8_loader: str = "auto", decode_path: str = "auto", device="cuda"):
         self.T, self.d, self.E, self.k, self.I = T, d, E, k, I
         if payload not in PAYLOADS:
             raise ValueError(f"payload must be one of {sorted(PAYLOADS)}")
@@ -114,6 +114,38 @@ class MoELayer:
             # stream from the start of the step, beside routing and permutation
             # (which leave the tensor cores idle), and joins before the combine.
             self.side = torch.cuda.Stream(dev)
+        # Decode-sized batches (at most 64 routes) can run the whole layer as one launch
+        # (moe_decode_layer, decode_path="fused").  "auto" keeps the per-stage calls:
+        # on the decode shape they measured faster at every size (T = 1: 37.8 against
+        # 47.6 us per step; T = 8: 78.5 against 107 us), the tensor-core passes
+        # streaming the weights faster than the one-launch kernel's CUDA-core units.
+        if decode_path not in ("auto", "fused", "separate"):
+            raise ValueError("decode_path must be 'auto', 'fused' or 'separate'")
+        ok = self.decode_supported(T, d, E, k, I, score_fn, n_group) and payload == "bf16" \
+            and not self.gather and shared_weights is None
+        if decode_path == "fused" and not ok:
+            raise ValueError("this layer's shape or options do not allow the one-launch decode path")
+        self.fused = ok and decode_path == "fused"
+        if self.fused:
+            self.decode_ws_bytes = abi.moe_decode_workspace_size(T, d, E, k, I)
+            # zero-filled once: every call leaves its counters zero again
+            self.decode_ws = torch.zeros(self.decode_ws_bytes, dtype=torch.uint8, device=dev)
+
+    @staticmethod
+    def decode_supported(T, d, E, k, I, score_fn=abi.MOE_SCORE_SOFTMAX, n_group=1) -> bool:
+        """Whether moe_decode_layer takes this shape (the library's limits: at most 64
+        routes and 16 tokens, T*d <= 16384, I <= 2048, d and I multiples of 64; a grouped
+        router's groups spanning a power of two of lanes)."""
+        if abi.moe_decode_workspace_size(T, d, E, k, I) == 0:
+            return False
+        if score_fn == abi.MOE_SCORE_SIGMOID_GROUP:
+            vpl = next(v for v in (1, 2, 4, 8, 12, 16) if v * 32 >= E)
+            gs = E // n_group
+            if gs % vpl:
+                return False
+            lpg = gs // vpl
+            return 0 < lpg <= 32 and lpg & (lpg - 1) == 0
+        return True
 
     @property
     def H(self) -> torch.Tensor:
@@ -211,12 +243,24 @@ class MoELayer:
                         self.shared_y if self.shared is not None else None, 0,
                         self.out if out is None else out, self.dev_status, stream)
 
+    def decode_layer(self, logits, x, stream=None, out=None, valid_tokens=None):
+        """The whole layer in one launch (moe_decode_layer): the same routing, maps,
+        permuted rows, H, y and fp32 output as the per-stage calls."""
+        abi.moe_decode_layer(self.params, self.d, self.I, self.capacity, valid_tokens, logits,
+                             self.sel_bias, x, self.w_gate, self.w_up, self.w_down,
+                             self.topk_ids, self.gates, self.counts, self.offsets,
+                             self.row_to_route, self.route_to_row, self.n_dropped, self.x_perm,
+                             self.H, self.y, self.out if out is None else out, self.decode_ws,
+                             self.decode_ws_bytes, self.dev_status, stream)
+
     def stages(self, logits, x, out=None):
         """The layer as (name, callable(stream), side_stream) steps in launch order.  A
         step with a side stream launches there whatever stream it is given (the fork
         and join steps order it against the main stream); the others launch on the
         stream they are given.  The fp32 result goes to `out` (default: the layer's
         own buffer)."""
+        if self.fused:
+            return [("decode_layer", lambda s: self.decode_layer(logits, x, s, out), None)]
         st = []
         if self.shared is not None:
             st += [("shared_fork", self.shared_fork, None),
@@ -516,6 +560,9 @@ class DecodeBucket:
         """The bucketed layer on the stable buffers (what the graph holds)."""
         L = self.layer
         R = self.B * self.k
+        if L.fused:
+            L.decode_layer(self.logits, self.x, stream, valid_tokens=self.valid)
+            return
         abi.moe_route_bucket(L.params, self.valid, self.logits, L.sel_bias, L.topk_ids, L.gates,
                              L.dev_status, stream)
         abi.moe_permute_bucket(self.B, self.d, self.E, self.k, L.capacity, self.valid,

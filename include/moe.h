@@ -272,6 +272,52 @@ moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64
                        uint32_t* dev_status, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* One-launch layer for small batches (decode)                              */
+/* ------------------------------------------------------------------------ */
+/* The whole layer -- moe_route, moe_permute, moe_grouped_swiglu and
+ * moe_combine of [M6.6] 0x03-0x04 and 0x0AE -- as ONE kernel launch, for
+ * decode-sized batches (at most 64 routes).  At that size the step is a stream
+ * of the touched experts' weights ([M6.6] 0x05: decode is latency-bound), so one
+ * launch whose every SM streams weights replaces six dependent kernels.
+ * Arguments and outputs are those of the four calls, with:
+ *   p            router parameters (p->T tokens; either score function);
+ *   capacity     per-expert capacity, -1 for dropless (admission in route-id
+ *                order, as moe_permute);
+ *   valid_tokens NULL, or a device int32: tokens t >= *valid_tokens are padding
+ *                slots of a fixed token bucket, as moe_route_bucket /
+ *                moe_permute_bucket / moe_combine_bucket treat them;
+ *   x [T,d] bf16 token rows; w_gate, w_up [E,d,I], w_down [E,I,d] bf16;
+ *   topk_ids, gates [T,k]; counts [E]; offsets [E+1]; row_to_route,
+ *   route_to_row [T*k]; n_dropped [1] -- exactly as moe_route / moe_permute;
+ *   x_perm [T*k,d] the permuted rows (may be NULL: not written);
+ *   h [T*k,I] the SwiGLU intermediate, y [T*k,d] the expert rows (row space of
+ *   the permutation); out [T,d] fp32, accumulate = 0, no shared expert.
+ * Integer outputs are identical to those calls'.  The expert arithmetic runs on
+ * CUDA cores with fp32 accumulation (a segment holds a row or two) in a fixed
+ * order, so h and y can differ from the tensor-core pass by a bf16 rounding
+ * where the two fp32 sums straddle a rounding boundary; out is summed in slot
+ * order in fp32 exactly like moe_combine.  Results are deterministic.
+ * Workspace: moe_decode_workspace_size() bytes (0 = shape unsupported; a few
+ * hundred bytes of counters), owned by the caller and ZERO-FILLED before its
+ * first use; every call leaves the counters zero again, so it can be reused
+ * (and the call replayed from a CUDA graph) without clearing.  Two calls whose work overlaps on the GPU
+ * must not share one workspace.  A bounded wait inside the kernel that gives up
+ * sets MOE_DEV_TIMEOUT (outputs then invalid).
+ * Limits (else MOE_ERR_UNSUPPORTED): 1 <= T <= 16, T*k <= 64, T*d <= 16384,
+ * I <= 2048, d % 64 == 0, I % 64 == 0, E <= 512, k <= 16; grouped routers as moe_route
+ * plus (E/n_group) a multiple of ceil-to-{1,2,4,8,12,16}(E/32) spanning a power
+ * of two of lanes; pointers 16-byte aligned.                                 */
+size_t moe_decode_workspace_size(int32_t T, int32_t d, int32_t E, int32_t k, int32_t I);
+moe_status moe_decode_layer(const moe_route_params* p, int32_t d, int32_t I, int32_t capacity,
+                            const int32_t* valid_tokens, const float* logits,
+                            const float* sel_bias, const moe_bf16* x, const moe_bf16* w_gate,
+                            const moe_bf16* w_up, const moe_bf16* w_down, int32_t* topk_ids,
+                            float* gates, int32_t* counts, int32_t* offsets,
+                            int32_t* row_to_route, int32_t* route_to_row, int32_t* n_dropped,
+                            moe_bf16* x_perm, moe_bf16* h, moe_bf16* y, float* out, void* ws,
+                            size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Pooled-wave static-shape layout (in-memory only; no communication)       */
 /* ------------------------------------------------------------------------ */
 typedef struct {

@@ -108,7 +108,7 @@ def test_replay_equals_eager_on_the_real_tokens(bucket, T):
     assert path == "replay"
     L = bucket.layer
     assert int(L.dev_status.item()) == 0
-    eager = g.MoELayer(T, **bucket.cfg)
+    eager = g.MoELayer(T, **bucket.cfg, decode_path="separate")  # the 128-slot bucket's path
     ref = eager.forward(logits, x)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)  # same routes, rows, tiles: identical bits
