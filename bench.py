@@ -53,6 +53,10 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=None,
                     help="token count T (decode: 1, 8, 32 or 128, default 128; other workloads: "
                          "a smaller T for short profiling runs)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="a smaller expert count E (the same recipe otherwise; for short "
+                         "profiling runs that keep per-expert shapes, e.g. v3 with 32 experts "
+                         "and 1,024 tokens has the full workload's 256 rows per expert)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--bucket", default="",
                     help="decode: replay one captured graph over a fixed bucket of this many "
@@ -96,6 +100,10 @@ def workload_for(args) -> workloads.Workload:
          "pooled": workloads.pooled}[args.config]()
     if args.tokens:
         w = workloads.scaled(w, T=args.tokens, name=f"{w.name}_T{args.tokens}")
+    if args.experts:
+        if w.pooled:
+            raise SystemExit("--experts applies to the routed (non-pooled) workloads")
+        w = workloads.scaled(w, E=args.experts, name=f"{w.name}_E{args.experts}")
     return w
 
 
@@ -291,13 +299,15 @@ def kernel_source_sha(name):
 
 def lookup_traffic(stage, workload_name):
     """DRAM bytes per launch of `stage` from a committed ncu summary, if it was taken
-    on the current kernel source (profiles/*.md lines 'traffic: <stage> <workload>
-    <bytes_per_launch> <source sha256[:16]>')."""
+    on the current kernel source: (bytes, note) from profiles/*.md lines
+    'traffic: <stage> <workload> <bytes_per_launch> <source sha256[:16]> [note]', the
+    note saying how a capture of a smaller case was scaled to a full launch; else
+    (None, None)."""
     prof = os.path.join(ROOT, "profiles")
     if not os.path.isdir(prof):
-        return None
+        return None, None
     sha = kernel_source_sha(stage)
-    pat = re.compile(r"^traffic:\s+(\S+)\s+(\S+)\s+(\d+)\s+([0-9a-f]{16})\s*$")
+    pat = re.compile(r"^traffic:\s+(\S+)\s+(\S+)\s+(\d+)\s+([0-9a-f]{16})(?:\s+(.*))?$")
     for fn in sorted(os.listdir(prof)):
         if not fn.endswith(".md"):
             continue
@@ -305,8 +315,8 @@ def lookup_traffic(stage, workload_name):
             for line in f:
                 m = pat.match(line.strip())
                 if m and m.group(1) == stage and m.group(2) == workload_name and m.group(4) == sha:
-                    return int(m.group(3))
-    return None
+                    return int(m.group(3)), (m.group(5) or None)
+    return None, None
 
 
 # ----------------------------------------------------------------------------
@@ -543,7 +553,7 @@ def run_ours(args, dist, w):
                         "bound": bound, "achieved": round(achieved, 2),
                         "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                         "frac": round(frac, 4), "alg_bytes": int(b), "alg_flops": int(f),
-                        "traffic": lookup_traffic(n, traffic_key(w, layer))}
+                        "traffic": lookup_traffic(n, traffic_key(w, layer))[0]}
         if n == "permute" and getattr(layer, "gather", False):
             per_stage[n]["note"] = ("maps only (counts, offsets, both maps): the gate/up loader "
                                     "gathers the expert rows from token order, so no row is "
@@ -555,10 +565,13 @@ def run_ours(args, dist, w):
     # the dominant kernel among the main-stream stages (a side-stream figure is a span)
     dom = max((n for n in stage_ms if n not in side_names), key=lambda n: stage_ms[n])
     ds = per_stage[dom]
+    traffic, traffic_note = lookup_traffic(dom, traffic_key(w, layer))
     roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"],
                 "peak": tf_peak if ds["bound"] == "tensor" else hbm, "unit": ds["unit"],
-                "frac": ds["frac"], "traffic": lookup_traffic(dom, traffic_key(w, layer)),
+                "frac": ds["frac"], "traffic": traffic,
                 "peak_source": f"{peak_src} ({'sustained' if long_region and ds['bound'] == 'tensor' else 'burst'})"}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": dist.world,
@@ -1198,7 +1211,7 @@ def run_reference(args, dist, w):
 
 RUN_KEYS = ("impl", "gpus", "steps", "warmup", "config", "tokens", "bucket", "payload",
             "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras",
-            "route_only", "decode_path")
+            "route_only", "decode_path", "experts")
 
 
 def run_key(args) -> dict:

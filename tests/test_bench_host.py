@@ -74,9 +74,24 @@ def test_traffic_keys_name_workload_payload_and_gather():
 
 
 def test_committed_traffic_lines_are_read_only_for_the_current_source():
-    line = bench.lookup_traffic("gate_up", "decode_T128")
+    line, _ = bench.lookup_traffic("gate_up", "decode_T128")
     # the profiles committed with this source carry the gate/up pass's DRAM bytes
     assert line is None or 7e8 < line < 9e8
+
+
+def test_traffic_lines_with_a_scaling_note(tmp_path, monkeypatch):
+    """A capture of a smaller case carries a note saying how it was scaled."""
+    sha = bench.kernel_source_sha("combine")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "x.md").write_text(f"traffic: combine pooled 123 {sha} scaled x4 from T=16384\n"
+                               f"traffic: combine v3 77 {sha}\n"
+                               f"traffic: combine tiny 5 0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda name: sha)
+    assert bench.lookup_traffic("combine", "pooled") == (123, "scaled x4 from T=16384")
+    assert bench.lookup_traffic("combine", "v3") == (77, None)
+    assert bench.lookup_traffic("combine", "tiny") == (None, None)
 
 
 def test_nearest_rank_quantiles():
