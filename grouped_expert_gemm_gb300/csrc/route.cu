@@ -3,16 +3,22 @@
 //
 // [M6.2] 0x06L1 (family table), 0x06A-0x06D and 0x06I (V3 group rule and gate).
 //
-// Two kernels.  route_rank_kernel (every softmax router, and grouped routers
-// whose expert groups span whole lanes) selects by threshold and rank, see
-// route_token in route_dev.cuh.  route_kernel (the remaining grouped shapes)
-// gives lane l the experts 32*i + l and runs k rounds of a warp all-reduce of
-// 64-bit keys (orderable score bits << 32 | ~expert), so the maximum key is the
-// highest score and, among equal scores, the lowest expert index.  In both,
-// +0.0 and -0.0 tie, and NaN logits are reported and rank below every number.
+// Three kernels.  route_quarter_kernel (softmax batches of tens of thousands of
+// tokens with E = 128, 256, 384 or 512) gives each token four lanes.
+// route_rank_kernel (the other softmax batches, and grouped routers whose expert
+// groups span whole lanes) gives each token a warp and selects by threshold and
+// rank, see route_token in route_dev.cuh.  route_kernel (the remaining grouped
+// shapes) gives lane l the experts 32*i + l and runs k rounds of a warp
+// all-reduce of 64-bit keys (orderable score bits << 32 | ~expert), so the
+// maximum key is the highest score and, among equal scores, the lowest expert
+// index.  In all three, +0.0 and -0.0 tie, NaN logits are reported and rank
+// below every number, and the softmax normaliser is summed in slot order: the
+// first two give bit-identical ids and gates.
 #include "route_dev.cuh"
+#include "tma.cuh"
 
 #include <atomic>
+#include <mutex>
 
 namespace moe {
 namespace {
@@ -264,6 +270,386 @@ void launch_rank(const RouteArgs& a, cudaStream_t s) {
          one_wave(grid));
 }
 
+// ---- quarter-row router (large softmax batches) --------------------------------
+//
+// For batches far larger than the GPU (tens of thousands of tokens) the router
+// is a stream of logits, and the warp-per-token kernel spends hundreds of warp
+// instructions per token on warp-wide steps.  Here four lanes select one token,
+// each lane a quarter of its row.  A warp takes 8 consecutive tokens at a time:
+// their rows arrive by 2-D TMA boxes (8 rows x 32 experts, 128-byte swizzle) in a
+// 12 KB (E = 384) stage per warp, so 16 warps share an SM.  Lane 4r + h holds row
+// r's boxes h, h + 4, ...; the parts read their chunks in different orders so no
+// two lanes of a phase meet in a bank.  Then
+//   1. each lane takes the maxima of 4 chunks of its quarter; two shuffles give
+//      all four lanes the row's 16 chunk maxima, and theta = the k-th largest of
+//      them is a lower bound of the row's k-th largest score (the k chunks
+//      holding those maxima hold k scores >= theta);
+//   2. each lane marks the scores of its quarter that are not below theta (NaN
+//      included) and inserts them, in expert order, into a sorted list of KS
+//      orderable keys (0 = empty; ties keep the lower expert first), a NaN as
+//      -inf (reported);
+//   3. the row's four lanes merge their lists with shuffles (larger key first,
+//      then the lower expert) and form the gates exactly as the warp router does
+//      (exp against the top score, the normaliser summed in the warp's slot-order
+//      butterfly), each lane storing a quarter of the slots.
+// Selection, ids and gates are therefore identical to the warp router's.
+constexpr int kQuarter = 4;                       // lanes per token
+constexpr int kQuarterRows = 32 / kQuarter;       // tokens per warp batch
+constexpr int kQuarterWarps = 16;                 // warps per block, at most
+
+template <int NM, int KS>
+struct QuarterRouter {
+  static constexpr int E = 32 * NM;
+  static constexpr int kBoxBytes = kQuarterRows * 128;       // 1 KB: 8 rows x 32 fp32
+  static constexpr int kStage = NM * kBoxBytes;              // one warp's rows
+  static constexpr int kLists = kQuarterRows * kQuarter * KS * 8;  // keys and ids to merge
+  static constexpr int kWarpBytes = ((kStage + kLists) + 1023) & ~1023;
+  static constexpr int kFit = (227 * 1024 - 1024) / kWarpBytes;
+  static constexpr int kWarps = kFit < kQuarterWarps ? kFit : kQuarterWarps;
+  static constexpr int kSmem = 1024 + kWarps * kWarpBytes;
+  static_assert(NM % kQuarter == 0, "whole boxes per quarter");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds_f1(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// All ones when v is not below th (or either is NaN), else zero.
+__device__ __forceinline__ uint32_t not_below(float v, float th) {
+  uint32_t r;
+  asm("set.geu.u32.f32 %0, %1, %2;" : "=r"(r) : "f"(v), "f"(th));
+  return r;
+}
+
+// Sorts 8 values descending in place (a 19-comparator network).
+__device__ __forceinline__ void sort8_desc(float* x) {
+  auto ce = [&](int i, int j) {
+    const float hi = fmaxf(x[i], x[j]), lo = fminf(x[i], x[j]);
+    x[i] = hi;
+    x[j] = lo;
+  };
+  ce(0, 2); ce(1, 3); ce(4, 6); ce(5, 7);
+  ce(0, 4); ce(1, 5); ce(2, 6); ce(3, 7);
+  ce(0, 1); ce(2, 3); ce(4, 5); ce(6, 7);
+  ce(2, 4); ce(3, 5);
+  ce(1, 4); ce(3, 6);
+  ce(1, 2); ce(3, 4); ce(5, 6);
+}
+
+// Insert (key, e) into keys sorted descending; an equal key stays ahead (the
+// candidates arrive in expert order, so ties keep the lower expert first).
+template <int KS>
+__device__ __forceinline__ void key_insert(uint32_t (&tk)[KS], int (&ti)[KS], uint32_t key, int e) {
+#pragma unroll
+  for (int j = KS - 1; j > 0; --j) {
+    const bool sh = key > tk[j - 1];
+    const bool here = key > tk[j];
+    ti[j] = sh ? ti[j - 1] : (here ? e : ti[j]);
+    tk[j] = sh ? tk[j - 1] : (here ? key : tk[j]);
+  }
+  if (key > tk[0]) { tk[0] = key; ti[0] = e; }
+}
+
+template <int NM, int KS>  // E = 32 * NM experts; k <= KS
+__global__ void __launch_bounds__(QuarterRouter<NM, KS>::kWarps * 32, 1)
+route_quarter_kernel(const __grid_constant__ CUtensorMap map, RouteArgs a, bool early) {
+  using R = QuarterRouter<NM, KS>;
+  constexpr int kPer = NM / kQuarter;  // boxes of one quarter
+  extern __shared__ unsigned char q_raw[];
+  __shared__ uint64_t bar[R::kWarps];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int r = lane / kQuarter, h = lane % kQuarter;
+  const uint32_t stage = ((smem_u32(q_raw) + 1023u) & ~1023u) + static_cast<uint32_t>(w * R::kWarpBytes);
+  const uint32_t lists = stage + R::kStage;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R::kWarps; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map)) : "memory");
+  }
+  __syncthreads();
+  pdl_wait_then_trigger(early);
+  const int k = a.k;
+  const int valid = a.valid != nullptr ? min(max(__ldg(a.valid), 0), a.T) : a.T;
+  const int n_batches = static_cast<int>(ceil_div(a.T, kQuarterRows));
+  const uint32_t b_addr = smem_u32(&bar[w]);
+  // Logical chunk c of this lane's box rows sits at physical slot c ^ (r & 7) (the
+  // copy's swizzle); part h walks its chunks in the order c ^ 2h, so the 8 lanes of
+  // a phase (2 rows x 4 parts) read 8 different bank groups.
+  uint32_t slot[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) slot[c] = static_cast<uint32_t>(r * 128 + (((c ^ (2 * h)) ^ (r & 7)) << 4));
+  uint32_t ph = 0;
+  bool saw_nan = false, pending = false;
+  for (int bt = blockIdx.x * R::kWarps + w; bt < n_batches; bt += gridDim.x * R::kWarps) {
+    const int t0 = bt * kQuarterRows, t = t0 + r;
+    if (lane == 0 && !pending) {  // the first batch (later ones were issued ahead);
+                                  // rows past T are zero-filled by the copy
+      mbar_arrive_expect_tx(b_addr, R::kStage);
+#pragma unroll
+      for (int b = 0; b < NM; ++b)
+        tma_load_2d(stage + static_cast<uint32_t>(b * R::kBoxBytes), &map, b_addr, b * 32, t0);
+    }
+    pending = true;
+    if (!__all_sync(0xFFFFFFFFu, wait_bounded(b_addr, ph, &abort_flag, a.dev_status))) break;
+    pending = false;
+    ph ^= 1u;
+    const bool live = t < valid;  // every lane works; only live rows are written
+    // 1. maxima of this quarter's 4 chunks (NaN ignored: an all-NaN chunk is -inf),
+    //    then the row's 16 from the other quarters
+    float cm[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cm[j] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
+      float4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) v[c] = lds_f4(bx + slot[c]);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int j = (8 * i + c) / (2 * kPer);  // 4 chunks of 2 * kPer float4 each
+        cm[j] = fmaxf(cm[j], fmaxf(fmaxf(v[c].x, v[c].y), fmaxf(v[c].z, v[c].w)));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cm[4 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cm[8 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 2);
+    // theta, a lower bound of the row's k-th largest score: with KS = 8 (k <= 8) the
+    // 8th largest chunk maximum (the two sorted halves' pairwise maxima are the top
+    // 8, theta their minimum); with KS = 16 the smallest of the 16
+    float th;
+    if (KS == 8) {
+      sort8_desc(cm);
+      sort8_desc(cm + 8);
+      th = fmaxf(cm[0], cm[15]);
+#pragma unroll
+      for (int j = 1; j < 8; ++j) th = fminf(th, fmaxf(cm[j], cm[15 - j]));
+    } else {
+      th = cm[0];
+#pragma unroll
+      for (int j = 1; j < 16; ++j) th = fminf(th, cm[j]);
+    }
+    // (a warp barrier orders the shared memory: the second pass reloads the rows
+    // instead of keeping the first pass's values live across the sort)
+    __syncwarp();
+    // 2. this quarter's candidates (not below theta; a NaN compares unordered), in
+    //    expert order, into a sorted list
+    uint32_t msk[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
+      uint32_t m = 0u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 v = lds_f4(bx + slot[c]);
+        const int sh = 4 * (c ^ (2 * h));
+        m |= (not_below(v.x, th) & (1u << sh)) | (not_below(v.y, th) & (2u << sh)) |
+             (not_below(v.z, th) & (4u << sh)) | (not_below(v.w, th) & (8u << sh));
+      }
+      msk[i] = m;
+    }
+    uint32_t tk[KS];
+    int ti[KS];
+#pragma unroll
+    for (int j = 0; j < KS; ++j) { tk[j] = 0u; ti[j] = 0; }
+    {
+      int i = 0;
+      uint32_t m = msk[0];
+      for (;;) {
+        while (m == 0u && i + 1 < kPer) {  // the next box with candidates
+          ++i;
+#pragma unroll
+          for (int ii = 1; ii < kPer; ++ii) m = ii == i ? msk[ii] : m;
+        }
+        if (m == 0u) break;
+        const int e = __ffs(m) - 1;
+        m &= m - 1u;
+        const int b = h + kQuarter * i;
+        float v = lds_f1(stage + static_cast<uint32_t>(b * R::kBoxBytes + r * 128 +
+                                                       ((((e >> 2) ^ (r & 7)) & 7) << 4) + ((e & 3) << 2)));
+        if (v != v) { saw_nan |= live; v = -INFINITY; }
+        key_insert<KS>(tk, ti, ord_bits(v), 32 * b + e);
+      }
+    }
+    // 3. each lane's list to shared memory (entry-major: entry j of lane l at
+    //    j * 32 + l), where the merge reads a lane's next entry; the staged rows are
+    //    free, so the next batch's rows start to arrive during the merge
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(lists + static_cast<uint32_t>((j * 32 + lane) * 8)),
+                   "r"(tk[j]), "r"(static_cast<uint32_t>(ti[j])) : "memory");
+    __syncwarp();
+    {
+      const int nb = bt + gridDim.x * R::kWarps;
+      if (lane == 0 && nb < n_batches) {
+        mbar_arrive_expect_tx(b_addr, R::kStage);
+#pragma unroll
+        for (int b = 0; b < NM; ++b)
+          tma_load_2d(stage + static_cast<uint32_t>(b * R::kBoxBytes), &map, b_addr, b * 32,
+                      nb * kQuarterRows);
+      }
+      pending = nb < n_batches;
+    }
+    // merge: KS rounds; in each, the row's four lanes agree (two shuffle steps) on the
+    // best head -- larger key, then the lower expert -- and its lane advances
+    {
+      int pos = 0;
+      uint32_t hk = tk[0];
+      int hi = ti[0];
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        uint32_t bk = hk;
+        int bi = hi, bl = h;
+#pragma unroll
+        for (int o = 1; o < kQuarter; o <<= 1) {
+          const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+          const int ol = __shfl_xor_sync(0xFFFFFFFFu, bl, o);
+          const bool better = ok > bk || (ok == bk && oi < bi);
+          bk = better ? ok : bk;
+          bi = better ? oi : bi;
+          bl = better ? ol : bl;
+        }
+        tk[j] = bk;
+        ti[j] = bi;
+        if (bl == h && j + 1 < KS) {  // this lane's head was taken: the next entry
+          ++pos;
+          uint32_t kk = 0u, ii = 0u;
+          if (pos < KS)
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(kk), "=r"(ii)
+                         : "r"(lists + static_cast<uint32_t>((pos * 32 + lane) * 8)) : "memory");
+          hk = kk;
+          hi = static_cast<int>(ii);
+        }
+      }
+    }
+    {
+      // gates: exp against the top score; the normaliser in the warp's order; each of
+      // the row's lanes divides and stores the slots j = h, h + 4, ...
+      const float top = ord_to_float(tk[0]);
+      float ex[KS];
+#pragma unroll
+      for (int j = 0; j < KS; ++j) ex[j] = j < k ? expf(ord_to_float(tk[j]) - top) : 0.0f;
+      float wv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) wv[j] = j < KS ? ex[j < KS ? j : 0] : 0.0f;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+        for (int ii = 0; ii < o; ++ii) wv[ii] = wv[ii] + wv[ii + o];
+      const float ssum = wv[0];
+      int32_t* ids_t = a.topk_ids + static_cast<int64_t>(t) * k;
+      float* gates_t = a.gates + static_cast<int64_t>(t) * k;
+      if (live) {
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          if (j % kQuarter == h && j < k) {
+            ids_t[j] = ti[j];
+            gates_t[j] = ex[j] / ssum;
+          }
+        }
+      } else if (t < a.T) {
+        // padding slot of a fixed token bucket: no expert identity, zero gate
+        for (int j = h; j < k; j += kQuarter) { ids_t[j] = MOE_ROUTE_MASKED; gates_t[j] = 0.0f; }
+      }
+    }
+    __syncwarp();  // every lane is done with the stage and the lists before the refill
+  }
+  if (pending && lane == 0) wait_drain(b_addr, ph);  // a copy still in flight after a timeout
+  if (__any_sync(0xFFFFFFFFu, saw_nan) && lane == 0) report(a.dev_status, MOE_DEV_NONFINITE_LOGIT);
+  if (!early) pdl_trigger();
+}
+
+// The logits as a 2-D TMA view [T, E] fp32, boxes of 32 experts x 8 rows with the
+// 128-byte swizzle, kept in a small cache (an encoding depends only on these values).
+bool lane_map(CUtensorMap* out, const float* logits, int T, int E) {
+  struct Entry {
+    const float* p;
+    int T, E;
+    CUtensorMap map;
+  };
+  constexpr int kCache = 8;
+  static Entry cache[kCache];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].p == logits && cache[i].T == T && cache[i].E == E) { *out = cache[i].map; return true; }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(E), static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(E) * 4};
+  const cuuint32_t box[2] = {32, kQuarterRows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(logits), dims, strides, box,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache[next] = Entry{logits, T, E, m};
+  next = (next + 1) % kCache;
+  if (used < kCache) ++used;
+  *out = m;
+  return true;
+}
+
+template <int NM, int KS>
+moe_status launch_lane(const RouteArgs& a, const CUtensorMap& map, cudaStream_t s) {
+  using R = QuarterRouter<NM, KS>;
+  auto kern = route_quarter_kernel<NM, KS>;
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> ready[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MOE_ERR_CUDA;
+  if (!ready[dev].load(std::memory_order_relaxed)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, R::kSmem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    ready[dev].store(1, std::memory_order_relaxed);
+  }
+  const int64_t batches = ceil_div(a.T, kQuarterRows);
+  const int64_t need = ceil_div(batches, R::kWarps);
+  const int grid = static_cast<int>(need < sm_count() ? need : sm_count());
+  launch(kern, dim3(grid), dim3(R::kWarps * 32), R::kSmem, s, map, a, one_wave(grid));
+  return launch_status();
+}
+
+// The quarter-row router takes softmax batches of at least two 8-token batches per
+// warp of a full wave (below that the warp-per-token kernel has more parallelism
+// and the lower latency), E = 32 * NM with NM in {4, 8, 12, 16}, 16-byte aligned rows.
+bool lane_shape(int T, int E, int k, const float* logits) {
+  const int nm = E / 32;
+  if (E % 32 != 0 || (nm != 4 && nm != 8 && nm != 12 && nm != 16) || k > 16) return false;
+  if (!aligned16(logits)) return false;
+  return static_cast<int64_t>(T) >= static_cast<int64_t>(2) * kQuarterRows * kQuarterWarps * sm_count();
+}
+
+moe_status launch_lane_any(const RouteArgs& a, cudaStream_t s, bool* done) {
+  *done = false;
+  CUtensorMap map;
+  if (!lane_map(&map, a.logits, a.T, a.E)) return MOE_OK;  // the warp router instead
+  *done = true;
+  const bool k8 = a.k <= 8;
+  switch (a.E / 32) {
+    case 4: return k8 ? launch_lane<4, 8>(a, map, s) : launch_lane<4, 16>(a, map, s);
+    case 8: return k8 ? launch_lane<8, 8>(a, map, s) : launch_lane<8, 16>(a, map, s);
+    case 12: return k8 ? launch_lane<12, 8>(a, map, s) : launch_lane<12, 16>(a, map, s);
+    default: return k8 ? launch_lane<16, 8>(a, map, s) : launch_lane<16, 16>(a, map, s);
+  }
+}
+
 // Lanes per expert group of the rank kernel's layout when groups span whole
 // lanes in a power of two, else 0 (the grouped router then takes the one-slot-
 // per-lane kernel above).
@@ -283,6 +669,11 @@ moe_status launch_route(const moe_route_params* p, const float* logits, const fl
   if (!GROUPED || lanes_per_group(p->E, p->n_group, vpl) > 0) {
     const RouteArgs a{p->T, p->E, p->k, p->n_group, p->topk_group, p->route_scale, logits,
                       sel_bias, ids, gates, st, valid};
+    if (!GROUPED && lane_shape(p->T, p->E, p->k, logits)) {
+      bool done = false;
+      const moe_status r = launch_lane_any(a, s, &done);
+      if (done) return r;
+    }
     const bool vec = vpl % 4 == 0 && p->E % 4 == 0 && aligned16(logits);
 #define MOE_RANK_CASE(V)                                                   \
   do {                                                                     \

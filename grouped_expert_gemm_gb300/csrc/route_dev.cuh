@@ -89,7 +89,8 @@ __device__ __forceinline__ void load_row(const float* __restrict__ row, int E, i
 }
 
 // Per-warp shared scratch of the selection: the row's scores (and, grouped, the
-// affinities) by expert, and the candidates' keys and affinities.
+// affinities) by expert, the candidates' keys and affinities, then the selected
+// terms of the gate normaliser by slot.
 template <int VPL, bool GROUPED>
 struct RouteSmem {
   __align__(16) float val[32 * VPL];
@@ -265,14 +266,17 @@ __device__ __forceinline__ RouteLane route_token(const float (&z)[VPL], const fl
       if (lane == j) { out.slot = j; out.id = e; my_val = ord_to_float(gm); my_aff = av; }
     }
   }
-  if (GROUPED) {
-    const float s = warp_sum(out.slot >= 0 ? my_aff : 0.0f);
-    out.gate = route_scale * my_aff / s;
-  } else {
-    const float ex = out.slot >= 0 ? expf(my_val - ord_to_float(top_u)) : 0.0f;
-    const float s = warp_sum(ex);
-    out.gate = ex / s;
-  }
+  // the normaliser: the selected terms summed in slot order (slot j's term at lane j,
+  // then the warp's xor butterfly), so every router kernel forms the same sum
+  const float term = out.slot < 0 ? 0.0f
+                     : GROUPED    ? my_aff
+                                  : expf(my_val - ord_to_float(top_u));
+  __syncwarp();
+  if (out.slot >= 0) sm.kaff[out.slot] = term;
+  __syncwarp();
+  const float s = warp_sum(lane < k ? sm.kaff[lane] : 0.0f);
+  __syncwarp();  // kaff is free for the next token
+  out.gate = GROUPED ? route_scale * my_aff / s : term / s;
   return out;
 }
 
