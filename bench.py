@@ -76,6 +76,9 @@ def parse_args():
     ap.add_argument("--decode-path", default="auto", choices=["auto", "fused", "separate"],
                     help="decode-sized batches: the one-launch layer (fused), the per-stage "
                          "calls (separate), or whichever the layer picks for the size (auto)")
+    ap.add_argument("--pool-sequential", action="store_true",
+                    help="pooled: run every stage of every wave on one stream (the default "
+                         "overlaps pack, compact and combine with the expert passes)")
     ap.add_argument("--gather", action="store_true",
                     help="bf16 payload: permute the maps only and gather the expert rows in the "
                          "gate/up loader instead of copying them in the permute")
@@ -323,7 +326,8 @@ def lookup_traffic(stage, workload_name):
 # our arm
 # ----------------------------------------------------------------------------
 
-def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", decode_path="auto"):
+def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", decode_path="auto",
+                overlap=True):
     import grouped_expert_gemm_gb300 as g
     if w.pooled and payload != "bf16":
         raise SystemExit("--payload applies to the routed (non-pooled) workloads")
@@ -334,7 +338,8 @@ def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", deco
         pool_cap = g.capacity_from_factor(w.sender_cf, w.R, w.n_dest * w.n_waves)
         local_cap = g.capacity_from_factor(w.receiver_cf, w.R, w.local_per_dest * w.n_waves)
         layer = g.PooledMoELayer(w.T, w.d, w.k, w.I, w.n_dest, w.local_per_dest, w.n_waves,
-                                 pool_cap, local_cap, wg, wu, wd, device=device)
+                                 pool_cap, local_cap, wg, wu, wd, device=device,
+                                 overlap=overlap)
     else:
         cap = -1 if w.capacity_factor is None else g.capacity_from_factor(w.capacity_factor, w.R, w.E)
         score = g.MOE_SCORE_SOFTMAX if w.score_fn == "softmax" else g.MOE_SCORE_SIGMOID_GROUP
@@ -369,7 +374,8 @@ def run_ours(args, dist, w):
     torch.cuda.set_device(device)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
     layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather,
-                                             args.fp8_loader, args.decode_path)
+                                             args.fp8_loader, args.decode_path,
+                                             overlap=not getattr(args, "pool_sequential", False))
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _, _ in stages]
@@ -511,10 +517,14 @@ def run_ours(args, dist, w):
             else:
                 dt = prev.elapsed_time(evs[s]["after"][i])
                 prev = evs[s]["after"][i]
-            if not (n.endswith("_fork") or n.endswith("_join")):  # ordering steps, no kernels
+            # ordering steps launch no kernels
+            if not (n.endswith("_fork") or n.endswith("_join") or n.startswith("sync_")):
                 stage_ms[n] = stage_ms.get(n, 0.0) + dt
     per_step = {n: names.count(n) for n in names}
-    side_names = {n for n, _, side in stages if side is not None}
+    # stages on a side stream overlap others; a layer's compute stream (the expert passes
+    # of the overlapped pooled layer) holds the step's critical path like a main stream
+    compute = getattr(layer, "compute_stream", None)
+    side_names = {n for n, _, side in stages if side is not None and side is not compute}
     step_ms = max_ms / steps
     value = dist.world * w.T * steps / (max_ms / 1e3)
 
@@ -905,7 +915,11 @@ def config_dict(w, layer, ws_bytes=None, flush_l2=False):
     if w.pooled:
         c.update({"n_dest": w.n_dest, "local_per_dest": w.local_per_dest, "n_waves": w.n_waves,
                   "pool_cap": layer.pool_cap, "local_cap": layer.local_cap,
-                  "wave_policy": "stripe"})
+                  "wave_policy": "stripe",
+                  "schedule": ("pack, compact and combine of the waves on a second stream beside "
+                               "the expert passes (double-buffered wave buffers)"
+                               if getattr(layer, "overlap", False) else
+                               "every stage of every wave in order on one stream")})
     wbytes = sum(t.numel() * 2 for t in (layer.w_gate, layer.w_up, layer.w_down))
     c["expert_weight_bytes"] = wbytes
     if ws_bytes is not None:
@@ -1211,7 +1225,7 @@ def run_reference(args, dist, w):
 
 RUN_KEYS = ("impl", "gpus", "steps", "warmup", "config", "tokens", "bucket", "payload",
             "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras",
-            "route_only", "decode_path", "experts")
+            "route_only", "decode_path", "experts", "pool_sequential")
 
 
 def run_key(args) -> dict:

@@ -303,11 +303,22 @@ class MoELayer:
 
 
 class PooledMoELayer:
-    """8-of-384-style static pooled waves on one GPU (one emulated sender and receiver)."""
+    """8-of-384-style static pooled waves on one GPU (one emulated sender and receiver).
+
+    With ``overlap`` (the default) the forward pass runs the HBM-bound stages of the
+    waves (pack, compact, combine) on a second stream beside the tensor-bound expert
+    passes: wave w+2's pools and compact arrays are built while wave w+1's experts run,
+    and wave w's combine runs under wave w+1's experts.  The per-wave buffers
+    (pools, the route -> pool-row map, fills, compact rows, local counts, the pool-row
+    -> row map and the expert outputs y) are then held twice, wave w using set w % 2;
+    the attributes of those names show the set of the wave last packed.  Every kernel
+    and every accumulation order is that of the sequential pass, so the output is the
+    same bit for bit."""
 
     def __init__(self, T: int, d: int, k: int, I: int, n_dest: int, local_per_dest: int,
                  n_waves: int, pool_cap: int, local_cap: int, w_gate, w_up, w_down,
-                 wave_policy: int = abi.MOE_WAVE_STRIPE, first_source: int = 0, device="cuda"):
+                 wave_policy: int = abi.MOE_WAVE_STRIPE, first_source: int = 0, device="cuda",
+                 overlap: bool = True):
         self.T, self.d, self.k, self.I = T, d, k, I
         self.E = n_dest * local_per_dest
         self.n_dest, self.L, self.n_waves = n_dest, local_per_dest, n_waves
@@ -323,28 +334,57 @@ class PooledMoELayer:
         R = T * k
         self.topk_ids = torch.empty((T, k), **i32)
         self.gates = torch.empty((T, k), dtype=torch.float32, device=dev)
-        self.pools = torch.empty((n_dest, pool_cap + 1, d), dtype=torch.bfloat16, device=dev)
-        self.route_to_poolrow = torch.empty((R,), **i32)
-        self.pool_fill = torch.empty((n_dest,), **i32)
+        self.overlap = bool(overlap) and n_waves > 1
+        self.rows = local_per_dest * local_cap
+        n_sets = 2 if self.overlap else 1
+        self._sets = [dict(
+            pools=torch.empty((n_dest, pool_cap + 1, d), dtype=torch.bfloat16, device=dev),
+            route_to_poolrow=torch.empty((R,), **i32),
+            pool_fill=torch.empty((n_dest,), **i32),
+            compact=torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev),
+            local_counts=torch.empty((local_per_dest,), **i32),
+            poolrow_to_row=torch.empty((n_dest * pool_cap,), **i32),
+            y=torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev))
+            for _ in range(n_sets)]
+        self._cur = 0
+        if self.overlap:
+            # expert passes on a high-priority stream (their persistent CTAs take an SM
+            # before the copies' blocks), the HBM-bound stages on a default-priority one
+            lo, hi = torch.cuda.Stream.priority_range()
+            self.compute_stream = torch.cuda.Stream(dev, priority=hi)
+            self.mem_stream = torch.cuda.Stream(dev, priority=lo)
+            ev = lambda: torch.cuda.Event()  # noqa: E731
+            self._ev = dict(start=ev(), C=[ev() for _ in range(n_waves)],
+                            D=[ev() for _ in range(n_waves)], M=[ev() for _ in range(n_waves)])
         self.sender_drops = torch.zeros((n_waves,), **i32)
         self.demand = torch.zeros((self.E,), **i32)
         self.pack_ws_bytes = abi.moe_pool_pack_workspace_size(self.pool_params, T, k)
         self.pack_ws = _u8(self.pack_ws_bytes, dev)
-        self.rows = local_per_dest * local_cap
-        self.compact = torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev)
-        self.local_counts = torch.empty((local_per_dest,), **i32)
         self.local_begin = torch.arange(local_per_dest, **i32) * local_cap
-        self.poolrow_to_row = torch.empty((n_dest * pool_cap,), **i32)
         self.receiver_drops = torch.zeros((n_waves,), **i32)
         self.compact_ws_bytes = abi.moe_pool_compact_workspace_size(n_dest, pool_cap,
                                                                     local_per_dest)
         self.compact_ws = _u8(self.compact_ws_bytes, dev)
-        self.y = torch.empty((self.rows, d), dtype=torch.bfloat16, device=dev)
         self.gemm_ws_bytes = abi.moe_grouped_swiglu_workspace_size(self.rows, I)
         self.gemm_ws = _u8(self.gemm_ws_bytes, dev)
         self.route_to_row = torch.empty((R,), **i32)
         self.out = torch.empty((T, d), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    # the per-wave buffers of the current set (the wave last packed, or named by a call)
+    pools = property(lambda self: self._sets[self._cur]["pools"])
+    route_to_poolrow = property(lambda self: self._sets[self._cur]["route_to_poolrow"])
+    pool_fill = property(lambda self: self._sets[self._cur]["pool_fill"])
+    compact = property(lambda self: self._sets[self._cur]["compact"])
+    local_counts = property(lambda self: self._sets[self._cur]["local_counts"])
+    poolrow_to_row = property(lambda self: self._sets[self._cur]["poolrow_to_row"])
+    y = property(lambda self: self._sets[self._cur]["y"])
+
+    def _set(self, wave):
+        """Buffer set of a wave (None: the current one); it becomes the current set."""
+        if wave is not None:
+            self._cur = wave % len(self._sets)
+        return self._sets[self._cur]
 
     def route(self, logits, stream=None):
         abi.moe_route(self.params, logits, None, self.topk_ids, self.gates, self.dev_status, stream)
@@ -356,40 +396,46 @@ class PooledMoELayer:
         return self.demand
 
     def pack(self, x, wave, stream=None):
+        b = self._set(wave)
         abi.moe_pool_pack(self.pool_params, self.T, self.d, self.k, wave, self.topk_ids, x,
-                          self.pools, self.route_to_poolrow, self.pool_fill,
+                          b["pools"], b["route_to_poolrow"], b["pool_fill"],
                           self.sender_drops[wave:wave + 1], self.pack_ws, self.pack_ws_bytes,
                           self.dev_status, stream)
 
     def compact_wave(self, wave, stream=None):
+        b = self._set(wave)
         abi.moe_pool_compact_rotated(self.n_dest, self.pool_cap, self.d, self.L, self.local_cap,
-                                     self.first_source, self.pools, self.compact,
-                                     self.local_counts, self.poolrow_to_row,
+                                     self.first_source, b["pools"], b["compact"],
+                                     b["local_counts"], b["poolrow_to_row"],
                                      self.receiver_drops[wave:wave + 1], self.compact_ws,
                                      self.compact_ws_bytes, self.dev_status, stream)
 
-    def experts(self, stream=None):
-        abi.moe_grouped_swiglu(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,
-                               self.local_counts, self.w_gate, self.w_up, self.w_down, self.y,
+    def experts(self, stream=None, wave=None):
+        b = self._set(wave)
+        abi.moe_grouped_swiglu(self.L, self.d, self.I, self.rows, b["compact"], self.local_begin,
+                               b["local_counts"], self.w_gate, self.w_up, self.w_down, b["y"],
                                self.gemm_ws, self.gemm_ws_bytes, self.dev_status, stream)
 
     def combine_wave(self, wave, stream=None, out=None):
-        abi.moe_compose_map(self.T * self.k, self.route_to_poolrow, self.poolrow_to_row,
+        b = self._set(wave)
+        abi.moe_compose_map(self.T * self.k, b["route_to_poolrow"], b["poolrow_to_row"],
                             self.n_dest * self.pool_cap, self.route_to_row, self.dev_status,
                             stream)
-        abi.moe_combine(self.T, self.k, self.d, self.y, self.rows, self.route_to_row, self.gates,
+        abi.moe_combine(self.T, self.k, self.d, b["y"], self.rows, self.route_to_row, self.gates,
                         None, 1 if wave > 0 else 0, self.out if out is None else out,
                         self.dev_status, stream)
 
-    def experts_gate_up(self, stream=None):
-        abi.moe_grouped_gate_up(self.L, self.d, self.I, self.rows, self.compact, self.local_begin,
-                                self.local_counts, self.w_gate, self.w_up, self.H,
+    def experts_gate_up(self, stream=None, wave=None):
+        b = self._set(wave)
+        abi.moe_grouped_gate_up(self.L, self.d, self.I, self.rows, b["compact"], self.local_begin,
+                                b["local_counts"], self.w_gate, self.w_up, self.H,
                                 self.dev_status, stream)
 
-    def experts_down(self, stream=None):
+    def experts_down(self, stream=None, wave=None):
         """The down pass; it follows experts_gate_up on the same stream (as in `stages`)."""
+        b = self._set(wave)
         abi.moe_grouped_down_chained(self.L, self.I, self.d, self.rows, self.H, self.local_begin,
-                                     self.local_counts, self.w_down, self.y, self.dev_status,
+                                     b["local_counts"], self.w_down, b["y"], self.dev_status,
                                      stream)
 
     @property
@@ -397,14 +443,51 @@ class PooledMoELayer:
         return self.gemm_ws[: self.rows * self.I * 2].view(torch.bfloat16).view(self.rows, self.I)
 
     def stages(self, logits, x, out=None):
-        """(name, callable(stream), side_stream=None) steps in launch order."""
+        """(name, callable(stream), side_stream) steps in launch order.  A step with a
+        side stream launches there whatever stream it is given; the `sync_*` steps
+        order the streams (they launch nothing)."""
         st = [("route", lambda s: self.route(logits, s), None)]
-        for w in range(self.n_waves):
-            st += [("pool_pack", lambda s, w=w: self.pack(x, w, s), None),
-                   ("pool_compact", lambda s, w=w: self.compact_wave(w, s), None),
-                   ("gate_up", self.experts_gate_up, None),
-                   ("down", self.experts_down, None),
-                   ("combine", lambda s, w=w: self.combine_wave(w, s, out), None)]
+        if not self.overlap:
+            for w in range(self.n_waves):
+                st += [("pool_pack", lambda s, w=w: self.pack(x, w, s), None),
+                       ("pool_compact", lambda s, w=w: self.compact_wave(w, s), None),
+                       ("gate_up", lambda s, w=w: self.experts_gate_up(s, w), None),
+                       ("down", lambda s, w=w: self.experts_down(s, w), None),
+                       ("combine", lambda s, w=w: self.combine_wave(w, s, out), None)]
+            return st
+        tc, mem, ev, n = self.compute_stream, self.mem_stream, self._ev, self.n_waves
+
+        def cur(s):
+            return torch.cuda.current_stream() if s is None else s
+
+        def fork(s):
+            ev["start"].record(cur(s))
+            tc.wait_event(ev["start"])
+            mem.wait_event(ev["start"])
+
+        def build(w):  # wave w's pools and compact arrays, on the memory stream
+            return [("pool_pack", lambda s, w=w: self.pack(x, w, mem), mem),
+                    ("pool_compact", lambda s, w=w: self.compact_wave(w, mem), mem),
+                    ("sync_built", lambda s, w=w: ev["C"][w].record(mem), None)]
+
+        st.append(("sync_fork", fork, None))
+        for w in range(min(2, n)):
+            st += build(w)
+        for w in range(n):
+            st.append(("sync_wait_built", lambda s, w=w: tc.wait_event(ev["C"][w]), None))
+            st.append(("gate_up", lambda s, w=w: self.experts_gate_up(tc, w), tc))
+            if w >= 2:  # y of this set was last read by the combine two waves back
+                st.append(("sync_wait_combined", lambda s, w=w: tc.wait_event(ev["M"][w - 2]),
+                           None))
+            st.append(("down", lambda s, w=w: self.experts_down(tc, w), tc))
+            st.append(("sync_experts_done", lambda s, w=w: ev["D"][w].record(tc), None))
+            st.append(("sync_wait_experts", lambda s, w=w: mem.wait_event(ev["D"][w]), None))
+            st.append(("combine", lambda s, w=w: self.combine_wave(w, mem, out), mem))
+            st.append(("sync_combined", lambda s, w=w: ev["M"][w].record(mem), None))
+            if w + 2 < n:  # this set is free again: wave w+2's pools and compact arrays
+                st += build(w + 2)
+        # join: the caller's stream waits for the last combine (and so for everything)
+        st.append(("sync_join", lambda s: cur(s).wait_event(ev["M"][n - 1]), None))
         return st
 
     def forward(self, logits, x, stream=None, out=None) -> torch.Tensor:

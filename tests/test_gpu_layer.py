@@ -421,3 +421,50 @@ def test_host_pipeline_pooled_layer():
         ref = ref_layer.forward(lh.to(DEV), xh.to(DEV))
         torch.cuda.synchronize()
         assert torch.equal(oh, ref.cpu())
+
+
+def test_pooled_overlap_equals_the_sequential_schedule():
+    """The overlapped pooled forward (pack, compact and combine on a second stream, wave
+    buffers held twice) gives the sequential forward's output bit for bit, eagerly and
+    replayed from a captured graph over changing inputs."""
+    import grouped_expert_gemm_gb300 as g
+    w = workloads.scaled(workloads.pooled(), T=2048, d=256, I=256, n_dest=32, E=32 * 6)
+    wg, wu, wd = workloads.make_expert_weights(w, DEV)
+    pool_cap = g.capacity_from_factor(w.sender_cf, w.R, w.n_dest * w.n_waves)
+    local_cap = g.capacity_from_factor(w.receiver_cf, w.R, w.local_per_dest * w.n_waves)
+
+    def mk(overlap):
+        return g.PooledMoELayer(w.T, w.d, w.k, w.I, w.n_dest, w.local_per_dest, w.n_waves,
+                                pool_cap, local_cap, wg, wu, wd, device=DEV, overlap=overlap)
+    ov, seq = mk(True), mk(False)
+    assert ov.overlap and not seq.overlap
+    logits, _ = workloads.make_router_inputs(w, DEV)
+    x = workloads.make_activations(w, DEV)
+    ov.forward(logits, x)
+    seq.forward(logits, x)
+    torch.cuda.synchronize()
+    assert int(ov.dev_status.item()) == 0
+    assert torch.equal(ov.out, seq.out)
+    assert torch.equal(ov.sender_drops, seq.sender_drops)
+    assert torch.equal(ov.receiver_drops, seq.receiver_drops)
+    # graph replays on new inputs
+    stream = torch.cuda.Stream(DEV)
+    lg = logits.clone()
+    xx = x.clone()
+    with torch.cuda.stream(stream):
+        ov.forward(lg, xx)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ov.forward(lg, xx)
+    for seed in range(2):
+        gen = torch.Generator(device=DEV).manual_seed(100 + seed)
+        lg.copy_(torch.randn(lg.shape, generator=gen, device=DEV))
+        xx.copy_(torch.randn(xx.shape, generator=gen, device=DEV).to(torch.bfloat16))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        seq.forward(lg, xx)
+        torch.cuda.synchronize()
+        assert torch.equal(ov.out, seq.out)
