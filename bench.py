@@ -407,8 +407,11 @@ def run_ours(args, dist, w):
     # A step whose working set fits L2 would find it resident from the step before
     # (the same inputs every step): such workloads flush L2 before every timed step
     # by reading a buffer four times the L2 size, outside the timed spans, and are
-    # timed step by step from eager launches (the flush gives the host time to queue
-    # the step's launches, so the GPU does not wait for them).
+    # timed step by step.  With graphs, the flush and the step are one captured graph
+    # with event nodes right after the flush and after the step: a step's span runs
+    # from the end of the flush to the end of its last kernel (the device time of the
+    # step), with the graph's own launch before the flush.  Without graphs the step's
+    # launches follow the flush eagerly (the flush gives the host time to queue them).
     ws_bytes = working_set_bytes(w, layer)
     flush_l2 = ws_bytes < 2 * L2_BYTES
     flush_buf = torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=device) if flush_l2 else None
@@ -416,15 +419,23 @@ def run_ours(args, dist, w):
     spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(steps)]
     step_graph = None
+    span_ms = []
     if flush_l2 and not args.no_graph:
-        # one step as a graph, replayed after each flush (one launch per step, so the
-        # host never holds the GPU back inside a step's span)
+        # flush + step as one graph, with event nodes after the flush and after the step
         step_graph = torch.cuda.CUDAGraph()
-        l0 = abi.launch_count()
+        g_start = torch.cuda.Event(enable_timing=True)
+        g_end = torch.cuda.Event(enable_timing=True)
+        for e in (g_start, g_end):
+            e.record(stream)  # creates the event objects
+        stream.synchronize()
         with torch.cuda.graph(step_graph, stream=stream):
+            flush_buf.max()  # reads 4 x L2 of clean lines
+            record_external(g_start, stream)
+            l0 = abi.launch_count()
             for _, fn, _ in stages:
                 fn(None)
-        step_launches = abi.launch_count() - l0
+            step_launches = abi.launch_count() - l0
+            record_external(g_end, stream)
         with torch.cuda.stream(stream):
             step_graph.replay()
         stream.synchronize()
@@ -467,17 +478,20 @@ def run_ours(args, dist, w):
         with torch.cuda.stream(stream):
             if use_graph:
                 graph.replay()
+            elif step_graph is not None:
+                # one replay per step; its span is read before the next replay re-records
+                # the events (only the step boundaries carry events: an event between two
+                # kernels would cut their programmatic launch overlap)
+                for s in range(steps):
+                    step_graph.replay()
+                    stream.synchronize()
+                    span_ms.append(g_start.elapsed_time(g_end))
             elif flush_l2:
-                # only the step boundaries carry events: an event between two kernels
-                # would cut their programmatic launch overlap
                 for s in range(steps):
                     flush_buf.max()  # reads 4 x L2 of clean lines
                     spans[s][0].record(stream)
-                    if step_graph is not None:
-                        step_graph.replay()
-                    else:
-                        for _, fn, _ in stages:
-                            fn(stream)
+                    for _, fn, _ in stages:
+                        fn(stream)
                     spans[s][1].record(stream)
             else:
                 for s in range(steps):
@@ -502,9 +516,11 @@ def run_ours(args, dist, w):
         launches = step_launches * steps
     elapsed_ms = t_start.elapsed_time(t_end)
     if flush_l2:  # the steps' own spans, without the flushes between them
-        elapsed_ms = sum(a.elapsed_time(b) for a, b in spans)
+        if not span_ms:
+            span_ms = [a.elapsed_time(b) for a, b in spans]
+        elapsed_ms = sum(span_ms)
     max_ms = dist.max(elapsed_ms)
-    quantiles = step_quantiles(spans if flush_l2 else None, stages, stream, steps, use_graph)
+    quantiles = step_quantiles(span_ms if flush_l2 else None, stages, stream, steps, use_graph)
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())} after timed steps")
 
@@ -594,10 +610,11 @@ def run_ours(args, dist, w):
                    "events between the stages of every step (on the stream each stage runs on) "
                    "of an instrumented replay of the "
                    "same K steps right after, on the launching stream" if use_graph else
-                   "L2 flushed before every step, then the step (a one-step CUDA graph replay, "
-                   "or eager launches with --no-graph); value from the sum of the steps' own "
-                   "spans (CUDA events at each step's start and end only), stage times from a "
-                   "second eager pass of the same steps with events between the stages"
+                   "L2 flushed before every step: flush and step replayed as one captured graph "
+                   "with event nodes after the flush and after the step (eager launches after "
+                   "the flush with --no-graph); value from the sum of the steps' own spans "
+                   "(events at each step's start and end only), stage times from a second "
+                   "eager pass of the same steps with events between the stages"
                    if flush_l2 else
                    "eager launches with CUDA events between the stages of every timed step"),
         "clocks": sampler.summary(),
@@ -619,12 +636,13 @@ def nearest_rank(xs, q):
     return xs[max(0, min(len(xs) - 1, int(np.ceil(q * len(xs))) - 1))]
 
 
-def step_quantiles(spans, stages, stream, steps, use_graph):
+def step_quantiles(span_ms, stages, stream, steps, use_graph):
     """Nearest-rank p50 / p90 of single steps, beside the K-step mean `value`: the spans
-    of the timed steps when they were timed one by one (L2 flushed), else K more steps
-    replayed one at a time from a one-step graph (or launched eagerly) with events at
-    each step's start and end only."""
-    if spans is None:
+    (ms) of the timed steps when they were timed one by one (L2 flushed), else K more
+    steps replayed one at a time from a one-step graph (or launched eagerly) with events
+    at each step's start and end only."""
+    spans = None
+    if span_ms is None:
         spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(steps)]
         g1 = None
@@ -643,7 +661,7 @@ def step_quantiles(spans, stages, stream, steps, use_graph):
                         fn(stream)
                 b.record(stream)
         stream.synchronize()
-    ms = [a.elapsed_time(b) for a, b in spans]
+    ms = span_ms if span_ms is not None else [a.elapsed_time(b) for a, b in spans]
     return {"p50": round(nearest_rank(ms, 0.5), 5), "p90": round(nearest_rank(ms, 0.9), 5),
             "n": len(ms), "note": "single-step spans; nearest-rank quantiles"}
 
