@@ -89,13 +89,20 @@ constexpr int kASlotCols = kBK / 2;  // 64 bf16 of a row = 32 columns
 constexpr int kSmallABytes = 32 * kBK * 2;  // 4 KB
 constexpr int kFixedSmem = 1024 + (3 * kMaxSeg + 16) * 4 + 64 * 8;  // alignment, tables, barriers
 
-template <int N_ATOMS, bool FP8A = false, bool SMALLA = false>
+// KS = K per stage.  Deep stages (KS = 128, small-A bf16 only) stage each B atom as
+// one [128 K x 64 N] box and the A rows as two [rows x 64 K] boxes: half as many
+// TMA boxes per byte of weights, which streams them faster when a pass has few
+// tiles (one-token decode: 44 -> 67 GB/s per SM in a producer-only measurement).
+template <int N_ATOMS, bool FP8A = false, bool SMALLA = false, int KS = kBK>
 struct Geometry {
   static constexpr int kN = 64 * N_ATOMS;                  // MMA N
-  static constexpr int kASlotBytes = SMALLA ? kSmallABytes : kABytes;
+  static constexpr int kAtom = KS * 64 * 2;                // one B atom box [KS x 64]
+  static constexpr int kABoxes = KS / kBK;                 // A boxes per stage
+  static constexpr int kABoxSlot = SMALLA ? kSmallABytes : kABytes;  // bytes per A box slot
+  static constexpr int kASlotBytes = kABoxSlot * kABoxes;
   static constexpr int kBOff = FP8A ? 0 : kASlotBytes;     // B atoms in a TMA slot
-  static constexpr int kRawOff = N_ATOMS * kAtomBytes;     // E4M3 tile in a TMA slot
-  static constexpr int kStageBytes = N_ATOMS * kAtomBytes + (FP8A ? kRawBytes : kASlotBytes);
+  static constexpr int kRawOff = N_ATOMS * kAtom;          // E4M3 tile in a TMA slot
+  static constexpr int kStageBytes = N_ATOMS * kAtom + (FP8A ? kRawBytes : kASlotBytes);
   // As many stages as fit the shared memory: narrower tiles keep more loads in flight.
   static constexpr int kSmallAStages = (227 * 1024 - kFixedSmem) / kStageBytes;
   static constexpr int kStages = SMALLA ? (kSmallAStages > 12 ? 12 : kSmallAStages)
@@ -116,7 +123,9 @@ struct Geometry {
   static_assert(!FP8A || (kStages % 2 == 0 && kASlots % 2 == 0), "even rings");
   static_assert(kRawOff % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
   static_assert(!(FP8A && SMALLA), "the E4M3 loader has its own slot layout");
-  static_assert(!SMALLA || kStageBytes >= kABytes, "the MMA's 128 A rows stay inside the stage");
+  static_assert(!SMALLA || kStageBytes >= kABytes + (kABoxes - 1) * kABoxSlot,
+                "the MMA's 128 A rows stay inside the stage");
+  static_assert(KS == kBK || (KS == 2 * kBK && SMALLA && !FP8A), "deep stages: small-A bf16");
 };
 
 // Pair kernel, per CTA: TMA slot [A bf16 tile 16 KB][2 B atoms 16 KB], or with an
@@ -683,12 +692,12 @@ __device__ __forceinline__ bool forward_conversions(int n_stages_total, int slot
 
 // ------------------------- single-CTA kernel --------------------------------
 
-template <int N_ATOMS, bool SWIGLU, bool FP8A, bool SMALLA>
-__global__ void __launch_bounds__(Geometry<N_ATOMS, FP8A, SMALLA>::kThreads, 1)
+template <int N_ATOMS, bool SWIGLU, bool FP8A, bool SMALLA, int KS>
+__global__ void __launch_bounds__(Geometry<N_ATOMS, FP8A, SMALLA, KS>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b0,
                     const __grid_constant__ CUtensorMap tmap_b1, const GemmArgs args) {
-  using G = Geometry<N_ATOMS, FP8A, SMALLA>;
+  using G = Geometry<N_ATOMS, FP8A, SMALLA, KS>;
   constexpr int kStages = G::kStages;
   constexpr int kASlots = G::kASlots;
   constexpr int kAccBufs = G::kAccBufs;
@@ -705,7 +714,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_seg = args.n_seg;
   const int n_blocks = args.N / kBnOut;
-  const int k_steps = args.K / kBK;
+  const int k_steps = args.K / KS;
+  const int stage_tx = G::kABoxes * args.a_box_bytes + N_ATOMS * G::kAtom;
 
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
@@ -758,13 +768,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int total_tiles = sm.s_tile_start[n_seg];
 
   bool gathered = false;
-  if constexpr (SWIGLU && !FP8A) gathered = args.gather != nullptr;
+  if constexpr (SWIGLU && !FP8A && KS == kBK) gathered = args.gather != nullptr;
   if (warp == 0 && gathered) {
     // ============ TMA producer, A rows gathered from token order ============
     // The whole warp: lane 0 waits and arms the stage, lanes 0 .. bm/4-1 each
     // gather four A rows (512 bytes at offset 512 * lane of the A tile), lane 0
     // loads the B atoms.
-    if constexpr (SWIGLU && !FP8A) {
+    if constexpr (SWIGLU && !FP8A && KS == kBK) {
       const int lanes_a = args.bm / 4;
       int s = 0;
       uint32_t ph = 0;
@@ -818,11 +828,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           staged = min(kStages, k_steps);
           for (int ks = 0; ks < staged; ++ks) {  // the ring's first round: all slots free
             const uint32_t st = smem_u32(stage_base + ks * G::kStageBytes);
-            mbar_arrive_expect_tx(full_bar(ks), args.a_box_bytes + N_ATOMS * kAtomBytes);
+            mbar_arrive_expect_tx(full_bar(ks), stage_tx);
 #pragma unroll
             for (int a = 0; a < N_ATOMS; ++a)
-              tma_load_2d(st + G::kBOff + a * kAtomBytes, &tmap_b0, full_bar(ks), tl.n0 + a * 64,
-                          b_row0 + ks * kBK);
+              tma_load_2d(st + G::kBOff + a * G::kAtom, &tmap_b0, full_bar(ks), tl.n0 + a * 64,
+                          b_row0 + ks * KS);
           }
         }
         pdl_wait();  // the A rows (H) are the gate/up pass's output
@@ -836,24 +846,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
           if (!pre) {
             if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
-            mbar_arrive_expect_tx(full_bar(s), args.a_box_bytes + N_ATOMS * kAtomBytes);
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);
           }
-          // A: the bf16 tile, or the E4M3 tile for the converter warps
-          tma_load_2d(FP8A ? st + G::kRawOff : st, &tmap_a, full_bar(s), ks * kBK, tl.row0);
+          // A: the bf16 tile (KS / 64 boxes), or the E4M3 tile for the converter warps
+#pragma unroll
+          for (int h = 0; h < G::kABoxes; ++h)
+            tma_load_2d(FP8A ? st + G::kRawOff : st + h * G::kABoxSlot, &tmap_a, full_bar(s),
+                        ks * KS + h * kBK, tl.row0);
           if (pre) {  // its weight atoms are already on their way
             if (++s == kStages) { s = 0; ph ^= 1u; }
             continue;
           }
 #pragma unroll
           for (int a = 0; a < N_ATOMS; ++a) {
-            const uint32_t dst = st + G::kBOff + a * kAtomBytes;
+            const uint32_t dst = st + G::kBOff + a * G::kAtom;
             if constexpr (SWIGLU) {
               const int half = N_ATOMS / 2;
               const CUtensorMap* m = a < half ? &tmap_b0 : &tmap_b1;
               const int col = tl.n0 + (a % half) * 64;
-              tma_load_2d(dst, m, full_bar(s), col, b_row0 + ks * kBK);
+              tma_load_2d(dst, m, full_bar(s), col, b_row0 + ks * KS);
             } else {
-              tma_load_2d(dst, &tmap_b0, full_bar(s), tl.n0 + a * 64, b_row0 + ks * kBK);
+              tma_load_2d(dst, &tmap_b0, full_bar(s), tl.n0 + a * 64, b_row0 + ks * KS);
             }
           }
           if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -891,17 +904,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
           const uint32_t b_addr = st + G::kBOff;
 #pragma unroll
-          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+          for (int kk = 0; kk < KS / kUmmaK; ++kk) {
             // B: N-major, advance 16 K rows = 2048 bytes; atoms of 64 columns
-            // are kAtomBytes apart (LBO), 8-row K groups 1024 bytes apart (SBO).
-            const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 128, kAtomBytes, 1024);
+            // are G::kAtom apart (LBO), 8-row K groups 1024 bytes apart (SBO).
+            const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 128, G::kAtom, 1024);
             if constexpr (FP8A) {
               // A in tensor memory: 16 K values = 8 columns of slot a
               const uint32_t ta = tmem_base + static_cast<uint32_t>(G::kACol + a * kASlotCols + kk * (kUmmaK / 2));
               mma_bf16_ta(d_tmem, ta, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
             } else {
-              // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
-              const uint64_t ad = smem_desc_sw128(st + kk * kUmmaK * 2, 16, 1024);
+              // A: K-major, advance 16 elements = 32 bytes inside the swizzle row
+              // of the stage's (kk / 4)-th A box.
+              constexpr int kPerBox = kBK / kUmmaK;
+              const uint64_t ad = smem_desc_sw128(
+                  st + (kk / kPerBox) * G::kABoxSlot + (kk % kPerBox) * kUmmaK * 2, 16, 1024);
               mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
             }
           }
@@ -1340,11 +1356,11 @@ int num_sms() {
   return n;
 }
 
-template <int N_ATOMS, bool SWIGLU, bool FP8A = false, bool SMALLA = false>
+template <int N_ATOMS, bool SWIGLU, bool FP8A = false, bool SMALLA = false, int KS = kBK>
 moe_status launch_gemm_shape(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                              const GemmArgs& args, cudaStream_t s) {
-  using G = Geometry<N_ATOMS, FP8A, SMALLA>;
-  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU, FP8A, SMALLA>;
+  using G = Geometry<N_ATOMS, FP8A, SMALLA, KS>;
+  auto kern = grouped_gemm_kernel<N_ATOMS, SWIGLU, FP8A, SMALLA, KS>;
   // The shared-memory opt-in and the SM count are per device: set/read once.
   constexpr int kMaxDev = 64;
   static int sms[kMaxDev] = {};
@@ -1368,10 +1384,15 @@ moe_status launch_gemm_shape(const CUtensorMap& a, const CUtensorMap& b0, const 
 
 // Single-CTA launch: the small-A slot layout (deeper pipeline) when the row
 // boxes hold at most 32 rows, the A operand is bf16 and a stage (at least two B
-// atoms) covers the 128 rows the MMA reads.
+// atoms) covers the 128 rows the MMA reads; with `deep` (weight maps of 128-row
+// boxes, see deep_stages; two B atoms per stage only) its stages take 128 K each.
 template <int N_ATOMS, bool SWIGLU, bool FP8A = false>
 moe_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                       const GemmArgs& args, cudaStream_t s) {
+                       const GemmArgs& args, cudaStream_t s, bool deep = false) {
+  if constexpr (!FP8A && N_ATOMS == 2) {
+    if (deep) return launch_gemm_shape<N_ATOMS, SWIGLU, false, true, 2 * kBK>(a, b0, b1, args, s);
+  }
+  if (deep) return MOE_ERR_UNSUPPORTED;  // maps of 128-row boxes need the deep kernel
   if constexpr (!FP8A && N_ATOMS >= 2) {
     if (args.bm <= 32) return launch_gemm_shape<N_ATOMS, SWIGLU, false, true>(a, b0, b1, args, s);
   }
@@ -1462,6 +1483,14 @@ bool wide_gate_up(int32_t n_seg, int32_t max_rows, int32_t I) {
   return I % 128 == 0 && wide_tiles(n_seg, max_rows, I / 128);
 }
 
+// Deep stages (128 K per stage, weight boxes of 128 rows) for the small-A
+// single-CTA kernel with two B atoms per stage (the narrow tiles): bf16 rows staged
+// by tile loads (not gathered) and K a multiple of 128.  (With four atoms a deep
+// stage is 72 KB and only two fit the shared memory.)
+bool deep_stages(bool pair, int bm, bool gathered, int32_t K, bool narrow) {
+  return !pair && bm <= 32 && !gathered && K % (2 * kBK) == 0 && narrow;
+}
+
 bool pair_shape(int32_t n_seg, int32_t max_rows) {
   return static_cast<int64_t>(max_rows) >= static_cast<int64_t>(kBM) * n_seg;
 }
@@ -1511,18 +1540,21 @@ static moe_status gate_up_impl(int32_t n_seg, int32_t d, int32_t I, int32_t max_
   const bool pair = I % 128 == 0 && pair_shape(n_seg, max_rows);
   const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
   CUtensorMap m_x, m_wg, m_wu;
+  const bool wide = !pair && wide_gate_up(n_seg, max_rows, I);
+  const bool deep = deep_stages(pair, bm, gather != nullptr, d, !wide);
+  const uint32_t b_rows = deep ? 2 * kBK : kBK;
   const bool x_ok = gather == nullptr ? make_map(&m_x, x, max_rows, d, bm)
                                       : make_map(&m_x, x, T, d, 1);  // one-row boxes
-  if (!x_ok || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, kBK) ||
-      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, kBK))
+  if (!x_ok || !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, b_rows) ||
+      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, b_rows))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
              dev_status, choose_m_outer(n_seg, max_rows, d, 2 * static_cast<int64_t>(I)),
              nullptr, 0, 0, bm, bm * kBK * 2, gather, k, T};
   cudaStream_t s = as_cuda(stream);
   if (pair) return launch_gemm_pair<true>(m_x, m_wg, m_wu, a, s);
-  if (wide_gate_up(n_seg, max_rows, I)) return launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
-  return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s);
+  if (wide) return launch_gemm<4, true>(m_x, m_wg, m_wu, a, s);
+  return launch_gemm<2, true>(m_x, m_wg, m_wu, a, s, deep);
 }
 
 MOE_API moe_status moe_grouped_gate_up(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
@@ -1608,17 +1640,19 @@ static moe_status down_impl(int32_t n_seg, int32_t I, int32_t d, int32_t max_row
   if (!aligned16(h) || !aligned16(y) || !aligned16(w_down)) return MOE_ERR_UNSUPPORTED;
   const bool pair = d % 256 == 0 && pair_shape(n_seg, max_rows);
   const int bm = pair ? kBM : choose_bm(n_seg, max_rows);
+  const bool wide = !pair && d % 256 == 0 && wide_tiles(n_seg, max_rows, d / 256);
+  const bool deep = deep_stages(pair, bm, false, I, !wide && d % 128 == 0);
   CUtensorMap m_h, m_wd;
-  if (!make_map(&m_h, h, max_rows, I, bm) || !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, kBK))
+  if (!make_map(&m_h, h, max_rows, I, bm) ||
+      !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, deep ? 2 * kBK : kBK))
     return MOE_ERR_CUDA;
   GemmArgs a{seg_begin, seg_count, n_seg, I, d, max_rows, reinterpret_cast<uint16_t*>(y),
              dev_status, choose_m_outer(n_seg, max_rows, I, d), nullptr, 0, 0, bm, bm * kBK * 2,
              nullptr, 0, 0, chained};
   cudaStream_t s = as_cuda(stream);
   if (pair) return launch_gemm_pair<false>(m_h, m_wd, m_wd, a, s);
-  if (d % 256 == 0 && wide_tiles(n_seg, max_rows, d / 256))
-    return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
-  if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s);
+  if (wide) return launch_gemm<4, false>(m_h, m_wd, m_wd, a, s);
+  if (d % 128 == 0) return launch_gemm<2, false>(m_h, m_wd, m_wd, a, s, deep);
   return launch_gemm<1, false>(m_h, m_wd, m_wd, a, s);
 }
 

@@ -373,8 +373,27 @@ def test_grouped_swiglu_max_segments():
     _gemm_case(1024, 64, 128, rng.integers(0, 4, size=1024), sample=256)
 
 
+_R5 = np.random.default_rng(5)
+DEEP_CASES = [
+    # (n_seg, d, I, counts): narrow tiles with at most 32 rows per box and K a multiple
+    # of 128, so both passes run 128-K stages of 128-row weight boxes
+    (128, 2048, 768, [1 if e % 16 == 3 else 0 for e in range(128)]),  # one-token decode
+    (32, 256, 768, list(_R5.integers(1, 4, size=32))),     # gate/up: 384 tiles, ring wraps
+    (24, 2048, 256, list(_R5.integers(1, 5, size=24))),    # down: 384 tiles, 2 k-steps
+    (16, 384, 384, [7, 0, 8, 5, 6, 8, 8, 1, 0, 7, 3, 8, 40, 6, 2, 8]),  # 32-row boxes, ragged
+]
+
+
+@pytest.mark.parametrize("n_seg,d,I,counts", DEEP_CASES)
+def test_grouped_swiglu_deep_stages(n_seg, d, I, counts):
+    """Decode-sized segments on the single-CTA kernel's 128-K stages (two A boxes and
+    one 128-row box per weight atom per stage) against the oracle, every row."""
+    _gemm_case(n_seg, d, I, counts)
+
+
 @pytest.mark.parametrize("n_seg,d,I,counts", [
-    (128, 2048, 768, [1 if e % 16 == 3 else 0 for e in range(128)]),  # one-token decode, 4 atoms
+    (128, 2048, 768, [1 if e % 16 == 3 else 0 for e in range(128)]),  # one-token decode, 128-K stages
+    DEEP_CASES[2],                                  # 128-K stages, several down tiles per CTA
     (8, 192, 128, [3, 0, 5, 1, 0, 2, 7, 4]),       # one 64-column atom, 2 k-steps < ring depth
     (4, 128, 256, [40, 0, 17, 90]),                 # two atoms, 64-row boxes
     (64, 512, 1024, [30 + (e * 7) % 11 for e in range(64)]),  # several tiles per CTA
