@@ -276,34 +276,38 @@ void launch_rank(const RouteArgs& a, cudaStream_t s) {
 // is a stream of logits, and the warp-per-token kernel spends hundreds of warp
 // instructions per token on warp-wide steps.  Here four lanes select one token,
 // each lane a quarter of its row.  A warp takes 8 consecutive tokens at a time:
-// their rows arrive by 2-D TMA boxes (8 rows x 32 experts, 128-byte swizzle) in a
-// 12 KB (E = 384) stage per warp, so 16 warps share an SM.  Lane 4r + h holds row
+// their rows arrive by 2-D TMA boxes (8 rows x 32 experts, 128-byte swizzle) in
+// one of the warp's two 12 KB (E = 384) stages, so the next batch's rows arrive
+// while the current one is selected (9 warps share an SM).  Lane 4r + h holds row
 // r's boxes h, h + 4, ...; the parts read their chunks in different orders so no
-// two lanes of a phase meet in a bank.  Then
-//   1. each lane takes the maxima of 4 chunks of its quarter; two shuffles give
-//      all four lanes the row's 16 chunk maxima, and theta = the k-th largest of
-//      them is a lower bound of the row's k-th largest score (the k chunks
-//      holding those maxima hold k scores >= theta);
-//   2. each lane marks the scores of its quarter that are not below theta (NaN
-//      included) and inserts them, in expert order, into a sorted list of KS
-//      orderable keys (0 = empty; ties keep the lower expert first), a NaN as
-//      -inf (reported);
-//   3. the row's four lanes merge their lists with shuffles (larger key first,
-//      then the lower expert) and form the gates exactly as the warp router does
-//      (exp against the top score, the normaliser summed in the warp's slot-order
-//      butterfly), each lane storing a quarter of the slots.
-// Selection, ids and gates are therefore identical to the warp router's.
+// two lanes of a phase meet in a bank.  For k <= 8 (quarter_select_fast):
+//   1. each lane takes the maxima of the 8 chunks of its quarter; theta, the 8th
+//      largest of the row's 32, is a lower bound of its k-th largest score (the
+//      8 chunks holding those maxima hold 8 scores >= theta);
+//   2. exactly 8 chunks reach theta (else the general selection below), and every
+//      score not below theta lies in them: the row's four lanes scan two each and
+//      write those scores (at most 16, else the general selection) as orderable
+//      64-bit keys into the row's 16 shared-memory slots;
+//   3. a bitonic network over the four lanes sorts the slots, and the gates are
+//      formed exactly as the warp router does (exp against the top score, the
+//      normaliser summed in the warp's slot-order butterfly).
+// The general selection (any k <= 16, NaN logits, ties at theta) takes theta
+// from 16 chunk maxima, inserts every score of its quarter not below theta into a
+// per-lane sorted list of KS keys and merges the four lists with shuffles.
+// Selection, ids and gates are identical to the warp router's either way.
 constexpr int kQuarter = 4;                       // lanes per token
 constexpr int kQuarterRows = 32 / kQuarter;       // tokens per warp batch
 constexpr int kQuarterWarps = 16;                 // warps per block, at most
 
 template <int NM, int KS>
 struct QuarterRouter {
-  static constexpr int E = 32 * NM;
   static constexpr int kBoxBytes = kQuarterRows * 128;       // 1 KB: 8 rows x 32 fp32
   static constexpr int kStage = NM * kBoxBytes;              // one warp's rows
-  static constexpr int kLists = kQuarterRows * kQuarter * KS * 8;  // keys and ids to merge
-  static constexpr int kWarpBytes = ((kStage + kLists) + 1023) & ~1023;
+  // the fast selection's 16 candidate slots per row (the general selection merges
+  // in the stage it has just read)
+  static constexpr int kLists = KS == 8 ? kQuarterRows * 16 * 8 : 0;
+  static constexpr int kStages = 2;                          // the next batch in flight
+  static constexpr int kWarpBytes = ((kStages * kStage + kLists) + 1023) & ~1023;
   static constexpr int kFit = (227 * 1024 - 1024) / kWarpBytes;
   static constexpr int kWarps = kFit < kQuarterWarps ? kFit : kQuarterWarps;
   static constexpr int kSmem = 1024 + kWarps * kWarpBytes;
@@ -359,20 +363,370 @@ __device__ __forceinline__ void key_insert(uint32_t (&tk)[KS], int (&ti)[KS], ui
   if (key > tk[0]) { tk[0] = key; ti[0] = e; }
 }
 
+// Bitonic merge network for 8 values that form a bitonic sequence: sorts them
+// descending in place.
+__device__ __forceinline__ void bitonic8_desc(float* x) {
+  auto ce = [&](int i, int j) {
+    const float hi = fmaxf(x[i], x[j]), lo = fminf(x[i], x[j]);
+    x[i] = hi;
+    x[j] = lo;
+  };
+  ce(0, 4); ce(1, 5); ce(2, 6); ce(3, 7);
+  ce(0, 2); ce(1, 3); ce(4, 6); ce(5, 7);
+  ce(0, 1); ce(2, 3); ce(4, 5); ce(6, 7);
+}
+
+// Maxima that propagate NaN: a NaN among the inputs gives NaN.
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float max2_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Compare-exchange of two 64-bit selection keys, the larger first.
+__device__ __forceinline__ void ce_desc(uint64_t& a, uint64_t& b) {
+  const bool sw = b > a;
+  const uint64_t hi = sw ? b : a;
+  b = sw ? a : b;
+  a = hi;
+}
+
+// The larger (keep_max) or the smaller of a lane's key and its partner's.
+__device__ __forceinline__ uint64_t keep_key(uint64_t own, uint64_t other, bool keep_max) {
+  return ((own > other) == keep_max) ? own : other;
+}
+
+// Shared-memory address of float4 p (0 .. 8 * NM / 4 - 1, in the order part hp reads
+// its quarter) of row r: box hp + 4 * (p / 8), logical 16-byte column (p % 8) ^ 2hp,
+// stored at column ((p % 8) ^ 2hp) ^ (r % 8) by the copy's 128-byte swizzle.  The
+// column's first expert is 32 * box + 4 * column.
+__device__ __forceinline__ uint32_t quarter_f4(uint32_t stage, int r, int hp, int p, int& e0) {
+  const int b = hp + kQuarter * (p >> 3), cc = (p & 7) ^ (2 * hp);
+  e0 = 32 * b + 4 * cc;
+  return stage + static_cast<uint32_t>(b * kQuarterRows * 128 + r * 128 + ((cc ^ (r & 7)) << 4));
+}
+
+// The general selection (any k <= KS, NaN logits, ties): theta from the row's 16
+// chunk maxima (4 per lane, NaN ignored), every candidate of the lane's quarter
+// inserted in expert order into a sorted list of KS keys, the four lists merged
+// through the stage's first KS KB once its rows have been read.  Leaves the row's
+// top KS keys and experts, sorted, in tk/ti of all four lanes; issue_next() runs
+// after the merge, when the stage is free.
+template <int NM, int KS, class F>
+__device__ __forceinline__ void quarter_select_general(uint32_t stage, const uint32_t (&slot)[8],
+                                                       int lane, int r,
+                                                       int h, bool live, bool& saw_nan,
+                                                       uint32_t (&tk)[KS], int (&ti)[KS],
+                                                       F&& issue_next) {
+  using R = QuarterRouter<NM, KS>;
+  constexpr int kPer = NM / kQuarter;  // boxes of one quarter
+  // 1. maxima of this quarter's 4 chunks (NaN ignored: an all-NaN chunk is -inf),
+  //    then the row's 16 from the other quarters
+  float cm[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cm[j] = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
+    float4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = lds_f4(bx + slot[c]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int j = (8 * i + c) / (2 * kPer);  // 4 chunks of 2 * kPer float4 each
+      cm[j] = fmaxf(cm[j], fmaxf(fmaxf(v[c].x, v[c].y), fmaxf(v[c].z, v[c].w)));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cm[4 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 1);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cm[8 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 2);
+  // theta, a lower bound of the row's k-th largest score: with KS = 8 (k <= 8) the
+  // 8th largest chunk maximum (the two sorted halves' pairwise maxima are the top
+  // 8, theta their minimum); with KS = 16 the smallest of the 16
+  float th;
+  if (KS == 8) {
+    sort8_desc(cm);
+    sort8_desc(cm + 8);
+    th = fmaxf(cm[0], cm[15]);
+#pragma unroll
+    for (int j = 1; j < 8; ++j) th = fminf(th, fmaxf(cm[j], cm[15 - j]));
+  } else {
+    th = cm[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) th = fminf(th, cm[j]);
+  }
+  // (a warp barrier orders the shared memory: the second pass reloads the rows
+  // instead of keeping the first pass's values live across the sort)
+  __syncwarp();
+  // 2. this quarter's candidates (not below theta; a NaN compares unordered), in
+  //    expert order, into a sorted list
+  uint32_t msk[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
+    uint32_t m = 0u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 v = lds_f4(bx + slot[c]);
+      const int sh = 4 * (c ^ (2 * h));
+      m |= (not_below(v.x, th) & (1u << sh)) | (not_below(v.y, th) & (2u << sh)) |
+           (not_below(v.z, th) & (4u << sh)) | (not_below(v.w, th) & (8u << sh));
+    }
+    msk[i] = m;
+  }
+#pragma unroll
+  for (int j = 0; j < KS; ++j) { tk[j] = 0u; ti[j] = 0; }
+  {
+    int i = 0;
+    uint32_t m = msk[0];
+    for (;;) {
+      while (m == 0u && i + 1 < kPer) {  // the next box with candidates
+        ++i;
+#pragma unroll
+        for (int ii = 1; ii < kPer; ++ii) m = ii == i ? msk[ii] : m;
+      }
+      if (m == 0u) break;
+      const int e = __ffs(m) - 1;
+      m &= m - 1u;
+      const int b = h + kQuarter * i;
+      float v = lds_f1(stage + static_cast<uint32_t>(b * R::kBoxBytes + r * 128 +
+                                                     ((((e >> 2) ^ (r & 7)) & 7) << 4) + ((e & 3) << 2)));
+      if (v != v) { saw_nan |= live; v = -INFINITY; }
+      key_insert<KS>(tk, ti, ord_bits(v), 32 * b + e);
+    }
+  }
+  // 3. each lane's list to shared memory over the read rows (entry-major: entry j
+  //    of lane l at j * 32 + l), where the merge reads a lane's next entry
+  const uint32_t lists = stage;
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < KS; ++j)
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(lists + static_cast<uint32_t>((j * 32 + lane) * 8)),
+                 "r"(tk[j]), "r"(static_cast<uint32_t>(ti[j])) : "memory");
+  __syncwarp();
+  // merge: KS rounds; in each, the row's four lanes agree (two shuffle steps) on the
+  // best head -- larger key, then the lower expert -- and its lane advances
+  int pos = 0;
+  uint32_t hk = tk[0];
+  int hi = ti[0];
+#pragma unroll
+  for (int j = 0; j < KS; ++j) {
+    uint32_t bk = hk;
+    int bi = hi, bl = h;
+#pragma unroll
+    for (int o = 1; o < kQuarter; o <<= 1) {
+      const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      const int ol = __shfl_xor_sync(0xFFFFFFFFu, bl, o);
+      const bool better = ok > bk || (ok == bk && oi < bi);
+      bk = better ? ok : bk;
+      bi = better ? oi : bi;
+      bl = better ? ol : bl;
+    }
+    tk[j] = bk;
+    ti[j] = bi;
+    if (bl == h && j + 1 < KS) {  // this lane's head was taken: the next entry
+      ++pos;
+      uint32_t kk = 0u, ii = 0u;
+      if (pos < KS)
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(kk), "=r"(ii)
+                     : "r"(lists + static_cast<uint32_t>((pos * 32 + lane) * 8)) : "memory");
+      hk = kk;
+      hi = static_cast<int>(ii);
+    }
+  }
+  // the lists were written through the generic proxy; the copy into the same
+  // bytes goes through the async proxy
+  __syncwarp();
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  issue_next();
+}
+
+// The selection for k <= 8 on rows without NaN.  theta = the 8th largest of the
+// row's 32 chunk maxima (8 per lane) bounds the k-th largest score from below; when
+// exactly 8 chunks reach it, every score not below theta lies in those 8, and the
+// row's four lanes scan two of them each (the 1st and 5th, 2nd and 6th, ... in chunk
+// order), so a lane reads a quarter of what it would scan in its own quarter.  The
+// candidates (at most 16 per row) go as 64-bit keys -- orderable score bits, then
+// the complement of the expert, so larger means the higher score and, among equal
+// scores, the lower expert -- into the row's 16 slots in shared memory, 4 per lane,
+// and a bitonic network over the four lanes sorts them.  Returns false, having
+// written nothing, when a live row of the batch holds a NaN, more than 8 chunks
+// reach theta (a tie at theta) or more than 16 scores do; otherwise lane h < 2 of
+// each row holds the row's ranks 4h .. 4h + 3 in key[], and issue_next() has run.
+template <int NM, class F>
+__device__ __forceinline__ bool quarter_select_fast(uint32_t stage, uint32_t lists,
+                                                    const uint32_t (&slot)[8], int r, int h,
+                                                    bool live, uint64_t (&key)[4],
+                                                    F&& issue_next) {
+  constexpr int kPer = NM / kQuarter;  // boxes of one quarter
+  constexpr int kF = kPer;             // float4 per chunk: a quarter is 8 chunks
+  constexpr unsigned kAll = 0xFFFFFFFFu;
+  // 1. this quarter's 8 chunk maxima (a NaN anywhere in a chunk gives NaN)
+  float cm[8];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * kQuarterRows * 128);
+    float4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = lds_f4(bx + slot[c]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int p = 8 * i + c, j = p / kF;
+      const float m = max3_nan(v[c].x, v[c].y, v[c].z);
+      if (p % kF == 0)
+        cm[j] = max2_nan(m, v[c].w);
+      else
+        cm[j] = max3_nan(cm[j], m, v[c].w);
+    }
+  }
+  bool nan_row = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) nan_row |= cm[j] != cm[j];
+  if (__any_sync(kAll, live && nan_row)) return false;
+  // 2. theta: this lane's 8 maxima sorted, the top 8 of each lane pair (half-cleaner
+  //    of the two sorted lists, then a bitonic merge), and the smallest of the top 8
+  //    over the two pairs
+  float w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = cm[j];
+  sort8_desc(w);
+  {
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __shfl_xor_sync(kAll, w[7 - j], 1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = fmaxf(w[j], o[j]);
+    bitonic8_desc(w);
+  }
+  float th;
+  {
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __shfl_xor_sync(kAll, w[7 - j], 2);
+    th = fmaxf(w[0], o[0]);
+#pragma unroll
+    for (int j = 1; j < 8; ++j) th = fminf(th, fmaxf(w[j], o[j]));
+  }
+  // 3. the row's chunks that reach theta, as a mask over chunk ids 8 * part + chunk
+  uint32_t qm = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) qm |= (cm[j] >= th ? 1u : 0u) << j;
+  qm <<= 8 * h;
+  qm |= __shfl_xor_sync(kAll, qm, 1);
+  qm |= __shfl_xor_sync(kAll, qm, 2);
+  if (__any_sync(kAll, live && __popc(qm) != 8)) return false;
+  // lane h takes the row's qualifying chunks h and h + 4 (rows that are not live
+  // read two of their own chunks and keep nothing)
+  uint32_t wm = qm;
+#pragma unroll
+  for (int s = 0; s < 3; ++s)
+    if (s < h) wm &= wm - 1u;
+  const int c0 = live ? __ffs(wm) - 1 : 8 * h;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) wm &= wm - 1u;
+  const int c1 = live ? __ffs(wm) - 1 : 8 * h + 1;
+  // 4. their candidates: bit 16 * (second chunk) + 4 * float4 + component
+  uint32_t lm = 0u;
+#pragma unroll
+  for (int u2 = 0; u2 < 2; ++u2) {
+    const int cid = u2 ? c1 : c0;
+#pragma unroll
+    for (int u = 0; u < kF; ++u) {
+      int e0;
+      const float4 v = lds_f4(quarter_f4(stage, r, cid >> 3, kF * (cid & 7) + u, e0));
+      const int sh = 16 * u2 + 4 * u;
+      lm |= (not_below(v.x, th) & (1u << sh)) | (not_below(v.y, th) & (2u << sh)) |
+            (not_below(v.z, th) & (4u << sh)) | (not_below(v.w, th) & (8u << sh));
+    }
+  }
+  if (!live) lm = 0u;
+  // 5. the row's candidate count and this lane's first slot (the lanes before it)
+  const int cnt = __popc(lm);
+  const int s1 = __shfl_xor_sync(kAll, cnt, 1);
+  const int s2 = __shfl_xor_sync(kAll, cnt + s1, 2);
+  const int ct = cnt + s1 + s2;
+  if (__any_sync(kAll, ct > 16)) return false;
+  int n = ((h & 1) ? s1 : 0) + ((h & 2) ? s2 : 0);
+  const uint32_t row_slots = lists + static_cast<uint32_t>(r * 128);
+  while (lm != 0u) {
+    const int s = __ffs(lm) - 1;
+    lm &= lm - 1u;
+    const int cid = (s >> 4) ? c1 : c0;
+    int e0;
+    const uint32_t a = quarter_f4(stage, r, cid >> 3, kF * (cid & 7) + ((s >> 2) & 3), e0);
+    const float v = lds_f1(a + static_cast<uint32_t>((s & 3) << 2));
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(row_slots + static_cast<uint32_t>(8 * n)),
+                 "r"(0xFFFFFFFFu - static_cast<uint32_t>(e0 + (s & 3))), "r"(ord_bits(v)) : "memory");
+    ++n;
+  }
+  __syncwarp();
+  issue_next();  // the staged rows are free
+  // 6. this lane's 4 slots (slots past the row's count are empty: key 0, below any
+  //    score's key), then the bitonic network over the row's 16
+  {
+    uint32_t q[8];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+                 : "r"(row_slots + static_cast<uint32_t>(32 * h)) : "memory");
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7])
+                 : "r"(row_slots + static_cast<uint32_t>(32 * h + 16)) : "memory");
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      key[s] = 4 * h + s < ct ? (static_cast<uint64_t>(q[2 * s + 1]) << 32) | q[2 * s] : 0ull;
+  }
+  // each lane's 4 sorted
+  ce_desc(key[0], key[1]); ce_desc(key[2], key[3]);
+  ce_desc(key[0], key[2]); ce_desc(key[1], key[3]);
+  ce_desc(key[1], key[2]);
+  // lane pairs: half-cleaner of the two sorted 4s (the even lane keeps the larger
+  // half), then each half sorted
+  {
+    uint64_t o[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) o[s] = __shfl_xor_sync(kAll, key[3 - s], 1);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) key[s] = keep_key(key[s], o[s], (h & 1) == 0);
+    ce_desc(key[0], key[2]); ce_desc(key[1], key[3]);
+    ce_desc(key[0], key[1]); ce_desc(key[2], key[3]);
+  }
+  // the row: the top 8 of the two sorted 8s (lanes 0-1 against lanes 3-2), then
+  // sorted across lanes 0 and 1
+  {
+    uint64_t o[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) o[s] = __shfl_xor_sync(kAll, key[3 - s], 3);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) key[s] = keep_key(key[s], o[s], h < 2);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) o[s] = __shfl_xor_sync(kAll, key[s], 1);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) key[s] = keep_key(key[s], o[s], (h & 1) == 0);
+    ce_desc(key[0], key[2]); ce_desc(key[1], key[3]);
+    ce_desc(key[0], key[1]); ce_desc(key[2], key[3]);
+  }
+  return true;
+}
+
 template <int NM, int KS>  // E = 32 * NM experts; k <= KS
 __global__ void __launch_bounds__(QuarterRouter<NM, KS>::kWarps * 32, 1)
 route_quarter_kernel(const __grid_constant__ CUtensorMap map, RouteArgs a, bool early) {
   using R = QuarterRouter<NM, KS>;
-  constexpr int kPer = NM / kQuarter;  // boxes of one quarter
+  constexpr unsigned kAll = 0xFFFFFFFFu;
   extern __shared__ unsigned char q_raw[];
-  __shared__ uint64_t bar[R::kWarps];
+  __shared__ uint64_t bar[R::kWarps * R::kStages];
   __shared__ int abort_flag;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int r = lane / kQuarter, h = lane % kQuarter;
-  const uint32_t stage = ((smem_u32(q_raw) + 1023u) & ~1023u) + static_cast<uint32_t>(w * R::kWarpBytes);
-  const uint32_t lists = stage + R::kStage;
+  const uint32_t base = ((smem_u32(q_raw) + 1023u) & ~1023u) + static_cast<uint32_t>(w * R::kWarpBytes);
+  const uint32_t lists = base + R::kStages * R::kStage;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < R::kWarps; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    for (int i = 0; i < R::kWarps * R::kStages; ++i) mbar_init(smem_u32(&bar[i]), 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map)) : "memory");
@@ -382,160 +736,91 @@ route_quarter_kernel(const __grid_constant__ CUtensorMap map, RouteArgs a, bool 
   const int k = a.k;
   const int valid = a.valid != nullptr ? min(max(__ldg(a.valid), 0), a.T) : a.T;
   const int n_batches = static_cast<int>(ceil_div(a.T, kQuarterRows));
-  const uint32_t b_addr = smem_u32(&bar[w]);
   // Logical chunk c of this lane's box rows sits at physical slot c ^ (r & 7) (the
   // copy's swizzle); part h walks its chunks in the order c ^ 2h, so the 8 lanes of
   // a phase (2 rows x 4 parts) read 8 different bank groups.
   uint32_t slot[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) slot[c] = static_cast<uint32_t>(r * 128 + (((c ^ (2 * h)) ^ (r & 7)) << 4));
-  uint32_t ph = 0;
-  bool saw_nan = false, pending = false;
-  for (int bt = blockIdx.x * R::kWarps + w; bt < n_batches; bt += gridDim.x * R::kWarps) {
-    const int t0 = bt * kQuarterRows, t = t0 + r;
-    if (lane == 0 && !pending) {  // the first batch (later ones were issued ahead);
-                                  // rows past T are zero-filled by the copy
-      mbar_arrive_expect_tx(b_addr, R::kStage);
+  // A warp's batches alternate between its two stages, so the next batch's rows
+  // arrive while the current one is selected; rows past T are zero-filled by the copy.
+  // pend bit s: a copy into stage s is in flight; ph bit s: the parity of its phase.
+  auto issue = [&](int st, int batch) {
+    if (lane == 0) {
+      const uint32_t ba = smem_u32(&bar[w * R::kStages + st]);
+      mbar_arrive_expect_tx(ba, R::kStage);
 #pragma unroll
       for (int b = 0; b < NM; ++b)
-        tma_load_2d(stage + static_cast<uint32_t>(b * R::kBoxBytes), &map, b_addr, b * 32, t0);
+        tma_load_2d(base + static_cast<uint32_t>(st * R::kStage + b * R::kBoxBytes), &map, ba, b * 32,
+                    batch * kQuarterRows);
     }
-    pending = true;
-    if (!__all_sync(0xFFFFFFFFu, wait_bounded(b_addr, ph, &abort_flag, a.dev_status))) break;
-    pending = false;
-    ph ^= 1u;
+  };
+  const int stride = gridDim.x * R::kWarps, first = blockIdx.x * R::kWarps + w;
+  uint32_t pend = 0u, ph = 0u;
+  bool saw_nan = false;
+  for (int st = 0; st < R::kStages; ++st)
+    if (first + st * stride < n_batches) { issue(st, first + st * stride); pend |= 1u << st; }
+  int it = 0;
+  for (int bt = first; bt < n_batches; bt += stride, ++it) {
+    const int t0 = bt * kQuarterRows, t = t0 + r;
+    const int st = it % R::kStages;
+    const uint32_t stage = base + static_cast<uint32_t>(st * R::kStage);
+    if (!__all_sync(kAll, wait_bounded(smem_u32(&bar[w * R::kStages + st]), (ph >> st) & 1u,
+                                       &abort_flag, a.dev_status)))
+      break;
+    pend &= ~(1u << st);
+    ph ^= 1u << st;
     const bool live = t < valid;  // every lane works; only live rows are written
-    // 1. maxima of this quarter's 4 chunks (NaN ignored: an all-NaN chunk is -inf),
-    //    then the row's 16 from the other quarters
-    float cm[16];
+    // the batch after next into this stage, as soon as this batch's rows are no
+    // longer read
+    auto issue_next = [&]() {
+      const int nb = bt + R::kStages * stride;
+      if (nb < n_batches) { issue(st, nb); pend |= 1u << st; }
+    };
+    int32_t* ids_t = a.topk_ids + static_cast<int64_t>(t) * k;
+    float* gates_t = a.gates + static_cast<int64_t>(t) * k;
+    if constexpr (KS == 8) {
+      uint64_t key[4];
+      if (!quarter_select_fast<NM>(stage, lists, slot, r, h, live, key, issue_next)) {
+        uint32_t tk[8];
+        int ti[8];
+        quarter_select_general<NM, 8>(stage, slot, lane, r, h, live, saw_nan, tk, ti, issue_next);
+        const bool odd = (h & 1) != 0;  // lane h < 2 holds ranks 4h .. 4h + 3
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cm[j] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
-      float4 v[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) v[c] = lds_f4(bx + slot[c]);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int j = (8 * i + c) / (2 * kPer);  // 4 chunks of 2 * kPer float4 each
-        cm[j] = fmaxf(cm[j], fmaxf(fmaxf(v[c].x, v[c].y), fmaxf(v[c].z, v[c].w)));
+        for (int s = 0; s < 4; ++s)
+          key[s] = (static_cast<uint64_t>(odd ? tk[4 + s] : tk[s]) << 32) |
+                   (0xFFFFFFFFu - static_cast<uint32_t>(odd ? ti[4 + s] : ti[s]));
       }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cm[4 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 1);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) cm[8 + j] = __shfl_xor_sync(0xFFFFFFFFu, cm[j], 2);
-    // theta, a lower bound of the row's k-th largest score: with KS = 8 (k <= 8) the
-    // 8th largest chunk maximum (the two sorted halves' pairwise maxima are the top
-    // 8, theta their minimum); with KS = 16 the smallest of the 16
-    float th;
-    if (KS == 8) {
-      sort8_desc(cm);
-      sort8_desc(cm + 8);
-      th = fmaxf(cm[0], cm[15]);
-#pragma unroll
-      for (int j = 1; j < 8; ++j) th = fminf(th, fmaxf(cm[j], cm[15 - j]));
+      // gates: lane h takes ranks j0 = 4 (h % 2) + 2 (h / 2) and j0 + 1 (lanes 2 and 3
+      // from lanes 0 and 1), exp against the top score, and the normaliser in the warp
+      // router's slot order ((e0 + e4) + (e2 + e6)) + ((e1 + e5) + (e3 + e7)): the
+      // xor-1 partner holds the rank 4 apart, the xor-2 partner the rank 2 apart
+      const float top = ord_to_float(__shfl_sync(kAll, static_cast<uint32_t>(key[0] >> 32), lane & ~3));
+      const bool far = h >= 2;
+      const uint64_t f2 = __shfl_xor_sync(kAll, key[2], 2), f3 = __shfl_xor_sync(kAll, key[3], 2);
+      const uint64_t ka = far ? f2 : key[0], kb = far ? f3 : key[1];
+      const int j0 = 4 * (h & 1) + 2 * (h >> 1);
+      const float ea = j0 < k ? expf(ord_to_float(static_cast<uint32_t>(ka >> 32)) - top) : 0.0f;
+      const float eb = j0 + 1 < k ? expf(ord_to_float(static_cast<uint32_t>(kb >> 32)) - top) : 0.0f;
+      const float pa = ea + __shfl_xor_sync(kAll, ea, 1), pb = eb + __shfl_xor_sync(kAll, eb, 1);
+      const float ssum = (pa + __shfl_xor_sync(kAll, pa, 2)) + (pb + __shfl_xor_sync(kAll, pb, 2));
+      if (live) {
+        if (j0 < k) {
+          ids_t[j0] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(ka));
+          gates_t[j0] = ea / ssum;
+        }
+        if (j0 + 1 < k) {
+          ids_t[j0 + 1] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(kb));
+          gates_t[j0 + 1] = eb / ssum;
+        }
+      } else if (t < a.T) {
+        // padding slot of a fixed token bucket: no expert identity, zero gate
+        for (int j = h; j < k; j += kQuarter) { ids_t[j] = MOE_ROUTE_MASKED; gates_t[j] = 0.0f; }
+      }
     } else {
-      th = cm[0];
-#pragma unroll
-      for (int j = 1; j < 16; ++j) th = fminf(th, cm[j]);
-    }
-    // (a warp barrier orders the shared memory: the second pass reloads the rows
-    // instead of keeping the first pass's values live across the sort)
-    __syncwarp();
-    // 2. this quarter's candidates (not below theta; a NaN compares unordered), in
-    //    expert order, into a sorted list
-    uint32_t msk[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t bx = stage + static_cast<uint32_t>((h + kQuarter * i) * R::kBoxBytes);
-      uint32_t m = 0u;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v = lds_f4(bx + slot[c]);
-        const int sh = 4 * (c ^ (2 * h));
-        m |= (not_below(v.x, th) & (1u << sh)) | (not_below(v.y, th) & (2u << sh)) |
-             (not_below(v.z, th) & (4u << sh)) | (not_below(v.w, th) & (8u << sh));
-      }
-      msk[i] = m;
-    }
-    uint32_t tk[KS];
-    int ti[KS];
-#pragma unroll
-    for (int j = 0; j < KS; ++j) { tk[j] = 0u; ti[j] = 0; }
-    {
-      int i = 0;
-      uint32_t m = msk[0];
-      for (;;) {
-        while (m == 0u && i + 1 < kPer) {  // the next box with candidates
-          ++i;
-#pragma unroll
-          for (int ii = 1; ii < kPer; ++ii) m = ii == i ? msk[ii] : m;
-        }
-        if (m == 0u) break;
-        const int e = __ffs(m) - 1;
-        m &= m - 1u;
-        const int b = h + kQuarter * i;
-        float v = lds_f1(stage + static_cast<uint32_t>(b * R::kBoxBytes + r * 128 +
-                                                       ((((e >> 2) ^ (r & 7)) & 7) << 4) + ((e & 3) << 2)));
-        if (v != v) { saw_nan |= live; v = -INFINITY; }
-        key_insert<KS>(tk, ti, ord_bits(v), 32 * b + e);
-      }
-    }
-    // 3. each lane's list to shared memory (entry-major: entry j of lane l at
-    //    j * 32 + l), where the merge reads a lane's next entry; the staged rows are
-    //    free, so the next batch's rows start to arrive during the merge
-#pragma unroll
-    for (int j = 0; j < KS; ++j)
-      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(lists + static_cast<uint32_t>((j * 32 + lane) * 8)),
-                   "r"(tk[j]), "r"(static_cast<uint32_t>(ti[j])) : "memory");
-    __syncwarp();
-    {
-      const int nb = bt + gridDim.x * R::kWarps;
-      if (lane == 0 && nb < n_batches) {
-        mbar_arrive_expect_tx(b_addr, R::kStage);
-#pragma unroll
-        for (int b = 0; b < NM; ++b)
-          tma_load_2d(stage + static_cast<uint32_t>(b * R::kBoxBytes), &map, b_addr, b * 32,
-                      nb * kQuarterRows);
-      }
-      pending = nb < n_batches;
-    }
-    // merge: KS rounds; in each, the row's four lanes agree (two shuffle steps) on the
-    // best head -- larger key, then the lower expert -- and its lane advances
-    {
-      int pos = 0;
-      uint32_t hk = tk[0];
-      int hi = ti[0];
-#pragma unroll
-      for (int j = 0; j < KS; ++j) {
-        uint32_t bk = hk;
-        int bi = hi, bl = h;
-#pragma unroll
-        for (int o = 1; o < kQuarter; o <<= 1) {
-          const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
-          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-          const int ol = __shfl_xor_sync(0xFFFFFFFFu, bl, o);
-          const bool better = ok > bk || (ok == bk && oi < bi);
-          bk = better ? ok : bk;
-          bi = better ? oi : bi;
-          bl = better ? ol : bl;
-        }
-        tk[j] = bk;
-        ti[j] = bi;
-        if (bl == h && j + 1 < KS) {  // this lane's head was taken: the next entry
-          ++pos;
-          uint32_t kk = 0u, ii = 0u;
-          if (pos < KS)
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(kk), "=r"(ii)
-                         : "r"(lists + static_cast<uint32_t>((pos * 32 + lane) * 8)) : "memory");
-          hk = kk;
-          hi = static_cast<int>(ii);
-        }
-      }
-    }
-    {
+      uint32_t tk[KS];
+      int ti[KS];
+      quarter_select_general<NM, KS>(stage, slot, lane, r, h, live, saw_nan, tk, ti, issue_next);
       // gates: exp against the top score; the normaliser in the warp's order; each of
       // the row's lanes divides and stores the slots j = h, h + 4, ...
       const float top = ord_to_float(tk[0]);
@@ -550,8 +835,6 @@ route_quarter_kernel(const __grid_constant__ CUtensorMap map, RouteArgs a, bool 
 #pragma unroll
         for (int ii = 0; ii < o; ++ii) wv[ii] = wv[ii] + wv[ii + o];
       const float ssum = wv[0];
-      int32_t* ids_t = a.topk_ids + static_cast<int64_t>(t) * k;
-      float* gates_t = a.gates + static_cast<int64_t>(t) * k;
       if (live) {
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
@@ -567,8 +850,10 @@ route_quarter_kernel(const __grid_constant__ CUtensorMap map, RouteArgs a, bool 
     }
     __syncwarp();  // every lane is done with the stage and the lists before the refill
   }
-  if (pending && lane == 0) wait_drain(b_addr, ph);  // a copy still in flight after a timeout
-  if (__any_sync(0xFFFFFFFFu, saw_nan) && lane == 0) report(a.dev_status, MOE_DEV_NONFINITE_LOGIT);
+  if (lane == 0)  // copies still in flight after a timeout
+    for (int st = 0; st < R::kStages; ++st)
+      if (pend & (1u << st)) wait_drain(smem_u32(&bar[w * R::kStages + st]), (ph >> st) & 1u);
+  if (__any_sync(kAll, saw_nan) && lane == 0) report(a.dev_status, MOE_DEV_NONFINITE_LOGIT);
   if (!early) pdl_trigger();
 }
 
