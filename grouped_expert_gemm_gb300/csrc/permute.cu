@@ -103,6 +103,14 @@ permute_rank(int R, int E, int k, int routes_per_tile, int n_tiles, int capacity
   const int tile = blockIdx.x;
 
   for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cnt[i] = 0;
+  if (x_perm != nullptr) {
+    // the block copies the token rows itself (a handful of tokens): they do not
+    // depend on the routes, so their first read from HBM overlaps the router
+    const char* xb = reinterpret_cast<const char*>(x);
+    const int64_t bytes = static_cast<int64_t>(R / k) * chunks * 16;
+    for (int64_t o = static_cast<int64_t>(threadIdx.x) * 128; o < bytes; o += 128 * kRankThreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(xb + o));
+  }
   pdl_wait_then_trigger(early);
   __syncthreads();
   // Routes at or past R_live belong to masked padding tokens of a fixed bucket:
