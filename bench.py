@@ -76,6 +76,9 @@ def parse_args():
     ap.add_argument("--decode-path", default="auto", choices=["auto", "fused", "separate"],
                     help="decode-sized batches: the one-launch layer (fused), the per-stage "
                          "calls (separate), or whichever the layer picks for the size (auto)")
+    ap.add_argument("--expert-passes", default="auto", choices=["auto", "separate", "onepass"],
+                    help="the two expert passes as two launches (separate) or one persistent "
+                         "launch (onepass), or whichever the layer picks (auto)")
     ap.add_argument("--pool-sequential", action="store_true",
                     help="pooled: run every stage of every wave on one stream (the default "
                          "overlaps pack, compact and combine with the expert passes)")
@@ -255,6 +258,10 @@ def stage_work(w, layer, name, counts, acc_rows, n_seg_w, I, d, pool=None):
         return touched * 2 * d * I * 2 + acc_rows * a_row + acc_rows * I * 2, 4 * acc_rows * d * I
     if name == "down":
         return touched * I * d * 2 + acc_rows * I * 2 + acc_rows * d * 2, 2 * acc_rows * I * d
+    if name == "gate_up_down":  # both passes in one launch: their bytes and flops added
+        gb, gf = stage_work(w, layer, "gate_up", counts, acc_rows, n_seg_w, I, d, pool)
+        db, df = stage_work(w, layer, "down", counts, acc_rows, n_seg_w, I, d, pool)
+        return gb + db, gf + df
     if name == "shared_expert":
         Is = w.shared_I
         return 3 * d * Is * 2 + T * d * 2 * 2 + 2 * T * Is * 2, 6 * T * d * Is
@@ -286,6 +293,7 @@ def load_peaks():
 
 def kernel_source_sha(name):
     src = {"gate_up": "grouped_swiglu.cu", "down": "grouped_swiglu.cu",
+           "gate_up_down": "grouped_swiglu.cu",
            "decode_layer": "decode.cu",
            "shared_expert": "grouped_swiglu.cu", "route": "route.cu", "permute": "permute.cu",
            "quantize": "fp8.cu", "dequantize": "fp8.cu",
@@ -327,7 +335,7 @@ def lookup_traffic(stage, workload_name):
 # ----------------------------------------------------------------------------
 
 def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", decode_path="auto",
-                overlap=True):
+                overlap=True, expert_passes="auto"):
     import grouped_expert_gemm_gb300 as g
     if w.pooled and payload != "bf16":
         raise SystemExit("--payload applies to the routed (non-pooled) workloads")
@@ -347,7 +355,7 @@ def build_layer(w, device, payload="bf16", gather=False, fp8_loader="auto", deco
                            n_group=w.n_group, topk_group=w.topk_group, route_scale=w.route_scale,
                            sel_bias=sel_bias, shared_weights=workloads.make_shared_weights(w, device),
                            payload=payload, gather=gather, fp8_loader=fp8_loader,
-                           decode_path=decode_path, device=device)
+                           decode_path=decode_path, expert_passes=expert_passes, device=device)
     return layer, logits, sel_bias, x
 
 
@@ -375,7 +383,8 @@ def run_ours(args, dist, w):
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
     layer, logits, sel_bias, x = build_layer(w, device, args.payload, args.gather,
                                              args.fp8_loader, args.decode_path,
-                                             overlap=not getattr(args, "pool_sequential", False))
+                                             overlap=not getattr(args, "pool_sequential", False),
+                                             expert_passes=getattr(args, "expert_passes", "auto"))
     stream = torch.cuda.Stream(device)
     stages = layer.stages(logits, x)
     names = [n for n, _, _ in stages]
@@ -1243,7 +1252,7 @@ def run_reference(args, dist, w):
 
 RUN_KEYS = ("impl", "gpus", "steps", "warmup", "config", "tokens", "bucket", "payload",
             "fp8_loader", "gather", "no_graph", "no_e2e", "no_cpu_baseline", "extras",
-            "route_only", "decode_path", "experts", "pool_sequential")
+            "route_only", "decode_path", "experts", "pool_sequential", "expert_passes")
 
 
 def run_key(args) -> dict:

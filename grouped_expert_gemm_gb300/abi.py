@@ -49,6 +49,7 @@ EXPORTED = [
     "moe_permute_workspace_size", "moe_permute", "moe_permute_noalloc",
     "moe_grouped_swiglu_workspace_size",
     "moe_grouped_swiglu", "moe_grouped_gate_up", "moe_grouped_down", "moe_grouped_down_chained",
+    "moe_grouped_swiglu_onepass", "moe_grouped_swiglu_onepass_taken",
     "moe_combine", "moe_pool_pack_workspace_size", "moe_pool_pack",
     "moe_pool_compact_workspace_size", "moe_pool_compact", "moe_pool_compact_rotated",
     "moe_compose_map",
@@ -106,6 +107,9 @@ _SIGS = {
     "moe_grouped_gate_up": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_down": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_down_chained": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_grouped_swiglu_onepass": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _P, _P, _P]),
+    "moe_grouped_swiglu_onepass_taken": (_I32, [_I32, _I32, _I32, _I32]),
     "moe_combine": (_I32, [_I32, _I32, _I32, _P, _I64, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_pool_pack_workspace_size": (_SZ, [ctypes.POINTER(PoolParams), _I32, _I32]),
     "moe_pool_pack": (_I32, [ctypes.POINTER(PoolParams), _I32, _I32, _I32, _I32, _P, _P, _P, _P,
@@ -271,6 +275,20 @@ def moe_grouped_swiglu(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w
         n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
         _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
     _count(2 if max_rows > 0 else 0)
+
+
+def moe_grouped_swiglu_onepass_taken(n_seg, d, I, max_rows) -> bool:
+    return bool(lib().moe_grouped_swiglu_onepass_taken(n_seg, d, I, max_rows))
+
+
+def moe_grouped_swiglu_onepass(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up,
+                               w_down, h, y, sync, dev_status=None, stream=None):
+    _check("moe_grouped_swiglu_onepass", lib().moe_grouped_swiglu_onepass(
+        n_seg, d, I, max_rows, _ptr(x), _ptr(seg_begin), _ptr(seg_count), _ptr(w_gate),
+        _ptr(w_up), _ptr(w_down), _ptr(h), _ptr(y), _ptr(sync), _ptr(dev_status),
+        _stream(stream)))
+    if max_rows > 0:
+        _count(1 if moe_grouped_swiglu_onepass_taken(n_seg, d, I, max_rows) else 2)
 
 
 def moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, h,

@@ -1289,6 +1289,303 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
   pdl_trigger();
 }
 
+// ------------------- both passes in one persistent launch ---------------------
+//
+// Decode-sized batches (row boxes of at most 32 rows, d and I multiples of 128) can
+// run the gate/up and the down pass as one launch of the narrow single-CTA tiles
+// with 128-K stages.  The units are the gate/up tiles, then the down tiles, dealt
+// round robin to one CTA per SM.  A CTA's producer streams a down tile's weights
+// into the stage ring right behind its own gate/up weights (or at once, on an SM
+// without a gate/up tile) and waits only before the tile's H rows, until every
+// gate/up tile of the tile's expert has stored its H columns.  The weights of the
+// two passes so stream back to back, with no kernel boundary between them.
+// Per expert q, two counters in `sync` (all zero before a launch, all zero after it):
+// sync[q] counts, four per tile (one release add per epilogue warp after its lanes'
+// stores), the gate/up tiles that stored their H columns, sync[n_seg + q] the stored
+// down tiles; the last count of q's down tiles resets both.  A down tile waits only on gate/up tiles, which
+// come before every down tile in every CTA's order and wait on nothing, and every
+// CTA is resident (one per SM), so each wait ends; it is bounded all the same.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spin (bounded) until *c >= need; false when the CTA is aborting or the wait times out.
+__device__ __forceinline__ bool wait_count(const int32_t* c, int need, volatile int* abort_flag,
+                                           uint32_t* dev_status) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire_gpu(c) >= need) return true;
+    if (*abort_flag) return false;
+    if ((i & 255u) == 255u && global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      report(dev_status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Down tile t of the one-launch kernel: the same segment order as the gate/up tiles
+// (whose table counts n_blocks_gu tiles per m-block), n_blocks_dn tiles per m-block.
+__device__ __forceinline__ Tile down_tile_of(int t, const int* tile_start_gu, const int* s_begin,
+                                             const int* s_count, int n_seg, int bm, int n_blocks_gu,
+                                             int n_blocks_dn) {
+  int lo = 0, hi = n_seg - 1;
+  while (lo < hi) {  // last q whose first down tile is at or before t
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start_gu[mid] / n_blocks_gu * n_blocks_dn <= t) lo = mid; else hi = mid - 1;
+  }
+  const int q = lo;
+  const int local = t - tile_start_gu[q] / n_blocks_gu * n_blocks_dn;
+  const int m_blocks = (s_count[q] + bm - 1) / bm;
+  const int nb = local / m_blocks, mb = local % m_blocks;
+  Tile tl;
+  tl.seg = q;
+  tl.row0 = s_begin[q] + mb * bm;
+  tl.rows = min(bm, s_count[q] - mb * bm);
+  tl.n0 = nb * 128;
+  return tl;
+}
+
+__global__ void __launch_bounds__(192, 1)
+grouped_swiglu_onepass_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                              const __grid_constant__ CUtensorMap tmap_wg,
+                              const __grid_constant__ CUtensorMap tmap_wu,
+                              const __grid_constant__ CUtensorMap tmap_h,
+                              const __grid_constant__ CUtensorMap tmap_wd, const GemmArgs args,
+                              uint16_t* __restrict__ y, int32_t* __restrict__ sync) {
+  using G = Geometry<2, false, true, 2 * kBK>;
+  constexpr int KS = 2 * kBK;
+  constexpr int kStages = G::kStages;
+  constexpr int kN = G::kN;  // 128 accumulator columns in both passes
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Smem sm = carve(stage_base + kStages * G::kStageBytes, G::kBars);
+  uint64_t* bars = sm.bars;
+  volatile int* abort_flag = sm.abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_seg = args.n_seg;
+  const int d = args.K, I = args.N;                        // gate/up: K = d, N = I
+  const int nb_gu = I / 64, nb_dn = d / 128;               // tiles per m-block
+  const int ks_gu = d / KS, ks_dn = I / KS;                // k-steps per tile
+  const int stage_tx = G::kABoxes * args.a_box_bytes + 2 * G::kAtom;
+
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
+  auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * kStages + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_wg)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_wu)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_h)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_wd)) : "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(sm.tmem_slot), G::kTmemAlloc);
+  // everything above is local; global data only after the wait (one CTA per SM, all
+  // resident, so the dependents may launch right away)
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x >= 64 && threadIdx.x < 192)
+    build_segment_table(args, args.bm, nb_gu, sm.s_begin, sm.s_count, sm.s_tile_start, sm.warp_tot);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+  const int total_gu = sm.s_tile_start[n_seg];
+  const int total = total_gu + total_gu / nb_gu * nb_dn;
+  auto unit_tile = [&](int u) {
+    return u < total_gu ? tile_of(u, sm.s_tile_start, sm.s_begin, sm.s_count, n_seg, args.bm, 64,
+                                  nb_gu, 0)
+                        : down_tile_of(u - total_gu, sm.s_tile_start, sm.s_begin, sm.s_count,
+                                       n_seg, args.bm, nb_gu, nb_dn);
+  };
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Tile tl = unit_tile(u);
+        if (u < total_gu) {
+          const int b_row0 = tl.seg * d;
+          for (int ks = 0; ks < ks_gu; ++ks) {
+            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+            const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);
+#pragma unroll
+            for (int hb = 0; hb < G::kABoxes; ++hb)
+              tma_load_2d(st + hb * G::kABoxSlot, &tmap_x, full_bar(s), ks * KS + hb * kBK, tl.row0);
+            tma_load_2d(st + G::kBOff, &tmap_wg, full_bar(s), tl.n0, b_row0 + ks * KS);
+            tma_load_2d(st + G::kBOff + G::kAtom, &tmap_wu, full_bar(s), tl.n0, b_row0 + ks * KS);
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+          }
+        } else {
+          // the weights of the first stages at once, the H rows once the expert's
+          // gate/up tiles have stored them
+          const int b_row0 = tl.seg * I;
+          const int staged = ks_dn < kStages ? ks_dn : kStages;
+          const int s0 = s;
+          for (int ks = 0; ks < staged && ok; ++ks) {
+            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+            const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);
+            tma_load_2d(st + G::kBOff, &tmap_wd, full_bar(s), tl.n0, b_row0 + ks * KS);
+            tma_load_2d(st + G::kBOff + G::kAtom, &tmap_wd, full_bar(s), tl.n0 + 64, b_row0 + ks * KS);
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          const int need = 4 * ((sm.s_count[tl.seg] + args.bm - 1) / args.bm) * nb_gu;
+          if (!wait_count(sync + tl.seg, need, abort_flag, args.dev_status)) { ok = false; break; }
+          // H was stored by other SMs through the generic proxy; the copies read it
+          // through the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          for (int ks = 0; ks < staged; ++ks) {
+            const int ss = (s0 + ks) % kStages;
+            const uint32_t st = smem_u32(stage_base + ss * G::kStageBytes);
+#pragma unroll
+            for (int hb = 0; hb < G::kABoxes; ++hb)
+              tma_load_2d(st + hb * G::kABoxSlot, &tmap_h, full_bar(ss), ks * KS + hb * kBK, tl.row0);
+          }
+          for (int ks = staged; ks < ks_dn; ++ks) {
+            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+            const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+            mbar_arrive_expect_tx(full_bar(s), stage_tx);
+#pragma unroll
+            for (int hb = 0; hb < G::kABoxes; ++hb)
+              tma_load_2d(st + hb * G::kABoxSlot, &tmap_h, full_bar(s), ks * KS + hb * kBK, tl.row0);
+            tma_load_2d(st + G::kBOff, &tmap_wd, full_bar(s), tl.n0, b_row0 + ks * KS);
+            tma_load_2d(st + G::kBOff + G::kAtom, &tmap_wd, full_bar(s), tl.n0 + 64, b_row0 + ks * KS);
+            if (++s == kStages) { s = 0; ph ^= 1u; }
+          }
+        }
+      }
+      if (!ok) {
+        // the copies this thread issued land (or time out) before the CTA goes away
+        int ss = s;
+        uint32_t pp = ph;
+        for (int i = 0; i < kStages; ++i) {
+          if (--ss < 0) { ss = kStages - 1; pp ^= 1u; }
+          wait_drain(full_bar(ss), pp);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kN);
+      constexpr int kPerBox = kBK / kUmmaK;
+      int s = 0, buf = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      bool ok = true, issued_any = false;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const int k_steps = u < total_gu ? ks_gu : ks_dn;
+        if (!wait_bounded(tempty_bar(buf), acc_ph ^ 1u, abort_flag, args.dev_status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kN);
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, args.dev_status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stage_base + s * G::kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < KS / kUmmaK; ++kk) {
+            const uint64_t bd = smem_desc_sw128(st + G::kBOff + kk * kUmmaK * 128, G::kAtom, 1024);
+            const uint64_t ad = smem_desc_sw128(
+                st + (kk / kPerBox) * G::kABoxSlot + (kk % kPerBox) * kUmmaK * 2, 16, 1024);
+            mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit(empty_bar(s));
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(buf));
+        if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      }
+      if (!ok && issued_any) {
+        mma_commit(drain_bar);
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // =========== epilogue (warps 2..5): H with SwiGLU, or y; then the count ===========
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    int buf = 0;
+    uint32_t acc_ph = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Tile tl = unit_tile(u);
+      const bool gu = u < total_gu;
+      if (!__all_sync(0xFFFFFFFFu, wait_bounded(tfull_bar(buf), acc_ph, abort_flag, args.dev_status)))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(buf * kN);
+      const bool live = r < tl.rows;
+      const int row = tl.row0 + (live ? r : 0);
+      if (gu)
+        epilogue_row<64, true>(taddr, live, args.out + static_cast<int64_t>(row) * I + tl.n0);
+      else
+        epilogue_row<128, false>(taddr, live, y + static_cast<int64_t>(row) * d + tl.n0);
+      tc_fence_before();
+      mbar_arrive(tempty_bar(buf));
+      if (++buf == 2) { buf = 0; acc_ph ^= 1u; }
+      // each epilogue warp counts its own quarter of the tile once its lanes' stores
+      // are visible GPU-wide (no barrier across the warps: a warp that leaves the loop
+      // on an abort holds up no other)
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        if (gu) {
+          red_release_gpu_add(sync + tl.seg, 1);
+        } else {
+          const int m_blocks = (sm.s_count[tl.seg] + args.bm - 1) / args.bm;
+          if (atomicAdd(sync + n_seg + tl.seg, 1) == 4 * m_blocks * nb_dn - 1) {
+            // the expert's last down count: every down tile of the expert has passed
+            // its wait, so both counts return to zero for the next launch
+            sync[tl.seg] = 0;
+            sync[n_seg + tl.seg] = 0;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, G::kTmemAlloc);
+  }
+  pdl_trigger();
+}
+
 // ------------------------------ host side ----------------------------------
 
 // 2-D tensor [rows, cols] (cols contiguous) with a box of [box_rows, 64]
@@ -1694,6 +1991,73 @@ MOE_API moe_status moe_grouped_swiglu(int32_t n_seg, int32_t d, int32_t I, int32
   if (st != MOE_OK) return st;
   return moe_grouped_down_chained(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y,
                                   dev_status, stream);
+}
+
+// Whether moe_grouped_swiglu_onepass runs as one launch: the row boxes hold at most 32
+// rows, d and I are multiples of 128, and the two-launch gate/up pass would take the
+// narrow tiles too (measured on the decode shape, µs per step, two launches against one:
+// T = 1 33.84 against 32.73, T = 4 61.05 against 59.0; where the gate/up pass takes the
+// wide tiles the one launch, narrow only, lost: T = 2 42.7 against 45.9, T = 8 77.8
+// against 78.6).
+static bool onepass_taken(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows) {
+  if (n_seg <= 0 || max_rows <= 0 || pair_shape(n_seg, max_rows)) return false;
+  return choose_bm(n_seg, max_rows) <= 32 && d % (2 * kBK) == 0 && I % (2 * kBK) == 0 &&
+         !wide_gate_up(n_seg, max_rows, I);
+}
+
+MOE_API int32_t moe_grouped_swiglu_onepass_taken(int32_t n_seg, int32_t d, int32_t I,
+                                                 int32_t max_rows) {
+  return onepass_taken(n_seg, d, I, max_rows) ? 1 : 0;
+}
+
+// One launch for both passes when onepass_taken; the two launches otherwise.
+MOE_API moe_status moe_grouped_swiglu_onepass(int32_t n_seg, int32_t d, int32_t I,
+                                              int32_t max_rows, const moe_bf16* x,
+                                              const int32_t* seg_begin, const int32_t* seg_count,
+                                              const moe_bf16* w_gate, const moe_bf16* w_up,
+                                              const moe_bf16* w_down, moe_bf16* h, moe_bf16* y,
+                                              int32_t* sync, uint32_t* dev_status,
+                                              moe_stream_t stream) {
+  moe_status st = check_common(n_seg, d, I, max_rows);
+  if (st == MOE_OK) st = check_common(n_seg, I, d, max_rows);
+  if (st != MOE_OK || max_rows == 0) return st;
+  if (x == nullptr || seg_begin == nullptr || seg_count == nullptr || w_gate == nullptr ||
+      w_up == nullptr || w_down == nullptr || h == nullptr || y == nullptr || sync == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(h) || !aligned16(y) || !aligned16(w_gate) ||
+      !aligned16(w_up) || !aligned16(w_down) || (reinterpret_cast<uintptr_t>(sync) & 3u) != 0)
+    return MOE_ERR_UNSUPPORTED;
+  const int bm = choose_bm(n_seg, max_rows);
+  if (!onepass_taken(n_seg, d, I, max_rows)) {
+    st = moe_grouped_gate_up(n_seg, d, I, max_rows, x, seg_begin, seg_count, w_gate, w_up, h,
+                             dev_status, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_down_chained(n_seg, I, d, max_rows, h, seg_begin, seg_count, w_down, y,
+                                    dev_status, stream);
+  }
+  using G = Geometry<2, false, true, 2 * kBK>;
+  CUtensorMap m_x, m_wg, m_wu, m_h, m_wd;
+  if (!make_map(&m_x, x, max_rows, d, bm) ||
+      !make_map(&m_wg, w_gate, int64_t(n_seg) * d, I, 2 * kBK) ||
+      !make_map(&m_wu, w_up, int64_t(n_seg) * d, I, 2 * kBK) ||
+      !make_map(&m_h, h, max_rows, I, bm) ||
+      !make_map(&m_wd, w_down, int64_t(n_seg) * I, d, 2 * kBK))
+    return MOE_ERR_CUDA;
+  GemmArgs a{seg_begin, seg_count, n_seg, d, I, max_rows, reinterpret_cast<uint16_t*>(h),
+             dev_status, 0, nullptr, 0, 0, bm, bm * kBK * 2, nullptr, 0, 0, 0};
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> ready[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MOE_ERR_CUDA;
+  if (!ready[dev].load(std::memory_order_relaxed)) {
+    if (cudaFuncSetAttribute(grouped_swiglu_onepass_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ready[dev].store(1, std::memory_order_relaxed);
+  }
+  launch(grouped_swiglu_onepass_kernel, dim3(num_sms()), dim3(G::kThreads), G::kSmemBytes,
+         as_cuda(stream), m_x, m_wg, m_wu, m_h, m_wd, a, reinterpret_cast<uint16_t*>(y), sync);
+  return launch_status();
 }
 
 MOE_API moe_status moe_debug_wait_timeout(int64_t limit_ns, uint32_t* dev_status,

@@ -253,6 +253,32 @@ moe_status moe_grouped_down_chained(int32_t n_seg, int32_t I, int32_t d, int32_t
                                     const int32_t* seg_count, const moe_bf16* w_down,
                                     moe_bf16* y, uint32_t* dev_status, moe_stream_t stream);
 
+/* Both passes of moe_grouped_swiglu in one persistent launch ([M6.6] 0x04C:
+ * the gate/up pass, then the down pass, over the same segment table), for
+ * decode-sized batches: h[b:b+c] as moe_grouped_gate_up, then y[b:b+c] as
+ * moe_grouped_down on that h, bit for bit.  The units are the gate/up tiles,
+ * then the down tiles, dealt to one CTA per SM; a down tile loads its W_down
+ * atoms at once and waits (bounded) only before reading its h rows, until every
+ * gate/up tile of its segment has stored them, so the weights of the two passes
+ * stream back to back.  Taken when moe_grouped_swiglu_onepass_taken says so
+ * (row boxes of at most 32 rows, d and I multiples of 128, and the two-launch
+ * gate/up pass would take its narrow tiles too); otherwise this call issues
+ * moe_grouped_gate_up and moe_grouped_down_chained and does not touch sync.
+ * sync: int32 [2 * n_seg] device scratch, caller-owned, all zero before the
+ * first call on it; every call that completes leaves it all zero again.  Calls
+ * that overlap on the GPU must not share it.  After a MOE_DEV_TIMEOUT report its
+ * contents are undefined: zero it before reuse.
+ * h [max_rows, I] and y [max_rows, d] are outputs (only segment rows written).
+ * Limits and errors as moe_grouped_gate_up and moe_grouped_down; sync 4-byte
+ * aligned.                                                                 */
+int32_t moe_grouped_swiglu_onepass_taken(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows);
+moe_status moe_grouped_swiglu_onepass(int32_t n_seg, int32_t d, int32_t I, int32_t max_rows,
+                                      const moe_bf16* x, const int32_t* seg_begin,
+                                      const int32_t* seg_count, const moe_bf16* w_gate,
+                                      const moe_bf16* w_up, const moe_bf16* w_down, moe_bf16* h,
+                                      moe_bf16* y, int32_t* sync, uint32_t* dev_status,
+                                      moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Combine                                                                  */
 /* ------------------------------------------------------------------------ */
