@@ -681,8 +681,7 @@ class DecodeBucket:
                                None if L.gather else L.x_perm, L.counts, L.offsets,
                                L.row_to_route, L.route_to_row, L.n_dropped, L.perm_ws,
                                L.perm_ws_bytes, L.dev_status, stream)
-        L.experts_gate_up(stream, self.x)
-        L.experts_down(stream)
+        L.experts(stream, self.x)
         abi.moe_combine_bucket(self.B, self.k, self.d, self.valid, L.y, R, L.route_to_row,
                                L.gates, None, 0, L.out, L.dev_status, stream)
 
