@@ -374,6 +374,34 @@ def record_external(ev, stream):
         raise RuntimeError(f"cuEventRecordWithFlags failed ({r})")
 
 
+def isolated_stage_ms(layer, logits, x, stream, reps=3):
+    """Milliseconds per launch of each stage of a pooled layer's sequential schedule (every
+    stage on `stream`, CUDA events between the stages, eager launches), the layer switched
+    back to its overlapped schedule afterwards."""
+    layer.overlap = False
+    try:
+        stages = layer.stages(logits, x)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for _, fn, _ in stages:  # one untimed pass first
+                fn(stream)
+            for r in range(reps):
+                evs[r][0].record(stream)
+                for i, (_, fn, _) in enumerate(stages):
+                    fn(stream)
+                    evs[r][i + 1].record(stream)
+        stream.synchronize()
+    finally:
+        layer.overlap = True
+    tot, cnt = {}, {}
+    for r in range(reps):
+        for i, (n, _, _) in enumerate(stages):
+            tot[n] = tot.get(n, 0.0) + evs[r][i].elapsed_time(evs[r][i + 1])
+            cnt[n] = cnt.get(n, 0) + 1
+    return {n: tot[n] / cnt[n] for n in tot}
+
+
 def run_ours(args, dist, w):
     import grouped_expert_gemm_gb300 as g
     from grouped_expert_gemm_gb300 import abi, build
@@ -597,6 +625,17 @@ def run_ours(args, dist, w):
             per_stage[n]["timing"] = ("side stream, overlapping the main-stream stages: the "
                                       "figure is the wall-clock span of its work, not a kernel "
                                       "duration")
+    if side_names and getattr(layer, "overlap", False):
+        # the side-stream stages once more, alone: a few eager steps of the same layer's
+        # sequential schedule on one stream, events between the stages, so each of those
+        # stages also carries its own kernel time beside its span in the overlapped step
+        iso = isolated_stage_ms(layer, logits, x, stream, reps=3)
+        for n in side_names & set(iso):
+            b, _ = stage_work(w, layer, n, counts, acc_rows, w.E, I, d, pool)
+            ach = b / (iso[n] * 1e-3) / 1e9
+            per_stage[n]["isolated"] = {"ms_per_launch": round(iso[n], 5),
+                                        "achieved": round(ach, 2), "unit": "GB/s",
+                                        "frac": round(ach / hbm, 4)}
     # the dominant kernel among the main-stream stages (a side-stream figure is a span)
     dom = max((n for n in stage_ms if n not in side_names), key=lambda n: stage_ms[n])
     ds = per_stage[dom]
