@@ -268,6 +268,12 @@ moe_status moe_grouped_down_chained(int32_t n_seg, int32_t I, int32_t d, int32_t
  * first call on it; every call that completes leaves it all zero again.  Calls
  * that overlap on the GPU must not share it.  After a MOE_DEV_TIMEOUT report its
  * contents are undefined: zero it before reuse.
+ * Residency: the down tiles' waits end once every CTA of the launch has reached
+ * an SM.  A kernel running beside it on another stream only delays that until it
+ * ends; but a second launch of this call on another stream at the same time
+ * (its units also dealt to CTAs in advance) can hold the SMs this one needs while
+ * it waits in turn, and a wait then gives up with MOE_DEV_TIMEOUT (outputs
+ * invalid).  Order such calls on one stream or by events.
  * h [max_rows, I] and y [max_rows, d] are outputs (only segment rows written).
  * Limits and errors as moe_grouped_gate_up and moe_grouped_down; sync 4-byte
  * aligned.                                                                 */
@@ -328,7 +334,8 @@ moe_status moe_combine(int32_t T, int32_t k, int32_t d, const moe_bf16* y, int64
  * first use; every call leaves the counters zero again, so it can be reused
  * (and the call replayed from a CUDA graph) without clearing.  Two calls whose work overlaps on the GPU
  * must not share one workspace.  A bounded wait inside the kernel that gives up
- * sets MOE_DEV_TIMEOUT (outputs then invalid).
+ * sets MOE_DEV_TIMEOUT (outputs then invalid).  Its units are claimed from a global
+ * counter by running CTAs only, so its waits end whatever else runs beside it.
  * Limits (else MOE_ERR_UNSUPPORTED): 1 <= T <= 16, T*k <= 64, T*d <= 16384,
  * I <= 2048, d % 64 == 0, I % 64 == 0, E <= 512, k <= 16; grouped routers as moe_route
  * plus (E/n_group) a multiple of ceil-to-{1,2,4,8,12,16}(E/32) spanning a power
