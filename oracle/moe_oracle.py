@@ -249,7 +249,9 @@ def gather_rows(x_bits: np.ndarray, row_to_route: np.ndarray, k: int) -> np.ndar
 # ----------------------------------------------------------------------------
 
 def silu(g: np.ndarray) -> np.ndarray:
-    return g / (1.0 + np.exp(-g))
+    # below g = -709 exp(-g) overflows to inf, and g / inf = -0.0 is SiLU's limit there
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
 
 
 def swiglu(x_f64: np.ndarray, wg_f64: np.ndarray, wu_f64: np.ndarray, wd_f64: np.ndarray,
